@@ -1,0 +1,371 @@
+#!/usr/bin/env python
+"""Throughput of the VLA forward recurrence on GB300.
+
+One step = one vla_forward call over the whole workload (every head, every
+token: eq. 9-11 of "Variational Linear Attention", §3.3). The default workload
+is the d_h = 96 configuration (B=8, H=16, T=4096, bf16 q/k/v/u drawn N(0,1)
+with ||v_t|| <= 4, fp32 state); its inputs (403 MB) are larger than L2, so no
+L2 flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun, one rank per GPU) every
+rank runs its own copy of the workload (heads are independent: weak scaling,
+no collective on the data path); the time is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead, on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "VLA head-tokens/sec at d_h=96,T=4096; % of FP32-FMA roofline"
+UNIT = "head-tokens/s"
+FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM (sm_103)
+FALLBACK_SM_MAX_MHZ = 2070.0
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of vla_fused_kernel on the default workload, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only while
+# the kernel sources hash to SOURCE_SHA; otherwise reported as null.
+NCU_TRAFFIC = {"source_sha": None, "bytes_per_launch": None}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sherman_morrison_memory_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host logic is exercised on CPU with gloo in the tests)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own copy of the workload (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world <= 1:
+        return
+    import torch.distributed as dist
+
+    if device is not None and device.type == "cuda":
+        dist.barrier(device_ids=[device.index])
+    else:
+        dist.barrier()
+
+
+def aggregate_value(units_per_rank: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units all ranks processed / max-over-ranks time."""
+    return units_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="vla_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.close()
+
+    def summary(self) -> dict:
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        sm = float(parts[1].split()[0])
+                        smax = float(parts[2].split()[0])
+                    except ValueError:
+                        continue
+                    rows.append((sm, smax, parts))
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, p in rows for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the fp64 oracle on the host cores (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_time(arrs, w, tokens: int, heads: int):
+    import oracle
+
+    orc = oracle.load()
+    sub = [a.reshape(-1, w.T, w.d)[:heads, :tokens] for a in arrs]
+    t0 = time.perf_counter()
+    r = orc.forward(*sub, lambda0=w.lambda0, eps=w.eps, want_o=True)
+    dt = time.perf_counter() - t0
+    return heads * tokens / dt, r.threads, dt
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from sherman_morrison_memory_gb300 import workloads as W
+
+    arrs = W.make(w)
+    heads = w.heads
+    # size each step's sample so that warmup + steps end within about 2.5 minutes
+    probe_tokens = min(w.T, 16)
+    rate, threads, dt = oracle_time(arrs, w, probe_tokens, heads)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(1, min(w.T, probe_tokens * budget / max(dt, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_time(arrs, w, tokens, heads)
+    total_units, total_time = 0, 0.0
+    for _ in range(args.steps):
+        rate, threads, dt = oracle_time(arrs, w, tokens, heads)
+        total_units += heads * tokens
+        total_time += dt
+    value = total_units / total_time
+    sample = f"all {heads} heads x first {tokens} of {w.T} tokens per step (fp64 oracle, OpenMP over heads)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_time / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.describe()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from sherman_morrison_memory_gb300 import (VLA_OK, vla_forward, vla_get_last_device_status,
+                                               vla_linear_attention_state)
+    from sherman_morrison_memory_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    wr = W.Workload(w.name, w.B, w.H, w.T, w.d, w.dtype, w.structure, w.lambda0, w.eps,
+                    seed=rank_seed(w.seed, rank))
+    arrs = W.make(wr)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    q, k, v, u = (torch.from_numpy(a).to(dev).to(tdt) for a in arrs)
+    B, H, T, d = w.B, w.H, w.T, w.d
+    o = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
+    S = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    A = torch.empty_like(S)
+    zk = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    out = (o, S, A, zk)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        vla_forward(q, k, v, u, w.lambda0, w.eps, out=out)
+    st, detail = vla_get_last_device_status(dev)
+    if st != VLA_OK:
+        raise RuntimeError(f"device status {st} {detail} after warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", "") or "")
+    gpu_id = ("GPU-" + gpu_id) if gpu_id and not gpu_id.startswith("GPU-") else (gpu_id or str(local))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id) as clk:
+        barrier(world, dev)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            vla_forward(q, k, v, u, w.lambda0, w.eps, out=out)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    st, detail = vla_get_last_device_status(dev)
+    if st != VLA_OK:
+        raise RuntimeError(f"device status {st} {detail} in the timed region")
+    ms_max = max_over_ranks(ms, world, dev)
+    units = w.head_tokens
+    value = aggregate_value(units, world, ms_max / 1e3)
+
+    # roofline of the one kernel (vla_fused_kernel) that a step launches
+    peaks = load_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", FALLBACK_SM_MAX_MHZ))
+    n_sm = props.multi_processor_count
+    peak_tflops = n_sm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    flops = 12.0 * d * d * units
+    achieved = flops / (ms / 1e3) / 1e12
+    in_bytes = 4 * units * d * (2 if w.dtype == "bf16" else 4)
+    out_bytes = units * d * 4 + w.heads * (2 * d * d + d) * 4
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
+    sha = kernel_source_sha()
+    traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["source_sha"] == sha else None
+
+    # the same metric end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hu = (x.cpu().pin_memory() for x in (q, k, v, u))
+        hout = tuple(torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in out)
+        ksteps = max(3, min(args.steps, args.e2e_steps))
+        for _ in range(2):
+            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        e0.record(stream)
+        for _ in range(ksteps):
+            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ksteps, world, dev)
+        e2e = {"value": aggregate_value(units, world, e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (hq, hk, hv, hu)),
+               "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in hout),
+               "ms_per_step": e2e_ms, "steps": ksteps}
+
+    # ||S_T||_F of VLA next to plain cumulative linear attention on the same inputs
+    vla_fro = torch.linalg.matrix_norm(S).mean().item()
+    S_la = vla_linear_attention_state(k, v)
+    la_fro = torch.linalg.matrix_norm(S_la).mean().item()
+    torch.cuda.synchronize(dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, dt = oracle_time(arrs, w, w.T, w.heads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"the full workload once ({w.heads} heads x {w.T} tokens, fp64, {dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.describe(), "B": B, "H": H, "T": T, "d_h": d, "input_dtype": w.dtype,
+                       "per_rank_heads": w.heads,
+                       "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB per step), no flush"},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+                         "frac": achieved / peak_tflops, "traffic": traffic,
+                         "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FP32 FMA lanes x 2 x {sm_max:.0f} MHz",
+                         "flop_per_head_token": 12 * d * d, "kernel": "vla_fused_kernel"},
+            "fp32_roofline_pct": 100.0 * achieved / peak_tflops,
+            "hbm": {"achieved_gbs": hbm_gbs, "peak_gbs": hbm_peak, "frac": hbm_gbs / hbm_peak,
+                    "algorithmic_bytes_per_launch": in_bytes + out_bytes},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "state_norm_fro_mean": {"vla": vla_fro, "linear_attention": la_fro},
+            "kernel_source_sha": sha,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=3, help="workload id (1-5); 3 is d_h=96, T=4096")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from sherman_morrison_memory_gb300 import workloads as W
+
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,141 @@
+/*
+ * vla.h -- C ABI of the GB300 (sm_103a) Variational Linear Attention forward
+ * recurrence library (libvla_gb300.so).
+ *
+ * The operation is the per-token recurrence of "Variational Linear
+ * Attention: Stable Associative Memory for Long-Context Transformers"
+ * (Pandey, Singh; arXiv 2605.11196), §3.3, for every (batch, head):
+ *
+ *   eq. 9   z_t = A_{t-1} u^_t,  delta_t = 1 + u^_t . z_t,
+ *           A_t = A_{t-1} - z_t z_t^T / delta_t             (Sherman-Morrison)
+ *   eq. 10  e_t = v_t - S_{t-1} k^_t,
+ *           alpha^_t = A_t k^_t / ||A_t k^_t||,
+ *           S_t = S_{t-1} + e_t alpha^_t^T
+ *   eq. 11  z^key_t = z^key_{t-1} + phi(k_t),
+ *           o_t = S_t phi(q_t) / max(phi(q_t) . z^key_t, eps),  phi = ELU + 1
+ *
+ * with u^ = u / max(||u||, 1e-12) and k^ = k / max(||k||, 1e-12) formed inside
+ * the op (§3.2: unit penalty directions; §3.3: unit keys), the same guard on
+ * ||A_t k^_t||, phi applied to the raw q and k, and, by default,
+ * S_0 = 0, A_0 = I / lambda0 (§3.2), z^key_0 = 0.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or keeps them.
+ *  - Sequences are [B, H, T, d] row-major (d fastest); states are
+ *    S, A: [B, H, d, d] row-major with S[i][j] mapping key coordinate j to
+ *    output coordinate i; z^key: [B, H, d].
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Calls are asynchronous on that stream: argument errors are
+ *    returned at once, failures inside the kernel are recorded in the
+ *    workspace and read back by vla_get_last_device_status().
+ *  - Supported head dimensions d: 32, 64, 96, 128 (else VLA_ERR_UNSUPPORTED).
+ *  - Arithmetic and state are fp32 on the device.
+ */
+#ifndef VLA_GB300_H
+#define VLA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VLA_OK = 0,
+    VLA_ERR_INVALID_ARG = 1,   /* NULL/misaligned pointer, bad size, dtype or scalar */
+    VLA_ERR_UNSUPPORTED = 2,   /* head dimension not in {32, 64, 96, 128} */
+    VLA_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+    VLA_ERR_TIMEOUT = 4,       /* a bounded in-kernel wait ran out; outputs are invalid */
+    VLA_ERR_NONFINITE = 5      /* a NaN/Inf appeared in delta_t or the gate norm */
+} vla_status;
+
+typedef enum {
+    VLA_F32 = 0,               /* q, k, v, u are float32 */
+    VLA_BF16 = 1               /* q, k, v, u are bfloat16 (widened to fp32 on load) */
+} vla_dtype;
+
+/* Optional knobs of vla_forward_ex(). Zero-fill for the defaults. */
+typedef struct {
+    unsigned int wait_limit_us;  /* limit of every in-kernel wait, microseconds; 0 = 2,000,000 */
+    int test_stall_producer;     /* TESTING ONLY: nonzero makes the input-staging warp publish
+                                    nothing, so every consumer's bounded wait runs out and the
+                                    call reports VLA_ERR_TIMEOUT without faulting the GPU */
+} vla_options;
+
+/* Bytes of device workspace vla_forward() needs (one status record). The
+ * workspace must be zero-filled before its first use (cudaMemset or
+ * vla_workspace_reset); vla_get_last_device_status() clears it again. */
+size_t vla_workspace_bytes(void);
+
+/* Zero the status record in `workspace` (asynchronous on `stream`). */
+vla_status vla_workspace_reset(void* workspace, void* stream);
+
+/*
+ * vla_forward -- run eq. 9-11 over T tokens for all B*H heads (§3.3).
+ *
+ *  q, k, v, u   [B, H, T, d] device arrays of `dtype`, 16-byte aligned.
+ *               May be NULL only when T == 0.
+ *  B, H, T      sizes, >= 0 (B*H <= 2^31-1). T == 0 copies the initial
+ *               state to the state outputs.
+ *  d            head dimension, one of 32, 64, 96, 128.
+ *  lambda0      > 0, finite: the default A_0 = I / lambda0 (the paper uses 0.1).
+ *  eps          > 0, finite: the readout floor of eq. 11 (the paper uses 1e-4).
+ *  S0, A0       [B, H, d, d] float32 carried-in state, or NULL for the defaults
+ *               S_0 = 0 and A_0 = I / lambda0 (chunked or decode use passes the
+ *               previous call's S_out / A_out here).
+ *  zk0          [B, H, d] float32 carried-in z^key, or NULL for 0.
+ *  o            [B, H, T, d] float32 output, 16-byte aligned (NULL only if T == 0).
+ *  S_out, A_out [B, H, d, d] float32 final state, 16-byte aligned, required.
+ *  zk_out       [B, H, d] float32 final z^key, or NULL to skip.
+ *  workspace    >= vla_workspace_bytes() bytes of zero-filled device memory,
+ *               16-byte aligned; holds the device status record.
+ *  stream       cudaStream_t as void*.
+ *
+ * Inputs and outputs must not overlap (S0/S_out, A0/A_out, zk0/zk_out may be
+ * the same buffer: each head reads its initial state before it writes the
+ * final one). Returns VLA_OK once the kernel is enqueued, or the first
+ * argument / launch error.
+ */
+vla_status vla_forward(const void* q, const void* k, const void* v, const void* u,
+                       vla_dtype dtype, int B, int H, int T, int d,
+                       float lambda0, float eps,
+                       const float* S0, const float* A0, const float* zk0,
+                       float* o, float* S_out, float* A_out, float* zk_out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* vla_forward with options (opts may be NULL = defaults). */
+vla_status vla_forward_ex(const void* q, const void* k, const void* v, const void* u,
+                          vla_dtype dtype, int B, int H, int T, int d,
+                          float lambda0, float eps,
+                          const float* S0, const float* A0, const float* zk0,
+                          float* o, float* S_out, float* A_out, float* zk_out,
+                          void* workspace, size_t workspace_bytes, void* stream,
+                          const vla_options* opts);
+
+/*
+ * Synchronise `stream`, read and clear the status record that kernels on it
+ * wrote into `workspace`. Returns VLA_OK, VLA_ERR_TIMEOUT (takes precedence)
+ * or VLA_ERR_NONFINITE, or VLA_ERR_CUDA if the copy/sync itself failed.
+ * If `detail` is not NULL it receives {role, head, token} of the first
+ * recorded failure (role: 0 staging, 1 gate, 2 A-pass, 3 S-pass), or -1s.
+ */
+vla_status vla_get_last_device_status(void* workspace, void* stream, int* detail);
+
+/* Static text for a status code. */
+const char* vla_status_string(vla_status s);
+
+/*
+ * Plain cumulative linear-attention state, the comparison of §4.1:
+ * S_out[b, h] = sum_t v_t phi(k_t)^T ([B, H, d, d] float32, 16-byte aligned),
+ * for k, v [B, H, T, d] of `dtype`. Used to report ||S_T||_F next to VLA's.
+ */
+vla_status vla_linear_attention_state(const void* k, const void* v, vla_dtype dtype,
+                                      int B, int H, int T, int d,
+                                      float* S_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VLA_GB300_H */

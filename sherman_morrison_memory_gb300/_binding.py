@@ -1,0 +1,227 @@
+"""ctypes binding of libvla_gb300.so (C ABI in include/vla.h).
+
+Argument marshalling only: shapes, dtypes and devices are checked, outputs
+and the status workspace are allocated with torch, and the C entry points are
+called on the current CUDA stream. All arithmetic happens in the library.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+
+VLA_OK = 0
+VLA_ERR_INVALID_ARG = 1
+VLA_ERR_UNSUPPORTED = 2
+VLA_ERR_CUDA = 3
+VLA_ERR_TIMEOUT = 4
+VLA_ERR_NONFINITE = 5
+
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+_lock = threading.Lock()
+_LIB = None
+_WORKSPACES = {}
+
+
+class VLAError(RuntimeError):
+    def __init__(self, status: int, where: str, detail=None):
+        self.status = status
+        self.detail = detail
+        msg = f"{where}: {vla_status_string(status)} (status {status})"
+        if detail is not None and detail[0] >= 0:
+            msg += f"; role={detail[0]} head={detail[1]} token={detail[2]}"
+        super().__init__(msg)
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("wait_limit_us", ctypes.c_uint), ("test_stall_producer", ctypes.c_int)]
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "_build", "libvla_gb300.so")
+
+
+def load_library():
+    """Load libvla_gb300.so; raises if it has not been built."""
+    global _LIB
+    with _lock:
+        if _LIB is not None:
+            return _LIB
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library not built: {path} is missing. "
+                "Build it with `python -m sherman_morrison_memory_gb300.build`.")
+        lib = ctypes.CDLL(path)
+        vp, cp, ci, cf = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fwd_args = [vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, cf, vp, vp, vp, vp, vp, vp, vp, vp,
+                    ctypes.c_size_t, vp]
+        lib.vla_forward.argtypes = fwd_args
+        lib.vla_forward.restype = ci
+        lib.vla_forward_ex.argtypes = fwd_args + [ctypes.POINTER(_Options)]
+        lib.vla_forward_ex.restype = ci
+        lib.vla_workspace_bytes.argtypes = []
+        lib.vla_workspace_bytes.restype = ctypes.c_size_t
+        lib.vla_workspace_reset.argtypes = [vp, vp]
+        lib.vla_workspace_reset.restype = ci
+        lib.vla_get_last_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+        lib.vla_get_last_device_status.restype = ci
+        lib.vla_status_string.argtypes = [ci]
+        lib.vla_status_string.restype = ctypes.c_char_p
+        lib.vla_linear_attention_state.argtypes = [vp, vp, ci, ci, ci, ci, ci, vp, vp]
+        lib.vla_linear_attention_state.restype = ci
+        del cp
+        _LIB = lib
+        return lib
+
+
+def vla_status_string(status: int) -> str:
+    try:
+        return load_library().vla_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def vla_workspace_bytes() -> int:
+    return int(load_library().vla_workspace_bytes())
+
+
+def _stream_handle(device: torch.device, stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _workspace(device: torch.device) -> torch.Tensor:
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _WORKSPACES.get(idx)
+    if ws is None:
+        nbytes = vla_workspace_bytes()
+        ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=torch.device("cuda", idx))
+        _WORKSPACES[idx] = ws
+    return ws
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_state(x, shape, device, name):
+    if x is None:
+        return None
+    if x.dtype != torch.float32 or tuple(x.shape) != shape:
+        raise ValueError(f"{name} must be float32 of shape {shape}, got {x.dtype} {tuple(x.shape)}")
+    if x.device != device:
+        x = x.to(device, non_blocking=True)
+    return x.contiguous()
+
+
+def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tensor,
+                lambda0: float = 0.1, eps: float = 1e-4, state=None, *, out=None, stream=None,
+                check: bool = False, wait_limit_us: int = 0, test_stall_producer: bool = False):
+    """VLA forward recurrence (§3.3 eq. 9-11) over all heads.
+
+    Returns ``(o, (S, A, zk))``: o [B,H,T,d] float32, S and A [B,H,d,d], zk [B,H,d].
+    ``state`` = (S0, A0, zk0), each optional, continues a previous call.
+    ``out`` = (o, S, A, zk) preallocated outputs on the inputs' device.
+    CPU inputs run on the current CUDA device with host<->device copies.
+    ``check=True`` synchronises and raises on an in-kernel failure.
+    """
+    if q.device.type == "cpu":
+        return _forward_host(q, k, v, u, lambda0, eps, state, out=out, check=check)
+    lib = load_library()
+    for name, x in (("k", k), ("v", v), ("u", u)):
+        if x.shape != q.shape or x.dtype != q.dtype or x.device != q.device:
+            raise ValueError(f"{name} must match q in shape, dtype and device")
+    if q.dim() != 4:
+        raise ValueError("q, k, v, u must be [B, H, T, d]")
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported input dtype {q.dtype} (float32 or bfloat16)")
+    q, k, v, u = (x.contiguous() for x in (q, k, v, u))
+    B, H, T, d = q.shape
+    dev = q.device
+    S0 = A0 = zk0 = None
+    if state is not None:
+        S0, A0, zk0 = state
+        S0 = _check_state(S0, (B, H, d, d), dev, "S0")
+        A0 = _check_state(A0, (B, H, d, d), dev, "A0")
+        zk0 = _check_state(zk0, (B, H, d), dev, "zk0")
+    if out is None:
+        o = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
+        S = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+        A = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+        zk = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    else:
+        o, S, A, zk = out
+    ws = _workspace(dev)
+    with torch.cuda.device(dev):
+        sh = _stream_handle(dev, stream)
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d,
+                float(lambda0), float(eps), _ptr(S0), _ptr(A0), _ptr(zk0),
+                _ptr(o), _ptr(S), _ptr(A), _ptr(zk), _ptr(ws), ws.numel() * 4, ctypes.c_void_p(sh))
+        if wait_limit_us or test_stall_producer:
+            opts = _Options(int(wait_limit_us), 1 if test_stall_producer else 0)
+            st = lib.vla_forward_ex(*args, ctypes.byref(opts))
+        else:
+            st = lib.vla_forward(*args)
+    if st != VLA_OK:
+        raise VLAError(st, "vla_forward")
+    if check:
+        st, detail = vla_get_last_device_status(dev, stream)
+        if st != VLA_OK:
+            raise VLAError(st, "vla_forward (device)", detail)
+    return o, (S, A, zk)
+
+
+def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False):
+    """Host buffers in, host buffers out: H2D copies, the kernel, D2H copies,
+    all on the current stream of the current CUDA device. ``out`` may hold
+    preallocated (pinned) host outputs (o, S, A, zk)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dq, dk, dv, du = (x.to(dev, non_blocking=True) for x in (q, k, v, u))
+    dstate = None
+    if state is not None:
+        dstate = tuple(None if x is None else x.to(dev, non_blocking=True) for x in state)
+    o, (S, A, zk) = vla_forward(dq, dk, dv, du, lambda0, eps, dstate, check=check)
+    pin = q.is_pinned()
+    outs = []
+    for i, x in enumerate((o, S, A, zk)):
+        h = out[i] if out is not None else torch.empty(x.shape, dtype=x.dtype, pin_memory=pin)
+        h.copy_(x, non_blocking=h.is_pinned())
+        outs.append(h)
+    return outs[0], (outs[1], outs[2], outs[3])
+
+
+def vla_get_last_device_status(device=None, stream=None) -> Tuple[int, tuple]:
+    """Synchronise the stream, read and clear the device status record.
+
+    Returns (status, (role, head, token))."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws = _workspace(dev)
+    detail = (ctypes.c_int * 3)()
+    with torch.cuda.device(dev):
+        st = lib.vla_get_last_device_status(_ptr(ws), ctypes.c_void_p(_stream_handle(dev, stream)), detail)
+    return int(st), (detail[0], detail[1], detail[2])
+
+
+def vla_linear_attention_state(k: torch.Tensor, v: torch.Tensor, stream=None) -> torch.Tensor:
+    """S = sum_t v_t phi(k_t)^T per head (plain cumulative linear attention)."""
+    lib = load_library()
+    if k.shape != v.shape or k.dtype != v.dtype or k.dim() != 4:
+        raise ValueError("k, v must be matching [B, H, T, d] tensors")
+    k, v = k.contiguous(), v.contiguous()
+    B, H, T, d = k.shape
+    S = torch.empty((B, H, d, d), dtype=torch.float32, device=k.device)
+    with torch.cuda.device(k.device):
+        st = lib.vla_linear_attention_state(_ptr(k), _ptr(v), _DTYPES[k.dtype], B, H, T, d, _ptr(S),
+                                            ctypes.c_void_p(_stream_handle(k.device, stream)))
+    if st != VLA_OK:
+        raise VLAError(st, "vla_linear_attention_state")
+    return S

@@ -1,0 +1,89 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/vla.h declares, and rejects bad arguments before any CUDA work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sherman_morrison_memory_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from sherman_morrison_memory_gb300 import _binding
+    return _binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vla_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("vla_forward", "vla_forward_ex", "vla_workspace_bytes", "vla_workspace_reset",
+              "vla_get_last_device_status", "vla_status_string", "vla_linear_attention_state"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in vla.h but not exported"
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.vla_status_string(s)
+    assert lib.vla_workspace_bytes() >= 16
+
+
+FAKE = 1 << 20  # an aligned non-null address that the validation paths never dereference
+
+
+def _call(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, u=FAKE, dtype=1, B=1, H=1, T=4, d=64, lambda0=0.1, eps=1e-4,
+             S0=None, A0=None, zk0=None, o=FAKE, S=FAKE, A=FAKE, zk=None, ws=FAKE, wsb=256)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.vla_forward(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["u"]), a["dtype"], a["B"], a["H"], a["T"],
+                           a["d"], a["lambda0"], a["eps"], vp(a["S0"]), vp(a["A0"]), vp(a["zk0"]), vp(a["o"]),
+                           vp(a["S"]), vp(a["A"]), vp(a["zk"]), vp(a["ws"]), a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=48), 2), (dict(d=256), 2), (dict(d=0), 2),
+    (dict(B=-1), 1), (dict(T=-3), 1), (dict(dtype=7), 1),
+    (dict(lambda0=0.0), 1), (dict(lambda0=-1.0), 1), (dict(lambda0=float("inf")), 1),
+    (dict(eps=0.0), 1), (dict(eps=float("nan")), 1),
+    (dict(ws=None), 1), (dict(ws=FAKE + 4), 1), (dict(wsb=8), 1),
+    (dict(q=None), 1), (dict(o=None), 1), (dict(S=None), 1), (dict(A=None), 1),
+    (dict(k=FAKE + 2), 1), (dict(o=FAKE + 8), 1), (dict(S=FAKE + 4), 1),
+    (dict(zk=FAKE + 2), 1), (dict(A0=FAKE + 1), 1),
+    (dict(B=1 << 20, H=1 << 12), 1),
+])
+def test_argument_errors(lib, kw, status):
+    assert _call(lib, **kw) == status
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _call(lib, B=0) == 0
+    assert _call(lib, H=0, q=None, o=None) == 0
+
+
+def test_linear_attention_argument_errors(lib):
+    vp = ctypes.c_void_p
+    assert lib.vla_linear_attention_state(vp(FAKE), vp(FAKE), 0, 1, 1, 4, 40, vp(FAKE), None) == 2
+    assert lib.vla_linear_attention_state(vp(FAKE), vp(FAKE), 5, 1, 1, 4, 64, vp(FAKE), None) == 1
+    assert lib.vla_linear_attention_state(vp(FAKE), vp(FAKE), 0, 1, 1, 4, 64, None, None) == 1
+
+
+def test_status_read_rejects_null(lib):
+    d = (ctypes.c_int * 3)()
+    assert lib.vla_get_last_device_status(None, None, d) == 1
+    assert list(d) == [-1, -1, -1]

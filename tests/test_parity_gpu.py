@@ -1,0 +1,238 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Small cases span several staged chunks (8 tokens each) and a ragged tail, every
+supported head dimension and both input dtypes; the five workloads run at
+full size. Tolerance: 2e-3 relative (parity_util.TOL) on o, final S, final A
+and z^key, with the metric defined in parity_util.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import TOL, assert_close, errors, rel_heads, rel_rows, to_dev
+from sherman_morrison_memory_gb300 import (VLA_ERR_NONFINITE, VLA_ERR_TIMEOUT, VLA_OK, vla_forward,
+                                           vla_get_last_device_status, vla_linear_attention_state)
+from sherman_morrison_memory_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+def _inputs(B, H, T, d, dtype, seed):
+    arrs = W.normal(B, H, T, d, seed=seed)
+    if dtype == "bf16":
+        arrs = tuple(W.to_bf16_values(a) for a in arrs)
+    return arrs
+
+
+def _state_dev(state):
+    if state is None:
+        return None
+    return tuple(None if x is None else torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+                 for x in state)
+
+
+def _state_ref(state):
+    if state is None:
+        return {}
+    S0, A0, zk0 = state
+    f = lambda x: None if x is None else np.asarray(x, dtype=np.float32).astype(np.float64)
+    return dict(S0=f(S0), A0=f(A0), zk0=f(zk0))
+
+
+def _run(orc, arrs, dtype, lambda0=0.1, eps=1e-4, state=None):
+    out = vla_forward(*to_dev(arrs, dtype), lambda0=lambda0, eps=eps, state=_state_dev(state), check=True)
+    ref = orc.forward(*arrs, lambda0=lambda0, eps=eps, **_state_ref(state))
+    return out, ref
+
+
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
+@pytest.mark.parametrize("T", [1, 3, 9, 37, 200])
+def test_small_f32(orc, d, T):
+    arrs = _inputs(1, 3, T, d, "f32", seed=d * 1000 + T)
+    out, ref = _run(orc, arrs, "f32")
+    assert_close(errors(out, ref), what=f"d={d} T={T} f32")
+
+
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
+def test_small_bf16(orc, d):
+    arrs = _inputs(2, 2, 45, d, "bf16", seed=d)
+    out, ref = _run(orc, arrs, "bf16")
+    assert_close(errors(out, ref), what=f"d={d} bf16")
+
+
+@pytest.mark.parametrize("d", [32, 96])
+def test_zero_tokens_returns_initial_state(orc, d):
+    arrs = _inputs(1, 2, 0, d, "f32", seed=1)
+    out, _ = _run(orc, arrs, "f32", lambda0=0.25)
+    o, (S, A, zk) = out
+    assert o.numel() == 0
+    assert torch.all(S == 0) and torch.all(zk == 0)
+    assert torch.equal(A.cpu(), (torch.eye(d) * 4.0).expand(1, 2, d, d))
+    warm = orc.forward(*_inputs(1, 2, 30, d, "f32", seed=2))
+    state = (warm.S, warm.A, warm.zk)
+    out, _ = _run(orc, arrs, "f32", state=state)
+    _, (S, A, zk) = out
+    assert np.array_equal(S.cpu().numpy(), warm.S.astype(np.float32))
+    assert np.array_equal(A.cpu().numpy(), warm.A.astype(np.float32))
+    assert np.array_equal(zk.cpu().numpy(), warm.zk.astype(np.float32))
+
+
+@pytest.mark.parametrize("d", [64, 96, 128])
+def test_carried_state_chunks(orc, d):
+    """Calls over [0, t1), [t1, t2), [t2, T) with carried (S, A, z^key) match the oracle's one-shot run."""
+    T, cuts = 150, (13, 64)
+    arrs = _inputs(2, 2, T, d, "bf16", seed=7 + d)
+    warm = orc.forward(*_inputs(2, 2, 40, d, "bf16", seed=99))
+    state0 = (warm.S, warm.A, warm.zk)
+    ref = orc.forward(*arrs, **_state_ref(state0))
+    state = _state_dev(state0)
+    outs = []
+    bounds = (0,) + cuts + (T,)
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        part = to_dev([x[:, :, a:b] for x in arrs], "bf16")
+        o, state = vla_forward(*part, state=state, check=True)
+        outs.append(o)
+    o = torch.cat(outs, dim=2)
+    assert_close(errors((o, state), ref), what=f"chunked d={d}")
+
+
+def test_decode_one_token_at_a_time(orc):
+    d, T = 64, 20
+    arrs = _inputs(1, 2, T, d, "f32", seed=5)
+    ref = orc.forward(*arrs)
+    state = None
+    outs = []
+    for t in range(T):
+        o, state = vla_forward(*to_dev([x[:, :, t:t + 1] for x in arrs], "f32"), state=state, check=True)
+        outs.append(o)
+    assert_close(errors((torch.cat(outs, dim=2), state), ref), what="decode")
+
+
+def test_lambda_and_eps(orc):
+    arrs = _inputs(1, 2, 50, 64, "f32", seed=3)
+    out, ref = _run(orc, arrs, "f32", lambda0=0.7, eps=0.5)
+    assert_close(errors(out, ref), what="lambda0=0.7 eps=0.5")
+
+
+@pytest.mark.parametrize("case", ["zero_key", "zero_u", "zero_v", "den_floor", "large"])
+def test_edge_inputs(orc, case):
+    d, T = 96, 40
+    q, k, v, u = _inputs(1, 2, T, d, "f32", seed=17)
+    if case == "zero_key":
+        k[:, :, 5] = 0.0
+        k[:, :, 21] = 0.0
+    elif case == "zero_u":  # fixed A = I / lambda0: the delta-rule ablation
+        u[:] = 0.0
+    elif case == "zero_v":
+        v[:] = 0.0
+    elif case == "den_floor":
+        q = (q - 60.0).astype(np.float32)
+    elif case == "large":
+        q, k, v, u = (x * np.float32(300.0) for x in (q, k, v, u))
+    out, ref = _run(orc, (q, k, v, u), "f32")
+    if case == "zero_v":
+        o, (S, A, zk) = out
+        assert torch.all(o == 0) and torch.all(S == 0)
+        assert_close({"A": errors(out, ref)["A"]}, what=case)
+    else:
+        assert_close(errors(out, ref), what=case)
+
+
+def test_non_default_stream(orc):
+    arrs = _inputs(1, 4, 33, 96, "bf16", seed=8)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = vla_forward(*to_dev(arrs, "bf16"))
+    s.synchronize()
+    assert_close(errors(out, orc.forward(*arrs)), what="side stream")
+
+
+def test_host_buffers_path(orc):
+    arrs = _inputs(1, 2, 70, 64, "f32", seed=9)
+    host = [torch.from_numpy(a).pin_memory() for a in arrs]
+    o, (S, A, zk) = vla_forward(*host)
+    torch.cuda.synchronize()
+    assert o.device.type == "cpu"
+    assert_close(errors((o, (S, A, zk)), orc.forward(*arrs)), what="host path")
+
+
+def test_linear_attention_state(orc):
+    arrs = _inputs(2, 3, 300, 96, "bf16", seed=10)
+    S = vla_linear_attention_state(*to_dev([arrs[1], arrs[2]], "bf16"))
+    want = orc.linear_attention_state(arrs[1], arrs[2])
+    assert rel_heads(S.cpu().numpy(), want) < 1e-4
+
+
+def test_timeout_is_reported_and_context_survives(orc):
+    """A stalled staging warp makes every consumer's bounded wait run out; the
+    call reports VLA_ERR_TIMEOUT and the next call on the same context works."""
+    arrs = _inputs(1, 2, 64, 96, "f32", seed=11)
+    vla_forward(*to_dev(arrs, "f32"), wait_limit_us=20000, test_stall_producer=True)
+    st, detail = vla_get_last_device_status()
+    assert st == VLA_ERR_TIMEOUT, (st, detail)
+    assert detail[0] in (1, 2, 3)
+    out, ref = _run(orc, arrs, "f32")
+    assert_close(errors(out, ref), what="after timeout")
+    assert vla_get_last_device_status()[0] == VLA_OK
+
+
+def test_nonfinite_input_is_reported():
+    arrs = _inputs(1, 1, 16, 64, "f32", seed=12)
+    arrs[0][0, 0, 7, 3] = np.nan
+    vla_forward(*to_dev(arrs, "f32"))
+    st, _ = vla_get_last_device_status()
+    assert st == VLA_ERR_NONFINITE
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 5])
+def test_workload_full(orc, wid):
+    w = W.WORKLOADS[wid]
+    arrs = W.make(w)
+    out, ref = _run(orc, arrs, w.dtype, lambda0=w.lambda0, eps=w.eps)
+    errs = errors(out, ref)
+    print(f"workload {wid} ({w.describe()}): {errs}")
+    assert_close(errs, what=f"workload {wid}")
+
+
+def test_workload_long_context_sampled(orc):
+    """T = 65536, d = 128, 32 heads: the oracle runs 3 sampled heads in full; o is
+    compared on every token of those heads (and reported at t = 1K, 16K, 64K),
+    and S, A, z^key at t = 1K, 16K, 64K via chunked GPU calls ending there."""
+    w = W.WORKLOADS[4]
+    arrs = W.make(w)
+    heads = [0, 13, 31]
+    sub = [np.ascontiguousarray(a[:, heads]) for a in arrs]
+    dev = to_dev(arrs, w.dtype)
+    del arrs
+    o_full, _ = vla_forward(*dev, lambda0=w.lambda0, eps=w.eps, check=True)
+    o_sub = o_full[:, heads].cpu().numpy()
+    del o_full
+    bounds = [0, 1024, 16384, 65536]
+    state = None
+    st_ref = {}
+    o_ref = []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        part = [x[:, :, a:b] for x in dev]
+        o, state = vla_forward(*part, lambda0=w.lambda0, eps=w.eps, state=state, check=True)
+        ref = orc.forward(*[x[:, :, a:b] for x in sub], lambda0=w.lambda0, eps=w.eps, **st_ref)
+        st_ref = dict(S0=ref.S, A0=ref.A, zk0=ref.zk)
+        o_ref.append(ref.o)
+        sub_state = tuple(x[:, heads] for x in state)
+        e = errors((None, sub_state), ref)
+        e["o_chunk"] = rel_rows(o[:, heads].cpu().numpy(), ref.o)
+        e["o_at_end"] = rel_rows(o_sub[:, :, b - 1], ref.o[:, :, -1])
+        print(f"t={b}: {e}")
+        assert_close(e, what=f"long context t={b}")
+    e = rel_rows(o_sub, np.concatenate(o_ref, axis=2))
+    print(f"one-shot o over all tokens of sampled heads: {e:.3e}")
+    assert e <= TOL
