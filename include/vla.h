@@ -61,6 +61,9 @@ typedef struct {
     int test_stall_producer;     /* TESTING ONLY: nonzero makes the input-staging warp publish
                                     nothing, so every consumer's bounded wait runs out and the
                                     call reports VLA_ERR_TIMEOUT without faulting the GPU */
+    unsigned long long* trace;   /* PROFILING ONLY, builds compiled with -DVLA_TRACE: device buffer
+                                    of 16*T u64 that receives per-token SM clock stamps of head 0
+                                    (roles and sub-steps of the pipeline); else ignored */
 } vla_options;
 
 /* Bytes of device workspace vla_forward() needs (one status record). The

@@ -40,7 +40,8 @@ class VLAError(RuntimeError):
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("wait_limit_us", ctypes.c_uint), ("test_stall_producer", ctypes.c_int)]
+    _fields_ = [("wait_limit_us", ctypes.c_uint), ("test_stall_producer", ctypes.c_int),
+                ("trace", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -166,7 +167,7 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
                 float(lambda0), float(eps), _ptr(S0), _ptr(A0), _ptr(zk0),
                 _ptr(o), _ptr(S), _ptr(A), _ptr(zk), _ptr(ws), ws.numel() * 4, ctypes.c_void_p(sh))
         if wait_limit_us or test_stall_producer:
-            opts = _Options(int(wait_limit_us), 1 if test_stall_producer else 0)
+            opts = _Options(int(wait_limit_us), 1 if test_stall_producer else 0, None)
             st = lib.vla_forward_ex(*args, ctypes.byref(opts))
         else:
             st = lib.vla_forward(*args)

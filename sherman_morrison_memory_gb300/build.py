@@ -31,9 +31,14 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def build(verbose: bool = False, extra=()) -> str:
+TRACE_LIB = os.path.join(BUILD_DIR, "libvla_gb300_trace.so")
+
+
+def build(verbose: bool = False, extra=(), out: str = LIB) -> str:
+    """Compile the library; ``out``/``extra`` select a variant (e.g. the
+    -DVLA_TRACE profiling build written to TRACE_LIB)."""
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     cmd = [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
            "-I", INCLUDE, *SOURCES, "-o", tmp, *extra]
     if verbose:
@@ -41,10 +46,14 @@ def build(verbose: bool = False, extra=()) -> str:
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
     if verbose:
         sys.stderr.write(r.stdout + r.stderr)
-    return LIB
+    return out
+
+
+def build_trace() -> str:
+    return build(extra=("-DVLA_TRACE",), out=TRACE_LIB)
 
 
 if __name__ == "__main__":

@@ -59,26 +59,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns`
+// while the phase is incomplete (it resumes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 
-// Wait until the phase of `bar` with parity `parity` has completed. Returns
-// false if `limit_ns` elapsed or the abort flag (if not null) was raised first.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
-                                       uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait: suspend in hardware between checks (no polling
+// loop that would take issue slots from working warps), give up after
+// `limit_ns` or when the abort flag (if not null) is raised.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
+                                            uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0; it < (1u << 28); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 15u) {
-            if (abort_flag && *abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
-        }
+    for (uint32_t it = 0; it < (1u << 24); ++it) {
+        if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return false;
+}
+
+// Wait until the phase of `bar` with parity `parity` has completed. Returns
+// false if `limit_ns` elapsed or the abort flag (if not null) was raised first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
+                                          uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag, limit_ns);
 }
 
 // 1-D TMA bulk copy global -> shared, completing on `bar` (tx bytes).
@@ -160,6 +180,27 @@ __device__ __forceinline__ int rs_index(int lane, int i) {
         return r;
     } else {
         return i < N ? i : -1;
+    }
+}
+
+// Inverse of rs_index: the lane bits (within the group) and slot that hold
+// original value number r after reduce_scatter<N, H>.
+template <int N, int H>
+__host__ __device__ constexpr int rs_owner_lane(int r) {
+    if constexpr (H >= 1) {
+        constexpr int M = (N + 1) / 2;
+        return r < M ? rs_owner_lane<M, H / 2>(r) : (H | rs_owner_lane<M, H / 2>(r - M));
+    } else {
+        return 0;
+    }
+}
+template <int N, int H>
+__host__ __device__ constexpr int rs_owner_slot(int r) {
+    if constexpr (H >= 1) {
+        constexpr int M = (N + 1) / 2;
+        return r < M ? rs_owner_slot<M, H / 2>(r) : rs_owner_slot<M, H / 2>(r - M);
+    } else {
+        return r;
     }
 }
 

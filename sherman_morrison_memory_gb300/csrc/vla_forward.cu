@@ -40,7 +40,9 @@ namespace vla {
 // ---------------------------------------------------------------------------
 // Per-head-dimension configuration.
 //   NA/NS   A and S warps;  CBA/CBS  column blocks per row (lanes sharing a row)
-//   CH      tokens per staged chunk;  NP  prepped chunk slots;  NRAW  raw slots
+//   NG      gate warps (token t goes to gate warp t mod NG)
+//   CH      tokens per staged chunk;  TB  tokens the staging warp prepares at once
+//   NP      prepped chunk slots;  NRAW  raw chunk slots
 //   RZ/RG   token slots of the A->gate and gate->S rings
 //   PAD     pad shared vectors by 4 floats per 32 (bank spread for the
 //           column-block strides of these layouts)
@@ -50,23 +52,23 @@ template <int D>
 struct Cfg;
 template <>
 struct Cfg<32> {
-    static constexpr int NA = 1, CBA = 4, NS = 1, CBS = 4, CH = 8, NP = 6, NRAW = 3, RZ = 16, RG = 16, PAD = 1,
-                         MINB = 4;
+    static constexpr int NA = 1, CBA = 4, NS = 1, CBS = 4, NG = 1, CH = 8, TB = 4, NP = 6, NRAW = 3, RZ = 16,
+                         RG = 16, PAD = 1, MINB = 4;
 };
 template <>
 struct Cfg<64> {
-    static constexpr int NA = 4, CBA = 8, NS = 2, CBS = 4, CH = 8, NP = 4, NRAW = 3, RZ = 16, RG = 16, PAD = 1,
-                         MINB = 2;
+    static constexpr int NA = 4, CBA = 8, NS = 2, CBS = 4, NG = 1, CH = 8, TB = 4, NP = 4, NRAW = 3, RZ = 16,
+                         RG = 16, PAD = 1, MINB = 2;
 };
 template <>
 struct Cfg<96> {
-    static constexpr int NA = 8, CBA = 8, NS = 4, CBS = 4, CH = 8, NP = 8, NRAW = 3, RZ = 16, RG = 16, PAD = 0,
-                         MINB = 1;
+    static constexpr int NA = 4, CBA = 8, NS = 4, CBS = 8, NG = 2, CH = 8, TB = 4, NP = 8, NRAW = 3, RZ = 16,
+                         RG = 16, PAD = 0, MINB = 1;
 };
 template <>
 struct Cfg<128> {
-    static constexpr int NA = 8, CBA = 8, NS = 8, CBS = 4, CH = 8, NP = 6, NRAW = 2, RZ = 16, RG = 16, PAD = 1,
-                         MINB = 1;
+    static constexpr int NA = 8, CBA = 8, NS = 8, CBS = 4, NG = 1, CH = 8, TB = 2, NP = 6, NRAW = 2, RZ = 16,
+                         RG = 16, PAD = 1, MINB = 1;
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -87,8 +89,8 @@ struct Layout {
     static constexpr int G_A = 0, G_S = VD;
     static constexpr int GSTRIDE = VD + 4;
     // warp roles
-    static constexpr int W_PROD = 0, W_GATE = 1, W_A0 = 2, W_S0 = 2 + C::NA;
-    static constexpr int NWARPS = 2 + C::NA + C::NS, THREADS = 32 * NWARPS;
+    static constexpr int W_PROD = 0, W_GATE = 1, W_A0 = 1 + C::NG, W_S0 = 1 + C::NG + C::NA;
+    static constexpr int NWARPS = 1 + C::NG + C::NA + C::NS, THREADS = 32 * NWARPS;
     // shared memory map (bytes)
     static constexpr int NBAR = C::NRAW + 2 * C::NP + 2 * C::RZ + 2 * C::RG;
     static constexpr size_t OFF_FLAG = 8 * (size_t)NBAR;
@@ -127,12 +129,30 @@ struct Params {
     float eps;
     unsigned long long wait_ns;
     int stall_producer;
+    unsigned long long* trace;
 };
+
+// Per-token clock stamps of head 0 for pipeline analysis (-DVLA_TRACE builds only).
+#ifdef VLA_TRACE
+#define VLA_TRACE_AT(p, role, t)                                                              \
+    do {                                                                                      \
+        if ((p).trace && blockIdx.x == 0) (p).trace[(size_t)(role) * (p).T + (t)] = clock64(); \
+    } while (0)
+// sub-step stamps of one thread (rows 5.. of the trace buffer)
+#define VLA_TRACE_PT(p, row, t) VLA_TRACE_AT(p, row, t)
+#else
+#define VLA_TRACE_AT(p, role, t) \
+    do {                         \
+    } while (0)
+#define VLA_TRACE_PT(p, row, t) \
+    do {                        \
+    } while (0)
+#endif
 
 struct Smem {
     uint64_t* full_r;   // raw chunk landed (TMA tx)
     uint64_t* full_p;   // prepped chunk published
-    uint64_t* empty_p;  // prepped chunk released by A, gate and S warps
+    uint64_t* empty_p;  // prepped chunk released by the S warps (its last readers)
     uint64_t* full_z;   // z/w of a token published by the A warps
     uint64_t* empty_z;  // ... released by the gate
     uint64_t* full_g;   // alpha^ of a token published by the gate
@@ -162,18 +182,55 @@ __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast
 enum Role { ROLE_STAGE = 0, ROLE_GATE = 1, ROLE_A = 2, ROLE_S = 3 };
 
 // ---------------------------------------------------------------------------
-// staging warp
+// small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+
+// Sum of N per-warp partials stored contiguously (N a multiple of 4 is read
+// with float4 loads), in a fixed tree order so every reader gets the same bits.
+template <int N>
+__device__ __forceinline__ float sum_partials(const float* p) {
+    if constexpr (N % 4 == 0) {
+        float4 acc = ld4(p);
+#pragma unroll
+        for (int i = 4; i < N; i += 4) {
+            const float4 x = ld4(p + i);
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+        }
+        return (acc.x + acc.y) + (acc.z + acc.w);
+    } else {
+        float s = p[0];
+#pragma unroll
+        for (int i = 1; i < N; ++i) s += p[i];
+        return s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// staging warp: TMA bulk copies of raw q, k, v, u chunks, then per token
+// u^, k^ (unit), phi(q), v (fp32), z^key += phi(k), den = max(phi(q).z^key, eps)
+// (§3.2-3.3, eq. 11). Tokens are processed TB at a time so that the
+// cross-lane reductions of several tokens overlap.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn>
 __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int bh, int lane) {
     using C = Cfg<D>;
     using LY = Layout<D, TIn>;
     constexpr int E = D / 32;
+    constexpr int TB = C::TB;
+    static_assert(C::CH % TB == 0, "token batch divides the chunk");
     const int T = p.T;
     const int nch = (T + C::CH - 1) / C::CH;
     const size_t head = (size_t)bh * T * D;
     const TIn* src[4] = {static_cast<const TIn*>(p.q) + head, static_cast<const TIn*>(p.k) + head,
                          static_cast<const TIn*>(p.v) + head, static_cast<const TIn*>(p.u) + head};
+
+    // testing hook: publish nothing and raise no flag, so that every consumer
+    // runs into its own wait limit
+    if (p.stall_producer) return;
 
     float zk[E];
 #pragma unroll
@@ -190,65 +247,77 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
                      sm.full_r + rs);
     };
 
-    // testing hook: publish nothing and raise no flag, so that every consumer
-    // runs into its own wait limit
-    if (p.stall_producer) return;
     bool abort = false;
     int issued = min(C::NRAW, nch), landed = 0, c = 0;
     if (lane == 0)
         for (int i = 0; i < issued; ++i) issue(i);
-    for (; !abort && c < nch; ++c) {
+    for (; c < nch; ++c) {
         const int rs = c % C::NRAW, ps = c % C::NP;
         if (!mbar_wait(sm.full_r + rs, (c / C::NRAW) & 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
         landed = c + 1;
+        if (lane == 0) VLA_TRACE_PT(p, 14, c * C::CH);
         if (!mbar_wait(sm.empty_p + ps, ((c / C::NP) & 1) ^ 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
+        if (lane == 0) VLA_TRACE_PT(p, 15, c * C::CH);
         const int nt = min(C::CH, T - c * C::CH);
-        const TIn* rq = reinterpret_cast<const TIn*>(sm.raw + (size_t)(rs * 4 + 0) * LY::RAW_TENSOR);
-        const TIn* rk = reinterpret_cast<const TIn*>(sm.raw + (size_t)(rs * 4 + 1) * LY::RAW_TENSOR);
-        const TIn* rv = reinterpret_cast<const TIn*>(sm.raw + (size_t)(rs * 4 + 2) * LY::RAW_TENSOR);
-        const TIn* ru = reinterpret_cast<const TIn*>(sm.raw + (size_t)(rs * 4 + 3) * LY::RAW_TENSOR);
+        const TIn* raw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) raw[i] = reinterpret_cast<const TIn*>(sm.raw + (size_t)(rs * 4 + i) * LY::RAW_TENSOR);
         float* P0 = sm.prep + (size_t)ps * C::CH * LY::PSTRIDE;
-        for (int tc = 0; tc < nt; ++tc) {
-            float qv[E], kv[E], vv[E], uv[E];
-            float red[3] = {0.f, 0.f, 0.f};  // ||u||^2, ||k||^2, phi(q) . z^key
+        for (int tb = 0; tb < nt; tb += TB) {
+            float qv[TB][E], kv[TB][E], vv[TB][E], uv[TB][E];
+            float red[3 * TB];  // per token: ||u||^2, ||k||^2, phi(q) . z^key
 #pragma unroll
-            for (int m = 0; m < E; ++m) {
-                const int j = tc * D + lane + 32 * m;
-                qv[m] = ld_in<TIn>(rq, j);
-                kv[m] = ld_in<TIn>(rk, j);
-                vv[m] = ld_in<TIn>(rv, j);
-                uv[m] = ld_in<TIn>(ru, j);
-                red[0] = fmaf(uv[m], uv[m], red[0]);
-                red[1] = fmaf(kv[m], kv[m], red[1]);
-                zk[m] += phi(kv[m]);
-                qv[m] = phi(qv[m]);
-                red[2] = fmaf(qv[m], zk[m], red[2]);
-            }
-            allreduce<3, 16>(red);
-            const float iu = 1.f / fmaxf(sqrtf(red[0]), 1e-12f);
-            const float ik = 1.f / fmaxf(sqrtf(red[1]), 1e-12f);
-            float* P = P0 + tc * LY::PSTRIDE;
+            for (int b = 0; b < TB; ++b) {
+                const bool live = tb + b < nt;
+                float uu = 0.f, kk = 0.f, qz = 0.f;
 #pragma unroll
-            for (int m = 0; m < E; ++m) {
-                const int j = lane + 32 * m;
-                P[LY::P_U + vidx<D>(j)] = uv[m] * iu;
-                P[LY::P_K + vidx<D>(j)] = kv[m] * ik;
-                P[LY::P_Q + vidx<D>(j)] = qv[m];
-                P[LY::P_V + j] = vv[m];
+                for (int m = 0; m < E; ++m) {
+                    const int j = (tb + b) * D + lane + 32 * m;
+                    qv[b][m] = live ? ld_in<TIn>(raw[0], j) : 0.f;
+                    kv[b][m] = live ? ld_in<TIn>(raw[1], j) : 0.f;
+                    vv[b][m] = live ? ld_in<TIn>(raw[2], j) : 0.f;
+                    uv[b][m] = live ? ld_in<TIn>(raw[3], j) : 0.f;
+                    uu = fmaf(uv[b][m], uv[b][m], uu);
+                    kk = fmaf(kv[b][m], kv[b][m], kk);
+                    if (live) zk[m] += phi(kv[b][m]);
+                    qv[b][m] = phi(qv[b][m]);
+                    qz = fmaf(qv[b][m], zk[m], qz);
+                }
+                red[3 * b] = uu;
+                red[3 * b + 1] = kk;
+                red[3 * b + 2] = qz;
             }
-            if (lane == 0) P[LY::P_DEN] = fmaxf(red[2], p.eps);
+            allreduce<3 * TB, 16>(red);
+#pragma unroll
+            for (int b = 0; b < TB; ++b) {
+                if (tb + b < nt) {
+                    const float iu = rsqrtf(fmaxf(red[3 * b], 1e-24f));  // 1 / max(||u||, 1e-12)
+                    const float ik = rsqrtf(fmaxf(red[3 * b + 1], 1e-24f));
+                    float* P = P0 + (tb + b) * LY::PSTRIDE;
+#pragma unroll
+                    for (int m = 0; m < E; ++m) {
+                        const int j = lane + 32 * m;
+                        P[LY::P_U + vidx<D>(j)] = uv[b][m] * iu;
+                        P[LY::P_K + vidx<D>(j)] = kv[b][m] * ik;
+                        P[LY::P_Q + vidx<D>(j)] = qv[b][m];
+                        P[LY::P_V + j] = vv[b][m];
+                    }
+                    if (lane == 0) P[LY::P_DEN] = fmaxf(red[3 * b + 2], p.eps);
+                }
+            }
         }
         // our generic-proxy reads of raw slot rs are done before the TMA refill
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(sm.full_p + ps);
+            VLA_TRACE_AT(p, 0, c * C::CH);
             if (c + C::NRAW < nch) issue(c + C::NRAW);
         }
         issued = min(c + 1 + C::NRAW, nch);
@@ -268,35 +337,33 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
 }
 
 // ---------------------------------------------------------------------------
-// gate warp: alpha^_t = A_t k^ / ||A_t k^|| (eq. 10) from the published z, w
+// gate warps: alpha^_t = A_t k^ / ||A_t k^|| (eq. 10) from the published z, w,
+// with A_t k^ = w - z (z . k^) / delta. Gate warp g handles tokens t = g mod NG.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn>
-__device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int bh, int lane) {
+__device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int bh, int g, int lane) {
     using C = Cfg<D>;
     using LY = Layout<D, TIn>;
     constexpr int E = D / 32;
     bool abort = false, nonfinite = false;
-    int t = 0;
-    for (; t < p.T; ++t) {
+    int t = g;
+    for (; t < p.T; t += C::NG) {
         const int zs = t % C::RZ;
         if (!mbar_wait(sm.full_z + zs, (t / C::RZ) & 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
         const int chunk = t / C::CH, tc = t - chunk * C::CH, ps = chunk % C::NP;
-        if (tc == 0 && !mbar_wait(sm.full_p + ps, (chunk / C::NP) & 1, sm.abort, p.wait_ns)) {
+        if (tc < C::NG && !mbar_wait(sm.full_p + ps, (chunk / C::NP) & 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
         const float* Z = sm.zr + (size_t)zs * LY::ZSTRIDE;
         const float* P = sm.prep + (size_t)(ps * C::CH + tc) * LY::PSTRIDE;
-        float delta = 1.f, zkd = 0.f;
-#pragma unroll
-        for (int w = 0; w < C::NA; ++w) {
-            delta += Z[LY::Z_DD + w];
-            zkd += Z[LY::Z_DK + w];
-        }
-        const float cf = zkd / delta;
+        if (lane == 0 && g == 0) VLA_TRACE_PT(p, 11, t);
+        const float delta = 1.f + sum_partials<C::NA>(Z + LY::Z_DD);
+        const float zkd = sum_partials<C::NA>(Z + LY::Z_DK);
+        const float cf = zkd * __frcp_rn(delta);
         float av[E];
         float red[2] = {0.f, 0.f};  // ||a||^2, a . phi(q)
 #pragma unroll
@@ -307,13 +374,15 @@ __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int b
             red[1] = fmaf(av[m], P[LY::P_Q + j], red[1]);
         }
         allreduce<2, 16>(red);
-        const float inv = 1.f / fmaxf(sqrtf(red[0]), 1e-12f);
+        if (lane == 0 && g == 0) VLA_TRACE_PT(p, 12, t);
+        const float inv = rsqrtf(fmaxf(red[0], 1e-24f));  // 1 / max(||a||, 1e-12)
         if (!(isfinite(delta) && isfinite(red[0]) && isfinite(red[1]))) nonfinite = true;
         const int gs = t % C::RG;
         if (!mbar_wait(sm.empty_g + gs, ((t / C::RG) & 1) ^ 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
+        if (lane == 0 && g == 0) VLA_TRACE_PT(p, 13, t);
         float* G = sm.gr + (size_t)gs * LY::GSTRIDE;
 #pragma unroll
         for (int m = 0; m < E; ++m) G[LY::G_A + vidx<D>(lane + 32 * m)] = av[m] * inv;
@@ -321,8 +390,8 @@ __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int b
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(sm.full_g + gs);
+            VLA_TRACE_AT(p, 2, t);
             mbar_arrive(sm.empty_z + zs);
-            if (tc == C::CH - 1 || t == p.T - 1) mbar_arrive(sm.empty_p + ps);
         }
     }
     if (abort) {
@@ -333,7 +402,10 @@ __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int b
 }
 
 // ---------------------------------------------------------------------------
-// A warps: Sherman-Morrison chain (eq. 9), A resident in registers
+// A warps: Sherman-Morrison chain (eq. 9), A resident in registers as float2
+// pairs (packed fp32 FMA). Per token one pass over A applies the pending
+// update of the previous token, A -= (z/delta) z^T, and accumulates
+// z = A u^ and w = A k^.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn>
 __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, int warp, int lane) {
@@ -342,6 +414,7 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
     constexpr int RPW = 32 / C::CBA;              // row groups per warp
     constexpr int RA = D / (C::NA * RPW);         // rows per thread
     constexpr int CA = D / C::CBA;                // columns per thread
+    constexpr int C2 = CA / 2;                    // float2 columns
     constexpr int NV = 2 * RA + 2;                // z rows, w rows, u^.z and k^.z partials
     constexpr int HR = C::CBA / 2;
     constexpr int NOUT = rs_count<NV, HR>();
@@ -351,62 +424,81 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
     const int cb = lane % C::CBA, rgl = lane / C::CBA;
     const int row0 = (wa * RPW + rgl) * RA, col0 = cb * CA;
 
-    float a[RA][CA];
+    float2 a[RA][C2];
     {
         const float* A0 = p.A0 ? p.A0 + (size_t)bh * D * D : nullptr;
 #pragma unroll
         for (int r = 0; r < RA; ++r)
 #pragma unroll
-            for (int c = 0; c < CA; ++c)
-                a[r][c] = A0 ? A0[(size_t)(row0 + r) * D + col0 + c]
-                             : ((row0 + r == col0 + c) ? p.inv_lambda0 : 0.f);
+            for (int c = 0; c < C2; ++c) {
+                const int i = row0 + r, j = col0 + 2 * c;
+                a[r][c] = A0 ? f2(A0[(size_t)i * D + j], A0[(size_t)i * D + j + 1])
+                             : f2(i == j ? p.inv_lambda0 : 0.f, i == j + 1 ? p.inv_lambda0 : 0.f);
+            }
     }
     // pending rank-1 update of the previous token: A -= (z/delta) z^T
-    float yr[RA], zj[CA];
+    float2 nyr[RA], zj[C2];
 #pragma unroll
-    for (int r = 0; r < RA; ++r) yr[r] = 0.f;
+    for (int r = 0; r < RA; ++r) nyr[r] = f2(0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < CA; ++c) zj[c] = 0.f;
+    for (int c = 0; c < C2; ++c) zj[c] = f2(0.f, 0.f);
 
-    bool abort = false;
-    int t = 0;
-    for (; t < p.T; ++t) {
-        const int chunk = t / C::CH, tc = t - chunk * C::CH, ps = chunk % C::NP;
-        if (tc == 0 && !abort && !mbar_wait(sm.full_p + ps, (chunk / C::NP) & 1, sm.abort, p.wait_ns))
-            abort = true;
-        const float* P = sm.prep + (size_t)(ps * C::CH + tc) * LY::PSTRIDE;
-
-        // one pass over A: apply the pending update, then z = A u^, w = A k^
-        float pz[RA], pw[RA];
-#pragma unroll
-        for (int r = 0; r < RA; ++r) pz[r] = pw[r] = 0.f;
+    // this token's u^, k^ (columns, and rows for the scalar partials)
+    float2 uj[C2], kj[C2];
+    float ui[RA], ki[RA];
+    auto load_token = [&](const float* P) {
 #pragma unroll
         for (int c4 = 0; c4 < CA; c4 += 4) {
             const float4 u4 = ld4(P + LY::P_U + vidx<D>(col0 + c4));
             const float4 k4 = ld4(P + LY::P_K + vidx<D>(col0 + c4));
-            const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
-            const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int r = 0; r < RA; ++r) {
-                    const float x = fmaf(-yr[r], zj[c4 + cc], a[r][c4 + cc]);
-                    a[r][c4 + cc] = x;
-                    pz[r] = fmaf(x, uu[cc], pz[r]);
-                    pw[r] = fmaf(x, kk[cc], pw[r]);
-                }
+            uj[c4 / 2] = f2(u4.x, u4.y);
+            uj[c4 / 2 + 1] = f2(u4.z, u4.w);
+            kj[c4 / 2] = f2(k4.x, k4.y);
+            kj[c4 / 2 + 1] = f2(k4.z, k4.w);
         }
+#pragma unroll
+        for (int r = 0; r < RA; ++r) {
+            ui[r] = P[LY::P_U + vidx<D>(row0 + r)];
+            ki[r] = P[LY::P_K + vidx<D>(row0 + r)];
+        }
+    };
+
+    bool abort = false;
+    int t = 0;
+    if (p.T > 0) {
+        if (!mbar_wait(sm.full_p, 0, sm.abort, p.wait_ns)) abort = true;
+        load_token(sm.prep);
+    }
+    for (; t < p.T; ++t) {
+        const bool tr0 = (wa == 0 && lane == 0);
+        if (tr0) VLA_TRACE_PT(p, 5, t);
+
+        // one pass over A: apply the pending update, then z = A u^, w = A k^
+        float2 pz[RA], pw[RA];
+#pragma unroll
+        for (int r = 0; r < RA; ++r) pz[r] = pw[r] = f2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < C2; ++c)
+#pragma unroll
+            for (int r = 0; r < RA; ++r) {
+                const float2 x = __ffma2_rn(nyr[r], zj[c], a[r][c]);
+                a[r][c] = x;
+                pz[r] = __ffma2_rn(x, uj[c], pz[r]);
+                pw[r] = __ffma2_rn(x, kj[c], pw[r]);
+            }
         float vals[NV];
         float dd = 0.f, dk = 0.f;
 #pragma unroll
         for (int r = 0; r < RA; ++r) {
-            dd = fmaf(P[LY::P_U + vidx<D>(row0 + r)], pz[r], dd);
-            dk = fmaf(P[LY::P_K + vidx<D>(row0 + r)], pz[r], dk);
-            vals[r] = pz[r];
-            vals[RA + r] = pw[r];
+            const float z = pz[r].x + pz[r].y;
+            vals[r] = z;
+            vals[RA + r] = pw[r].x + pw[r].y;
+            dd = fmaf(ui[r], z, dd);
+            dk = fmaf(ki[r], z, dk);
         }
         vals[2 * RA] = dd;
         vals[2 * RA + 1] = dk;
+        if (tr0) VLA_TRACE_PT(p, 6, t);
         reduce_scatter<NV, HR>(vals, lane);
         // the two scalar partials also need the sum over this warp's row groups
         float sc[NOUT];
@@ -418,7 +510,9 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
             for (int j = 0; j < NOUT; ++j) sc[j] += __shfl_xor_sync(0xffffffffu, sc[j], h);
 
         const int zs = t % C::RZ;
+        if (tr0) VLA_TRACE_PT(p, 7, t);
         if (!abort && !mbar_wait(sm.empty_z + zs, ((t / C::RZ) & 1) ^ 1, sm.abort, p.wait_ns)) abort = true;
+        if (tr0) VLA_TRACE_PT(p, 8, t);
         float* Z = sm.zr + (size_t)zs * LY::ZSTRIDE;
 #pragma unroll
         for (int j = 0; j < NOUT; ++j) {
@@ -434,28 +528,37 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
             else if (rgl == 0 && idx == 2 * RA + 1)
                 Z[LY::Z_DK + wa] = sc[j];
         }
+        // prefetch the next token's vectors while the other A warps catch up
+        if (t + 1 < p.T) {
+            const int t1 = t + 1, chunk1 = t1 / C::CH, tc1 = t1 - chunk1 * C::CH, ps1 = chunk1 % C::NP;
+            if (tc1 == 0 && !abort && !mbar_wait(sm.full_p + ps1, (chunk1 / C::NP) & 1, sm.abort, p.wait_ns))
+                abort = true;
+            load_token(sm.prep + (size_t)(ps1 * C::CH + tc1) * LY::PSTRIDE);
+        }
         // publish among the A warps; every A thread takes the same abort decision
         if (bar_red_or(1, C::NA * 32, abort || (*sm.abort != 0))) {
             abort = true;
             break;
         }
-        if (wa == 0 && lane == 0) mbar_arrive(sm.full_z + zs);
-        if (lane == 0 && (tc == C::CH - 1 || t == p.T - 1)) mbar_arrive(sm.empty_p + ps);
-
-        float delta = 1.f;
+        if (tr0) VLA_TRACE_PT(p, 9, t);
+        if (wa == 0 && lane == 0) {
+            mbar_arrive(sm.full_z + zs);
+            VLA_TRACE_AT(p, 1, t);
+        }
+        const float delta = 1.f + sum_partials<C::NA>(Z + LY::Z_DD);
+        const float inv = __frcp_rn(delta);
 #pragma unroll
-        for (int w = 0; w < C::NA; ++w) delta += Z[LY::Z_DD + w];
-        const float inv = 1.f / delta;
-#pragma unroll
-        for (int r = 0; r < RA; ++r) yr[r] = Z[LY::Z_Z + vidx<D>(row0 + r)] * inv;
+        for (int r = 0; r < RA; ++r) {
+            const float y = -Z[LY::Z_Z + vidx<D>(row0 + r)] * inv;
+            nyr[r] = f2(y, y);
+        }
 #pragma unroll
         for (int c4 = 0; c4 < CA; c4 += 4) {
             const float4 z4 = ld4(Z + LY::Z_Z + vidx<D>(col0 + c4));
-            zj[c4] = z4.x;
-            zj[c4 + 1] = z4.y;
-            zj[c4 + 2] = z4.z;
-            zj[c4 + 3] = z4.w;
+            zj[c4 / 2] = f2(z4.x, z4.y);
+            zj[c4 / 2 + 1] = f2(z4.z, z4.w);
         }
+        if (tr0) VLA_TRACE_PT(p, 10, t);
     }
     if (abort) {
         if (wa == 0 && lane == 0) record_failure(p.status, BIT_TIMEOUT, ROLE_A, bh, t);
@@ -466,18 +569,16 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
 #pragma unroll
     for (int r = 0; r < RA; ++r)
 #pragma unroll
-        for (int c4 = 0; c4 < CA; c4 += 4) {
-            float4 x;
-            x.x = fmaf(-yr[r], zj[c4], a[r][c4]);
-            x.y = fmaf(-yr[r], zj[c4 + 1], a[r][c4 + 1]);
-            x.z = fmaf(-yr[r], zj[c4 + 2], a[r][c4 + 2]);
-            x.w = fmaf(-yr[r], zj[c4 + 3], a[r][c4 + 3]);
-            *reinterpret_cast<float4*>(Ao + (size_t)(row0 + r) * D + col0 + c4) = x;
+        for (int c = 0; c < C2; c += 2) {
+            const float2 x0 = __ffma2_rn(nyr[r], zj[c], a[r][c]);
+            const float2 x1 = __ffma2_rn(nyr[r], zj[c + 1], a[r][c + 1]);
+            *reinterpret_cast<float4*>(Ao + (size_t)(row0 + r) * D + col0 + 2 * c) = make_float4(x0.x, x0.y, x1.x, x1.y);
         }
 }
 
 // ---------------------------------------------------------------------------
-// S warps: residual write and readout (eq. 10-11), S resident in registers
+// S warps: residual write and readout (eq. 10-11), S resident in registers as
+// float2 pairs; each warp owns whole rows.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn>
 __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, int warp, int lane) {
@@ -486,6 +587,7 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
     constexpr int RPW = 32 / C::CBS;
     constexpr int RS = D / (C::NS * RPW);
     constexpr int CS = D / C::CBS;
+    constexpr int C2 = CS / 2;
     constexpr int HS = C::CBS / 2;
     constexpr int NOUT = rs_count<RS, HS>();
     static_assert(RS * C::NS * RPW == D && CS * C::CBS == D && CS % 4 == 0, "S layout");
@@ -494,13 +596,15 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
     const int cb = lane % C::CBS, rgl = lane / C::CBS;
     const int row0 = (ws * RPW + rgl) * RS, col0 = cb * CS;
 
-    float s[RS][CS];
+    float2 s[RS][C2];
     {
         const float* S0 = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
 #pragma unroll
         for (int r = 0; r < RS; ++r)
 #pragma unroll
-            for (int c = 0; c < CS; ++c) s[r][c] = S0 ? S0[(size_t)(row0 + r) * D + col0 + c] : 0.f;
+            for (int c = 0; c < C2; ++c)
+                s[r][c] = S0 ? f2(S0[(size_t)(row0 + r) * D + col0 + 2 * c], S0[(size_t)(row0 + r) * D + col0 + 2 * c + 1])
+                             : f2(0.f, 0.f);
     }
     float* o = p.o + (size_t)bh * p.T * D;
 
@@ -514,27 +618,39 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
         }
         const float* P = sm.prep + (size_t)(ps * C::CH + tc) * LY::PSTRIDE;
         // S_{t-1} k^ and S_{t-1} phi(q)
-        float sk[RS], sq[RS];
+        float2 sk2[RS], sq2[RS];
 #pragma unroll
-        for (int r = 0; r < RS; ++r) sk[r] = sq[r] = 0.f;
+        for (int r = 0; r < RS; ++r) sk2[r] = sq2[r] = f2(0.f, 0.f);
 #pragma unroll
         for (int c4 = 0; c4 < CS; c4 += 4) {
             const float4 k4 = ld4(P + LY::P_K + vidx<D>(col0 + c4));
             const float4 q4 = ld4(P + LY::P_Q + vidx<D>(col0 + c4));
-            const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-            const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+            const float2 ka = f2(k4.x, k4.y), kb = f2(k4.z, k4.w);
+            const float2 qa = f2(q4.x, q4.y), qb = f2(q4.z, q4.w);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int r = 0; r < RS; ++r) {
-                    sk[r] = fmaf(s[r][c4 + cc], kk[cc], sk[r]);
-                    sq[r] = fmaf(s[r][c4 + cc], qq[cc], sq[r]);
-                }
+            for (int r = 0; r < RS; ++r) {
+                sk2[r] = __ffma2_rn(s[r][c4 / 2], ka, sk2[r]);
+                sk2[r] = __ffma2_rn(s[r][c4 / 2 + 1], kb, sk2[r]);
+                sq2[r] = __ffma2_rn(s[r][c4 / 2], qa, sq2[r]);
+                sq2[r] = __ffma2_rn(s[r][c4 / 2 + 1], qb, sq2[r]);
+            }
         }
-        allreduce<RS, HS>(sk);
-        float e[RS];
+        float sk[RS], sq[RS];
 #pragma unroll
-        for (int r = 0; r < RS; ++r) e[r] = P[LY::P_V + row0 + r] - sk[r];
+        for (int r = 0; r < RS; ++r) {
+            sk[r] = sk2[r].x + sk2[r].y;
+            sq[r] = sq2[r].x + sq2[r].y;
+        }
+        // reduce both over the row group's lanes with one mapping: slot j of this
+        // lane holds row idx_j of S k^ and of S phi(q)
+        reduce_scatter<RS, HS>(sk, lane);
+        reduce_scatter<RS, HS>(sq, lane);
+        float ej[NOUT];
+#pragma unroll
+        for (int j = 0; j < NOUT; ++j) {
+            const int idx = rs_index<RS, HS>(cb, j);
+            ej[j] = idx >= 0 ? P[LY::P_V + row0 + idx] - sk[j] : 0.f;
+        }
 
         const int gs = t % C::RG;
         if (!mbar_wait(sm.full_g + gs, (t / C::RG) & 1, sm.abort, p.wait_ns)) {
@@ -542,30 +658,36 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
             break;
         }
         const float* G = sm.gr + (size_t)gs * LY::GSTRIDE;
-#pragma unroll
-        for (int c4 = 0; c4 < CS; c4 += 4) {
-            const float4 a4 = ld4(G + LY::G_A + vidx<D>(col0 + c4));
-            const float aa[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int r = 0; r < RS; ++r) s[r][c4 + cc] = fmaf(e[r], aa[cc], s[r][c4 + cc]);
-        }
         const float st = G[LY::G_S];
-        const float den = P[LY::P_DEN];
-        reduce_scatter<RS, HS>(sq, lane);
+        const float rden = __frcp_rn(P[LY::P_DEN]);
+        // o_t = (S_{t-1} phi(q) + e (alpha^ . phi(q))) / den = S_t phi(q) / den
 #pragma unroll
         for (int j = 0; j < NOUT; ++j) {
             const int idx = rs_index<RS, HS>(cb, j);
-            if (idx >= 0) {
-                float ei = e[0];
+            if (idx >= 0) o[(size_t)t * D + row0 + idx] = fmaf(ej[j], st, sq[j]) * rden;
+        }
+        // every lane of the row group needs the whole residual for the write
+        float2 e2[RS];
+        const int gbase = lane & ~(C::CBS - 1);
 #pragma unroll
-                for (int r = 1; r < RS; ++r) ei = (idx == r) ? e[r] : ei;
-                o[(size_t)t * D + row0 + idx] = (sq[j] + ei * st) / den;
+        for (int r = 0; r < RS; ++r) {
+            const float er = __shfl_sync(0xffffffffu, ej[rs_owner_slot<RS, HS>(r)], gbase | rs_owner_lane<RS, HS>(r));
+            e2[r] = f2(er, er);
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < CS; c4 += 4) {
+            const float4 a4 = ld4(G + LY::G_A + vidx<D>(col0 + c4));
+            const float2 aa = f2(a4.x, a4.y), ab = f2(a4.z, a4.w);
+#pragma unroll
+            for (int r = 0; r < RS; ++r) {
+                s[r][c4 / 2] = __ffma2_rn(e2[r], aa, s[r][c4 / 2]);
+                s[r][c4 / 2 + 1] = __ffma2_rn(e2[r], ab, s[r][c4 / 2 + 1]);
             }
         }
         __syncwarp();
         if (lane == 0) {
+            if (ws == 0) VLA_TRACE_AT(p, 3, t);
+            if (ws == C::NS - 1) VLA_TRACE_AT(p, 4, t);
             mbar_arrive(sm.empty_g + gs);
             if (tc == C::CH - 1 || t == p.T - 1) mbar_arrive(sm.empty_p + ps);
         }
@@ -579,9 +701,9 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
 #pragma unroll
     for (int r = 0; r < RS; ++r)
 #pragma unroll
-        for (int c4 = 0; c4 < CS; c4 += 4)
-            *reinterpret_cast<float4*>(So + (size_t)(row0 + r) * D + col0 + c4) =
-                make_float4(s[r][c4], s[r][c4 + 1], s[r][c4 + 2], s[r][c4 + 3]);
+        for (int c = 0; c < C2; c += 2)
+            *reinterpret_cast<float4*>(So + (size_t)(row0 + r) * D + col0 + 2 * c) =
+                make_float4(s[r][c].x, s[r][c].y, s[r][c + 1].x, s[r][c + 1].y);
 }
 
 template <int D, typename TIn>
@@ -610,7 +732,7 @@ __global__ void __launch_bounds__(Layout<D, TIn>::THREADS, Cfg<D>::MINB) vla_fus
         for (int i = 0; i < C::NRAW; ++i) mbar_init(sm.full_r + i, 1);
         for (int i = 0; i < C::NP; ++i) {
             mbar_init(sm.full_p + i, 1);
-            mbar_init(sm.empty_p + i, C::NA + C::NS + 1);
+            mbar_init(sm.empty_p + i, C::NS);  // the S warps are the last readers of a chunk
         }
         for (int i = 0; i < C::RZ; ++i) {
             mbar_init(sm.full_z + i, 1);
@@ -627,8 +749,8 @@ __global__ void __launch_bounds__(Layout<D, TIn>::THREADS, Cfg<D>::MINB) vla_fus
 
     if (warp == LY::W_PROD)
         stage_role<D, TIn>(p, sm, bh, lane);
-    else if (warp == LY::W_GATE)
-        gate_role<D, TIn>(p, sm, bh, lane);
+    else if (warp < LY::W_A0)
+        gate_role<D, TIn>(p, sm, bh, warp - LY::W_GATE, lane);
     else if (warp < LY::W_S0)
         a_role<D, TIn>(p, sm, bh, warp, lane);
     else
@@ -765,6 +887,7 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
     const unsigned wait_us = (opts && opts->wait_limit_us) ? opts->wait_limit_us : kDefaultWaitUs;
     p.wait_ns = 1000ull * wait_us;
     p.stall_producer = (opts && opts->test_stall_producer) ? 1 : 0;
+    p.trace = opts ? opts->trace : nullptr;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == VLA_BF16 ? launch_d<__nv_bfloat16>(d, p, (int)BH, s) : launch_d<float>(d, p, (int)BH, s);
