@@ -41,9 +41,10 @@ namespace vla {
 // Per-head-dimension configuration.
 //   NA/NS   A and S warps;  CBA/CBS  column blocks per row (lanes sharing a row)
 //   NG      gate warps (token t goes to gate warp t mod NG)
+//   NSTG    staging warps (chunk c goes to staging warp c mod NSTG)
 //   CH      tokens per staged chunk;  TB  tokens the staging warp prepares at once
 //   NP      prepped chunk slots;  NRAW  raw chunk slots
-//   RZ/RG   token slots of the A->gate and gate->S rings
+//   RZ      two-token step slots of the A->gate ring;  RG  token slots of gate->S
 //   PAD     pad shared vectors by 4 floats per 32 (bank spread for the
 //           column-block strides of these layouts)
 //   MINB    CTAs per SM the register budget is sized for
@@ -52,22 +53,22 @@ template <int D>
 struct Cfg;
 template <>
 struct Cfg<32> {
-    static constexpr int NA = 1, CBA = 4, NS = 1, CBS = 4, NG = 1, CH = 8, TB = 4, NP = 6, NRAW = 3, RZ = 16,
+    static constexpr int NA = 1, CBA = 4, NS = 1, CBS = 4, NG = 1, NSTG = 1, CH = 8, TB = 4, NP = 6, NRAW = 3, RZ = 8,
                          RG = 16, PAD = 1, MINB = 4;
 };
 template <>
 struct Cfg<64> {
-    static constexpr int NA = 4, CBA = 8, NS = 2, CBS = 4, NG = 1, CH = 8, TB = 4, NP = 4, NRAW = 3, RZ = 16,
+    static constexpr int NA = 4, CBA = 8, NS = 2, CBS = 4, NG = 1, NSTG = 1, CH = 8, TB = 4, NP = 4, NRAW = 3, RZ = 8,
                          RG = 16, PAD = 1, MINB = 2;
 };
 template <>
 struct Cfg<96> {
-    static constexpr int NA = 4, CBA = 8, NS = 4, CBS = 8, NG = 2, CH = 8, TB = 4, NP = 8, NRAW = 3, RZ = 16,
+    static constexpr int NA = 8, CBA = 8, NS = 4, CBS = 8, NG = 2, NSTG = 2, CH = 8, TB = 4, NP = 8, NRAW = 4, RZ = 8,
                          RG = 16, PAD = 0, MINB = 1;
 };
 template <>
 struct Cfg<128> {
-    static constexpr int NA = 8, CBA = 8, NS = 8, CBS = 4, NG = 1, CH = 8, TB = 2, NP = 6, NRAW = 2, RZ = 16,
+    static constexpr int NA = 8, CBA = 8, NS = 8, CBS = 4, NG = 1, NSTG = 1, CH = 8, TB = 2, NP = 6, NRAW = 2, RZ = 8,
                          RG = 16, PAD = 1, MINB = 1;
 };
 
@@ -82,20 +83,23 @@ struct Layout {
     // prepped token record: u^ | k^ | phi(q) (padded) | v | den, pad
     static constexpr int P_U = 0, P_K = VD, P_Q = 2 * VD, P_V = 3 * VD, P_DEN = 3 * VD + D;
     static constexpr int PSTRIDE = 3 * VD + D + 4;
-    // A -> gate record: z | w (padded) | per-warp partials of u^.z and k^.z
-    static constexpr int Z_Z = 0, Z_W = VD, Z_DD = 2 * VD, Z_DK = 2 * VD + NA4;
-    static constexpr int ZSTRIDE = 2 * VD + 2 * NA4;
+    // A -> gate record of one step (two tokens): z'_0 | z'_1 | w'_0 | w'_1
+    // (padded) | per-warp partials of g00 g01 g11 h00 h01 h11 ([6][NA4])
+    static constexpr int Z_Z0 = 0, Z_Z1 = VD, Z_W0 = 2 * VD, Z_W1 = 3 * VD, Z_SC = 4 * VD;
+    static constexpr int ZSTRIDE = 4 * VD + 6 * NA4;
     // gate -> S record: alpha^ (padded) | s = alpha^ . phi(q), pad
     static constexpr int G_A = 0, G_S = VD;
     static constexpr int GSTRIDE = VD + 4;
     // warp roles
-    static constexpr int W_PROD = 0, W_GATE = 1, W_A0 = 1 + C::NG, W_S0 = 1 + C::NG + C::NA;
-    static constexpr int NWARPS = 1 + C::NG + C::NA + C::NS, THREADS = 32 * NWARPS;
+    static constexpr int NSTG = C::NSTG;
+    static constexpr int W_PROD = 0, W_GATE = NSTG, W_A0 = NSTG + C::NG, W_S0 = NSTG + C::NG + C::NA;
+    static constexpr int NWARPS = NSTG + C::NG + C::NA + C::NS, THREADS = 32 * NWARPS;
     // shared memory map (bytes)
-    static constexpr int NBAR = C::NRAW + 2 * C::NP + 2 * C::RZ + 2 * C::RG;
+    static constexpr int NBAR = C::NRAW + 2 * C::NP + 2 * C::RZ + 2 * C::RG + 2;
     static constexpr size_t OFF_FLAG = 8 * (size_t)NBAR;
+    static constexpr size_t OFF_ZK = align_up(OFF_FLAG + 16, 16);  // z^key hand-off ring [2][D]
     static constexpr size_t RAW_TENSOR = (size_t)C::CH * D * sizeof(TIn);
-    static constexpr size_t OFF_RAW = align_up(OFF_FLAG + 16, 128);
+    static constexpr size_t OFF_RAW = align_up(OFF_ZK + 2 * D * 4, 128);
     static constexpr size_t OFF_PREP = align_up(OFF_RAW + (size_t)C::NRAW * 4 * RAW_TENSOR, 128);
     static constexpr size_t OFF_Z = align_up(OFF_PREP + (size_t)C::NP * C::CH * PSTRIDE * 4, 128);
     static constexpr size_t OFF_G = align_up(OFF_Z + (size_t)C::RZ * ZSTRIDE * 4, 128);
@@ -153,10 +157,12 @@ struct Smem {
     uint64_t* full_r;   // raw chunk landed (TMA tx)
     uint64_t* full_p;   // prepped chunk published
     uint64_t* empty_p;  // prepped chunk released by the S warps (its last readers)
-    uint64_t* full_z;   // z/w of a token published by the A warps
-    uint64_t* empty_z;  // ... released by the gate
+    uint64_t* full_z;   // a two-token A step published by the A warps
+    uint64_t* empty_z;  // ... released by the gate warps
     uint64_t* full_g;   // alpha^ of a token published by the gate
     uint64_t* empty_g;  // ... released by the S warps
+    uint64_t* zk_full;  // z^key at the end of a chunk handed to the next chunk's staging warp
+    float* zkr;
     volatile int* abort;
     unsigned char* raw;
     float* prep;
@@ -210,18 +216,21 @@ __device__ __forceinline__ float sum_partials(const float* p) {
 }
 
 // ---------------------------------------------------------------------------
-// staging warp: TMA bulk copies of raw q, k, v, u chunks, then per token
-// u^, k^ (unit), phi(q), v (fp32), z^key += phi(k), den = max(phi(q).z^key, eps)
-// (§3.2-3.3, eq. 11). Tokens are processed TB at a time so that the
-// cross-lane reductions of several tokens overlap.
+// staging warps: TMA bulk copies of raw q, k, v, u chunks, then per token
+// u^, k^ (unit), phi(q), v (fp32) and den = max(phi(q) . z^key, eps) with
+// z^key += phi(k) (§3.2-3.3, eq. 11). Staging warp s handles chunks c = s mod NSTG.
+// Everything but the key sum is independent per token; the running z^key
+// is handed from chunk to chunk through a shared ring guarded by mbarriers.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn>
-__device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int bh, int lane) {
+__device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int bh, int sw, int lane) {
     using C = Cfg<D>;
     using LY = Layout<D, TIn>;
     constexpr int E = D / 32;
     constexpr int TB = C::TB;
-    static_assert(C::CH % TB == 0, "token batch divides the chunk");
+    constexpr int NSTG = LY::NSTG;
+    constexpr int RPW = C::NRAW / NSTG;  // raw slots per staging warp
+    static_assert(C::CH % TB == 0 && C::NRAW % NSTG == 0, "staging layout");
     const int T = p.T;
     const int nch = (T + C::CH - 1) / C::CH;
     const size_t head = (size_t)bh * T * D;
@@ -232,11 +241,7 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
     // runs into its own wait limit
     if (p.stall_producer) return;
 
-    float zk[E];
-#pragma unroll
-    for (int m = 0; m < E; ++m) zk[m] = p.zk0 ? p.zk0[(size_t)bh * D + lane + 32 * m] : 0.f;
-
-    auto issue = [&](int c) {  // lane 0 only
+    auto issue = [&](int c) {  // lane 0 only; chunk c goes to raw slot c % NRAW
         const int rs = c % C::NRAW;
         const int nt = min(C::CH, T - c * C::CH);
         const uint32_t bytes = (uint32_t)(nt * D * sizeof(TIn));
@@ -248,34 +253,41 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
     };
 
     bool abort = false;
-    int issued = min(C::NRAW, nch), landed = 0, c = 0;
+    // this warp's chunks are sw, sw + NSTG, ...; keep RPW of them in flight
+    int issued = sw, landed = sw, c = sw;
     if (lane == 0)
-        for (int i = 0; i < issued; ++i) issue(i);
-    for (; c < nch; ++c) {
-        const int rs = c % C::NRAW, ps = c % C::NP;
-        if (!mbar_wait(sm.full_r + rs, (c / C::NRAW) & 1, sm.abort, p.wait_ns)) {
+        for (int i = 0; i < RPW && sw + i * NSTG < nch; ++i) issue(sw + i * NSTG);
+    for (int i = 0; i < RPW && sw + i * NSTG < nch; ++i) issued = sw + (i + 1) * NSTG;
+    float zk[E];
+    for (; c < nch; c += NSTG) {
+        const int rs = c % C::NRAW, ps = c % C::NP, use = c / C::NRAW;
+        if (!mbar_wait(sm.full_r + rs, use & 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
-        landed = c + 1;
-        if (lane == 0) VLA_TRACE_PT(p, 14, c * C::CH);
+        landed = c + NSTG;
+        if (lane == 0 && sw == 0) VLA_TRACE_PT(p, 14, c * C::CH);
         if (!mbar_wait(sm.empty_p + ps, ((c / C::NP) & 1) ^ 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
-        if (lane == 0) VLA_TRACE_PT(p, 15, c * C::CH);
+        if (lane == 0 && sw == 0) VLA_TRACE_PT(p, 15, c * C::CH);
         const int nt = min(C::CH, T - c * C::CH);
         const TIn* raw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) raw[i] = reinterpret_cast<const TIn*>(sm.raw + (size_t)(rs * 4 + i) * LY::RAW_TENSOR);
+        for (int i = 0; i < 4; ++i)
+            raw[i] = reinterpret_cast<const TIn*>(sm.raw + (size_t)(rs * 4 + i) * LY::RAW_TENSOR);
         float* P0 = sm.prep + (size_t)ps * C::CH * LY::PSTRIDE;
-        for (int tb = 0; tb < nt; tb += TB) {
+        float pk[C::CH][E], pq[C::CH][E];  // phi(k), phi(q) of the chunk's tokens
+#pragma unroll
+        for (int tb = 0; tb < C::CH; tb += TB) {
+            if (tb >= nt) break;
             float qv[TB][E], kv[TB][E], vv[TB][E], uv[TB][E];
-            float red[3 * TB];  // per token: ||u||^2, ||k||^2, phi(q) . z^key
+            float red[2 * TB];  // per token ||u||^2, ||k||^2
 #pragma unroll
             for (int b = 0; b < TB; ++b) {
                 const bool live = tb + b < nt;
-                float uu = 0.f, kk = 0.f, qz = 0.f;
+                float uu = 0.f, kk = 0.f;
 #pragma unroll
                 for (int m = 0; m < E; ++m) {
                     const int j = (tb + b) * D + lane + 32 * m;
@@ -285,60 +297,112 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
                     uv[b][m] = live ? ld_in<TIn>(raw[3], j) : 0.f;
                     uu = fmaf(uv[b][m], uv[b][m], uu);
                     kk = fmaf(kv[b][m], kv[b][m], kk);
-                    if (live) zk[m] += phi(kv[b][m]);
-                    qv[b][m] = phi(qv[b][m]);
-                    qz = fmaf(qv[b][m], zk[m], qz);
+                    pk[tb + b][m] = live ? phi(kv[b][m]) : 0.f;
+                    pq[tb + b][m] = phi(qv[b][m]);
                 }
-                red[3 * b] = uu;
-                red[3 * b + 1] = kk;
-                red[3 * b + 2] = qz;
+                red[2 * b] = uu;
+                red[2 * b + 1] = kk;
             }
-            allreduce<3 * TB, 16>(red);
+            // reduce-scatter the 2*TB squared norms, invert on the owner lane, gather back
+            reduce_scatter<2 * TB, 16>(red, lane);
+            float inv[rs_count<2 * TB, 16>()];
+#pragma unroll
+            for (int j = 0; j < rs_count<2 * TB, 16>(); ++j) inv[j] = rsqrtf(fmaxf(red[j], 1e-24f));
 #pragma unroll
             for (int b = 0; b < TB; ++b) {
+                constexpr int dummy = 0;
+                (void)dummy;
+                const float iu = __shfl_sync(0xffffffffu, inv[rs_owner_slot<2 * TB, 16>(2 * b)],
+                                             rs_owner_lane<2 * TB, 16>(2 * b));
+                const float ik = __shfl_sync(0xffffffffu, inv[rs_owner_slot<2 * TB, 16>(2 * b + 1)],
+                                             rs_owner_lane<2 * TB, 16>(2 * b + 1));
                 if (tb + b < nt) {
-                    const float iu = rsqrtf(fmaxf(red[3 * b], 1e-24f));  // 1 / max(||u||, 1e-12)
-                    const float ik = rsqrtf(fmaxf(red[3 * b + 1], 1e-24f));
                     float* P = P0 + (tb + b) * LY::PSTRIDE;
 #pragma unroll
                     for (int m = 0; m < E; ++m) {
                         const int j = lane + 32 * m;
                         P[LY::P_U + vidx<D>(j)] = uv[b][m] * iu;
                         P[LY::P_K + vidx<D>(j)] = kv[b][m] * ik;
-                        P[LY::P_Q + vidx<D>(j)] = qv[b][m];
+                        P[LY::P_Q + vidx<D>(j)] = pq[tb + b][m];
                         P[LY::P_V + j] = vv[b][m];
                     }
-                    if (lane == 0) P[LY::P_DEN] = fmaxf(red[3 * b + 2], p.eps);
                 }
             }
+        }
+        // the running key sum: z^key at the start of this chunk
+        if (c == 0) {
+#pragma unroll
+            for (int m = 0; m < E; ++m) zk[m] = p.zk0 ? p.zk0[(size_t)bh * D + lane + 32 * m] : 0.f;
+        } else {
+            const int cp = c - 1;
+            if (!mbar_wait(sm.zk_full + (cp % 2), (cp / 2) & 1, sm.abort, p.wait_ns)) {
+                abort = true;
+                break;
+            }
+#pragma unroll
+            for (int m = 0; m < E; ++m) zk[m] = sm.zkr[(cp % 2) * D + lane + 32 * m];
+        }
+        float qz[C::CH];
+#pragma unroll
+        for (int t = 0; t < C::CH; ++t) {
+            float s = 0.f;
+            if (t < nt) {  // tokens past the end of a partial chunk were never loaded
+#pragma unroll
+                for (int m = 0; m < E; ++m) {
+                    zk[m] += pk[t][m];
+                    s = fmaf(pq[t][m], zk[m], s);
+                }
+            }
+            qz[t] = s;
+        }
+        // hand z^key at the end of this chunk to the next one
+#pragma unroll
+        for (int m = 0; m < E; ++m) sm.zkr[(c % 2) * D + lane + 32 * m] = zk[m];
+        reduce_scatter<C::CH, 16>(qz, lane);
+#pragma unroll
+        for (int j = 0; j < rs_count<C::CH, 16>(); ++j) {
+            const int t = rs_index<C::CH, 16>(lane, j);
+            if (t >= 0 && t < nt) P0[t * LY::PSTRIDE + LY::P_DEN] = fmaxf(qz[j], p.eps);
         }
         // our generic-proxy reads of raw slot rs are done before the TMA refill
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
+            mbar_arrive(sm.zk_full + (c % 2));
             mbar_arrive(sm.full_p + ps);
-            VLA_TRACE_AT(p, 0, c * C::CH);
+            if (sw == 0) VLA_TRACE_AT(p, 0, c * C::CH);
             if (c + C::NRAW < nch) issue(c + C::NRAW);
         }
-        issued = min(c + 1 + C::NRAW, nch);
+        if (c + C::NRAW < nch) issued = c + C::NRAW + NSTG;
+        if (c + NSTG >= nch && p.zk_out) {
+#pragma unroll
+            for (int m = 0; m < E; ++m) p.zk_out[(size_t)bh * D + lane + 32 * m] = zk[m];
+        }
     }
     if (abort) {
         if (lane == 0) record_failure(p.status, BIT_TIMEOUT, ROLE_STAGE, bh, c * C::CH);
         *sm.abort = 1;
         // let copies already in flight land before the CTA can exit
-        for (int cc = landed; cc < issued; ++cc)
+        for (int cc = landed; cc < issued; cc += NSTG)
             (void)mbar_wait(sm.full_r + cc % C::NRAW, (cc / C::NRAW) & 1, nullptr, p.wait_ns);
         return;
     }
-    if (p.zk_out) {
+    if (T == 0 && sw == 0 && p.zk_out) {
 #pragma unroll
-        for (int m = 0; m < E; ++m) p.zk_out[(size_t)bh * D + lane + 32 * m] = zk[m];
+        for (int m = 0; m < E; ++m) p.zk_out[(size_t)bh * D + lane + 32 * m] = p.zk0 ? p.zk0[(size_t)bh * D + lane + 32 * m] : 0.f;
     }
 }
 
 // ---------------------------------------------------------------------------
-// gate warps: alpha^_t = A_t k^ / ||A_t k^|| (eq. 10) from the published z, w,
-// with A_t k^ = w - z (z . k^) / delta. Gate warp g handles tokens t = g mod NG.
+// gate warps: alpha^_t = A_t k^_t / ||A_t k^_t|| (eq. 10) for the tokens of a
+// published A block (two tokens t0 = 2b, t1 = 2b + 1). With z'_s = A u^_s and
+// w'_s = A k^_s for the block's starting A, delta0 = 1 + g00, rho = g01/delta0,
+// delta1 = 1 + g11 - g01 rho and kappa = (h11 - rho h01)/delta1:
+//   A_t0 k^_t0 = w'_0 - z'_0 h00/delta0
+//   A_t1 k^_t1 = w'_1 - z'_0 (h01/delta0 - rho kappa) - z'_1 kappa
+// (g_st = u^_s . z'_t, h_st = k^_t . z'_s: the sequential Sherman-Morrison
+// steps of eq. 9 written in the basis of the block's matrix-vector products).
+// Gate warp g handles the tokens at block position g (or both when NG == 1).
 // ---------------------------------------------------------------------------
 template <int D, typename TIn>
 __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int bh, int g, int lane) {
@@ -348,8 +412,9 @@ __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int b
     bool abort = false, nonfinite = false;
     int t = g;
     for (; t < p.T; t += C::NG) {
-        const int zs = t % C::RZ;
-        if (!mbar_wait(sm.full_z + zs, (t / C::RZ) & 1, sm.abort, p.wait_ns)) {
+        const int b = t >> 1, pos = t & 1;
+        const int zs = b % C::RZ;
+        if ((pos == 0 || C::NG == 2) && !mbar_wait(sm.full_z + zs, (b / C::RZ) & 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
@@ -361,22 +426,44 @@ __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int b
         const float* Z = sm.zr + (size_t)zs * LY::ZSTRIDE;
         const float* P = sm.prep + (size_t)(ps * C::CH + tc) * LY::PSTRIDE;
         if (lane == 0 && g == 0) VLA_TRACE_PT(p, 11, t);
-        const float delta = 1.f + sum_partials<C::NA>(Z + LY::Z_DD);
-        const float zkd = sum_partials<C::NA>(Z + LY::Z_DK);
-        const float cf = zkd * __frcp_rn(delta);
+        const float g00 = sum_partials<C::NA>(Z + LY::Z_SC + 0 * LY::NA4);
+        const float g01 = sum_partials<C::NA>(Z + LY::Z_SC + 1 * LY::NA4);
+        const float d0 = 1.f + g00;
+        const float rd0 = __frcp_rn(d0);
+        float c0, c1;
+        const float* W;
+        if (pos == 0) {
+            c0 = sum_partials<C::NA>(Z + LY::Z_SC + 3 * LY::NA4) * rd0;  // h00 / delta0
+            c1 = 0.f;
+            W = Z + LY::Z_W0;
+            if (!isfinite(d0)) nonfinite = true;
+        } else {
+            const float g11 = sum_partials<C::NA>(Z + LY::Z_SC + 2 * LY::NA4);
+            const float h01 = sum_partials<C::NA>(Z + LY::Z_SC + 4 * LY::NA4);
+            const float h11 = sum_partials<C::NA>(Z + LY::Z_SC + 5 * LY::NA4);
+            const float rho = g01 * rd0;
+            const float d1 = 1.f + fmaf(-g01, rho, g11);
+            const float kap = fmaf(-rho, h01, h11) * __frcp_rn(d1);
+            c0 = fmaf(-rho, kap, h01 * rd0);
+            c1 = kap;
+            W = Z + LY::Z_W1;
+            if (!isfinite(d1)) nonfinite = true;
+        }
         float av[E];
         float red[2] = {0.f, 0.f};  // ||a||^2, a . phi(q)
 #pragma unroll
         for (int m = 0; m < E; ++m) {
             const int j = vidx<D>(lane + 32 * m);
-            av[m] = fmaf(-cf, Z[LY::Z_Z + j], Z[LY::Z_W + j]);
-            red[0] = fmaf(av[m], av[m], red[0]);
-            red[1] = fmaf(av[m], P[LY::P_Q + j], red[1]);
+            float x = fmaf(-c0, Z[LY::Z_Z0 + j], W[j]);
+            if (pos == 1) x = fmaf(-c1, Z[LY::Z_Z1 + j], x);
+            av[m] = x;
+            red[0] = fmaf(x, x, red[0]);
+            red[1] = fmaf(x, P[LY::P_Q + j], red[1]);
         }
         allreduce<2, 16>(red);
         if (lane == 0 && g == 0) VLA_TRACE_PT(p, 12, t);
         const float inv = rsqrtf(fmaxf(red[0], 1e-24f));  // 1 / max(||a||, 1e-12)
-        if (!(isfinite(delta) && isfinite(red[0]) && isfinite(red[1]))) nonfinite = true;
+        if (!(isfinite(red[0]) && isfinite(red[1]))) nonfinite = true;
         const int gs = t % C::RG;
         if (!mbar_wait(sm.empty_g + gs, ((t / C::RG) & 1) ^ 1, sm.abort, p.wait_ns)) {
             abort = true;
@@ -391,7 +478,8 @@ __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int b
         if (lane == 0) {
             mbar_arrive(sm.full_g + gs);
             VLA_TRACE_AT(p, 2, t);
-            mbar_arrive(sm.empty_z + zs);
+            // release the A block once this warp is done with its last token in it
+            if (C::NG == 2 || pos == 1 || t + 1 >= p.T) mbar_arrive(sm.empty_z + zs);
         }
     }
     if (abort) {
@@ -402,10 +490,14 @@ __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int b
 }
 
 // ---------------------------------------------------------------------------
-// A warps: Sherman-Morrison chain (eq. 9), A resident in registers as float2
-// pairs (packed fp32 FMA). Per token one pass over A applies the pending
-// update of the previous token, A -= (z/delta) z^T, and accumulates
-// z = A u^ and w = A k^.
+// A warps: the Sherman-Morrison chain (eq. 9) two tokens per step. A is
+// resident in registers as float2 pairs. One pass over A per step applies the
+// previous step's rank-2 update A -= [z'_0 z'_1] Q [z'_0 z'_1]^T and forms
+// z'_s = A u^_s, w'_s = A k^_s for both tokens, plus this thread's parts of the
+// six scalars g_st, h_st; one named barrier per step publishes them. With
+// delta0, rho, delta1 as in the gate,
+//   Q = [[1/delta0 + rho^2/delta1, -rho/delta1], [-rho/delta1, 1/delta1]]
+// reproduces the two sequential updates A -= z z^T / delta of eq. 9.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn>
 __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, int warp, int lane) {
@@ -415,10 +507,11 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
     constexpr int RA = D / (C::NA * RPW);         // rows per thread
     constexpr int CA = D / C::CBA;                // columns per thread
     constexpr int C2 = CA / 2;                    // float2 columns
-    constexpr int NV = 2 * RA + 2;                // z rows, w rows, u^.z and k^.z partials
+    constexpr int NV = 4 * RA + 6;                // z'0, z'1, w'0, w'1 rows; g00 g01 g11 h00 h01 h11
     constexpr int HR = C::CBA / 2;
     constexpr int NOUT = rs_count<NV, HR>();
     static_assert(RA * C::NA * RPW == D && CA * C::CBA == D && CA % 4 == 0, "A layout");
+    static_assert(C::CH % 2 == 0, "steps of two tokens stay inside a chunk");
 
     const int wa = warp - LY::W_A0;
     const int cb = lane % C::CBA, rgl = lane / C::CBA;
@@ -436,71 +529,83 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
                              : f2(i == j ? p.inv_lambda0 : 0.f, i == j + 1 ? p.inv_lambda0 : 0.f);
             }
     }
-    // pending rank-1 update of the previous token: A -= (z/delta) z^T
-    float2 nyr[RA], zj[C2];
+    // pending rank-2 update of the previous step: A += nm0 z'_0^T + nm1 z'_1^T,
+    // with z'_s at this thread's columns read from the previous step's slot
+    float2 nm0[RA], nm1[RA];
 #pragma unroll
-    for (int r = 0; r < RA; ++r) nyr[r] = f2(0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < C2; ++c) zj[c] = f2(0.f, 0.f);
-
-    // this token's u^, k^ (columns, and rows for the scalar partials)
-    float2 uj[C2], kj[C2];
-    float ui[RA], ki[RA];
-    auto load_token = [&](const float* P) {
-#pragma unroll
-        for (int c4 = 0; c4 < CA; c4 += 4) {
-            const float4 u4 = ld4(P + LY::P_U + vidx<D>(col0 + c4));
-            const float4 k4 = ld4(P + LY::P_K + vidx<D>(col0 + c4));
-            uj[c4 / 2] = f2(u4.x, u4.y);
-            uj[c4 / 2 + 1] = f2(u4.z, u4.w);
-            kj[c4 / 2] = f2(k4.x, k4.y);
-            kj[c4 / 2 + 1] = f2(k4.z, k4.w);
-        }
-#pragma unroll
-        for (int r = 0; r < RA; ++r) {
-            ui[r] = P[LY::P_U + vidx<D>(row0 + r)];
-            ki[r] = P[LY::P_K + vidx<D>(row0 + r)];
-        }
-    };
+    for (int r = 0; r < RA; ++r) nm0[r] = nm1[r] = f2(0.f, 0.f);
+    const float* Zprev = nullptr;
 
     bool abort = false;
     int t = 0;
-    if (p.T > 0) {
-        if (!mbar_wait(sm.full_p, 0, sm.abort, p.wait_ns)) abort = true;
-        load_token(sm.prep);
-    }
-    for (; t < p.T; ++t) {
+    if (p.T > 0 && !mbar_wait(sm.full_p, 0, sm.abort, p.wait_ns)) abort = true;
+    for (int b = 0; t < p.T; ++b, t += 2) {
         const bool tr0 = (wa == 0 && lane == 0);
         if (tr0) VLA_TRACE_PT(p, 5, t);
+        const int chunk = t / C::CH, tc = t - chunk * C::CH, ps = chunk % C::NP;
+        const bool two = t + 1 < p.T;
+        const float* P0 = sm.prep + (size_t)(ps * C::CH + tc) * LY::PSTRIDE;
+        const float* P1 = P0 + LY::PSTRIDE;
 
-        // one pass over A: apply the pending update, then z = A u^, w = A k^
-        float2 pz[RA], pw[RA];
+        float2 pz0[RA], pz1[RA], pw0[RA], pw1[RA];
 #pragma unroll
-        for (int r = 0; r < RA; ++r) pz[r] = pw[r] = f2(0.f, 0.f);
+        for (int r = 0; r < RA; ++r) pz0[r] = pz1[r] = pw0[r] = pw1[r] = f2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < C2; ++c)
+        for (int c4 = 0; c4 < CA; c4 += 4) {
+            const int jv = vidx<D>(col0 + c4);
+            const float4 u04 = ld4(P0 + LY::P_U + jv), k04 = ld4(P0 + LY::P_K + jv);
+            const float4 u14 = two ? ld4(P1 + LY::P_U + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 k14 = two ? ld4(P1 + LY::P_K + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 z04 = Zprev ? ld4(Zprev + LY::Z_Z0 + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 z14 = Zprev ? ld4(Zprev + LY::Z_Z1 + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float2 u0[2] = {f2(u04.x, u04.y), f2(u04.z, u04.w)};
+            const float2 u1[2] = {f2(u14.x, u14.y), f2(u14.z, u14.w)};
+            const float2 k0[2] = {f2(k04.x, k04.y), f2(k04.z, k04.w)};
+            const float2 k1[2] = {f2(k14.x, k14.y), f2(k14.z, k14.w)};
+            const float2 z0[2] = {f2(z04.x, z04.y), f2(z04.z, z04.w)};
+            const float2 z1[2] = {f2(z14.x, z14.y), f2(z14.z, z14.w)};
 #pragma unroll
-            for (int r = 0; r < RA; ++r) {
-                const float2 x = __ffma2_rn(nyr[r], zj[c], a[r][c]);
-                a[r][c] = x;
-                pz[r] = __ffma2_rn(x, uj[c], pz[r]);
-                pw[r] = __ffma2_rn(x, kj[c], pw[r]);
-            }
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int r = 0; r < RA; ++r) {
+                    const int c = c4 / 2 + h;
+                    float2 x = __ffma2_rn(nm0[r], z0[h], a[r][c]);
+                    x = __ffma2_rn(nm1[r], z1[h], x);
+                    a[r][c] = x;
+                    pz0[r] = __ffma2_rn(x, u0[h], pz0[r]);
+                    pz1[r] = __ffma2_rn(x, u1[h], pz1[r]);
+                    pw0[r] = __ffma2_rn(x, k0[h], pw0[r]);
+                    pw1[r] = __ffma2_rn(x, k1[h], pw1[r]);
+                }
+        }
         float vals[NV];
-        float dd = 0.f, dk = 0.f;
+        float sg00 = 0.f, sg01 = 0.f, sg11 = 0.f, sh00 = 0.f, sh01 = 0.f, sh11 = 0.f;
 #pragma unroll
         for (int r = 0; r < RA; ++r) {
-            const float z = pz[r].x + pz[r].y;
-            vals[r] = z;
-            vals[RA + r] = pw[r].x + pw[r].y;
-            dd = fmaf(ui[r], z, dd);
-            dk = fmaf(ki[r], z, dk);
+            const int iv = vidx<D>(row0 + r);
+            const float ur0 = P0[LY::P_U + iv], kr0 = P0[LY::P_K + iv];
+            const float ur1 = two ? P1[LY::P_U + iv] : 0.f, kr1 = two ? P1[LY::P_K + iv] : 0.f;
+            const float z0 = pz0[r].x + pz0[r].y, z1 = pz1[r].x + pz1[r].y;
+            vals[r] = z0;
+            vals[RA + r] = z1;
+            vals[2 * RA + r] = pw0[r].x + pw0[r].y;
+            vals[3 * RA + r] = pw1[r].x + pw1[r].y;
+            sg00 = fmaf(ur0, z0, sg00);
+            sg01 = fmaf(ur1, z0, sg01);
+            sg11 = fmaf(ur1, z1, sg11);
+            sh00 = fmaf(kr0, z0, sh00);
+            sh01 = fmaf(kr1, z0, sh01);
+            sh11 = fmaf(kr1, z1, sh11);
         }
-        vals[2 * RA] = dd;
-        vals[2 * RA + 1] = dk;
+        vals[4 * RA + 0] = sg00;
+        vals[4 * RA + 1] = sg01;
+        vals[4 * RA + 2] = sg11;
+        vals[4 * RA + 3] = sh00;
+        vals[4 * RA + 4] = sh01;
+        vals[4 * RA + 5] = sh11;
         if (tr0) VLA_TRACE_PT(p, 6, t);
         reduce_scatter<NV, HR>(vals, lane);
-        // the two scalar partials also need the sum over this warp's row groups
+        // the scalar partials also need the sum over this warp's row groups
         float sc[NOUT];
 #pragma unroll
         for (int j = 0; j < NOUT; ++j) sc[j] = vals[j];
@@ -509,31 +614,28 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
 #pragma unroll
             for (int j = 0; j < NOUT; ++j) sc[j] += __shfl_xor_sync(0xffffffffu, sc[j], h);
 
-        const int zs = t % C::RZ;
+        const int zs = b % C::RZ;
         if (tr0) VLA_TRACE_PT(p, 7, t);
-        if (!abort && !mbar_wait(sm.empty_z + zs, ((t / C::RZ) & 1) ^ 1, sm.abort, p.wait_ns)) abort = true;
+        if (!abort && !mbar_wait(sm.empty_z + zs, ((b / C::RZ) & 1) ^ 1, sm.abort, p.wait_ns)) abort = true;
         if (tr0) VLA_TRACE_PT(p, 8, t);
         float* Z = sm.zr + (size_t)zs * LY::ZSTRIDE;
 #pragma unroll
         for (int j = 0; j < NOUT; ++j) {
             const int idx = rs_index<NV, HR>(cb, j);
-            if (idx < 0)
-                continue;
-            else if (idx < RA)
-                Z[LY::Z_Z + vidx<D>(row0 + idx)] = vals[j];
-            else if (idx < 2 * RA)
-                Z[LY::Z_W + vidx<D>(row0 + idx - RA)] = vals[j];
-            else if (rgl == 0 && idx == 2 * RA)
-                Z[LY::Z_DD + wa] = sc[j];
-            else if (rgl == 0 && idx == 2 * RA + 1)
-                Z[LY::Z_DK + wa] = sc[j];
+            if (idx < 0) continue;
+            if (idx < 4 * RA) {
+                const int vec = idx / RA, r = idx - vec * RA;
+                Z[vec * LY::VD + vidx<D>(row0 + r)] = vals[j];
+            } else if (rgl == 0) {
+                Z[LY::Z_SC + (idx - 4 * RA) * LY::NA4 + wa] = sc[j];
+            }
         }
-        // prefetch the next token's vectors while the other A warps catch up
-        if (t + 1 < p.T) {
-            const int t1 = t + 1, chunk1 = t1 / C::CH, tc1 = t1 - chunk1 * C::CH, ps1 = chunk1 % C::NP;
-            if (tc1 == 0 && !abort && !mbar_wait(sm.full_p + ps1, (chunk1 / C::NP) & 1, sm.abort, p.wait_ns))
+        // the next step's first token may start a new chunk
+        if (t + 2 < p.T) {
+            const int t2 = t + 2, chunk2 = t2 / C::CH;
+            if (t2 - chunk2 * C::CH == 0 && !abort &&
+                !mbar_wait(sm.full_p + chunk2 % C::NP, (chunk2 / C::NP) & 1, sm.abort, p.wait_ns))
                 abort = true;
-            load_token(sm.prep + (size_t)(ps1 * C::CH + tc1) * LY::PSTRIDE);
         }
         // publish among the A warps; every A thread takes the same abort decision
         if (bar_red_or(1, C::NA * 32, abort || (*sm.abort != 0))) {
@@ -544,20 +646,29 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
         if (wa == 0 && lane == 0) {
             mbar_arrive(sm.full_z + zs);
             VLA_TRACE_AT(p, 1, t);
+            if (two) VLA_TRACE_AT(p, 1, t + 1);
         }
-        const float delta = 1.f + sum_partials<C::NA>(Z + LY::Z_DD);
-        const float inv = __frcp_rn(delta);
+        // g00, g01, g11: lane (s * NA + w) reads warp w's part of scalar s; sum, broadcast
+        float gv = 0.f;
+        if (lane < 3 * C::NA) gv = Z[LY::Z_SC + (lane / C::NA) * LY::NA4 + (lane % C::NA)];
+#pragma unroll
+        for (int h = 1; h < C::NA; h <<= 1) gv += __shfl_xor_sync(0xffffffffu, gv, h);
+        const float g00 = __shfl_sync(0xffffffffu, gv, 0);
+        const float g01 = __shfl_sync(0xffffffffu, gv, C::NA);
+        const float g11 = __shfl_sync(0xffffffffu, gv, 2 * C::NA);
+        const float rd0 = __frcp_rn(1.f + g00);
+        const float rho = g01 * rd0;
+        const float rd1 = __frcp_rn(1.f + fmaf(-g01, rho, g11));
+        const float q11 = rd1, q01 = -rho * rd1, q00 = fmaf(rho * rho, rd1, rd0);
 #pragma unroll
         for (int r = 0; r < RA; ++r) {
-            const float y = -Z[LY::Z_Z + vidx<D>(row0 + r)] * inv;
-            nyr[r] = f2(y, y);
+            const int iv = vidx<D>(row0 + r);
+            const float z0 = Z[LY::Z_Z0 + iv], z1 = Z[LY::Z_Z1 + iv];
+            const float m0 = -fmaf(q00, z0, q01 * z1), m1 = -fmaf(q01, z0, q11 * z1);
+            nm0[r] = f2(m0, m0);
+            nm1[r] = f2(m1, m1);
         }
-#pragma unroll
-        for (int c4 = 0; c4 < CA; c4 += 4) {
-            const float4 z4 = ld4(Z + LY::Z_Z + vidx<D>(col0 + c4));
-            zj[c4 / 2] = f2(z4.x, z4.y);
-            zj[c4 / 2 + 1] = f2(z4.z, z4.w);
-        }
+        Zprev = Z;
         if (tr0) VLA_TRACE_PT(p, 10, t);
     }
     if (abort) {
@@ -569,10 +680,15 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
 #pragma unroll
     for (int r = 0; r < RA; ++r)
 #pragma unroll
-        for (int c = 0; c < C2; c += 2) {
-            const float2 x0 = __ffma2_rn(nyr[r], zj[c], a[r][c]);
-            const float2 x1 = __ffma2_rn(nyr[r], zj[c + 1], a[r][c + 1]);
-            *reinterpret_cast<float4*>(Ao + (size_t)(row0 + r) * D + col0 + 2 * c) = make_float4(x0.x, x0.y, x1.x, x1.y);
+        for (int c4 = 0; c4 < CA; c4 += 4) {
+            const int jv = vidx<D>(col0 + c4);
+            const float4 z04 = Zprev ? ld4(Zprev + LY::Z_Z0 + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 z14 = Zprev ? ld4(Zprev + LY::Z_Z1 + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float2 x0 = __ffma2_rn(nm0[r], f2(z04.x, z04.y), a[r][c4 / 2]);
+            x0 = __ffma2_rn(nm1[r], f2(z14.x, z14.y), x0);
+            float2 x1 = __ffma2_rn(nm0[r], f2(z04.z, z04.w), a[r][c4 / 2 + 1]);
+            x1 = __ffma2_rn(nm1[r], f2(z14.z, z14.w), x1);
+            *reinterpret_cast<float4*>(Ao + (size_t)(row0 + r) * D + col0 + c4) = make_float4(x0.x, x0.y, x1.x, x1.y);
         }
 }
 
@@ -720,6 +836,8 @@ __global__ void __launch_bounds__(Layout<D, TIn>::THREADS, Cfg<D>::MINB) vla_fus
     sm.empty_z = sm.full_z + C::RZ;
     sm.full_g = sm.empty_z + C::RZ;
     sm.empty_g = sm.full_g + C::RG;
+    sm.zk_full = sm.empty_g + C::RG;
+    sm.zkr = reinterpret_cast<float*>(smem + LY::OFF_ZK);
     sm.abort = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAG);
     sm.raw = smem + LY::OFF_RAW;
     sm.prep = reinterpret_cast<float*>(smem + LY::OFF_PREP);
@@ -736,19 +854,21 @@ __global__ void __launch_bounds__(Layout<D, TIn>::THREADS, Cfg<D>::MINB) vla_fus
         }
         for (int i = 0; i < C::RZ; ++i) {
             mbar_init(sm.full_z + i, 1);
-            mbar_init(sm.empty_z + i, 1);
+            mbar_init(sm.empty_z + i, C::NG);
         }
         for (int i = 0; i < C::RG; ++i) {
             mbar_init(sm.full_g + i, 1);
             mbar_init(sm.empty_g + i, C::NS);
         }
+        mbar_init(sm.zk_full, 1);
+        mbar_init(sm.zk_full + 1, 1);
         *sm.abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (warp == LY::W_PROD)
-        stage_role<D, TIn>(p, sm, bh, lane);
+    if (warp < LY::W_GATE)
+        stage_role<D, TIn>(p, sm, bh, warp - LY::W_PROD, lane);
     else if (warp < LY::W_A0)
         gate_role<D, TIn>(p, sm, bh, warp - LY::W_GATE, lane);
     else if (warp < LY::W_S0)
