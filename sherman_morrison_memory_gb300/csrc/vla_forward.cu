@@ -44,7 +44,8 @@ namespace vla {
 //   NSTG    staging warps (chunk c goes to staging warp c mod NSTG)
 //   CH      tokens per staged chunk;  TB  tokens the staging warp prepares at once
 //   NP      prepped chunk slots;  NRAW  raw chunk slots
-//   RZ      two-token step slots of the A->gate ring;  RG  token slots of gate->S
+//   CB      tokens per A step (blocked Sherman-Morrison update)
+//   RZ      A-step slots of the A->gate ring;  RG  token slots of gate->S
 //   PAD     pad shared vectors by 4 floats per 32 (bank spread for the
 //           column-block strides of these layouts)
 //   MINB    CTAs per SM the register budget is sized for
@@ -53,22 +54,22 @@ template <int D>
 struct Cfg;
 template <>
 struct Cfg<32> {
-    static constexpr int NA = 1, CBA = 4, NS = 1, CBS = 4, NG = 1, NSTG = 1, CH = 8, TB = 4, NP = 6, NRAW = 3, RZ = 8,
+    static constexpr int NA = 1, CBA = 4, NS = 1, CBS = 4, NG = 1, NSTG = 1, CB = 2, CH = 8, TB = 4, NP = 6, NRAW = 3, RZ = 8,
                          RG = 16, PAD = 1, MINB = 4;
 };
 template <>
 struct Cfg<64> {
-    static constexpr int NA = 4, CBA = 8, NS = 2, CBS = 4, NG = 1, NSTG = 1, CH = 8, TB = 4, NP = 4, NRAW = 3, RZ = 8,
+    static constexpr int NA = 4, CBA = 8, NS = 2, CBS = 4, NG = 1, NSTG = 1, CB = 2, CH = 8, TB = 4, NP = 4, NRAW = 3, RZ = 8,
                          RG = 16, PAD = 1, MINB = 2;
 };
 template <>
 struct Cfg<96> {
-    static constexpr int NA = 8, CBA = 8, NS = 4, CBS = 8, NG = 2, NSTG = 2, CH = 8, TB = 4, NP = 8, NRAW = 4, RZ = 8,
+    static constexpr int NA = 4, CBA = 8, NS = 4, CBS = 8, NG = 2, NSTG = 2, CB = 2, CH = 8, TB = 4, NP = 8, NRAW = 4, RZ = 8,
                          RG = 16, PAD = 0, MINB = 1;
 };
 template <>
 struct Cfg<128> {
-    static constexpr int NA = 8, CBA = 8, NS = 8, CBS = 4, NG = 1, NSTG = 1, CH = 8, TB = 2, NP = 6, NRAW = 2, RZ = 8,
+    static constexpr int NA = 8, CBA = 8, NS = 8, CBS = 4, NG = 1, NSTG = 1, CB = 2, CH = 8, TB = 2, NP = 6, NRAW = 2, RZ = 8,
                          RG = 16, PAD = 1, MINB = 1;
 };
 
@@ -83,10 +84,11 @@ struct Layout {
     // prepped token record: u^ | k^ | phi(q) (padded) | v | den, pad
     static constexpr int P_U = 0, P_K = VD, P_Q = 2 * VD, P_V = 3 * VD, P_DEN = 3 * VD + D;
     static constexpr int PSTRIDE = 3 * VD + D + 4;
-    // A -> gate record of one step (two tokens): z'_0 | z'_1 | w'_0 | w'_1
-    // (padded) | per-warp partials of g00 g01 g11 h00 h01 h11 ([6][NA4])
-    static constexpr int Z_Z0 = 0, Z_Z1 = VD, Z_W0 = 2 * VD, Z_W1 = 3 * VD, Z_SC = 4 * VD;
-    static constexpr int ZSTRIDE = 4 * VD + 6 * NA4;
+    // A -> gate record of one step (CB tokens): z'_0..z'_{CB-1} | w'_0..w'_{CB-1}
+    // (padded) | per-warp parts of the Gram upper triangles Guu, Guk ([2*NP2][NA4])
+    static constexpr int NP2 = C::CB * (C::CB + 1) / 2;
+    static constexpr int Z_Z0 = 0, Z_W0 = C::CB * VD, Z_SC = 2 * C::CB * VD;
+    static constexpr int ZSTRIDE = 2 * C::CB * VD + 2 * NP2 * NA4;
     // gate -> S record: alpha^ (padded) | s = alpha^ . phi(q), pad
     static constexpr int G_A = 0, G_S = VD;
     static constexpr int GSTRIDE = VD + 4;
@@ -157,8 +159,8 @@ struct Smem {
     uint64_t* full_r;   // raw chunk landed (TMA tx)
     uint64_t* full_p;   // prepped chunk published
     uint64_t* empty_p;  // prepped chunk released by the S warps (its last readers)
-    uint64_t* full_z;   // a two-token A step published by the A warps
-    uint64_t* empty_z;  // ... released by the gate warps
+    uint64_t* full_z;   // an A step (CB tokens) published by the A warps
+    uint64_t* empty_z;  // ... released by the gate warp that handled it
     uint64_t* full_g;   // alpha^ of a token published by the gate
     uint64_t* empty_g;  // ... released by the S warps
     uint64_t* zk_full;  // z^key at the end of a chunk handed to the next chunk's staging warp
@@ -329,6 +331,16 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
                 }
             }
         }
+        // a tail that ends inside an A step leaves the rest of the step empty:
+        // give those tokens zero u^ and k^ so that the A warps read them unconditionally
+        for (int tp = nt; tp < C::CH && tp % C::CB != 0; ++tp) {
+            float* P = P0 + tp * LY::PSTRIDE;
+#pragma unroll
+            for (int m = 0; m < E; ++m) {
+                P[LY::P_U + vidx<D>(lane + 32 * m)] = 0.f;
+                P[LY::P_K + vidx<D>(lane + 32 * m)] = 0.f;
+            }
+        }
         // the running key sum: z^key at the start of this chunk
         if (c == 0) {
 #pragma unroll
@@ -394,93 +406,153 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
 }
 
 // ---------------------------------------------------------------------------
-// gate warps: alpha^_t = A_t k^_t / ||A_t k^_t|| (eq. 10) for the tokens of a
-// published A block (two tokens t0 = 2b, t1 = 2b + 1). With z'_s = A u^_s and
-// w'_s = A k^_s for the block's starting A, delta0 = 1 + g00, rho = g01/delta0,
-// delta1 = 1 + g11 - g01 rho and kappa = (h11 - rho h01)/delta1:
-//   A_t0 k^_t0 = w'_0 - z'_0 h00/delta0
-//   A_t1 k^_t1 = w'_1 - z'_0 (h01/delta0 - rho kappa) - z'_1 kappa
-// (g_st = u^_s . z'_t, h_st = k^_t . z'_s: the sequential Sherman-Morrison
-// steps of eq. 9 written in the basis of the block's matrix-vector products).
-// Gate warp g handles the tokens at block position g (or both when NG == 1).
+// Blocked Sherman-Morrison step over CB tokens. For the step's starting A and
+// unit vectors u^_s, k^_s (s < CB), with z'_s = A u^_s, w'_s = A k^_s and the
+// Gram entries Guu[s][t] = u^_s . z'_t, Guk[s][t] = u^_s . w'_t (s <= t),
+// the sequential updates of eq. 9 give z_t = sum_s c[t][s] z'_s with
+//   c[t] = e_t - sum_{r<t} ((z_r . u^_t) / delta_r) c[r],
+//   delta_t = 1 + z_t . u^_t,      z_r . u^_t = sum_s c[r][s] Guu[s][t],
+// so that A after the step is A - Z' Q Z'^T with Q = sum_r c[r] c[r]^T / delta_r,
+// and the gate direction of token t (eq. 10) is
+//   A_t k^_t = w'_t - sum_{s<=t} beta[s][t] z'_s,
+//   beta[s][t] = sum_{r=s..t} c[r][s] (sum_{s'<=r} c[r][s'] Guk[s'][t]) / delta_r.
+// ---------------------------------------------------------------------------
+template <int CB>
+__host__ __device__ constexpr int upair(int s, int t) {  // index of (s <= t) in row-major upper triangle
+    return s * CB - s * (s - 1) / 2 + (t - s);
+}
+
+template <int CB>
+__device__ __forceinline__ void block_coeffs(const float* Guu, float (&c)[CB][CB], float (&rd)[CB]) {
+#pragma unroll
+    for (int t = 0; t < CB; ++t)
+#pragma unroll
+        for (int s = 0; s < CB; ++s) c[t][s] = (s == t) ? 1.f : 0.f;
+#pragma unroll
+    for (int t = 0; t < CB; ++t) {
+#pragma unroll
+        for (int r = 0; r < t; ++r) {
+            float g = 0.f;
+#pragma unroll
+            for (int s = 0; s <= r; ++s) g = fmaf(c[r][s], Guu[upair<CB>(s, t)], g);
+            g *= rd[r];
+#pragma unroll
+            for (int s = 0; s <= r; ++s) c[t][s] = fmaf(-g, c[r][s], c[t][s]);
+        }
+        float dl = 1.f;
+#pragma unroll
+        for (int s = 0; s <= t; ++s) dl = fmaf(c[t][s], Guu[upair<CB>(s, t)], dl);
+        rd[t] = __frcp_rn(dl);
+    }
+}
+
+// Sum NK scalars, each stored as NA per-warp parts at base[k * NA4 + w], with
+// the lanes of the warp: lane l reads part (l + 32 m) and a butterfly over NA
+// lanes adds the parts; the result for every k is broadcast to all lanes.
+// Every caller uses the same order of additions.
+template <int NK, int NA, int NA4>
+__device__ __forceinline__ void gather_scalars(const float* base, int lane, float (&out)[NK]) {
+    constexpr int NV = NK * NA, R = (NV + 31) / 32;
+    float v[R];
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int i = lane + 32 * m;
+        v[m] = i < NV ? base[(i / NA) * NA4 + (i % NA)] : 0.f;
+    }
+#pragma unroll
+    for (int h = 1; h < NA; h <<= 1)
+#pragma unroll
+        for (int m = 0; m < R; ++m) v[m] += __shfl_xor_sync(0xffffffffu, v[m], h);
+#pragma unroll
+    for (int k = 0; k < NK; ++k) out[k] = __shfl_sync(0xffffffffu, v[(k * NA) / 32], (k * NA) % 32);
+}
+
+// ---------------------------------------------------------------------------
+// gate warps: alpha^_t = A_t k^_t / ||A_t k^_t|| (eq. 10) and s_t = alpha^_t . phi(q_t)
+// for the tokens of published A steps; gate warp g handles steps b = g mod NG.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn>
 __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int bh, int g, int lane) {
     using C = Cfg<D>;
     using LY = Layout<D, TIn>;
-    constexpr int E = D / 32;
+    constexpr int E = D / 32, CB = C::CB, NP2 = CB * (CB + 1) / 2;
     bool abort = false, nonfinite = false;
-    int t = g;
-    for (; t < p.T; t += C::NG) {
-        const int b = t >> 1, pos = t & 1;
+    int t = g * CB;
+    const int nsteps = (p.T + CB - 1) / CB;
+    for (int b = g; b < nsteps && !abort; b += C::NG) {
         const int zs = b % C::RZ;
-        if ((pos == 0 || C::NG == 2) && !mbar_wait(sm.full_z + zs, (b / C::RZ) & 1, sm.abort, p.wait_ns)) {
+        t = b * CB;
+        if (!mbar_wait(sm.full_z + zs, (b / C::RZ) & 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
-        const int chunk = t / C::CH, tc = t - chunk * C::CH, ps = chunk % C::NP;
-        if (tc < C::NG && !mbar_wait(sm.full_p + ps, (chunk / C::NP) & 1, sm.abort, p.wait_ns)) {
+        const int chunk = t / C::CH, ps = chunk % C::NP;
+        if (!mbar_wait(sm.full_p + ps, (chunk / C::NP) & 1, sm.abort, p.wait_ns)) {
             abort = true;
             break;
         }
         const float* Z = sm.zr + (size_t)zs * LY::ZSTRIDE;
-        const float* P = sm.prep + (size_t)(ps * C::CH + tc) * LY::PSTRIDE;
-        if (lane == 0 && g == 0) VLA_TRACE_PT(p, 11, t);
-        const float g00 = sum_partials<C::NA>(Z + LY::Z_SC + 0 * LY::NA4);
-        const float g01 = sum_partials<C::NA>(Z + LY::Z_SC + 1 * LY::NA4);
-        const float d0 = 1.f + g00;
-        const float rd0 = __frcp_rn(d0);
-        float c0, c1;
-        const float* W;
-        if (pos == 0) {
-            c0 = sum_partials<C::NA>(Z + LY::Z_SC + 3 * LY::NA4) * rd0;  // h00 / delta0
-            c1 = 0.f;
-            W = Z + LY::Z_W0;
-            if (!isfinite(d0)) nonfinite = true;
-        } else {
-            const float g11 = sum_partials<C::NA>(Z + LY::Z_SC + 2 * LY::NA4);
-            const float h01 = sum_partials<C::NA>(Z + LY::Z_SC + 4 * LY::NA4);
-            const float h11 = sum_partials<C::NA>(Z + LY::Z_SC + 5 * LY::NA4);
-            const float rho = g01 * rd0;
-            const float d1 = 1.f + fmaf(-g01, rho, g11);
-            const float kap = fmaf(-rho, h01, h11) * __frcp_rn(d1);
-            c0 = fmaf(-rho, kap, h01 * rd0);
-            c1 = kap;
-            W = Z + LY::Z_W1;
-            if (!isfinite(d1)) nonfinite = true;
-        }
-        float av[E];
-        float red[2] = {0.f, 0.f};  // ||a||^2, a . phi(q)
+        float G2[2 * NP2];  // Guu then Guk (upper triangles)
+        gather_scalars<2 * NP2, C::NA, LY::NA4>(Z + LY::Z_SC, lane, G2);
+        float c[CB][CB], rd[CB];
+        block_coeffs<CB>(G2, c, rd);
 #pragma unroll
-        for (int m = 0; m < E; ++m) {
-            const int j = vidx<D>(lane + 32 * m);
-            float x = fmaf(-c0, Z[LY::Z_Z0 + j], W[j]);
-            if (pos == 1) x = fmaf(-c1, Z[LY::Z_Z1 + j], x);
-            av[m] = x;
-            red[0] = fmaf(x, x, red[0]);
-            red[1] = fmaf(x, P[LY::P_Q + j], red[1]);
-        }
-        allreduce<2, 16>(red);
-        if (lane == 0 && g == 0) VLA_TRACE_PT(p, 12, t);
-        const float inv = rsqrtf(fmaxf(red[0], 1e-24f));  // 1 / max(||a||, 1e-12)
-        if (!(isfinite(red[0]) && isfinite(red[1]))) nonfinite = true;
-        const int gs = t % C::RG;
-        if (!mbar_wait(sm.empty_g + gs, ((t / C::RG) & 1) ^ 1, sm.abort, p.wait_ns)) {
-            abort = true;
-            break;
-        }
-        if (lane == 0 && g == 0) VLA_TRACE_PT(p, 13, t);
-        float* G = sm.gr + (size_t)gs * LY::GSTRIDE;
+        for (int s = 0; s < CB; ++s)
+            if (!isfinite(rd[s])) nonfinite = true;
 #pragma unroll
-        for (int m = 0; m < E; ++m) G[LY::G_A + vidx<D>(lane + 32 * m)] = av[m] * inv;
-        if (lane == 0) G[LY::G_S] = red[1] * inv;
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(sm.full_g + gs);
-            VLA_TRACE_AT(p, 2, t);
-            // release the A block once this warp is done with its last token in it
-            if (C::NG == 2 || pos == 1 || t + 1 >= p.T) mbar_arrive(sm.empty_z + zs);
+        for (int j = 0; j < CB; ++j) {
+            const int tj = t + j;
+            if (tj >= p.T) break;
+            // beta[s][j] for s <= j
+            float beta[CB];
+#pragma unroll
+            for (int s = 0; s < CB; ++s) beta[s] = 0.f;
+#pragma unroll
+            for (int r = 0; r <= j; ++r) {
+                float zk = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 <= r; ++s2) zk = fmaf(c[r][s2], G2[NP2 + upair<CB>(s2, j)], zk);
+                zk *= rd[r];
+#pragma unroll
+                for (int s = 0; s <= r; ++s) beta[s] = fmaf(c[r][s], zk, beta[s]);
+            }
+            if (lane == 0 && g == 0) VLA_TRACE_PT(p, 11, tj);
+            const int tc = tj - chunk * C::CH;
+            const float* P = sm.prep + (size_t)(ps * C::CH + tc) * LY::PSTRIDE;
+            float av[E];
+            float red[2] = {0.f, 0.f};  // ||a||^2, a . phi(q)
+#pragma unroll
+            for (int m = 0; m < E; ++m) {
+                const int jv = vidx<D>(lane + 32 * m);
+                float x = Z[LY::Z_W0 + j * LY::VD + jv];
+#pragma unroll
+                for (int s = 0; s <= j; ++s) x = fmaf(-beta[s], Z[LY::Z_Z0 + s * LY::VD + jv], x);
+                av[m] = x;
+                red[0] = fmaf(x, x, red[0]);
+                red[1] = fmaf(x, P[LY::P_Q + jv], red[1]);
+            }
+            allreduce<2, 16>(red);
+            if (lane == 0 && g == 0) VLA_TRACE_PT(p, 12, tj);
+            const float inv = rsqrtf(fmaxf(red[0], 1e-24f));  // 1 / max(||a||, 1e-12)
+            if (!(isfinite(red[0]) && isfinite(red[1]))) nonfinite = true;
+            const int gs = tj % C::RG;
+            if (!mbar_wait(sm.empty_g + gs, ((tj / C::RG) & 1) ^ 1, sm.abort, p.wait_ns)) {
+                abort = true;
+                t = tj;
+                break;
+            }
+            if (lane == 0 && g == 0) VLA_TRACE_PT(p, 13, tj);
+            float* Gp = sm.gr + (size_t)gs * LY::GSTRIDE;
+#pragma unroll
+            for (int m = 0; m < E; ++m) Gp[LY::G_A + vidx<D>(lane + 32 * m)] = av[m] * inv;
+            if (lane == 0) Gp[LY::G_S] = red[1] * inv;
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(sm.full_g + gs);
+                VLA_TRACE_AT(p, 2, tj);
+            }
         }
+        if (!abort && lane == 0) mbar_arrive(sm.empty_z + zs);
     }
     if (abort) {
         if (lane == 0) record_failure(p.status, BIT_TIMEOUT, ROLE_GATE, bh, t);
@@ -490,28 +562,28 @@ __device__ __forceinline__ void gate_role(const Params& p, const Smem& sm, int b
 }
 
 // ---------------------------------------------------------------------------
-// A warps: the Sherman-Morrison chain (eq. 9) two tokens per step. A is
-// resident in registers as float2 pairs. One pass over A per step applies the
-// previous step's rank-2 update A -= [z'_0 z'_1] Q [z'_0 z'_1]^T and forms
-// z'_s = A u^_s, w'_s = A k^_s for both tokens, plus this thread's parts of the
-// six scalars g_st, h_st; one named barrier per step publishes them. With
-// delta0, rho, delta1 as in the gate,
-//   Q = [[1/delta0 + rho^2/delta1, -rho/delta1], [-rho/delta1, 1/delta1]]
-// reproduces the two sequential updates A -= z z^T / delta of eq. 9.
+// A warps: the Sherman-Morrison chain (eq. 9), CB tokens per step. A is
+// resident in registers as float2 pairs. One step: sub-pass 1 applies the
+// previous step's update A -= Z' Q Z'^T (as A += nm_s z'_s^T) and forms
+// z'_t = A u^_t; sub-pass 2 forms w'_t = A k^_t; the row sums and this thread's
+// parts of the Gram entries are reduced across the lanes of a row and
+// published with one named barrier per step.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn>
 __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, int warp, int lane) {
     using C = Cfg<D>;
     using LY = Layout<D, TIn>;
+    constexpr int CB = C::CB, NP2 = CB * (CB + 1) / 2;
     constexpr int RPW = 32 / C::CBA;              // row groups per warp
     constexpr int RA = D / (C::NA * RPW);         // rows per thread
     constexpr int CA = D / C::CBA;                // columns per thread
     constexpr int C2 = CA / 2;                    // float2 columns
-    constexpr int NV = 4 * RA + 6;                // z'0, z'1, w'0, w'1 rows; g00 g01 g11 h00 h01 h11
+    constexpr int NVV = 2 * CB * RA;              // z' and w' rows
+    constexpr int NV = NVV + 2 * NP2;             // + Guu, Guk parts
     constexpr int HR = C::CBA / 2;
     constexpr int NOUT = rs_count<NV, HR>();
     static_assert(RA * C::NA * RPW == D && CA * C::CBA == D && CA % 4 == 0, "A layout");
-    static_assert(C::CH % 2 == 0, "steps of two tokens stay inside a chunk");
+    static_assert(C::CH % CB == 0, "steps stay inside a chunk");
 
     const int wa = warp - LY::W_A0;
     const int cb = lane % C::CBA, rgl = lane / C::CBA;
@@ -529,83 +601,127 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
                              : f2(i == j ? p.inv_lambda0 : 0.f, i == j + 1 ? p.inv_lambda0 : 0.f);
             }
     }
-    // pending rank-2 update of the previous step: A += nm0 z'_0^T + nm1 z'_1^T,
-    // with z'_s at this thread's columns read from the previous step's slot
-    float2 nm0[RA], nm1[RA];
+    // pending update of the previous step: A += sum_s nm[s] (x) z'_s at this
+    // thread's columns (read from the previous step's slot; zeros before step 0)
+    float2 nm[CB][RA];
 #pragma unroll
-    for (int r = 0; r < RA; ++r) nm0[r] = nm1[r] = f2(0.f, 0.f);
-    const float* Zprev = nullptr;
+    for (int s = 0; s < CB; ++s)
+#pragma unroll
+        for (int r = 0; r < RA; ++r) nm[s][r] = f2(0.f, 0.f);
+    const float* Zprev = sm.zr + (size_t)(C::RZ - 1) * LY::ZSTRIDE;
+    {
+        float* Zw = sm.zr + (size_t)(C::RZ - 1) * LY::ZSTRIDE;
+        for (int i = wa * 32 + lane; i < CB * LY::VD; i += C::NA * 32) Zw[LY::Z_Z0 + i] = 0.f;
+        bar_red_or(1, C::NA * 32, false);
+    }
 
     bool abort = false;
     int t = 0;
     if (p.T > 0 && !mbar_wait(sm.full_p, 0, sm.abort, p.wait_ns)) abort = true;
-    for (int b = 0; t < p.T; ++b, t += 2) {
+    for (int b = 0; t < p.T; ++b, t += CB) {
         const bool tr0 = (wa == 0 && lane == 0);
         if (tr0) VLA_TRACE_PT(p, 5, t);
         const int chunk = t / C::CH, tc = t - chunk * C::CH, ps = chunk % C::NP;
-        const bool two = t + 1 < p.T;
-        const float* P0 = sm.prep + (size_t)(ps * C::CH + tc) * LY::PSTRIDE;
-        const float* P1 = P0 + LY::PSTRIDE;
+        const float* P0 = sm.prep + (size_t)(ps * C::CH + tc) * LY::PSTRIDE;  // tokens past T hold zeros
 
-        float2 pz0[RA], pz1[RA], pw0[RA], pw1[RA];
+        // sub-pass 1: pending update, then z'_s = A u^_s
+        float zr[CB][RA];
+        {
+            float2 pz[CB][RA];
 #pragma unroll
-        for (int r = 0; r < RA; ++r) pz0[r] = pz1[r] = pw0[r] = pw1[r] = f2(0.f, 0.f);
+            for (int s = 0; s < CB; ++s)
 #pragma unroll
-        for (int c4 = 0; c4 < CA; c4 += 4) {
-            const int jv = vidx<D>(col0 + c4);
-            const float4 u04 = ld4(P0 + LY::P_U + jv), k04 = ld4(P0 + LY::P_K + jv);
-            const float4 u14 = two ? ld4(P1 + LY::P_U + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 k14 = two ? ld4(P1 + LY::P_K + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 z04 = Zprev ? ld4(Zprev + LY::Z_Z0 + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 z14 = Zprev ? ld4(Zprev + LY::Z_Z1 + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float2 u0[2] = {f2(u04.x, u04.y), f2(u04.z, u04.w)};
-            const float2 u1[2] = {f2(u14.x, u14.y), f2(u14.z, u14.w)};
-            const float2 k0[2] = {f2(k04.x, k04.y), f2(k04.z, k04.w)};
-            const float2 k1[2] = {f2(k14.x, k14.y), f2(k14.z, k14.w)};
-            const float2 z0[2] = {f2(z04.x, z04.y), f2(z04.z, z04.w)};
-            const float2 z1[2] = {f2(z14.x, z14.y), f2(z14.z, z14.w)};
+                for (int r = 0; r < RA; ++r) pz[s][r] = f2(0.f, 0.f);
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int c4 = 0; c4 < CA; c4 += 4) {
+                const int jv = vidx<D>(col0 + c4);
 #pragma unroll
-                for (int r = 0; r < RA; ++r) {
-                    const int c = c4 / 2 + h;
-                    float2 x = __ffma2_rn(nm0[r], z0[h], a[r][c]);
-                    x = __ffma2_rn(nm1[r], z1[h], x);
-                    a[r][c] = x;
-                    pz0[r] = __ffma2_rn(x, u0[h], pz0[r]);
-                    pz1[r] = __ffma2_rn(x, u1[h], pz1[r]);
-                    pw0[r] = __ffma2_rn(x, k0[h], pw0[r]);
-                    pw1[r] = __ffma2_rn(x, k1[h], pw1[r]);
+                for (int h = 0; h < 2; ++h) {
+                    float2 zc[CB], uc[CB];
+#pragma unroll
+                    for (int s = 0; s < CB; ++s) {
+                        zc[s] = *reinterpret_cast<const float2*>(Zprev + LY::Z_Z0 + s * LY::VD + jv + 2 * h);
+                        uc[s] = *reinterpret_cast<const float2*>(P0 + s * LY::PSTRIDE + LY::P_U + jv + 2 * h);
+                    }
+#pragma unroll
+                    for (int r = 0; r < RA; ++r) {
+                        const int c = c4 / 2 + h;
+                        float2 x = a[r][c];
+#pragma unroll
+                        for (int s = 0; s < CB; ++s) x = __ffma2_rn(nm[s][r], zc[s], x);
+                        a[r][c] = x;
+#pragma unroll
+                        for (int s = 0; s < CB; ++s) pz[s][r] = __ffma2_rn(x, uc[s], pz[s][r]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < CB; ++s)
+#pragma unroll
+                for (int r = 0; r < RA; ++r) zr[s][r] = pz[s][r].x + pz[s][r].y;
+        }
+        // sub-pass 2: w'_s = A k^_s
+        float wr[CB][RA];
+        {
+            float2 pw[CB][RA];
+#pragma unroll
+            for (int s = 0; s < CB; ++s)
+#pragma unroll
+                for (int r = 0; r < RA; ++r) pw[s][r] = f2(0.f, 0.f);
+#pragma unroll
+            for (int c4 = 0; c4 < CA; c4 += 4) {
+                const int jv = vidx<D>(col0 + c4);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float2 kc[CB];
+#pragma unroll
+                    for (int s = 0; s < CB; ++s)
+                        kc[s] = *reinterpret_cast<const float2*>(P0 + s * LY::PSTRIDE + LY::P_K + jv + 2 * h);
+#pragma unroll
+                    for (int r = 0; r < RA; ++r) {
+                        const int c = c4 / 2 + h;
+#pragma unroll
+                        for (int s = 0; s < CB; ++s) pw[s][r] = __ffma2_rn(a[r][c], kc[s], pw[s][r]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < CB; ++s)
+#pragma unroll
+                for (int r = 0; r < RA; ++r) wr[s][r] = pw[s][r].x + pw[s][r].y;
+        }
+        // row sums and Gram parts, reduced across the lanes of each row
+        float vals[NV];
+#pragma unroll
+        for (int s = 0; s < CB; ++s)
+#pragma unroll
+            for (int r = 0; r < RA; ++r) {
+                vals[s * RA + r] = zr[s][r];
+                vals[(CB + s) * RA + r] = wr[s][r];
+            }
+        {
+            float ur[CB][RA];
+#pragma unroll
+            for (int s = 0; s < CB; ++s)
+#pragma unroll
+                for (int r = 0; r < RA; ++r) ur[s][r] = P0[s * LY::PSTRIDE + LY::P_U + vidx<D>(row0 + r)];
+#pragma unroll
+            for (int s = 0; s < CB; ++s)
+#pragma unroll
+                for (int tt = s; tt < CB; ++tt) {
+                    float gu = 0.f, gk = 0.f;
+#pragma unroll
+                    for (int r = 0; r < RA; ++r) {
+                        gu = fmaf(ur[s][r], zr[tt][r], gu);
+                        gk = fmaf(ur[s][r], wr[tt][r], gk);
+                    }
+                    vals[NVV + upair<CB>(s, tt)] = gu;
+                    vals[NVV + NP2 + upair<CB>(s, tt)] = gk;
                 }
         }
-        float vals[NV];
-        float sg00 = 0.f, sg01 = 0.f, sg11 = 0.f, sh00 = 0.f, sh01 = 0.f, sh11 = 0.f;
-#pragma unroll
-        for (int r = 0; r < RA; ++r) {
-            const int iv = vidx<D>(row0 + r);
-            const float ur0 = P0[LY::P_U + iv], kr0 = P0[LY::P_K + iv];
-            const float ur1 = two ? P1[LY::P_U + iv] : 0.f, kr1 = two ? P1[LY::P_K + iv] : 0.f;
-            const float z0 = pz0[r].x + pz0[r].y, z1 = pz1[r].x + pz1[r].y;
-            vals[r] = z0;
-            vals[RA + r] = z1;
-            vals[2 * RA + r] = pw0[r].x + pw0[r].y;
-            vals[3 * RA + r] = pw1[r].x + pw1[r].y;
-            sg00 = fmaf(ur0, z0, sg00);
-            sg01 = fmaf(ur1, z0, sg01);
-            sg11 = fmaf(ur1, z1, sg11);
-            sh00 = fmaf(kr0, z0, sh00);
-            sh01 = fmaf(kr1, z0, sh01);
-            sh11 = fmaf(kr1, z1, sh11);
-        }
-        vals[4 * RA + 0] = sg00;
-        vals[4 * RA + 1] = sg01;
-        vals[4 * RA + 2] = sg11;
-        vals[4 * RA + 3] = sh00;
-        vals[4 * RA + 4] = sh01;
-        vals[4 * RA + 5] = sh11;
         if (tr0) VLA_TRACE_PT(p, 6, t);
         reduce_scatter<NV, HR>(vals, lane);
-        // the scalar partials also need the sum over this warp's row groups
+        // the Gram parts also need the sum over this warp's row groups
         float sc[NOUT];
 #pragma unroll
         for (int j = 0; j < NOUT; ++j) sc[j] = vals[j];
@@ -623,16 +739,16 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
         for (int j = 0; j < NOUT; ++j) {
             const int idx = rs_index<NV, HR>(cb, j);
             if (idx < 0) continue;
-            if (idx < 4 * RA) {
+            if (idx < NVV) {
                 const int vec = idx / RA, r = idx - vec * RA;
                 Z[vec * LY::VD + vidx<D>(row0 + r)] = vals[j];
             } else if (rgl == 0) {
-                Z[LY::Z_SC + (idx - 4 * RA) * LY::NA4 + wa] = sc[j];
+                Z[LY::Z_SC + (idx - NVV) * LY::NA4 + wa] = sc[j];
             }
         }
-        // the next step's first token may start a new chunk
-        if (t + 2 < p.T) {
-            const int t2 = t + 2, chunk2 = t2 / C::CH;
+        // the next step may start a new chunk
+        if (t + CB < p.T) {
+            const int t2 = t + CB, chunk2 = t2 / C::CH;
             if (t2 - chunk2 * C::CH == 0 && !abort &&
                 !mbar_wait(sm.full_p + chunk2 % C::NP, (chunk2 / C::NP) & 1, sm.abort, p.wait_ns))
                 abort = true;
@@ -645,28 +761,39 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
         if (tr0) VLA_TRACE_PT(p, 9, t);
         if (wa == 0 && lane == 0) {
             mbar_arrive(sm.full_z + zs);
-            VLA_TRACE_AT(p, 1, t);
-            if (two) VLA_TRACE_AT(p, 1, t + 1);
+#pragma unroll
+            for (int j = 0; j < CB; ++j)
+                if (t + j < p.T) VLA_TRACE_AT(p, 1, t + j);
         }
-        // g00, g01, g11: lane (s * NA + w) reads warp w's part of scalar s; sum, broadcast
-        float gv = 0.f;
-        if (lane < 3 * C::NA) gv = Z[LY::Z_SC + (lane / C::NA) * LY::NA4 + (lane % C::NA)];
+        {
+            float Guu[NP2];
+            gather_scalars<NP2, C::NA, LY::NA4>(Z + LY::Z_SC, lane, Guu);
+            float c[CB][CB], rd[CB];
+            block_coeffs<CB>(Guu, c, rd);
+            float Q[CB][CB];
 #pragma unroll
-        for (int h = 1; h < C::NA; h <<= 1) gv += __shfl_xor_sync(0xffffffffu, gv, h);
-        const float g00 = __shfl_sync(0xffffffffu, gv, 0);
-        const float g01 = __shfl_sync(0xffffffffu, gv, C::NA);
-        const float g11 = __shfl_sync(0xffffffffu, gv, 2 * C::NA);
-        const float rd0 = __frcp_rn(1.f + g00);
-        const float rho = g01 * rd0;
-        const float rd1 = __frcp_rn(1.f + fmaf(-g01, rho, g11));
-        const float q11 = rd1, q01 = -rho * rd1, q00 = fmaf(rho * rho, rd1, rd0);
+            for (int s = 0; s < CB; ++s)
 #pragma unroll
-        for (int r = 0; r < RA; ++r) {
-            const int iv = vidx<D>(row0 + r);
-            const float z0 = Z[LY::Z_Z0 + iv], z1 = Z[LY::Z_Z1 + iv];
-            const float m0 = -fmaf(q00, z0, q01 * z1), m1 = -fmaf(q01, z0, q11 * z1);
-            nm0[r] = f2(m0, m0);
-            nm1[r] = f2(m1, m1);
+                for (int s2 = 0; s2 < CB; ++s2) {
+                    float q = 0.f;
+#pragma unroll
+                    for (int r = (s > s2 ? s : s2); r < CB; ++r) q = fmaf(c[r][s] * rd[r], c[r][s2], q);
+                    Q[s][s2] = q;
+                }
+            float zrow[CB][RA];
+#pragma unroll
+            for (int s = 0; s < CB; ++s)
+#pragma unroll
+                for (int r = 0; r < RA; ++r) zrow[s][r] = Z[LY::Z_Z0 + s * LY::VD + vidx<D>(row0 + r)];
+#pragma unroll
+            for (int s = 0; s < CB; ++s)
+#pragma unroll
+                for (int r = 0; r < RA; ++r) {
+                    float m = 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < CB; ++s2) m = fmaf(Q[s][s2], zrow[s2][r], m);
+                    nm[s][r] = f2(-m, -m);
+                }
         }
         Zprev = Z;
         if (tr0) VLA_TRACE_PT(p, 10, t);
@@ -682,12 +809,13 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
 #pragma unroll
         for (int c4 = 0; c4 < CA; c4 += 4) {
             const int jv = vidx<D>(col0 + c4);
-            const float4 z04 = Zprev ? ld4(Zprev + LY::Z_Z0 + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 z14 = Zprev ? ld4(Zprev + LY::Z_Z1 + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
-            float2 x0 = __ffma2_rn(nm0[r], f2(z04.x, z04.y), a[r][c4 / 2]);
-            x0 = __ffma2_rn(nm1[r], f2(z14.x, z14.y), x0);
-            float2 x1 = __ffma2_rn(nm0[r], f2(z04.z, z04.w), a[r][c4 / 2 + 1]);
-            x1 = __ffma2_rn(nm1[r], f2(z14.z, z14.w), x1);
+            float2 x0 = a[r][c4 / 2], x1 = a[r][c4 / 2 + 1];
+#pragma unroll
+            for (int s = 0; s < CB; ++s) {
+                const float4 z4 = ld4(Zprev + LY::Z_Z0 + s * LY::VD + jv);
+                x0 = __ffma2_rn(nm[s][r], f2(z4.x, z4.y), x0);
+                x1 = __ffma2_rn(nm[s][r], f2(z4.z, z4.w), x1);
+            }
             *reinterpret_cast<float4*>(Ao + (size_t)(row0 + r) * D + col0 + c4) = make_float4(x0.x, x0.y, x1.x, x1.y);
         }
 }
@@ -854,7 +982,7 @@ __global__ void __launch_bounds__(Layout<D, TIn>::THREADS, Cfg<D>::MINB) vla_fus
         }
         for (int i = 0; i < C::RZ; ++i) {
             mbar_init(sm.full_z + i, 1);
-            mbar_init(sm.empty_z + i, C::NG);
+            mbar_init(sm.empty_z + i, 1);
         }
         for (int i = 0; i < C::RG; ++i) {
             mbar_init(sm.full_g + i, 1);
