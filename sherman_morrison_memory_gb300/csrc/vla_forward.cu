@@ -1006,41 +1006,52 @@ __global__ void __launch_bounds__(Layout<D, TIn>::THREADS, Cfg<D>::MINB) vla_fus
 }
 
 // ---------------------------------------------------------------------------
-// plain cumulative linear-attention state S = sum_t v_t phi(k_t)^T (§4.1)
+// plain cumulative linear-attention state S = sum_t v_t phi(k_t)^T (§4.1).
+// One CTA per head; thread (ti, tj) of a 16 x 16 grid accumulates the
+// (D/16) x (D/16) block of S at rows ti*R.., columns tj*R.. from tokens staged
+// in shared memory LA_TT at a time.
 // ---------------------------------------------------------------------------
-constexpr int LA_THREADS = 256, LA_TT = 16;
+constexpr int LA_THREADS = 256, LA_TT = 32;
 
-template <typename TIn>
-__global__ void __launch_bounds__(LA_THREADS) la_state_kernel(const TIn* k, const TIn* v, int T, int D,
-                                                              float* S_out) {
-    __shared__ float sv[LA_TT][128], sk[LA_TT][128];
+template <int D, typename TIn>
+__global__ void __launch_bounds__(LA_THREADS) la_state_kernel(const TIn* k, const TIn* v, int T, float* S_out) {
+    constexpr int R = D / 16;
+    __shared__ float sv[LA_TT][D], sk[LA_TT][D];
     const size_t base = (size_t)blockIdx.x * T * D;
-    const int DD = D * D;
-    float acc[64];
+    const int ti = threadIdx.x / 16, tj = threadIdx.x % 16;
+    float acc[R][R];
 #pragma unroll
-    for (int m = 0; m < 64; ++m) acc[m] = 0.f;
+    for (int a = 0; a < R; ++a)
+#pragma unroll
+        for (int b = 0; b < R; ++b) acc[a][b] = 0.f;
     for (int t0 = 0; t0 < T; t0 += LA_TT) {
         const int nt = min(LA_TT, T - t0);
-        for (int i = threadIdx.x; i < nt * D; i += LA_THREADS) {
+        for (int i = threadIdx.x; i < LA_TT * D; i += LA_THREADS) {
             const int tt = i / D, j = i - tt * D;
-            sv[tt][j] = ld_in<TIn>(v + base + (size_t)t0 * D, i);
-            sk[tt][j] = phi(ld_in<TIn>(k + base + (size_t)t0 * D, i));
+            const bool live = tt < nt;
+            sv[tt][j] = live ? ld_in<TIn>(v + base + (size_t)t0 * D, i) : 0.f;
+            sk[tt][j] = live ? phi(ld_in<TIn>(k + base + (size_t)t0 * D, i)) : 0.f;
         }
         __syncthreads();
-        for (int tt = 0; tt < nt; ++tt) {
+        for (int tt = 0; tt < LA_TT; ++tt) {
+            float vi[R], kj[R];
 #pragma unroll
-            for (int m = 0; m < 64; ++m) {
-                const int e = threadIdx.x + LA_THREADS * m;
-                if (e < DD) acc[m] = fmaf(sv[tt][e / D], sk[tt][e % D], acc[m]);
+            for (int a = 0; a < R; ++a) {
+                vi[a] = sv[tt][ti * R + a];
+                kj[a] = sk[tt][tj * R + a];
             }
+#pragma unroll
+            for (int a = 0; a < R; ++a)
+#pragma unroll
+                for (int b = 0; b < R; ++b) acc[a][b] = fmaf(vi[a], kj[b], acc[a][b]);
         }
         __syncthreads();
     }
+    float* So = S_out + (size_t)blockIdx.x * D * D;
 #pragma unroll
-    for (int m = 0; m < 64; ++m) {
-        const int e = threadIdx.x + LA_THREADS * m;
-        if (e < DD) S_out[(size_t)blockIdx.x * DD + e] = acc[m];
-    }
+    for (int a = 0; a < R; ++a)
+#pragma unroll
+        for (int b = 0; b < R; ++b) So[(size_t)(ti * R + a) * D + tj * R + b] = acc[a][b];
 }
 
 }  // namespace vla
@@ -1074,6 +1085,16 @@ vla_status launch_d(int d, const vla::Params& p, int BH, cudaStream_t s) {
         case 96: return launch_fused<96, TIn>(p, BH, s);
         case 128: return launch_fused<128, TIn>(p, BH, s);
         default: return VLA_ERR_UNSUPPORTED;
+    }
+}
+
+template <typename TIn>
+void launch_la(int d, const TIn* k, const TIn* v, int T, float* S, int BH, cudaStream_t s) {
+    switch (d) {
+        case 32: vla::la_state_kernel<32, TIn><<<BH, vla::LA_THREADS, 0, s>>>(k, v, T, S); break;
+        case 64: vla::la_state_kernel<64, TIn><<<BH, vla::LA_THREADS, 0, s>>>(k, v, T, S); break;
+        case 96: vla::la_state_kernel<96, TIn><<<BH, vla::LA_THREADS, 0, s>>>(k, v, T, S); break;
+        default: vla::la_state_kernel<128, TIn><<<BH, vla::LA_THREADS, 0, s>>>(k, v, T, S); break;
     }
 }
 
@@ -1192,11 +1213,10 @@ vla_status vla_linear_attention_state(const void* k, const void* v, vla_dtype dt
     if (T > 0 && (!k || !v || !aligned4(k) || !aligned4(v))) return VLA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == VLA_BF16)
-        vla::la_state_kernel<__nv_bfloat16><<<(int)BH, vla::LA_THREADS, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), T, d, S_out);
+        launch_la<__nv_bfloat16>(d, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), T,
+                                 S_out, (int)BH, s);
     else
-        vla::la_state_kernel<float><<<(int)BH, vla::LA_THREADS, 0, s>>>(
-            static_cast<const float*>(k), static_cast<const float*>(v), T, d, S_out);
+        launch_la<float>(d, static_cast<const float*>(k), static_cast<const float*>(v), T, S_out, (int)BH, s);
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
 }
 

@@ -353,6 +353,23 @@ def pin_linear_attention_state(orc):
     assert _rel(S, want) < 1e-12
 
 
+def pin_linear_attention_closed_forms(orc):
+    """Linear attention with k = 0 gives phi(0) = 1, so every column of S is
+    sum_t v_t; and the sum is independent of the token order."""
+    rng = np.random.default_rng(27)
+    T, d = 23, 5
+    _, _, v, _ = _inputs(rng, T, d)
+    k0 = np.zeros_like(v)
+    S = orc.linear_attention_state(k0, v)[0]
+    col = v[0].astype(np.float64).sum(axis=0)
+    assert np.allclose(S, np.repeat(col[:, None], d, axis=1), rtol=1e-13, atol=1e-13)
+    _, k, v, _ = _inputs(rng, T, d)
+    perm = rng.permutation(T)
+    S1 = orc.linear_attention_state(k, v)[0]
+    S2 = orc.linear_attention_state(k[:, perm], v[:, perm])[0]
+    assert _rel(S2, S1) < 1e-13
+
+
 ALL_PINS = [
     pin_inverse_penalty,
     pin_delta,
@@ -370,4 +387,5 @@ ALL_PINS = [
     pin_chunked_state,
     pin_heads_independent,
     pin_linear_attention_state,
+    pin_linear_attention_closed_forms,
 ]
