@@ -125,6 +125,37 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
  */
 vla_status vla_get_last_device_status(void* workspace, void* stream, int* detail);
 
+/*
+ * vla_forward_noalloc -- the same operation as vla_forward, for callers that
+ * cannot allocate device memory: code running under a fixed device-memory
+ * budget that another runtime has already reserved in full (cudaMalloc would
+ * fail), real-time or serving loops that must not call the allocator (it can
+ * synchronise the device and fragment memory), and callers without any device
+ * allocator of their own. The paper has no counterpart; this is an interface
+ * convenience.
+ *
+ * Instead of a caller-provided workspace, the status record lives in a
+ * file-scope __device__ array of the library (256 bytes, held by every device
+ * that loads the library until the process exits). The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress) with the device
+ * current; make that first call before any stream capture. Every call clears
+ * the record before its launch, so a call starts from a zero status. All calls
+ * share the one record: calls that overlap on the GPU (different streams, no
+ * ordering) race on it and their statuses are unreliable. The call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine). It returns
+ * VLA_ERR_UNSUPPORTED if the status record the kernel needs does not fit in the
+ * array. Arguments are as for vla_forward, without workspace; if
+ * `device_status` is not NULL the call synchronises `stream` after the launch
+ * and stores there the device-side status (VLA_OK, VLA_ERR_TIMEOUT or
+ * VLA_ERR_NONFINITE); otherwise it returns as soon as the work is enqueued.
+ */
+vla_status vla_forward_noalloc(const void* q, const void* k, const void* v, const void* u,
+                               vla_dtype dtype, int B, int H, int T, int d,
+                               float lambda0, float eps,
+                               const float* S0, const float* A0, const float* zk0,
+                               float* o, float* S_out, float* A_out, float* zk_out,
+                               void* stream, int* device_status);
+
 /* Static text for a status code. */
 const char* vla_status_string(vla_status s);
 

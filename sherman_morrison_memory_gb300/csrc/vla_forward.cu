@@ -31,6 +31,7 @@
 #include <stdint.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "vla.h"
 #include "vla_device.cuh"
@@ -1187,6 +1188,66 @@ vla_status vla_get_last_device_status(void* workspace, void* stream, int* detail
     }
     if (h.bits & vla::BIT_TIMEOUT) return VLA_ERR_TIMEOUT;
     return VLA_ERR_NONFINITE;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// No-allocation variant: the status record lives in a file-scope device array.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 256;
+static_assert(sizeof(vla::DeviceStatus) <= kNoAllocScratchBytes, "status record fits the static scratch");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up once
+// per device, with that device current).
+vla_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VLA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return VLA_ERR_CUDA;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return VLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vla_status vla_forward_noalloc(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B,
+                               int H, int T, int d, float lambda0, float eps, const float* S0, const float* A0,
+                               const float* zk0, float* o, float* S_out, float* A_out, float* zk_out,
+                               void* stream, int* device_status) {
+    if (device_status) *device_status = VLA_OK;
+    // arguments that need no device are rejected before the one-time set-up
+    if (B < 0 || H < 0 || T < 0) return VLA_ERR_INVALID_ARG;
+    if (dtype != VLA_F32 && dtype != VLA_BF16) return VLA_ERR_INVALID_ARG;
+    if (d != 32 && d != 64 && d != 96 && d != 128) return VLA_ERR_UNSUPPORTED;
+    if (vla_workspace_bytes() > kNoAllocScratchBytes) return VLA_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    vla_status st = noalloc_scratch(&scratch);
+    if (st != VLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the record must start at zero: the previous call's contents stay in the array
+    if (cudaMemsetAsync(scratch, 0, sizeof(vla::DeviceStatus), s) != cudaSuccess) return VLA_ERR_CUDA;
+    st = vla_forward_ex(q, k, v, u, dtype, B, H, T, d, lambda0, eps, S0, A0, zk0, o, S_out, A_out, zk_out, scratch,
+                        kNoAllocScratchBytes, stream, nullptr);
+    if (st != VLA_OK || !device_status) return st;
+    vla::DeviceStatus h;
+    if (cudaMemcpyAsync(&h, scratch, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return VLA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return VLA_ERR_CUDA;
+    *device_status = h.bits == 0 ? VLA_OK : ((h.bits & vla::BIT_TIMEOUT) ? VLA_ERR_TIMEOUT : VLA_ERR_NONFINITE);
+    return VLA_OK;
 }
 
 const char* vla_status_string(vla_status st) {
