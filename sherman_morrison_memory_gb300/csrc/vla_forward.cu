@@ -106,7 +106,14 @@ struct Layout {
     static constexpr size_t OFF_PREP = align_up(OFF_RAW + (size_t)C::NRAW * 4 * RAW_TENSOR, 128);
     static constexpr size_t OFF_Z = align_up(OFF_PREP + (size_t)C::NP * C::CH * PSTRIDE * 4, 128);
     static constexpr size_t OFF_G = align_up(OFF_Z + (size_t)C::RZ * ZSTRIDE * 4, 128);
-    static constexpr size_t SMEM = align_up(OFF_G + (size_t)C::RG * GSTRIDE * 4, 128);
+    // per-warp transpose scratch for the cross-lane reductions: row v holds the
+    // 32 lanes' copies of item v (stride RST floats keeps the reads conflict-free)
+    static constexpr int RST = 36;
+    static constexpr int A_ROWS = 2 * C::CB * (D / (C::NA * (32 / C::CBA))) + C::CB * (C::CB + 1);
+    static constexpr int S_ROWS = 2 * (D / (C::NS * (32 / C::CBS))) + 1;
+    static constexpr size_t OFF_ARED = align_up(OFF_G + (size_t)C::RG * GSTRIDE * 4, 128);
+    static constexpr size_t OFF_SRED = align_up(OFF_ARED + (size_t)C::NA * A_ROWS * RST * 4, 128);
+    static constexpr size_t SMEM = align_up(OFF_SRED + (size_t)C::NS * S_ROWS * RST * 4, 128);
 
     static_assert(VD % 4 == 0 && PSTRIDE % 4 == 0 && ZSTRIDE % 4 == 0 && GSTRIDE % 4 == 0, "float4 records");
     static_assert(RAW_TENSOR % 16 == 0, "bulk-copy granularity");
@@ -171,6 +178,8 @@ struct Smem {
     float* prep;
     float* zr;
     float* gr;
+    float* ared;  // A warps' transpose scratch
+    float* sred;  // S warps' transpose scratch
 };
 
 __device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.f : expf(x); }
@@ -216,6 +225,37 @@ __device__ __forceinline__ float sum_partials(const float* p) {
         for (int i = 1; i < N; ++i) s += p[i];
         return s;
     }
+}
+
+// Sum of item v over the CBW lanes of row group g (columns g*CBW .. g*CBW+CBW-1
+// of row v of a per-warp transpose scratch), in a fixed order.
+template <int CBW, int RST>
+__device__ __forceinline__ float rowgroup_sum(const float* red, int v, int g) {
+    const float* q = red + v * RST + g * CBW;
+    if constexpr (CBW == 8) {
+        const float4 x = ld4(q), y = ld4(q + 4);
+        return ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
+    } else {
+        static_assert(CBW == 4, "row groups of 4 or 8 lanes");
+        const float4 x = ld4(q);
+        return (x.x + x.y) + (x.z + x.w);
+    }
+}
+
+// Sum of item v over all 32 lanes of a per-warp transpose scratch.
+template <int RST>
+__device__ __forceinline__ float warp_row_sum(const float* red, int v) {
+    const float* q = red + v * RST;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 x = ld4(q + 4 * i);
+        acc[0] += x.x;
+        acc[1] += x.y;
+        acc[2] += x.z;
+        acc[3] += x.w;
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -581,10 +621,9 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
     constexpr int C2 = CA / 2;                    // float2 columns
     constexpr int NVV = 2 * CB * RA;              // z' and w' rows
     constexpr int NV = NVV + 2 * NP2;             // + Guu, Guk parts
-    constexpr int HR = C::CBA / 2;
-    constexpr int NOUT = rs_count<NV, HR>();
     static_assert(RA * C::NA * RPW == D && CA * C::CBA == D && CA % 4 == 0, "A layout");
     static_assert(C::CH % CB == 0, "steps stay inside a chunk");
+    static_assert(NV == LY::A_ROWS && 2 * NP2 <= 32, "A transpose scratch");
 
     const int wa = warp - LY::W_A0;
     const int cb = lane % C::CBA, rgl = lane / C::CBA;
@@ -721,32 +760,30 @@ __device__ __forceinline__ void a_role(const Params& p, const Smem& sm, int bh, 
                 }
         }
         if (tr0) VLA_TRACE_PT(p, 6, t);
-        reduce_scatter<NV, HR>(vals, lane);
-        // the Gram parts also need the sum over this warp's row groups
-        float sc[NOUT];
+        // reduce the row sums and Gram parts through this warp's transpose scratch:
+        // row v holds the 32 lanes' copies of item v
+        float* red = sm.ared + (size_t)wa * LY::A_ROWS * LY::RST;
+        __syncwarp();
 #pragma unroll
-        for (int j = 0; j < NOUT; ++j) sc[j] = vals[j];
-#pragma unroll
-        for (int h = C::CBA; h < 32; h <<= 1)
-#pragma unroll
-            for (int j = 0; j < NOUT; ++j) sc[j] += __shfl_xor_sync(0xffffffffu, sc[j], h);
-
+        for (int v = 0; v < NV; ++v) red[v * LY::RST + lane] = vals[v];
+        __syncwarp();
         const int zs = b % C::RZ;
         if (tr0) VLA_TRACE_PT(p, 7, t);
         if (!abort && !mbar_wait(sm.empty_z + zs, ((b / C::RZ) & 1) ^ 1, sm.abort, p.wait_ns)) abort = true;
         if (tr0) VLA_TRACE_PT(p, 8, t);
         float* Z = sm.zr + (size_t)zs * LY::ZSTRIDE;
+        // row items: lane (row group, cb) finishes items cb, cb + CBA, ... of its row group
 #pragma unroll
-        for (int j = 0; j < NOUT; ++j) {
-            const int idx = rs_index<NV, HR>(cb, j);
-            if (idx < 0) continue;
-            if (idx < NVV) {
-                const int vec = idx / RA, r = idx - vec * RA;
-                Z[vec * LY::VD + vidx<D>(row0 + r)] = vals[j];
-            } else if (rgl == 0) {
-                Z[LY::Z_SC + (idx - NVV) * LY::NA4 + wa] = sc[j];
+        for (int j = 0; j < (NVV + C::CBA - 1) / C::CBA; ++j) {
+            const int v = cb + j * C::CBA;
+            if (v < NVV) {
+                const float sum = rowgroup_sum<C::CBA, LY::RST>(red, v, rgl);
+                const int vec = v / RA, r = v - vec * RA;
+                Z[vec * LY::VD + vidx<D>(row0 + r)] = sum;
             }
         }
+        // Gram parts: lane l finishes item NVV + l over the whole warp
+        if (lane < 2 * NP2) Z[LY::Z_SC + lane * LY::NA4 + wa] = warp_row_sum<LY::RST>(red, NVV + lane);
         // the next step may start a new chunk
         if (t + CB < p.T) {
             const int t2 = t + CB, chunk2 = t2 / C::CH;
@@ -833,9 +870,8 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
     constexpr int RS = D / (C::NS * RPW);
     constexpr int CS = D / C::CBS;
     constexpr int C2 = CS / 2;
-    constexpr int HS = C::CBS / 2;
-    constexpr int NOUT = rs_count<RS, HS>();
     static_assert(RS * C::NS * RPW == D && CS * C::CBS == D && CS % 4 == 0, "S layout");
+    static_assert(RS <= C::CBS && 2 * RS + 1 == LY::S_ROWS, "S transpose scratch");
 
     const int ws = warp - LY::W_S0;
     const int cb = lane % C::CBS, rgl = lane / C::CBS;
@@ -880,21 +916,22 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
                 sq2[r] = __ffma2_rn(s[r][c4 / 2 + 1], qb, sq2[r]);
             }
         }
-        float sk[RS], sq[RS];
+        // reduce S k^ and S phi(q) through this warp's transpose scratch; lane cb < RS
+        // of a row group finishes row cb of it
+        float* red = sm.sred + (size_t)ws * LY::S_ROWS * LY::RST;
+        __syncwarp();
 #pragma unroll
         for (int r = 0; r < RS; ++r) {
-            sk[r] = sk2[r].x + sk2[r].y;
-            sq[r] = sq2[r].x + sq2[r].y;
+            red[r * LY::RST + lane] = sk2[r].x + sk2[r].y;
+            red[(RS + r) * LY::RST + lane] = sq2[r].x + sq2[r].y;
         }
-        // reduce both over the row group's lanes with one mapping: slot j of this
-        // lane holds row idx_j of S k^ and of S phi(q)
-        reduce_scatter<RS, HS>(sk, lane);
-        reduce_scatter<RS, HS>(sq, lane);
-        float ej[NOUT];
-#pragma unroll
-        for (int j = 0; j < NOUT; ++j) {
-            const int idx = rs_index<RS, HS>(cb, j);
-            ej[j] = idx >= 0 ? P[LY::P_V + row0 + idx] - sk[j] : 0.f;
+        __syncwarp();
+        const bool own = cb < RS;
+        float e_own = 0.f, sq_own = 0.f;
+        if (own) {
+            const float sk_own = rowgroup_sum<C::CBS, LY::RST>(red, cb, rgl);
+            sq_own = rowgroup_sum<C::CBS, LY::RST>(red, RS + cb, rgl);
+            e_own = P[LY::P_V + row0 + cb] - sk_own;
         }
 
         const int gs = t % C::RG;
@@ -906,18 +943,23 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
         const float st = G[LY::G_S];
         const float rden = __frcp_rn(P[LY::P_DEN]);
         // o_t = (S_{t-1} phi(q) + e (alpha^ . phi(q))) / den = S_t phi(q) / den
-#pragma unroll
-        for (int j = 0; j < NOUT; ++j) {
-            const int idx = rs_index<RS, HS>(cb, j);
-            if (idx >= 0) o[(size_t)t * D + row0 + idx] = fmaf(ej[j], st, sq[j]) * rden;
+        if (own) {
+            o[(size_t)t * D + row0 + cb] = fmaf(e_own, st, sq_own) * rden;
+            red[2 * RS * LY::RST + rgl * C::CBS + cb] = e_own;
         }
+        __syncwarp();
         // every lane of the row group needs the whole residual for the write
         float2 e2[RS];
-        const int gbase = lane & ~(C::CBS - 1);
+        {
+            const float* er = red + 2 * RS * LY::RST + rgl * C::CBS;
 #pragma unroll
-        for (int r = 0; r < RS; ++r) {
-            const float er = __shfl_sync(0xffffffffu, ej[rs_owner_slot<RS, HS>(r)], gbase | rs_owner_lane<RS, HS>(r));
-            e2[r] = f2(er, er);
+            for (int r4 = 0; r4 < RS; r4 += 4) {
+                const float4 x = ld4(er + r4);
+                const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (r4 + i < RS) e2[r4 + i] = f2(xs[i], xs[i]);
+            }
         }
 #pragma unroll
         for (int c4 = 0; c4 < CS; c4 += 4) {
@@ -972,6 +1014,8 @@ __global__ void __launch_bounds__(Layout<D, TIn>::THREADS, Cfg<D>::MINB) vla_fus
     sm.prep = reinterpret_cast<float*>(smem + LY::OFF_PREP);
     sm.zr = reinterpret_cast<float*>(smem + LY::OFF_Z);
     sm.gr = reinterpret_cast<float*>(smem + LY::OFF_G);
+    sm.ared = reinterpret_cast<float*>(smem + LY::OFF_ARED);
+    sm.sred = reinterpret_cast<float*>(smem + LY::OFF_SRED);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
