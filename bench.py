@@ -37,9 +37,9 @@ FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM (sm_103)
 FALLBACK_SM_MAX_MHZ = 2070.0
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch of vla_fused_kernel on the default workload, from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only while
-# the kernel sources hash to SOURCE_SHA; otherwise reported as null.
+# DRAM bytes per launch of the default workload's kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
+# sources hash to SOURCE_SHA; otherwise reported as null.
 NCU_TRAFFIC = {"source_sha": "7c3f25ace9bde484", "bytes_per_launch": 402754048 + 175918848}
 
 
@@ -243,7 +243,7 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
-        vla_forward(q, k, v, u, w.lambda0, w.eps, out=out)
+        vla_forward(q, k, v, u, w.lambda0, w.eps, out=out, algo=args.algo)
     st, detail = vla_get_last_device_status(dev)
     if st != VLA_OK:
         raise RuntimeError(f"device status {st} {detail} after warm-up")
@@ -258,7 +258,7 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(args.steps):
-            vla_forward(q, k, v, u, w.lambda0, w.eps, out=out)
+            vla_forward(q, k, v, u, w.lambda0, w.eps, out=out, algo=args.algo)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world, dev)
@@ -270,7 +270,8 @@ def run_ours(args, w):
     units = w.head_tokens
     value = aggregate_value(units, world, ms_max / 1e3)
 
-    # roofline of the one kernel (vla_fused_kernel) that a step launches
+    # roofline of the one kernel that a step launches
+    kernel = "vla_tc_kernel" if args.algo == 2 or (args.algo == 0 and d <= 96) else "vla_fused_kernel"
     peaks = load_peaks()
     sm_max = float(peaks.get("sm_max_mhz", FALLBACK_SM_MAX_MHZ))
     n_sm = props.multi_processor_count
@@ -291,12 +292,12 @@ def run_ours(args, w):
         hout = tuple(torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in out)
         ksteps = max(3, min(args.steps, args.e2e_steps))
         for _ in range(2):
-            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout)
+            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout, algo=args.algo)
         torch.cuda.synchronize(dev)
         barrier(world, dev)
         e0.record(stream)
         for _ in range(ksteps):
-            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout)
+            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout, algo=args.algo)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world, dev)
@@ -329,7 +330,7 @@ def run_ours(args, w):
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                          "frac": achieved / peak_tflops, "traffic": traffic,
                          "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FP32 FMA lanes x 2 x {sm_max:.0f} MHz",
-                         "flop_per_head_token": 12 * d * d, "kernel": "vla_fused_kernel"},
+                         "flop_per_head_token": 12 * d * d, "kernel": kernel},
             "fp32_roofline_pct": 100.0 * achieved / peak_tflops,
             "hbm": {"achieved_gbs": hbm_gbs, "peak_gbs": hbm_peak, "frac": hbm_gbs / hbm_peak,
                     "algorithmic_bytes_per_launch": in_bytes + out_bytes},
@@ -355,6 +356,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--algo", type=int, default=0,
+                    help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96), 1 per-token, 2 chunked")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -63,8 +63,19 @@ typedef struct {
                                     call reports VLA_ERR_TIMEOUT without faulting the GPU */
     unsigned long long* trace;   /* PROFILING ONLY, builds compiled with -DVLA_TRACE: device buffer
                                     of 16*T u64 that receives per-token SM clock stamps of head 0
-                                    (roles and sub-steps of the pipeline); else ignored */
+                                    (roles and sub-steps of the per-token kernel); else ignored */
+    int algo;                    /* VLA_ALGO_*: which kernel runs the recurrence (0 = automatic) */
 } vla_options;
+
+/* Kernels behind vla_forward_ex() (vla_options.algo). Both compute eq. 9-11
+ * exactly up to rounding order.
+ *   VLA_ALGO_AUTO       chunked tensor-core kernel for d <= 96, per-token kernel for d = 128
+ *   VLA_ALGO_PER_TOKEN  one token at a time on the FMA pipes (any supported d)
+ *   VLA_ALGO_CHUNKED    16 tokens at a time: the Sherman-Morrison steps of a chunk as an
+ *                       LDL^T factorisation, the d x d products on the tcgen05 tensor cores
+ *                       in 3-term tf32 (fp32 accuracy); d in {32, 64, 96}, else
+ *                       VLA_ERR_UNSUPPORTED. Any other value: VLA_ERR_INVALID_ARG. */
+enum { VLA_ALGO_AUTO = 0, VLA_ALGO_PER_TOKEN = 1, VLA_ALGO_CHUNKED = 2 };
 
 /* Bytes of device workspace vla_forward() needs (one status record). The
  * workspace must be zero-filled before its first use (cudaMemset or

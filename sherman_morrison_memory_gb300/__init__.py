@@ -22,6 +22,9 @@ from ._binding import (  # noqa: F401
     VLA_ERR_CUDA,
     VLA_ERR_TIMEOUT,
     VLA_ERR_NONFINITE,
+    VLA_ALGO_AUTO,
+    VLA_ALGO_PER_TOKEN,
+    VLA_ALGO_CHUNKED,
     VLAError,
     library_path,
     load_library,

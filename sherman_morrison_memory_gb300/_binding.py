@@ -21,6 +21,9 @@ VLA_ERR_UNSUPPORTED = 2
 VLA_ERR_CUDA = 3
 VLA_ERR_TIMEOUT = 4
 VLA_ERR_NONFINITE = 5
+VLA_ALGO_AUTO = 0
+VLA_ALGO_PER_TOKEN = 1
+VLA_ALGO_CHUNKED = 2
 
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
@@ -41,7 +44,7 @@ class VLAError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("wait_limit_us", ctypes.c_uint), ("test_stall_producer", ctypes.c_int),
-                ("trace", ctypes.c_void_p)]
+                ("trace", ctypes.c_void_p), ("algo", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -125,7 +128,8 @@ def _check_state(x, shape, device, name):
 
 def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tensor,
                 lambda0: float = 0.1, eps: float = 1e-4, state=None, *, out=None, stream=None,
-                check: bool = False, wait_limit_us: int = 0, test_stall_producer: bool = False):
+                check: bool = False, wait_limit_us: int = 0, test_stall_producer: bool = False,
+                algo: int = 0):
     """VLA forward recurrence (§3.3 eq. 9-11) over all heads.
 
     Returns ``(o, (S, A, zk))``: o [B,H,T,d] float32, S and A [B,H,d,d], zk [B,H,d].
@@ -133,9 +137,11 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
     ``out`` = (o, S, A, zk) preallocated outputs on the inputs' device.
     CPU inputs run on the current CUDA device with host<->device copies.
     ``check=True`` synchronises and raises on an in-kernel failure.
+    ``algo`` selects the kernel: VLA_ALGO_AUTO (0), VLA_ALGO_PER_TOKEN (1) or
+    VLA_ALGO_CHUNKED (2, the tensor-core chunked kernel, d <= 96).
     """
     if q.device.type == "cpu":
-        return _forward_host(q, k, v, u, lambda0, eps, state, out=out, check=check)
+        return _forward_host(q, k, v, u, lambda0, eps, state, out=out, check=check, algo=algo)
     lib = load_library()
     for name, x in (("k", k), ("v", v), ("u", u)):
         if x.shape != q.shape or x.dtype != q.dtype or x.device != q.device:
@@ -166,8 +172,8 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
         args = (_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d,
                 float(lambda0), float(eps), _ptr(S0), _ptr(A0), _ptr(zk0),
                 _ptr(o), _ptr(S), _ptr(A), _ptr(zk), _ptr(ws), ws.numel() * 4, ctypes.c_void_p(sh))
-        if wait_limit_us or test_stall_producer:
-            opts = _Options(int(wait_limit_us), 1 if test_stall_producer else 0, None)
+        if wait_limit_us or test_stall_producer or algo:
+            opts = _Options(int(wait_limit_us), 1 if test_stall_producer else 0, None, int(algo))
             st = lib.vla_forward_ex(*args, ctypes.byref(opts))
         else:
             st = lib.vla_forward(*args)
@@ -180,7 +186,7 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
     return o, (S, A, zk)
 
 
-def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False):
+def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False, algo=0):
     """Host buffers in, host buffers out: H2D copies, the kernel, D2H copies,
     all on the current stream of the current CUDA device. ``out`` may hold
     preallocated (pinned) host outputs (o, S, A, zk)."""
@@ -189,7 +195,7 @@ def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False):
     dstate = None
     if state is not None:
         dstate = tuple(None if x is None else x.to(dev, non_blocking=True) for x in state)
-    o, (S, A, zk) = vla_forward(dq, dk, dv, du, lambda0, eps, dstate, check=check)
+    o, (S, A, zk) = vla_forward(dq, dk, dv, du, lambda0, eps, dstate, check=check, algo=algo)
     pin = q.is_pinned()
     outs = []
     for i, x in enumerate((o, S, A, zk)):

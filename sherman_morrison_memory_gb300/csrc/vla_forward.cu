@@ -889,7 +889,7 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
     }
     float* o = p.o + (size_t)bh * p.T * D;
 
-    bool abort = false;
+    bool abort = false, nonfinite = false;
     int t = 0;
     for (; t < p.T; ++t) {
         const int chunk = t / C::CH, tc = t - chunk * C::CH, ps = chunk % C::NP;
@@ -944,7 +944,9 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
         const float rden = __frcp_rn(P[LY::P_DEN]);
         // o_t = (S_{t-1} phi(q) + e (alpha^ . phi(q))) / den = S_t phi(q) / den
         if (own) {
-            o[(size_t)t * D + row0 + cb] = fmaf(e_own, st, sq_own) * rden;
+            const float ov = fmaf(e_own, st, sq_own) * rden;
+            o[(size_t)t * D + row0 + cb] = ov;
+            if (!isfinite(ov)) nonfinite = true;
             red[2 * RS * LY::RST + rgl * C::CBS + cb] = e_own;
         }
         __syncwarp();
@@ -979,6 +981,7 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
             if (tc == C::CH - 1 || t == p.T - 1) mbar_arrive(sm.empty_p + ps);
         }
     }
+    if (nonfinite) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
     if (abort) {
         if (ws == 0 && lane == 0) record_failure(p.status, BIT_TIMEOUT, ROLE_S, bh, t);
         *sm.abort = 1;
@@ -1099,6 +1102,8 @@ __global__ void __launch_bounds__(LA_THREADS) la_state_kernel(const TIn* k, cons
         for (int b = 0; b < R; ++b) So[(size_t)(ti * R + a) * D + tj * R + b] = acc[a][b];
 }
 
+#include "vla_tc.cuh"
+
 }  // namespace vla
 
 // ===========================================================================
@@ -1122,8 +1127,29 @@ vla_status launch_fused(const vla::Params& p, int BH, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
 }
 
+template <int D, typename TIn>
+vla_status launch_tc(const vla::Params& p, int BH, cudaStream_t s) {
+    using LY = vla::tc::Lay<D, TIn>;
+    auto kern = vla::vla_tc_kernel<D, TIn>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::SMEM) != cudaSuccess)
+        return VLA_ERR_CUDA;
+    kern<<<BH, vla::tc::THREADS, LY::SMEM, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
+}
+
+// algo: VLA_ALGO_AUTO picks the chunked tensor-core kernel where it exists
+// (d <= 96) and the per-token kernel otherwise.
 template <typename TIn>
-vla_status launch_d(int d, const vla::Params& p, int BH, cudaStream_t s) {
+vla_status launch_d(int d, int algo, const vla::Params& p, int BH, cudaStream_t s) {
+    const bool chunked = algo == VLA_ALGO_CHUNKED || (algo == VLA_ALGO_AUTO && d <= 96);
+    if (chunked) {
+        switch (d) {
+            case 32: return launch_tc<32, TIn>(p, BH, s);
+            case 64: return launch_tc<64, TIn>(p, BH, s);
+            case 96: return launch_tc<96, TIn>(p, BH, s);
+            default: return VLA_ERR_UNSUPPORTED;
+        }
+    }
     switch (d) {
         case 32: return launch_fused<32, TIn>(p, BH, s);
         case 64: return launch_fused<64, TIn>(p, BH, s);
@@ -1203,8 +1229,13 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
     p.stall_producer = (opts && opts->test_stall_producer) ? 1 : 0;
     p.trace = opts ? opts->trace : nullptr;
 
+    const int algo = opts ? opts->algo : VLA_ALGO_AUTO;
+    if (algo != VLA_ALGO_AUTO && algo != VLA_ALGO_PER_TOKEN && algo != VLA_ALGO_CHUNKED) return VLA_ERR_INVALID_ARG;
+    if (algo == VLA_ALGO_CHUNKED && d > 96) return VLA_ERR_UNSUPPORTED;
+
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return dtype == VLA_BF16 ? launch_d<__nv_bfloat16>(d, p, (int)BH, s) : launch_d<float>(d, p, (int)BH, s);
+    return dtype == VLA_BF16 ? launch_d<__nv_bfloat16>(d, algo, p, (int)BH, s)
+                             : launch_d<float>(d, algo, p, (int)BH, s);
 }
 
 vla_status vla_forward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B, int H,

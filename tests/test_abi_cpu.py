@@ -87,3 +87,16 @@ def test_status_read_rejects_null(lib):
     d = (ctypes.c_int * 3)()
     assert lib.vla_get_last_device_status(None, None, d) == 1
     assert list(d) == [-1, -1, -1]
+
+
+@pytest.mark.parametrize("algo,d,status", [(3, 64, 1), (-1, 64, 1), (2, 128, 2)])
+def test_algo_argument_errors(lib, algo, d, status):
+    """VLA_ALGO_* outside {0, 1, 2} is an argument error; the chunked kernel
+    reports d = 128 as unsupported. Both are decided before any CUDA call."""
+    from sherman_morrison_memory_gb300 import _binding
+    vp = ctypes.c_void_p
+    opts = _binding._Options(0, 0, None, algo)
+    st = lib.vla_forward_ex(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 1, 1, 1, 4, d, ctypes.c_float(0.1),
+                            ctypes.c_float(1e-4), None, None, None, vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE),
+                            ctypes.c_size_t(256), None, ctypes.byref(opts))
+    assert st == status

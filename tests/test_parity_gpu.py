@@ -1,8 +1,10 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle.
 
-Small cases span several staged chunks (8 tokens each) and a ragged tail, every
-supported head dimension and both input dtypes; the five workloads run at
-full size. Tolerance: 2e-3 relative (parity_util.TOL) on o, final S, final A
+Small cases span several staged chunks (8 tokens for the per-token kernel, 16
+for the chunked tensor-core kernel) and a ragged tail, every supported head
+dimension, both input dtypes and both kernels (VLA_ALGO_PER_TOKEN and
+VLA_ALGO_CHUNKED; the default VLA_ALGO_AUTO picks the chunked one for
+d <= 96); the five workloads run at full size. Tolerance: 2e-3 relative (parity_util.TOL) on o, final S, final A
 and z^key, with the metric defined in parity_util.
 """
 import numpy as np
@@ -11,8 +13,9 @@ import torch
 
 import oracle
 from parity_util import TOL, assert_close, errors, rel_heads, rel_rows, to_dev
-from sherman_morrison_memory_gb300 import (VLA_ERR_NONFINITE, VLA_ERR_TIMEOUT, VLA_OK, vla_forward,
-                                           vla_get_last_device_status, vla_linear_attention_state)
+from sherman_morrison_memory_gb300 import (VLA_ALGO_CHUNKED, VLA_ALGO_PER_TOKEN, VLA_ERR_NONFINITE,
+                                           VLA_ERR_TIMEOUT, VLA_OK, vla_forward, vla_get_last_device_status,
+                                           vla_linear_attention_state)
 from sherman_morrison_memory_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -45,25 +48,53 @@ def _state_ref(state):
     return dict(S0=f(S0), A0=f(A0), zk0=f(zk0))
 
 
-def _run(orc, arrs, dtype, lambda0=0.1, eps=1e-4, state=None):
-    out = vla_forward(*to_dev(arrs, dtype), lambda0=lambda0, eps=eps, state=_state_dev(state), check=True)
+ALGOS = [VLA_ALGO_PER_TOKEN, VLA_ALGO_CHUNKED]
+
+
+def _algo_ok(algo, d):
+    return not (algo == VLA_ALGO_CHUNKED and d > 96)
+
+
+def _run(orc, arrs, dtype, lambda0=0.1, eps=1e-4, state=None, algo=0):
+    out = vla_forward(*to_dev(arrs, dtype), lambda0=lambda0, eps=eps, state=_state_dev(state), check=True,
+                      algo=algo)
     ref = orc.forward(*arrs, lambda0=lambda0, eps=eps, **_state_ref(state))
     return out, ref
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("d", [32, 64, 96, 128])
 @pytest.mark.parametrize("T", [1, 3, 9, 37, 200])
-def test_small_f32(orc, d, T):
+def test_small_f32(orc, d, T, algo):
+    if not _algo_ok(algo, d):
+        pytest.skip("the chunked kernel covers d <= 96")
     arrs = _inputs(1, 3, T, d, "f32", seed=d * 1000 + T)
-    out, ref = _run(orc, arrs, "f32")
-    assert_close(errors(out, ref), what=f"d={d} T={T} f32")
+    out, ref = _run(orc, arrs, "f32", algo=algo)
+    assert_close(errors(out, ref), what=f"d={d} T={T} f32 algo={algo}")
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("d", [32, 64, 96, 128])
-def test_small_bf16(orc, d):
+def test_small_bf16(orc, d, algo):
+    if not _algo_ok(algo, d):
+        pytest.skip("the chunked kernel covers d <= 96")
     arrs = _inputs(2, 2, 45, d, "bf16", seed=d)
-    out, ref = _run(orc, arrs, "bf16")
-    assert_close(errors(out, ref), what=f"d={d} bf16")
+    out, ref = _run(orc, arrs, "bf16", algo=algo)
+    assert_close(errors(out, ref), what=f"d={d} bf16 algo={algo}")
+
+
+@pytest.mark.parametrize("d", [32, 64, 96])
+def test_kernels_agree(orc, d):
+    """Per-token and chunked kernels on the same inputs: many 16-token chunks
+    plus a ragged tail; each within tolerance of the oracle and of each other."""
+    arrs = _inputs(2, 3, 16 * 23 + 5, d, "bf16", seed=70 + d)
+    (o1, st1), ref = _run(orc, arrs, "bf16", algo=VLA_ALGO_PER_TOKEN)
+    (o2, st2), _ = _run(orc, arrs, "bf16", algo=VLA_ALGO_CHUNKED)
+    assert_close(errors((o1, st1), ref), what="per-token")
+    assert_close(errors((o2, st2), ref), what="chunked")
+    assert rel_rows(o2.cpu().numpy(), o1.cpu().numpy().astype(np.float64)) <= TOL
+    for a, b in zip(st2, st1):
+        assert rel_heads(a.cpu().numpy(), b.cpu().numpy().astype(np.float64)) <= TOL
 
 
 @pytest.mark.parametrize("d", [32, 96])
@@ -84,8 +115,11 @@ def test_zero_tokens_returns_initial_state(orc, d):
 
 
 @pytest.mark.parametrize("d", [64, 96, 128])
-def test_carried_state_chunks(orc, d):
+@pytest.mark.parametrize("algo", ALGOS)
+def test_carried_state_chunks(orc, d, algo):
     """Calls over [0, t1), [t1, t2), [t2, T) with carried (S, A, z^key) match the oracle's one-shot run."""
+    if not _algo_ok(algo, d):
+        pytest.skip("the chunked kernel covers d <= 96")
     T, cuts = 150, (13, 64)
     arrs = _inputs(2, 2, T, d, "bf16", seed=7 + d)
     warm = orc.forward(*_inputs(2, 2, 40, d, "bf16", seed=99))
@@ -96,22 +130,24 @@ def test_carried_state_chunks(orc, d):
     bounds = (0,) + cuts + (T,)
     for a, b in zip(bounds[:-1], bounds[1:]):
         part = to_dev([x[:, :, a:b] for x in arrs], "bf16")
-        o, state = vla_forward(*part, state=state, check=True)
+        o, state = vla_forward(*part, state=state, check=True, algo=algo)
         outs.append(o)
     o = torch.cat(outs, dim=2)
-    assert_close(errors((o, state), ref), what=f"chunked d={d}")
+    assert_close(errors((o, state), ref), what=f"chunked d={d} algo={algo}")
 
 
-def test_decode_one_token_at_a_time(orc):
+@pytest.mark.parametrize("algo", ALGOS)
+def test_decode_one_token_at_a_time(orc, algo):
     d, T = 64, 20
     arrs = _inputs(1, 2, T, d, "f32", seed=5)
     ref = orc.forward(*arrs)
     state = None
     outs = []
     for t in range(T):
-        o, state = vla_forward(*to_dev([x[:, :, t:t + 1] for x in arrs], "f32"), state=state, check=True)
+        o, state = vla_forward(*to_dev([x[:, :, t:t + 1] for x in arrs], "f32"), state=state, check=True,
+                               algo=algo)
         outs.append(o)
-    assert_close(errors((torch.cat(outs, dim=2), state), ref), what="decode")
+    assert_close(errors((torch.cat(outs, dim=2), state), ref), what=f"decode algo={algo}")
 
 
 def test_lambda_and_eps(orc):
@@ -121,7 +157,8 @@ def test_lambda_and_eps(orc):
 
 
 @pytest.mark.parametrize("case", ["zero_key", "zero_u", "zero_v", "den_floor", "large"])
-def test_edge_inputs(orc, case):
+@pytest.mark.parametrize("algo", ALGOS)
+def test_edge_inputs(orc, case, algo):
     d, T = 96, 40
     q, k, v, u = _inputs(1, 2, T, d, "f32", seed=17)
     if case == "zero_key":
@@ -135,7 +172,7 @@ def test_edge_inputs(orc, case):
         q = (q - 60.0).astype(np.float32)
     elif case == "large":
         q, k, v, u = (x * np.float32(300.0) for x in (q, k, v, u))
-    out, ref = _run(orc, (q, k, v, u), "f32")
+    out, ref = _run(orc, (q, k, v, u), "f32", algo=algo)
     if case == "zero_v":
         o, (S, A, zk) = out
         assert torch.all(o == 0) and torch.all(S == 0)
@@ -169,23 +206,26 @@ def test_linear_attention_state(orc):
     assert rel_heads(S.cpu().numpy(), want) < 1e-4
 
 
-def test_timeout_is_reported_and_context_survives(orc):
+@pytest.mark.parametrize("algo", ALGOS)
+def test_timeout_is_reported_and_context_survives(orc, algo):
     """A stalled staging warp makes every consumer's bounded wait run out; the
     call reports VLA_ERR_TIMEOUT and the next call on the same context works."""
     arrs = _inputs(1, 2, 64, 96, "f32", seed=11)
-    vla_forward(*to_dev(arrs, "f32"), wait_limit_us=20000, test_stall_producer=True)
+    vla_forward(*to_dev(arrs, "f32"), wait_limit_us=20000, test_stall_producer=True, algo=algo)
     st, detail = vla_get_last_device_status()
     assert st == VLA_ERR_TIMEOUT, (st, detail)
     assert detail[0] in (1, 2, 3)
-    out, ref = _run(orc, arrs, "f32")
+    out, ref = _run(orc, arrs, "f32", algo=algo)
     assert_close(errors(out, ref), what="after timeout")
     assert vla_get_last_device_status()[0] == VLA_OK
 
 
-def test_nonfinite_input_is_reported():
-    arrs = _inputs(1, 1, 16, 64, "f32", seed=12)
-    arrs[0][0, 0, 7, 3] = np.nan
-    vla_forward(*to_dev(arrs, "f32"))
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("tensor", [0, 1, 2, 3])
+def test_nonfinite_input_is_reported(algo, tensor):
+    arrs = _inputs(1, 1, 40, 64, "f32", seed=12)
+    arrs[tensor][0, 0, 7, 3] = np.nan
+    vla_forward(*to_dev(arrs, "f32"), algo=algo)
     st, _ = vla_get_last_device_status()
     assert st == VLA_ERR_NONFINITE
 
