@@ -54,20 +54,23 @@ struct Lay {
     static constexpr int LO_ROWS = F32IN ? 3 * C : C;
     static constexpr int SBO_D = (D / 4) * 128;   // bytes between 8-row groups, rows of D
     static constexpr int SBO_C = (C / 4) * 128;   // rows of C
-    static constexpr int SC_IU = 0, SC_IK = C, SC_DEN = 2 * C;  // per-token scalars
+    static constexpr int SC_IU = 0, SC_IK = C, SC_RDEN = 2 * C;  // per-token scalars: 1/||u||, 1/||k||, 1/den
     static constexpr int SLOT = (HI_ROWS + LO_ROWS) * D + 64;   // floats
     static constexpr int SCR_STRIDE = D + 4;
     static constexpr int GSTR = C + 4;            // row stride of the small C x C matrices (16-byte rows)
     static constexpr int XS = D + 4;              // row stride of the row-major d-vectors (z' | w, a)
 
     // TMEM columns
-    static constexpr uint32_t T_A = 0, T_AL = D, T_S = 2 * D, T_SL = 3 * D, T_XA = 4 * D, T_XS = 4 * D + 2 * C;
-    static constexpr uint32_t TCOLS = (4 * D + 4 * C) <= 256 ? 256 : 512;
-    static_assert(4 * D + 4 * C <= 512, "TMEM columns");
+    // (the chunk products [A u | A k] and [S k | S phi] accumulate their even
+    // and odd K steps in two column blocks each, summed when read)
+    static constexpr uint32_t T_A = 0, T_AL = D, T_S = 2 * D, T_SL = 3 * D, T_XA = 4 * D, T_XS = 4 * D + 2 * C,
+                              T_XA2 = 4 * D + 4 * C, T_XS2 = 4 * D + 6 * C;
+    static constexpr uint32_t TCOLS = (4 * D + 8 * C) <= 256 ? 256 : 512;
+    static_assert(4 * D + 8 * C <= 512, "TMEM columns");
 
     // shared memory map (bytes)
     static constexpr size_t al(size_t x) { return (x + 127) / 128 * 128; }
-    static constexpr int NBAR = NRAW + 2 * NP + 4 + 2;
+    static constexpr int NBAR = NRAW + 2 * NP + 4 + 4;
     static constexpr size_t OFF_BAR = 0;
     static constexpr size_t OFF_MISC = al(8 * NBAR);             // abort flag, TMEM base
     static constexpr size_t OFF_PREP = al(OFF_MISC + 16);
@@ -103,8 +106,10 @@ struct Bars {
     uint64_t* empty_p;   // [NP] released by both teams (count 2)
     uint64_t* full_al;   // [2] A team published a rows / a^T operands of a chunk
     uint64_t* empty_al;  // [2] S team done with them
-    uint64_t* mma_a;     // A-team tcgen05 commits
-    uint64_t* mma_s;     // S-team tcgen05 commits
+    uint64_t* mma_a;     // A-team tcgen05 commits (state update)
+    uint64_t* mma_s;     // S-team tcgen05 commits (state update)
+    uint64_t* mma_xa;    // [A u | A k] issued by two A warps (count 2)
+    uint64_t* mma_xs;    // [S k | S phi] issued by two S warps (count 2)
 };
 
 template <int D, typename TIn>
@@ -168,14 +173,12 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
     bool bad = false;
     for (c = 0; c < nch; ++c) {
         const int s = c % L::NP, rs = c % L::NRAW, n = min(C, T - c * C);
-        if (leader) VLA_TRACE_AT(p, 0, c);
         bool ok = c < L::NP || mbar_wait(x.b.empty_p + s, ((c / L::NP) & 1) ^ 1, x.abort, p.wait_ns);
         ok = ok && mbar_wait(x.b.full_r + rs, (c / L::NRAW) & 1, x.abort, p.wait_ns);
         if (bar_red_or(ID_ST, 32 * NSTAGE, !ok || *x.abort != 0)) {
             bad = true;
             break;
         }
-        if (leader) VLA_TRACE_AT(p, 2, c);
         const TIn* rq = reinterpret_cast<const TIn*>(x.raw(rs));
         const TIn* rk = reinterpret_cast<const TIn*>(x.raw(rs) + L::RAW_T);
         const TIn* ru = reinterpret_cast<const TIn*>(x.raw(rs) + 2 * L::RAW_T);
@@ -237,7 +240,7 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
             const int t = sw * TW + lane;
             sc[L::SC_IU + t] = t < n ? rsqrtf(fmaxf(r0, 1e-24f)) : 0.f;
             sc[L::SC_IK + t] = t < n ? rsqrtf(fmaxf(r1, 1e-24f)) : 0.f;
-            sc[L::SC_DEN + t] = t < n ? fmaxf(r2, p.eps) : 1.f;
+            sc[L::SC_RDEN + t] = t < n ? __frcp_rn(fmaxf(r2, p.eps)) : 1.f;  // 1 / den
         }
         named_bar(ID_ST, 32 * NSTAGE);
         // scratch rows -> operand tiles, one 8-row group per unit: lane =
@@ -406,6 +409,32 @@ __device__ __forceinline__ void put_gram16(float* G, int gs, const float (&acc)[
         }
 }
 
+// Sum of the gram16 partials of a warp pair (halves 0 and 1 of D): half 1
+// stores its accumulators in the scratch copy G + ms, the pair meets at named
+// barrier `bar_id` (64 threads), half 0 adds them and stores the result
+// (scaled by rs[row] if rs) to G[row][col] (transposed if asked).
+__device__ __forceinline__ void gram_pair_sum(float* G, int ms, int gs, float (&acc)[2][4], int lane, int half,
+                                              int bar_id, const float* rs, bool transpose) {
+    float* part = G + ms + lane * 8;
+    if (half) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+            *reinterpret_cast<float4*>(part + 4 * n) = make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
+    }
+    named_bar(bar_id, 64);
+    if (!half) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const float4 o = ld4(part + 4 * n);
+            acc[n][0] += o.x;
+            acc[n][1] += o.y;
+            acc[n][2] += o.z;
+            acc[n][3] += o.w;
+        }
+        put_gram16(G, gs, acc, lane, rs, transpose);
+    }
+}
+
 // 16 values -> four float4 stores at the K-major operand positions (row, 0..15)
 // of a tile with rows of C elements; `lo` selects the tf32 lo parts
 __device__ __forceinline__ void put_row16(float* tile, int row, const float (&v)[C], bool lo) {
@@ -492,34 +521,37 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         if (ta == 0) VLA_TRACE_AT(p, 4, c);
         const float* hi = x.hi(s);
         const float* sc = x.sc(s);
-        // [Z' | W] = A_c [u | k]^T (rows u, k of the chunk; scaled by 1/||.|| below)
-        if (ta == 0) {
+        // [Z' | W] = A_c [u | k]^T (rows u, k of the chunk; scaled by 1/||.|| below);
+        // warps 0 and 1 issue the even and odd K steps into separate accumulators
+        if (lane == 0 && warp < 2) {
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, 2 * C);
             const uint32_t bh0 = smem_u32(hi), bl0 = smem_u32(x.lo(s));
 #pragma unroll 1
-            for (int ks = 0; ks < D / 8; ++ks) {
+            for (int ks = warp; ks < D / 8; ks += 2) {
+                const uint32_t dst = tm + ((ks & 1) ? L::T_XA2 : L::T_XA);
                 const uint64_t bd = tc_sdesc(bh0 + ks * 256, 128, L::SBO_D);
-                tc_mma_ts(tm + L::T_XA, tm + L::T_A + 8 * ks, bd, id, ks > 0);
-                tc_mma_ts(tm + L::T_XA, tm + L::T_AL + 8 * ks, bd, id, 1);
+                tc_mma_ts(dst, tm + L::T_A + 8 * ks, bd, id, ks > 1);
+                tc_mma_ts(dst, tm + L::T_AL + 8 * ks, bd, id, 1);
                 if constexpr (L::F32IN)
-                    tc_mma_ts(tm + L::T_XA, tm + L::T_A + 8 * ks, tc_sdesc(bl0 + ks * 256, 128, L::SBO_D), id, 1);
+                    tc_mma_ts(dst, tm + L::T_A + 8 * ks, tc_sdesc(bl0 + ks * 256, 128, L::SBO_D), id, 1);
             }
-            tc_commit(x.b.mma_a);
+            tc_commit(x.b.mma_xa);
         }
-        bool ok = mbar_wait(x.b.mma_a, pa, nullptr, p.wait_ns);
-        pa ^= 1;
+        bool ok = mbar_wait(x.b.mma_xa, c & 1, nullptr, p.wait_ns);
         if (ta == 0) VLA_TRACE_AT(p, 5, c);
         tc_fence_after();
         if (rw) {
-            float v0[16], v1[16];
+            float v0[16], v1[16], v2[16], v3[16];
             tc_ld16(tl + L::T_XA, v0);
             tc_ld16(tl + L::T_XA + C, v1);
+            tc_ld16(tl + L::T_XA2, v2);
+            tc_ld16(tl + L::T_XA2 + C, v3);
             tc_wait_ld();
 #pragma unroll
             for (int t = 0; t < C; ++t) {
-                v0[t] *= sc[L::SC_IU + t];  // z'_t = A_c u^_t
-                v1[t] *= sc[L::SC_IK + t];  // w_t = A_c k^_t
+                v0[t] = (v0[t] + v2[t]) * sc[L::SC_IU + t];  // z'_t = A_c u^_t
+                v1[t] = (v1[t] + v3[t]) * sc[L::SC_IK + t];  // w_t = A_c k^_t
                 xr[t * XS + i] = v0[t];
                 xr[(C + t) * XS + i] = v1[t];
             }
@@ -527,12 +559,14 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             put_row16(zl, i, v0, true);
         }
         named_bar(ID_A, 128);
-        // Guu[s][t] = u^_s . z'_t, Guk[s][t] = u^_s . w_t; warp = (matrix, half of D)
+        // Guu[s][t] = u^_s . z'_t, Guk[s][t] = u^_s . w_t; warp = (matrix, half of D),
+        // the half-D partials of a warp pair summed through shared memory
         {
             const int mat = warp & 1, half = warp >> 1;
             float acc[2][4];
             gram16<D, true>(hi, 0, xr + mat * C * XS, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc);
-            put_gram16(sm + (mat ? L::SM_GUK : L::SM_GUU) + half * L::MS, L::GSTR, acc, lane, sc + L::SC_IU, false);
+            gram_pair_sum(sm + (mat ? L::SM_GUK : L::SM_GUU), L::MS, L::GSTR, acc, lane, half, 4 + mat,
+                          sc + L::SC_IU, false);
         }
         named_bar(ID_A, 128);
         if (ta == 0) VLA_TRACE_AT(p, 6, c);
@@ -547,8 +581,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             const float* src = sm + (mcol ? L::SM_GUU : L::SM_GUK);
             float col[C];
 #pragma unroll
-            for (int r = 0; r < C; ++r)
-                col[r] = (src[r * L::GSTR + j] + src[L::MS + r * L::GSTR + j]) + ((mcol && r == j) ? 1.f : 0.f);
+            for (int r = 0; r < C; ++r) col[r] = src[r * L::GSTR + j] + ((mcol && r == j) ? 1.f : 0.f);
             float myrd = 0.f;
 #pragma unroll 16
             for (int t = 0; t < C; ++t) {
@@ -767,38 +800,40 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         if (ts == 0) VLA_TRACE_AT(p, 11, c);
         const float* alr = x.f(L::OFF_AL) + (size_t)b * C * XS;
         // [S_c k | S_c phi] (rows k, phi of the chunk)
-        if (ts == 0) {
+        if (lane == 0 && wq < 2) {
             tc_fence_after();
             const uint32_t id32 = tc_idesc_tf32(128, 2 * C), id16 = tc_idesc_tf32(128, C);
             const uint32_t bh0 = smem_u32(hi) + 2 * L::SBO_D;
             const uint32_t bl0 = smem_u32(x.lo(s)) + (L::F32IN ? 2 * L::SBO_D : 0);
 #pragma unroll 1
-            for (int ks = 0; ks < D / 8; ++ks) {
+            for (int ks = wq; ks < D / 8; ks += 2) {
+                const uint32_t dst = tm + ((ks & 1) ? L::T_XS2 : L::T_XS);
                 const uint64_t bd = tc_sdesc(bh0 + ks * 256, 128, L::SBO_D);
                 const uint64_t bld = tc_sdesc(bl0 + ks * 256, 128, L::SBO_D);
-                tc_mma_ts(tm + L::T_XS, tm + L::T_S + 8 * ks, bd, id32, ks > 0);
-                tc_mma_ts(tm + L::T_XS, tm + L::T_SL + 8 * ks, bd, id32, 1);
+                tc_mma_ts(dst, tm + L::T_S + 8 * ks, bd, id32, ks > 1);
+                tc_mma_ts(dst, tm + L::T_SL + 8 * ks, bd, id32, 1);
                 if constexpr (L::F32IN)
-                    tc_mma_ts(tm + L::T_XS, tm + L::T_S + 8 * ks, bld, id32, 1);
+                    tc_mma_ts(dst, tm + L::T_S + 8 * ks, bld, id32, 1);
                 else
-                    tc_mma_ts(tm + L::T_XS + C, tm + L::T_S + 8 * ks, bld, id16, 1);
+                    tc_mma_ts(dst + C, tm + L::T_S + 8 * ks, bld, id16, 1);
             }
-            tc_commit(x.b.mma_s);
+            tc_commit(x.b.mma_xs);
         }
-        bool ok = mbar_wait(x.b.mma_s, ps, nullptr, p.wait_ns);
-        ps ^= 1;
+        bool ok = mbar_wait(x.b.mma_xs, c & 1, nullptr, p.wait_ns);
         if (ts == 0) VLA_TRACE_AT(p, 12, c);
         tc_fence_after();
         float sk[C], sq[C];
         if (rw) {
-            float v0[16], v1[16];
+            float v0[16], v1[16], v2[16], v3[16];
             tc_ld16(tl + L::T_XS, v0);
             tc_ld16(tl + L::T_XS + C, v1);
+            tc_ld16(tl + L::T_XS2, v2);
+            tc_ld16(tl + L::T_XS2 + C, v3);
             tc_wait_ld();
 #pragma unroll
             for (int t = 0; t < C; ++t) {
-                sk[t] = v0[t] * sc[L::SC_IK + t];  // S_c k^_t
-                sq[t] = v1[t];                     // S_c phi_t
+                sk[t] = (v0[t] + v2[t]) * sc[L::SC_IK + t];  // S_c k^_t
+                sq[t] = v1[t] + v3[t];                        // S_c phi_t
             }
         }
         // Lk[t][s] = k^_t . a_s, Lq[t][s] = phi_t . a_s; warp = (matrix, half of D)
@@ -807,9 +842,9 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             float acc[2][4];
             gram16<D, true>(hi + (mat ? 32 : 16) * D, 0, alr, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc);
             if (mat)
-                put_gram16(sm + L::SM_LQ + half * L::MS, L::GSTR, acc, lane, nullptr, false);
+                gram_pair_sum(sm + L::SM_LQ, L::MS, L::GSTR, acc, lane, half, 6 + mat, nullptr, false);
             else
-                put_gram16(sm + L::SM_LKT + half * L::MS, L::GSTR, acc, lane, sc + L::SC_IK, true);
+                gram_pair_sum(sm + L::SM_LKT, L::MS, L::GSTR, acc, lane, half, 6 + mat, sc + L::SC_IK, true);
         }
         named_bar(ID_S, 128);
         if (ts == 0) VLA_TRACE_AT(p, 13, c);
@@ -827,29 +862,27 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             for (int r = 0; r < C; ++r) {
                 vv[r] *= nr[r];
                 if (r < C - 1) {
-                    float l2[C];
                     ld_row16(sm + L::SM_LKT + r * L::GSTR, lr);  // Lk[t][r], t > r
-                    ld_row16(sm + L::SM_LKT + L::MS + r * L::GSTR, l2);
 #pragma unroll
-                    for (int t = r + 1; t < C; ++t) vv[t] = fmaf(-(lr[t] + l2[t]), vv[r], vv[t]);
+                    for (int t = r + 1; t < C; ++t) vv[t] = fmaf(-lr[t], vv[r], vv[t]);
                 }
             }
+            if (ts == 0) VLA_TRACE_AT(p, 0, c);
             // o_t = (S_c phi_t + sum_{s<=t} e_s (alpha^_s . phi_t)) / den_t = S_t phi_t / den_t (eq. 11)
-            ld_row16(sc + L::SC_DEN, nr);
+            ld_row16(sc + L::SC_RDEN, nr);
 #pragma unroll
             for (int t = 0; t < C; ++t) {
-                float l2[C];
                 ld_row16(sm + L::SM_LQ + t * L::GSTR, lr);
-                ld_row16(sm + L::SM_LQ + L::MS + t * L::GSTR, l2);
                 float a = sq[t];
 #pragma unroll
-                for (int q = 0; q <= t; ++q) a = fmaf(lr[q] + l2[q], vv[q], a);
-                const float ov = a * __frcp_rn(nr[t]);
+                for (int q = 0; q <= t; ++q) a = fmaf(lr[q], vv[q], a);
+                const float ov = a * nr[t];
                 if (t < n) {
                     go[(size_t)(c * C + t) * D + i] = ov;
                     if (!isfinite(ov)) nonfinite = true;
                 }
             }
+            if (ts == 0) VLA_TRACE_AT(p, 2, c);
             put_row16(eh, i, vv, false);
             put_row16(el, i, vv, true);
         }
@@ -923,6 +956,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1) vla_tc_kernel(const Params p) 
     x.b.empty_al = x.b.full_al + 2;
     x.b.mma_a = x.b.empty_al + 2;
     x.b.mma_s = x.b.mma_a + 1;
+    x.b.mma_xa = x.b.mma_s + 1;
+    x.b.mma_xs = x.b.mma_xa + 1;
     x.abort = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
     x.tmem_base = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC + 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -939,6 +974,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1) vla_tc_kernel(const Params p) 
         }
         mbar_init(x.b.mma_a, 1);
         mbar_init(x.b.mma_s, 1);
+        mbar_init(x.b.mma_xa, 2);
+        mbar_init(x.b.mma_xs, 2);
         *x.abort = 0;
         fence_mbar_init();
     }
