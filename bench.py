@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch of the default workload's kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
 # sources hash to SOURCE_SHA; otherwise reported as null.
-NCU_TRAFFIC = {"source_sha": "7c3f25ace9bde484", "bytes_per_launch": 402754048 + 175918848}
+NCU_TRAFFIC = {"source_sha": "757966978bd67c06", "bytes_per_launch": 402742272 + 175727360}
 
 
 def kernel_source_sha() -> str:

@@ -626,9 +626,11 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         float* alr = x.f(L::OFF_AL) + (size_t)b * C * XS;
         float* gh = x.f(L::OFF_GH) + (size_t)b * D * C;
         float* gl = x.f(L::OFF_GL) + (size_t)b * D * C;
+        // the -M operand first: the state update is issued before the gate,
+        // which only the S team needs, is computed
+        float y[C], lr[C];
         if (rw) {
             // y = z_i = z'_i L^-T (forward substitution, in place), then y D^-1
-            float y[C], lr[C];
 #pragma unroll
             for (int t = 0; t < C; ++t) y[t] = xr[t * XS + i];
 #pragma unroll
@@ -641,21 +643,40 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
 #pragma unroll
             for (int t = 0; t < C; ++t) y[t] *= lr[t];
             // m_i = (z_i D^-1) L^-1 (backward substitution); the operand is -m_i
-            {
-                float mv[C];
+            float mv[C];
 #pragma unroll
-                for (int t = 0; t < C; ++t) mv[t] = y[t];
+            for (int t = 0; t < C; ++t) mv[t] = y[t];
 #pragma unroll
-                for (int r = C - 1; r >= 1; --r) {
-                    ld_row16(sm + L::SM_LM + r * L::GSTR, lr);  // L[r][t], t < r
+            for (int r = C - 1; r >= 1; --r) {
+                ld_row16(sm + L::SM_LM + r * L::GSTR, lr);  // L[r][t], t < r
 #pragma unroll
-                    for (int t = 0; t < r; ++t) mv[t] = fmaf(-lr[t], mv[r], mv[t]);
-                }
-#pragma unroll
-                for (int t = 0; t < C; ++t) mv[t] = -mv[t];
-                put_row16(ph, i, mv, false);
-                put_row16(pl, i, mv, true);
+                for (int t = 0; t < r; ++t) mv[t] = fmaf(-lr[t], mv[r], mv[t]);
             }
+#pragma unroll
+            for (int t = 0; t < C; ++t) mv[t] = -mv[t];
+            put_row16(ph, i, mv, false);
+            put_row16(pl, i, mv, true);
+        }
+        fence_proxy_async_smem();
+        named_bar(ID_A, 128);
+        // A_{c+1} = A_c - M Z'^T
+        if (ta == 0) {
+            VLA_TRACE_AT(p, 8, c);
+            tc_fence_after();
+            const uint32_t id = tc_idesc_tf32(128, D);
+#pragma unroll
+            for (int ks = 0; ks < C / 8; ++ks) {
+                const uint64_t ah = tc_sdesc(smem_u32(ph) + ks * 256, 128, L::SBO_C);
+                const uint64_t alo = tc_sdesc(smem_u32(pl) + ks * 256, 128, L::SBO_C);
+                const uint64_t bhd = tc_sdesc(smem_u32(zh) + ks * 256, 128, L::SBO_C);
+                const uint64_t bld = tc_sdesc(smem_u32(zl) + ks * 256, 128, L::SBO_C);
+                tc_mma_ss(tm + L::T_A, ah, bhd, id, 1);
+                tc_mma_ss(tm + L::T_A, ah, bld, id, 1);
+                tc_mma_ss(tm + L::T_A, alo, bhd, id, 1);
+            }
+            tc_commit(x.b.mma_a);
+        }
+        if (rw) {
             // a_t = A_t k^_t = w_t - sum_{s<=t} z_s (z_s . k^_t) / delta_s (eq. 10)
             float av[C];
 #pragma unroll
@@ -686,23 +707,6 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(x.b.full_al + b);
-        }
-        // A_{c+1} = A_c - M Z'^T
-        if (ta == 0) {
-            VLA_TRACE_AT(p, 8, c);
-            tc_fence_after();
-            const uint32_t id = tc_idesc_tf32(128, D);
-#pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks) {
-                const uint64_t ah = tc_sdesc(smem_u32(ph) + ks * 256, 128, L::SBO_C);
-                const uint64_t alo = tc_sdesc(smem_u32(pl) + ks * 256, 128, L::SBO_C);
-                const uint64_t bhd = tc_sdesc(smem_u32(zh) + ks * 256, 128, L::SBO_C);
-                const uint64_t bld = tc_sdesc(smem_u32(zl) + ks * 256, 128, L::SBO_C);
-                tc_mma_ss(tm + L::T_A, ah, bhd, id, 1);
-                tc_mma_ss(tm + L::T_A, ah, bld, id, 1);
-                tc_mma_ss(tm + L::T_A, alo, bhd, id, 1);
-            }
-            tc_commit(x.b.mma_a);
         }
         bad = !mbar_wait(x.b.mma_a, pa, nullptr, p.wait_ns);
         pa ^= 1;
