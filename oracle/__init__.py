@@ -79,6 +79,13 @@ class Oracle:
         g = self.lib.vla_oracle_linear_attention_state
         g.restype = ctypes.c_int
         g.argtypes = [ctypes.c_int] * 3 + [_fp] * 2 + [_dp, ctypes.c_int]
+        h = self.lib.vla_oracle_forward_f64
+        h.restype = ctypes.c_int
+        h.argtypes = [ctypes.c_int] * 3 + [_dp] * 4 + [ctypes.c_double] * 2 + [_dp] * 3 + [_dp] * 4
+        b = self.lib.vla_oracle_backward
+        b.restype = ctypes.c_int
+        b.argtypes = ([ctypes.c_int] * 3 + [_dp] * 4 + [ctypes.c_double] * 2 + [_dp] * 3 + [_dp] * 4
+                      + [_dp] * 4 + [_dp] * 3 + [ctypes.c_int])
 
     def forward(self, q, k, v, u, lambda0=0.1, eps=1e-4, S0=None, A0=None, zk0=None,
                 want_o=True, trace=False, threads=0) -> OracleResult:
@@ -117,6 +124,41 @@ class Oracle:
             _ptr(tr.get("delta"), _dp), _ptr(tr.get("alpha"), _dp), _ptr(tr.get("khat"), _dp),
             _ptr(tr.get("uhat"), _dp), _ptr(tr.get("e"), _dp), int(threads))
         return OracleResult(o=o, S=S, A=A, zk=zk, threads=n, **tr)
+
+    def forward_f64(self, q, k, v, u, lambda0=0.1, eps=1e-4, S0=None, A0=None, zk0=None):
+        """The recurrence with fp64 inputs (for finite-difference checks):
+        returns (o, S, A, zk) as fp64 arrays shaped like the inputs."""
+        q, k, v, u = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, u))
+        lead = q.shape[:-2]
+        T, d = q.shape[-2], q.shape[-1]
+        BH = int(np.prod(lead)) if lead else 1
+        f = lambda x: None if x is None else np.ascontiguousarray(x, dtype=np.float64)
+        o, S, A, zk = np.empty(lead + (T, d)), np.empty(lead + (d, d)), np.empty(lead + (d, d)), np.empty(lead + (d,))
+        self.lib.vla_oracle_forward_f64(BH, T, d, _ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(u, _dp),
+                                        float(lambda0), float(eps), _ptr(f(S0), _dp), _ptr(f(A0), _dp),
+                                        _ptr(f(zk0), _dp), _ptr(o, _dp), _ptr(S, _dp), _ptr(A, _dp), _ptr(zk, _dp))
+        return o, S, A, zk
+
+    def backward(self, q, k, v, u, lambda0=0.1, eps=1e-4, S0=None, A0=None, zk0=None,
+                 gO=None, gS=None, gA=None, gzk=None, threads=0):
+        """Reverse-mode gradient of the recurrence (fp64) for the loss seeds
+        gO = dL/do [..., T, d] and gS, gA = dL/dS_T, dL/dA_T [..., d, d], gzk =
+        dL/dz^key_T [..., d] (each optional). Returns dict dq, dk, dv, du,
+        dS0, dA0, dzk0."""
+        q, k, v, u = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, u))
+        lead = q.shape[:-2]
+        T, d = q.shape[-2], q.shape[-1]
+        BH = int(np.prod(lead)) if lead else 1
+        f = lambda x: None if x is None else np.ascontiguousarray(x, dtype=np.float64)
+        out = {n: np.empty(lead + (T, d)) for n in ("dq", "dk", "dv", "du")}
+        out.update(dS0=np.empty(lead + (d, d)), dA0=np.empty(lead + (d, d)), dzk0=np.empty(lead + (d,)))
+        self.lib.vla_oracle_backward(
+            BH, T, d, _ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(u, _dp), float(lambda0), float(eps),
+            _ptr(f(S0), _dp), _ptr(f(A0), _dp), _ptr(f(zk0), _dp),
+            _ptr(f(gO), _dp), _ptr(f(gS), _dp), _ptr(f(gA), _dp), _ptr(f(gzk), _dp),
+            _ptr(out["dq"], _dp), _ptr(out["dk"], _dp), _ptr(out["dv"], _dp), _ptr(out["du"], _dp),
+            _ptr(out["dS0"], _dp), _ptr(out["dA0"], _dp), _ptr(out["dzk0"], _dp), int(threads))
+        return out
 
     def linear_attention_state(self, k, v, threads=0) -> np.ndarray:
         """S = sum_t v_t phi(k_t)^T per head, fp64, shape [..., d, d]."""

@@ -15,6 +15,7 @@ Sources (Pandey & Singh, "Variational Linear Attention", arXiv 2605.11196):
   §3.5       u_t = 0 with A fixed at lambda0^{-1} I (the fixed-A ablation)
   §4.1 (13)  Proposition 1: ||S_t||_F <= ||S_0||_F + sum_s ||e_s||
   §4.2 (14)  Proposition 2: Jacobian I - alpha^ k^^T (spectrum; see below)
+  §4.2       Corollary 1: the gradient through the recurrence (backward pass)
 """
 from __future__ import annotations
 
@@ -370,6 +371,86 @@ def pin_linear_attention_closed_forms(orc):
     assert _rel(S2, S1) < 1e-13
 
 
+# ---------------------------------------------------------------------------
+# backward pass: the oracle's reverse-mode gradient against central finite
+# differences of the oracle's forward (pinned above), and against eq. 14
+# ---------------------------------------------------------------------------
+
+def _spd(rng, d, lead=(1,)):
+    m = rng.standard_normal(tuple(lead) + (d, d))
+    return m @ np.swapaxes(m, -1, -2) / d + 2.0 * np.eye(d)
+
+
+def pin_backward_finite_differences(orc):
+    """dL/dx of L = sum gO.o + <gS, S_T> + <gA, A_T> + gzk.zk_T matches the
+    central difference (L(x + h r) - L(x - h r)) / 2h along a random direction r,
+    for every input and every piece of the initial state."""
+    rng = np.random.default_rng(31)
+    for T, d, with_state in ((6, 5, True), (4, 3, False)):
+        lead = (2,)
+        q, k, v, u = (rng.standard_normal(lead + (T, d)) for _ in range(4))
+        state = dict(S0=rng.standard_normal(lead + (d, d)), A0=_spd(rng, d, lead),
+                     zk0=rng.uniform(0.5, 1.5, lead + (d,))) if with_state else {}
+        seeds = dict(gO=rng.standard_normal(lead + (T, d)), gS=rng.standard_normal(lead + (d, d)),
+                     gA=rng.standard_normal(lead + (d, d)), gzk=rng.standard_normal(lead + (d,)))
+
+        def loss(**x):
+            o, S, A, zk = orc.forward_f64(x["q"], x["k"], x["v"], x["u"], LAMBDA0, EPS,
+                                          x.get("S0"), x.get("A0"), x.get("zk0"))
+            return (np.sum(seeds["gO"] * o) + np.sum(seeds["gS"] * S) + np.sum(seeds["gA"] * A)
+                    + np.sum(seeds["gzk"] * zk))
+
+        g = orc.backward(q, k, v, u, LAMBDA0, EPS, state.get("S0"), state.get("A0"), state.get("zk0"),
+                         **seeds)
+        args = dict(q=q, k=k, v=v, u=u, **state)
+        for name, x in args.items():
+            r = rng.standard_normal(x.shape)
+            h = 1e-6
+            xp, xm = dict(args), dict(args)
+            xp[name], xm[name] = x + h * r, x - h * r
+            fd = (loss(**xp) - loss(**xm)) / (2 * h)
+            an = float(np.sum(g["d" + name] * r))
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def pin_backward_state_jacobian(orc):
+    """One token, only dL/dS_1 = G seeded: dL/dS_0 = G (I - alpha^ k^^T), the
+    state Jacobian of eq. 14 in the orientation S_t = S_{t-1} (I - k^ alpha^^T)
+    + v alpha^^T; its largest singular value is the closed form
+    sqrt((3 - 2c + sqrt(5 - 4c)) / 2), c = alpha^ . k^."""
+    rng = np.random.default_rng(32)
+    d = 6
+    q, k, v, u = _inputs(rng, 1, d)
+    tr = orc.forward(q, k, v, u, LAMBDA0, EPS, trace=True)
+    al, kh = tr.alpha[0, 0], tr.khat[0, 0]
+    J = np.eye(d) - np.outer(al, kh)
+    G = rng.standard_normal((1, d, d))
+    g = orc.backward(q, k, v, u, LAMBDA0, EPS, gS=G)
+    assert _rel(g["dS0"][0], G[0] @ J) < 1e-12
+    c = float(al @ kh)
+    smax = np.sqrt((3 - 2 * c + np.sqrt(5 - 4 * c)) / 2)
+    # G = x y^T with y the top left singular vector of J: ||G J|| = smax ||G||
+    U, sv, Vt = np.linalg.svd(J)
+    G1 = np.outer(np.ones(d), U[:, 0])[None]
+    g1 = orc.backward(q, k, v, u, LAMBDA0, EPS, gS=G1)
+    assert abs(np.linalg.norm(g1["dS0"]) / np.linalg.norm(G1) - smax) < 1e-10
+
+
+def pin_backward_fixed_A_nonexpansive(orc):
+    """Fixed-A ablation (u = 0, A = lambda0^-1 I so alpha^ = k^): each state
+    Jacobian is the projection I - k^ k^^T, so ||dL/dS_0||_F <= ||dL/dS_T||_F
+    (Corollary 1 holds exactly there), and the gradient of A_0 through the
+    penalty directions get a zero gradient (u = 0 makes z = 0)."""
+    rng = np.random.default_rng(33)
+    T, d = 30, 8
+    q, k, v, _ = _inputs(rng, T, d)
+    u = np.zeros_like(q)
+    G = rng.standard_normal((1, d, d))
+    g = orc.backward(q, k, v, u, LAMBDA0, EPS, gS=G)
+    assert np.linalg.norm(g["dS0"]) <= np.linalg.norm(G) * (1 + 1e-12)
+    assert np.max(np.abs(g["du"])) == 0.0
+
+
 ALL_PINS = [
     pin_inverse_penalty,
     pin_delta,
@@ -388,4 +469,7 @@ ALL_PINS = [
     pin_heads_independent,
     pin_linear_attention_state,
     pin_linear_attention_closed_forms,
+    pin_backward_finite_differences,
+    pin_backward_state_jacobian,
+    pin_backward_fixed_A_nonexpansive,
 ]

@@ -36,6 +36,14 @@ MUTANTS = [
     ("readout without normaliser", "o[(size_t)t * d + i] = s / den;", "o[(size_t)t * d + i] = s;"),
     ("linear attention transposed", "S[i * d + j] += (double)vt[i] * phi((double)kt[j]);",
      "S[i * d + j] += (double)vt[j] * phi((double)kt[i]);"),
+    # backward pass
+    ("backward gate without the unit-norm projection", "(gal[j] - alpha[j] * ag) / n", "gal[j] / n"),
+    ("backward z adjoint without the transpose", "gz[i] = -(s1 + s2) / delta;", "gz[i] = -(2.0 * s1) / delta;"),
+    ("backward normaliser sign", "const double gden = cl[t] ? 0.0 : -go_o / den;",
+     "const double gden = cl[t] ? 0.0 : go_o / den;"),
+    ("backward residual with S_t", "s += Sp[i * d + j] * ge[i];", "s += S[i * d + j] * ge[i];"),
+    ("backward drops the key-sum path", "tmp[j] + gzk[j] * dphi(k[(size_t)t * d + j])", "tmp[j]"),
+    ("backward delta adjoint dropped", "gz[j] += gdelta * ut[j];", ""),
 ]
 
 
@@ -47,7 +55,9 @@ def source():
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(tmp_path, source, name, old, new):
-    assert source.count(old) == 1, f"mutation anchor not unique in oracle source: {old!r}"
+    # an anchor shared by the forward and the backward's own forward pass is
+    # mutated everywhere (the same mistake in both)
+    assert source.count(old) >= 1, f"mutation anchor not in oracle source: {old!r}"
     src = tmp_path / "mutant.c"
     src.write_text(source.replace(old, new))
     lib = oracle.build(str(src), str(tmp_path / "libmutant.so"))
