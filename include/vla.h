@@ -179,6 +179,43 @@ vla_status vla_linear_attention_state(const void* k, const void* v, vla_dtype dt
                                       int B, int H, int T, int d,
                                       float* S_out, void* stream);
 
+/* Bytes of device workspace vla_backward() needs for (B, H, T, d): one status
+ * record, a per-token tape of the forward pass (z_t, alpha^_t, e_t, delta_t,
+ * ||A_t k^_t||, den_t: 3d + 4 floats per head-token) and S, A checkpoints
+ * every 64 tokens (2 d^2 floats each). 0 if the sizes overflow. */
+size_t vla_backward_workspace_bytes(int B, int H, int T, int d);
+
+/* Reverse-mode gradient of vla_forward() (the backward pass of the recurrence
+ * of "Variational Linear Attention", §3.3 eq. 9-11; §4.2 eq. 14 is the state
+ * Jacobian it propagates, and Corollary 1 bounds the result).
+ *
+ * For a scalar loss L of the forward outputs, given the upstream gradients
+ *   dO    [B,H,T,d] = dL/do                    (NULL: zero)
+ *   dS_T, dA_T [B,H,d,d] = dL/dS_T, dL/dA_T     (NULL: zero)
+ *   dzk_T [B,H,d]   = dL/dz^key_T               (NULL: zero)
+ * it writes dq, dk, dv, du [B,H,T,d] = dL/dq_t ... (fp32) and, where not NULL,
+ * dS0, dA0 [B,H,d,d] and dzk0 [B,H,d] = dL/d(initial state). q, k, v, u,
+ * dtype, sizes, lambda0, eps and the optional initial state (S0, A0, zk0) are
+ * those of the forward call; the forward pass is recomputed inside.
+ *
+ * Layout and ownership as for vla_forward(); every gradient is fp32,
+ * row-major, caller-owned device memory, 16-byte aligned (state pointers
+ * 4-byte). workspace: device memory of vla_backward_workspace_bytes() bytes,
+ * 16-byte aligned, its first 16 bytes zero-filled (status record, read by
+ * vla_get_last_device_status). Asynchronous on `stream`.
+ * Errors: VLA_ERR_INVALID_ARG as for vla_forward() (including a workspace
+ * smaller than required); VLA_ERR_UNSUPPORTED for d = 128 (the state and its
+ * adjoint do not fit the kernel's shared memory) or any other d outside
+ * {32, 64, 96}; VLA_ERR_NONFINITE is recorded on the device when a gradient
+ * or an intermediate is NaN/Inf. */
+vla_status vla_backward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype,
+                        int B, int H, int T, int d, float lambda0, float eps,
+                        const float* S0, const float* A0, const float* zk0,
+                        const float* dO, const float* dS_T, const float* dA_T, const float* dzk_T,
+                        float* dq, float* dk, float* dv, float* du,
+                        float* dS0, float* dA0, float* dzk0,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

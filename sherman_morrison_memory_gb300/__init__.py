@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     VLAError,
     library_path,
     load_library,
+    vla_backward,
     vla_forward,
     vla_get_last_device_status,
     vla_linear_attention_state,

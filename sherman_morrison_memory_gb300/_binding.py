@@ -80,6 +80,11 @@ def load_library():
         lib.vla_status_string.restype = ctypes.c_char_p
         lib.vla_linear_attention_state.argtypes = [vp, vp, ci, ci, ci, ci, ci, vp, vp]
         lib.vla_linear_attention_state.restype = ci
+        lib.vla_backward_workspace_bytes.argtypes = [ci, ci, ci, ci]
+        lib.vla_backward_workspace_bytes.restype = ctypes.c_size_t
+        lib.vla_backward.argtypes = ([vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, cf, vp, vp, vp, vp, vp, vp, vp]
+                                     + [vp] * 7 + [vp, ctypes.c_size_t, vp])
+        lib.vla_backward.restype = ci
         del cp
         _LIB = lib
         return lib
@@ -216,6 +221,71 @@ def vla_get_last_device_status(device=None, stream=None) -> Tuple[int, tuple]:
     with torch.cuda.device(dev):
         st = lib.vla_get_last_device_status(_ptr(ws), ctypes.c_void_p(_stream_handle(dev, stream)), detail)
     return int(st), (detail[0], detail[1], detail[2])
+
+
+_BW_WORKSPACES = {}
+
+
+def vla_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tensor,
+                 lambda0: float = 0.1, eps: float = 1e-4, state=None, grad_o=None, grad_state=None, *,
+                 stream=None, check: bool = False):
+    """Gradient of a scalar loss through vla_forward (reverse mode, §3.3 eq. 9-11).
+
+    ``grad_o`` = dL/do [B,H,T,d] and ``grad_state`` = (dL/dS_T, dL/dA_T,
+    dL/dz^key_T) (each optional, None = zero); ``state`` = the forward's
+    optional initial (S0, A0, zk0). Returns ``((dq, dk, dv, du), (dS0, dA0,
+    dzk0))``, float32 on the inputs' device. d in {32, 64, 96}.
+    ``check=True`` synchronises and raises on an in-kernel failure.
+    """
+    lib = load_library()
+    for name, x in (("k", k), ("v", v), ("u", u)):
+        if x.shape != q.shape or x.dtype != q.dtype or x.device != q.device:
+            raise ValueError(f"{name} must match q in shape, dtype and device")
+    if q.dim() != 4 or q.dtype not in _DTYPES or q.device.type != "cuda":
+        raise ValueError("q, k, v, u must be [B, H, T, d] float32 or bfloat16 CUDA tensors")
+    q, k, v, u = (x.contiguous() for x in (q, k, v, u))
+    B, H, T, d = q.shape
+    dev = q.device
+    S0 = A0 = zk0 = None
+    if state is not None:
+        S0, A0, zk0 = state
+        S0 = _check_state(S0, (B, H, d, d), dev, "S0")
+        A0 = _check_state(A0, (B, H, d, d), dev, "A0")
+        zk0 = _check_state(zk0, (B, H, d), dev, "zk0")
+    gO = None if grad_o is None else _check_state(grad_o, (B, H, T, d), dev, "grad_o")
+    gS = gA = gzk = None
+    if grad_state is not None:
+        gS, gA, gzk = grad_state
+        gS = _check_state(gS, (B, H, d, d), dev, "dS_T")
+        gA = _check_state(gA, (B, H, d, d), dev, "dA_T")
+        gzk = _check_state(gzk, (B, H, d), dev, "dzk_T")
+    outs = [torch.empty((B, H, T, d), dtype=torch.float32, device=dev) for _ in range(4)]
+    dS0 = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    dA0 = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    dzk0 = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    nbytes = int(lib.vla_backward_workspace_bytes(B, H, T, d))
+    if nbytes == 0:
+        raise ValueError("sizes overflow the backward workspace")
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _BW_WORKSPACES.get(idx)
+    if ws is None or ws.numel() * 4 < nbytes:
+        ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=dev)
+        _BW_WORKSPACES[idx] = ws
+    with torch.cuda.device(dev):
+        sh = _stream_handle(dev, stream)
+        st = lib.vla_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d, float(lambda0),
+                              float(eps), _ptr(S0), _ptr(A0), _ptr(zk0), _ptr(gO), _ptr(gS), _ptr(gA), _ptr(gzk),
+                              *(_ptr(x) for x in outs), _ptr(dS0), _ptr(dA0), _ptr(dzk0), _ptr(ws),
+                              ws.numel() * 4, ctypes.c_void_p(sh))
+    if st != VLA_OK:
+        raise VLAError(st, "vla_backward")
+    if check:
+        detail = (ctypes.c_int * 3)()
+        with torch.cuda.device(dev):
+            st = lib.vla_get_last_device_status(_ptr(ws), ctypes.c_void_p(_stream_handle(dev, stream)), detail)
+        if st != VLA_OK:
+            raise VLAError(st, "vla_backward (device)", (detail[0], detail[1], detail[2]))
+    return tuple(outs), (dS0, dA0, dzk0)
 
 
 def vla_linear_attention_state(k: torch.Tensor, v: torch.Tensor, stream=None) -> torch.Tensor:

@@ -1103,6 +1103,7 @@ __global__ void __launch_bounds__(LA_THREADS) la_state_kernel(const TIn* k, cons
 }
 
 #include "vla_tc.cuh"
+#include "vla_backward.cuh"
 
 }  // namespace vla
 
@@ -1354,6 +1355,113 @@ vla_status vla_linear_attention_state(const void* k, const void* v, vla_dtype dt
     else
         launch_la<float>(d, static_cast<const float*>(k), static_cast<const float*>(v), T, S_out, (int)BH, s);
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// backward pass
+// ---------------------------------------------------------------------------
+namespace {
+
+struct BwSizes {
+    size_t tape, ckpt, total;
+};
+
+bool bw_sizes(int B, int H, int T, int d, BwSizes* out) {
+    if (B < 0 || H < 0 || T < 0 || d <= 0) return false;
+    const unsigned long long BH = (unsigned long long)B * (unsigned long long)H;
+    const unsigned long long nck = (unsigned long long)((T + vla::bw::CK - 1) / vla::bw::CK + 1);
+    const unsigned long long tape = BH * (unsigned long long)T * (unsigned long long)(3 * d + 4) * 4ull;
+    const unsigned long long ck = BH * nck * 2ull * (unsigned long long)d * (unsigned long long)d * 4ull;
+    if (BH > (1ull << 31) || tape > (1ull << 50) || ck > (1ull << 50)) return false;
+    auto al = [](unsigned long long x) { return (x + 255ull) / 256ull * 256ull; };
+    out->tape = (size_t)al(tape);
+    out->ckpt = (size_t)al(ck);
+    out->total = kWorkspaceBytes + out->tape + out->ckpt;
+    return true;
+}
+
+template <int D, typename TIn>
+vla_status launch_bw(const vla::Params& p, int BH, const float* dO, const float* dST, const float* dAT,
+                     const float* dzkT, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
+                     float* dzk0, float* tape, float* ckpt, cudaStream_t s) {
+    using BL = vla::bw::BLay<D>;
+    auto kern = vla::bw::vla_backward_kernel<D, TIn>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BL::SMEM) != cudaSuccess)
+        return VLA_ERR_CUDA;
+    kern<<<BH, BL::THREADS, BL::SMEM, s>>>(p, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt);
+    return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
+}
+
+template <typename TIn>
+vla_status launch_bw_d(int d, const vla::Params& p, int BH, const float* dO, const float* dST, const float* dAT,
+                       const float* dzkT, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
+                       float* dzk0, float* tape, float* ckpt, cudaStream_t s) {
+    switch (d) {
+        case 32: return launch_bw<32, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, s);
+        case 64: return launch_bw<64, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, s);
+        case 96: return launch_bw<96, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, s);
+        default: return VLA_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t vla_backward_workspace_bytes(int B, int H, int T, int d) {
+    BwSizes z;
+    return bw_sizes(B, H, T, d, &z) ? z.total : 0;
+}
+
+vla_status vla_backward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B,
+                        int H, int T, int d, float lambda0, float eps, const float* S0, const float* A0,
+                        const float* zk0, const float* dO, const float* dS_T, const float* dA_T,
+                        const float* dzk_T, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
+                        float* dzk0, void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || H < 0 || T < 0) return VLA_ERR_INVALID_ARG;
+    if (dtype != VLA_F32 && dtype != VLA_BF16) return VLA_ERR_INVALID_ARG;
+    if (d != 32 && d != 64 && d != 96 && d != 128) return VLA_ERR_UNSUPPORTED;
+    if (d == 128) return VLA_ERR_UNSUPPORTED;
+    if (!(lambda0 > 0.f) || !std::isfinite(lambda0)) return VLA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return VLA_ERR_INVALID_ARG;
+    BwSizes z;
+    if (!bw_sizes(B, H, T, d, &z)) return VLA_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < z.total) return VLA_ERR_INVALID_ARG;
+    const long long BH = (long long)B * H;
+    if (BH == 0) return VLA_OK;
+    if (T > 0) {
+        if (!q || !k || !v || !u || !dq || !dk || !dv || !du) return VLA_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(u) || !aligned16(dq) ||
+            !aligned16(dk) || !aligned16(dv) || !aligned16(du) || (dO && !aligned16(dO)))
+            return VLA_ERR_INVALID_ARG;
+    }
+    const float* st[] = {S0, A0, zk0, dS_T, dA_T, dzk_T, dS0, dA0, dzk0};
+    for (const float* x : st)
+        if (x && !aligned4(x)) return VLA_ERR_INVALID_ARG;
+
+    vla::Params p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.u = u;
+    p.S0 = S0;
+    p.A0 = A0;
+    p.zk0 = zk0;
+    p.status = static_cast<vla::DeviceStatus*>(workspace);
+    p.T = T;
+    p.inv_lambda0 = 1.0f / lambda0;
+    p.eps = eps;
+    p.wait_ns = 1000ull * kDefaultWaitUs;
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    float* tape = reinterpret_cast<float*>(w + kWorkspaceBytes);
+    float* ckpt = reinterpret_cast<float*>(w + kWorkspaceBytes + z.tape);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return dtype == VLA_BF16 ? launch_bw_d<__nv_bfloat16>(d, p, (int)BH, dO, dS_T, dA_T, dzk_T, dq, dk, dv, du, dS0,
+                                                          dA0, dzk0, tape, ckpt, s)
+                             : launch_bw_d<float>(d, p, (int)BH, dO, dS_T, dA_T, dzk_T, dq, dk, dv, du, dS0, dA0,
+                                                  dzk0, tape, ckpt, s);
 }
 
 }  // extern "C"

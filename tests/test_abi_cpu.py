@@ -100,3 +100,44 @@ def test_algo_argument_errors(lib, algo, d, status):
                             ctypes.c_float(1e-4), None, None, None, vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE),
                             ctypes.c_size_t(256), None, ctypes.byref(opts))
     assert st == status
+
+
+def test_backward_workspace_bytes(lib):
+    """Status record + tape (3d + 4 floats per head-token) + S, A checkpoints
+    every 64 tokens plus the initial one (2 d^2 floats each), 256-byte aligned."""
+    assert lib.vla_backward_workspace_bytes(1, 1, 64, 32) == 256 + 64 * 100 * 4 + 2 * 2 * 32 * 32 * 4
+    assert lib.vla_backward_workspace_bytes(2, 3, 65, 96) == 256 + (6 * 65 * 292 * 4 + 255) // 256 * 256 + 6 * 3 * 2 * 96 * 96 * 4
+    assert lib.vla_backward_workspace_bytes(1, 1, 0, 64) > 0
+    assert lib.vla_backward_workspace_bytes(-1, 1, 4, 64) == 0
+    assert lib.vla_backward_workspace_bytes(1 << 30, 1 << 30, 4, 64) == 0
+
+
+def _bw_call(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, u=FAKE, dtype=1, B=1, H=1, T=4, d=64, lambda0=0.1, eps=1e-4,
+             S0=None, A0=None, zk0=None, gO=FAKE, gS=None, gA=None, gzk=None,
+             dq=FAKE, dk=FAKE, dv=FAKE, du=FAKE, dS0=FAKE, dA0=FAKE, dzk0=FAKE, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    p = lambda n: vp(a[n])
+    return lib.vla_backward(p("q"), p("k"), p("v"), p("u"), a["dtype"], a["B"], a["H"], a["T"], a["d"],
+                            a["lambda0"], a["eps"], p("S0"), p("A0"), p("zk0"), p("gO"), p("gS"), p("gA"),
+                            p("gzk"), p("dq"), p("dk"), p("dv"), p("du"), p("dS0"), p("dA0"), p("dzk0"),
+                            p("ws"), a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=128), 2), (dict(d=48), 2), (dict(d=0), 2),
+    (dict(B=-1), 1), (dict(T=-1), 1), (dict(dtype=4), 1),
+    (dict(lambda0=0.0), 1), (dict(eps=float("inf")), 1),
+    (dict(ws=None), 1), (dict(ws=FAKE + 8), 1), (dict(wsb=1024), 1),
+    (dict(q=None), 1), (dict(dq=None), 1), (dict(du=None), 1),
+    (dict(k=FAKE + 4), 1), (dict(dv=FAKE + 8), 1), (dict(gO=FAKE + 4), 1),
+    (dict(dS0=FAKE + 2), 1), (dict(S0=FAKE + 1), 1),
+    (dict(B=1 << 30, H=1 << 30), 1),
+])
+def test_backward_argument_errors(lib, kw, status):
+    assert _bw_call(lib, **kw) == status
+
+
+def test_backward_empty_batch_is_a_no_op(lib):
+    assert _bw_call(lib, B=0) == 0

@@ -1,0 +1,180 @@
+"""Parity of the CUDA backward pass (vla_backward, through the C ABI) with the
+fp64 oracle's reverse-mode gradient.
+
+Cases span several 64-token checkpoint segments and a ragged tail, every
+supported head dimension, both input dtypes, with and without an initial
+state, each upstream seed alone, T = 0, and sampled heads of the d = 96,
+T = 4096 workload. Tolerance: 2e-3 relative (parity_util.TOL), per token
+(rows of dq, dk, dv, du) and per head (dS0, dA0, dzk0), as for the forward.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import assert_close, rel_heads, rel_rows
+from sherman_morrison_memory_gb300 import (VLA_ERR_NONFINITE, VLA_ERR_UNSUPPORTED, VLA_OK, VLAError,
+                                           vla_backward, vla_get_last_device_status)
+from sherman_morrison_memory_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+def _inputs(B, H, T, d, dtype, seed):
+    arrs = W.normal(B, H, T, d, seed=seed)
+    if dtype == "bf16":
+        arrs = tuple(W.to_bf16_values(a) for a in arrs)
+    return arrs
+
+
+def _seeds(B, H, T, d, seed, with_o=True, with_state=True):
+    rng = np.random.default_rng(1000 + seed)
+    gO = rng.standard_normal((B, H, T, d)).astype(np.float32) if with_o else None
+    gst = None
+    if with_state:
+        gst = (rng.standard_normal((B, H, d, d)).astype(np.float32),
+               rng.standard_normal((B, H, d, d)).astype(np.float32),
+               rng.standard_normal((B, H, d)).astype(np.float32))
+    return gO, gst
+
+
+def _warm_state(orc, B, H, d, seed):
+    """A reachable initial state: the oracle's state after 30 tokens, in fp32."""
+    warm = orc.forward(*W.normal(B, H, 30, d, seed=seed))
+    return tuple(np.asarray(x, dtype=np.float32) for x in (warm.S, warm.A, warm.zk))
+
+
+def _dev(x, dtype=torch.float32):
+    return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda().to(dtype)
+
+
+def _f64(x):
+    return None if x is None else np.asarray(x, dtype=np.float64)
+
+
+def _run(orc, arrs, dtype, gO, gst, state=None, lambda0=0.1, eps=1e-4):
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    q, k, v, u = (_dev(a, tdt) for a in arrs)
+    grads, dstate = vla_backward(q, k, v, u, lambda0, eps, None if state is None else tuple(_dev(x) for x in state),
+                                 _dev(gO), None if gst is None else tuple(_dev(x) for x in gst), check=True)
+    st = (None, None, None) if state is None else tuple(_f64(x) for x in state)
+    gs = (None, None, None) if gst is None else tuple(_f64(x) for x in gst)
+    ref = orc.backward(*(_f64(a) for a in arrs), lambda0, eps, *st, _f64(gO), *gs)
+    return grads, dstate, ref
+
+
+def _errors(grads, dstate, ref):
+    dq, dk, dv, du = (x.cpu().numpy() for x in grads)
+    dS0, dA0, dzk0 = (x.cpu().numpy() for x in dstate)
+    return dict(dq=rel_rows(dq, ref["dq"]), dk=rel_rows(dk, ref["dk"]), dv=rel_rows(dv, ref["dv"]),
+                du=rel_rows(du, ref["du"]), dS0=rel_heads(dS0, ref["dS0"]), dA0=rel_heads(dA0, ref["dA0"]),
+                dzk0=rel_heads(dzk0, ref["dzk0"]))
+
+
+@pytest.mark.parametrize("d", [32, 64, 96])
+@pytest.mark.parametrize("T", [1, 37, 129])
+def test_small_f32(orc, d, T):
+    arrs = _inputs(1, 2, T, d, "f32", seed=d + T)
+    gO, gst = _seeds(1, 2, T, d, seed=d + T)
+    assert_close(_errors(*_run(orc, arrs, "f32", gO, gst)), what=f"backward f32 d={d} T={T}")
+
+
+@pytest.mark.parametrize("d", [32, 64, 96])
+def test_bf16_with_initial_state(orc, d):
+    """Initial state carried in; 200 tokens = three checkpoint segments + tail."""
+    B, H, T = 1, 2, 200
+    arrs = _inputs(B, H, T, d, "bf16", seed=d)
+    state = _warm_state(orc, B, H, d, seed=d + 1)
+    gO, gst = _seeds(B, H, T, d, seed=d)
+    assert_close(_errors(*_run(orc, arrs, "bf16", gO, gst, state=state)), what=f"backward bf16+state d={d}")
+
+
+@pytest.mark.parametrize("which", ["o_only", "state_only"])
+def test_single_upstream_seed(orc, which):
+    B, H, T, d = 2, 2, 100, 64
+    arrs = _inputs(B, H, T, d, "f32", seed=5)
+    gO, gst = _seeds(B, H, T, d, seed=5, with_o=which == "o_only", with_state=which == "state_only")
+    assert_close(_errors(*_run(orc, arrs, "f32", gO, gst)), what=f"backward {which}")
+
+
+def test_lambda_and_eps(orc):
+    arrs = _inputs(1, 2, 80, 32, "f32", seed=6)
+    gO, gst = _seeds(1, 2, 80, 32, seed=6)
+    assert_close(_errors(*_run(orc, arrs, "f32", gO, gst, lambda0=0.7, eps=0.5)), what="backward lambda/eps")
+
+
+def test_long_sequence_bf16(orc):
+    B, H, T, d = 2, 2, 1000, 96
+    arrs = _inputs(B, H, T, d, "bf16", seed=7)
+    gO, gst = _seeds(B, H, T, d, seed=7)
+    assert_close(_errors(*_run(orc, arrs, "bf16", gO, gst)), what="backward T=1000")
+
+
+def test_zero_tokens_passes_state_gradient_through(orc):
+    """T = 0: the forward is the identity on the state, so dState0 = dState_T."""
+    B, H, d = 1, 3, 64
+    arrs = tuple(np.zeros((B, H, 0, d), np.float32) for _ in range(4))
+    _, gst = _seeds(B, H, 0, d, seed=8, with_o=False)
+    grads, dstate, ref = _run(orc, arrs, "f32", None, gst)
+    assert all(g.shape == (B, H, 0, d) for g in grads)
+    for got, want in zip(dstate, gst):
+        np.testing.assert_array_equal(got.cpu().numpy(), want)
+    assert_close(_errors(grads, dstate, ref), what="backward T=0")
+
+
+def test_workload_d96_sampled_heads(orc):
+    """The d = 96, T = 4096 bf16 workload in its full launch (128 heads); the
+    oracle checks two sampled heads."""
+    w = W.WORKLOADS[3]
+    arrs = W.make(w)
+    B, H, T, d = w.B, w.H, w.T, w.d
+    q, k, v, u = (_dev(a, torch.bfloat16) for a in arrs)
+    rng = np.random.default_rng(9)
+    gO = rng.standard_normal((B, H, T, d)).astype(np.float32)
+    grads, dstate = vla_backward(q, k, v, u, 0.1, 1e-4, None, _dev(gO), check=True)
+    heads = [0, B * H - 1, 77]
+    flat = lambda x: x.reshape((B * H,) + x.shape[2:])[heads][None]
+    ref = orc.backward(*(flat(a).astype(np.float64) for a in arrs), 0.1, 1e-4, gO=flat(gO).astype(np.float64))
+    pick = lambda x: flat(x.cpu().numpy())
+    dq, dk, dv, du = (pick(x) for x in grads)
+    dS0, dA0, dzk0 = (pick(x) for x in dstate)
+    errs = dict(dq=rel_rows(dq, ref["dq"]), dk=rel_rows(dk, ref["dk"]), dv=rel_rows(dv, ref["dv"]),
+                du=rel_rows(du, ref["du"]), dS0=rel_heads(dS0, ref["dS0"]), dA0=rel_heads(dA0, ref["dA0"]),
+                dzk0=rel_heads(dzk0, ref["dzk0"]))
+    assert_close(errs, what="backward d96 workload")
+    for g in grads + dstate:
+        assert torch.isfinite(g).all()
+
+
+@pytest.mark.parametrize("tensor", [0, 1, 2, 3])
+def test_nonfinite_input_is_reported(tensor):
+    arrs = [np.array(a) for a in _inputs(1, 1, 40, 64, "f32", seed=12)]
+    arrs[tensor][0, 0, 7, 3] = np.nan
+    q, k, v, u = (_dev(a) for a in arrs)
+    gO, _ = _seeds(1, 1, 40, 64, seed=12, with_state=False)
+    vla_backward(q, k, v, u, 0.1, 1e-4, None, _dev(gO))
+    with pytest.raises(VLAError) as ei:
+        vla_backward(q, k, v, u, 0.1, 1e-4, None, _dev(gO), check=True)
+    assert ei.value.status == VLA_ERR_NONFINITE
+
+
+def test_nonfinite_then_clean_call_succeeds(orc):
+    arrs = [np.array(a) for a in _inputs(1, 1, 40, 32, "f32", seed=13)]
+    bad = [a.copy() for a in arrs]
+    bad[1][0, 0, 3, 1] = np.inf
+    gO, _ = _seeds(1, 1, 40, 32, seed=13, with_state=False)
+    with pytest.raises(VLAError):
+        vla_backward(*(_dev(a) for a in bad), 0.1, 1e-4, None, _dev(gO), check=True)
+    assert_close(_errors(*_run(orc, arrs, "f32", gO, None)), what="backward after a non-finite call")
+
+
+def test_d128_is_unsupported():
+    x = torch.zeros((1, 1, 4, 128), device="cuda")
+    with pytest.raises(VLAError) as ei:
+        vla_backward(x, x, x, x, 0.1, 1e-4, None, x)
+    assert ei.value.status == VLA_ERR_UNSUPPORTED
