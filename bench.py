@@ -14,6 +14,10 @@ rank runs its own copy of the workload (heads are independent: weak scaling,
 no collective on the data path); the time is the max over ranks.
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead, on
 a bounded sample of the same workload.
+
+``--pass backward`` times the reverse-mode gradient instead (one step = one
+vla_backward call over the whole workload with a seeded upstream gradient
+dL/do; the forward recurrence is recomputed inside the call).
 """
 from __future__ import annotations
 
@@ -32,7 +36,13 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "VLA head-tokens/sec at d_h=96,T=4096; % of FP32-FMA roofline"
+METRIC_BW = "VLA backward head-tokens/sec at d_h=96,T=4096; % of FP32-FMA roofline"
 UNIT = "head-tokens/s"
+# algorithmic FP32 work per head-token, in units of d^2 FLOP: the forward is 6 matrix-vector
+# products / rank-1 updates of d x d matrices (2 d^2 FLOP each); the backward recomputes 5 of
+# them (A u^, A k^, S k^ and the rank-1 updates of A and S) and then runs 8 matrix-vector
+# products and 6 rank-1 updates on S, A and their adjoints (19 x 2 d^2)
+FLOP_D2 = {"forward": 12, "backward": 38}
 FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM (sm_103)
 FALLBACK_SM_MAX_MHZ = 2070.0
 FALLBACK_HBM_GBS = 6800.0
@@ -41,6 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
 # sources hash to SOURCE_SHA; otherwise reported as null.
 NCU_TRAFFIC = {"source_sha": "757966978bd67c06", "bytes_per_launch": 402742272 + 175727360}
+NCU_TRAFFIC_BW = {"source_sha": None, "bytes_per_launch": None}
 
 
 def kernel_source_sha() -> str:
@@ -179,6 +190,18 @@ def oracle_time(arrs, w, tokens: int, heads: int):
     return heads * tokens / dt, r.threads, dt
 
 
+def oracle_time_bw(arrs, gO, w, tokens: int, heads: int):
+    import oracle
+
+    orc = oracle.load()
+    sub = [a.reshape(-1, w.T, w.d)[:heads, :tokens].astype("float64") for a in arrs]
+    g = gO.reshape(-1, w.T, w.d)[:heads, :tokens].astype("float64")
+    t0 = time.perf_counter()
+    r = orc.backward(*sub, w.lambda0, w.eps, gO=g)
+    dt = time.perf_counter() - t0
+    return heads * tokens / dt, r["threads"], dt
+
+
 def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -187,22 +210,29 @@ def run_reference(args, w):
 
     arrs = W.make(w)
     heads = w.heads
+    bw = args.pass_ == "backward"
+    if bw:
+        gO = W.upstream_grad(w)
+        timer = lambda tok: oracle_time_bw(arrs, gO, w, tok, heads)
+    else:
+        timer = lambda tok: oracle_time(arrs, w, tok, heads)
     # size each step's sample so that warmup + steps end within about 2.5 minutes
     probe_tokens = min(w.T, 16)
-    rate, threads, dt = oracle_time(arrs, w, probe_tokens, heads)
+    rate, threads, dt = timer(probe_tokens)
     budget = 150.0 / max(1, args.steps + args.warmup)
     tokens = int(max(1, min(w.T, probe_tokens * budget / max(dt, 1e-6))))
     for _ in range(args.warmup):
-        oracle_time(arrs, w, tokens, heads)
+        timer(tokens)
     total_units, total_time = 0, 0.0
     for _ in range(args.steps):
-        rate, threads, dt = oracle_time(arrs, w, tokens, heads)
+        rate, threads, dt = timer(tokens)
         total_units += heads * tokens
         total_time += dt
     value = total_units / total_time
-    sample = f"all {heads} heads x first {tokens} of {w.T} tokens per step (fp64 oracle, OpenMP over heads)"
+    what = "fp64 oracle backward" if bw else "fp64 oracle"
+    sample = f"all {heads} heads x first {tokens} of {w.T} tokens per step ({what}, OpenMP over heads)"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_BW if bw else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_time / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.describe()},
@@ -346,6 +376,128 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_ours_backward(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from sherman_morrison_memory_gb300 import vla_backward
+    from sherman_morrison_memory_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    wr = W.Workload(w.name, w.B, w.H, w.T, w.d, w.dtype, w.structure, w.lambda0, w.eps,
+                    seed=rank_seed(w.seed, rank))
+    arrs = W.make(wr)
+    gO_np = W.upstream_grad(wr)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    q, k, v, u = (torch.from_numpy(a).to(dev).to(tdt) for a in arrs)
+    gO = torch.from_numpy(gO_np).to(dev)
+    B, H, T, d = w.B, w.H, w.T, w.d
+    shapes = [(B, H, T, d)] * 4 + [(B, H, d, d), (B, H, d, d), (B, H, d)]
+    out = tuple(torch.empty(sh, dtype=torch.float32, device=dev) for sh in shapes)
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(args.warmup):
+        vla_backward(q, k, v, u, w.lambda0, w.eps, None, gO, out=out, check=(i == args.warmup - 1))
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", "") or "")
+    gpu_id = ("GPU-" + gpu_id) if gpu_id and not gpu_id.startswith("GPU-") else (gpu_id or str(local))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id) as clk:
+        barrier(world, dev)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            vla_backward(q, k, v, u, w.lambda0, w.eps, None, gO, out=out)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    # the status record is sticky: a failure in any timed call is reported here
+    vla_backward(q, k, v, u, w.lambda0, w.eps, None, gO, out=out, check=True)
+    ms_max = max_over_ranks(ms, world, dev)
+    units = w.head_tokens
+    value = aggregate_value(units, world, ms_max / 1e3)
+
+    peaks = load_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", FALLBACK_SM_MAX_MHZ))
+    n_sm = props.multi_processor_count
+    peak_tflops = n_sm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    flops = FLOP_D2["backward"] * d * d * units
+    achieved = flops / (ms / 1e3) / 1e12
+    esz = 2 if w.dtype == "bf16" else 4
+    in_bytes = 4 * units * d * esz + units * d * 4
+    out_bytes = 4 * units * d * 4 + w.heads * (2 * d * d + d) * 4
+    tape_bytes = 2 * units * (3 * d + 8) * 4
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
+    sha = kernel_source_sha()
+    traffic = NCU_TRAFFIC_BW["bytes_per_launch"] if NCU_TRAFFIC_BW["source_sha"] == sha else None
+
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hu = (x.cpu().pin_memory() for x in (q, k, v, u))
+        hg = gO.cpu().pin_memory()
+        hout = tuple(torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in out)
+        ksteps = max(3, min(args.steps, args.e2e_steps))
+        for _ in range(2):
+            vla_backward(hq, hk, hv, hu, w.lambda0, w.eps, None, hg, out=hout)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        e0.record(stream)
+        for _ in range(ksteps):
+            vla_backward(hq, hk, hv, hu, w.lambda0, w.eps, None, hg, out=hout)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ksteps, world, dev)
+        e2e = {"value": aggregate_value(units, world, e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (hq, hk, hv, hu, hg)),
+               "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in hout),
+               "ms_per_step": e2e_ms, "steps": ksteps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        probe = min(w.T, 16)
+        _, _, dt = oracle_time_bw(arrs, gO_np, w, probe, w.heads)
+        tokens = int(max(1, min(w.T, probe * 15.0 / max(dt, 1e-6))))
+        rate, threads, dt = oracle_time_bw(arrs, gO_np, w, tokens, w.heads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"all {w.heads} heads x first {tokens} of {w.T} tokens (fp64 oracle backward, {dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC_BW, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.describe(), "pass": "backward", "B": B, "H": H, "T": T, "d_h": d,
+                       "input_dtype": w.dtype, "upstream": "dL/do ~ N(0,1) fp32, no state gradients",
+                       "per_rank_heads": w.heads,
+                       "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB per step), no flush"},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+                         "frac": achieved / peak_tflops, "traffic": traffic,
+                         "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FP32 FMA lanes x 2 x {sm_max:.0f} MHz",
+                         "flop_per_head_token": FLOP_D2["backward"] * d * d, "kernel": "vla_backward_kernel"},
+            "fp32_roofline_pct": 100.0 * achieved / peak_tflops,
+            "hbm": {"achieved_gbs": hbm_gbs, "peak_gbs": hbm_peak, "frac": hbm_gbs / hbm_peak,
+                    "algorithmic_bytes_per_launch": in_bytes + out_bytes,
+                    "tape_bytes_per_launch": tape_bytes},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "kernel_source_sha": sha,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -358,6 +510,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--algo", type=int, default=0,
                     help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96), 1 per-token, 2 chunked")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
+                    help="time the forward recurrence (default) or its reverse-mode gradient")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -366,6 +520,8 @@ def main(argv=None):
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.pass_ == "backward":
+        run_ours_backward(args, w)
     else:
         run_ours(args, w)
 

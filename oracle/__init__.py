@@ -144,7 +144,7 @@ class Oracle:
         """Reverse-mode gradient of the recurrence (fp64) for the loss seeds
         gO = dL/do [..., T, d] and gS, gA = dL/dS_T, dL/dA_T [..., d, d], gzk =
         dL/dz^key_T [..., d] (each optional). Returns dict dq, dk, dv, du,
-        dS0, dA0, dzk0."""
+        dS0, dA0, dzk0 and the number of threads used."""
         q, k, v, u = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, u))
         lead = q.shape[:-2]
         T, d = q.shape[-2], q.shape[-1]
@@ -152,12 +152,13 @@ class Oracle:
         f = lambda x: None if x is None else np.ascontiguousarray(x, dtype=np.float64)
         out = {n: np.empty(lead + (T, d)) for n in ("dq", "dk", "dv", "du")}
         out.update(dS0=np.empty(lead + (d, d)), dA0=np.empty(lead + (d, d)), dzk0=np.empty(lead + (d,)))
-        self.lib.vla_oracle_backward(
+        n = self.lib.vla_oracle_backward(
             BH, T, d, _ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(u, _dp), float(lambda0), float(eps),
             _ptr(f(S0), _dp), _ptr(f(A0), _dp), _ptr(f(zk0), _dp),
             _ptr(f(gO), _dp), _ptr(f(gS), _dp), _ptr(f(gA), _dp), _ptr(f(gzk), _dp),
             _ptr(out["dq"], _dp), _ptr(out["dk"], _dp), _ptr(out["dv"], _dp), _ptr(out["du"], _dp),
             _ptr(out["dS0"], _dp), _ptr(out["dA0"], _dp), _ptr(out["dzk0"], _dp), int(threads))
+        out["threads"] = n
         return out
 
     def linear_attention_state(self, k, v, threads=0) -> np.ndarray:

@@ -226,17 +226,40 @@ def vla_get_last_device_status(device=None, stream=None) -> Tuple[int, tuple]:
 _BW_WORKSPACES = {}
 
 
+def _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, check):
+    """Host buffers in, host buffers out: H2D copies, the kernel, D2H copies,
+    all on the current stream of the current CUDA device."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    to = lambda x: None if x is None else x.to(dev, non_blocking=True)
+    dq_, dk_, dv_, du_ = (to(x) for x in (q, k, v, u))
+    dstate = None if state is None else tuple(to(x) for x in state)
+    dgs = None if grad_state is None else tuple(to(x) for x in grad_state)
+    grads, dst = vla_backward(dq_, dk_, dv_, du_, lambda0, eps, dstate, to(grad_o), dgs, check=check)
+    pin = q.is_pinned()
+    outs = []
+    for i, x in enumerate(grads + dst):
+        h = out[i] if out is not None else torch.empty(x.shape, dtype=x.dtype, pin_memory=pin)
+        h.copy_(x, non_blocking=h.is_pinned())
+        outs.append(h)
+    return tuple(outs[:4]), tuple(outs[4:])
+
+
 def vla_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tensor,
                  lambda0: float = 0.1, eps: float = 1e-4, state=None, grad_o=None, grad_state=None, *,
-                 stream=None, check: bool = False):
+                 out=None, stream=None, check: bool = False):
     """Gradient of a scalar loss through vla_forward (reverse mode, §3.3 eq. 9-11).
 
     ``grad_o`` = dL/do [B,H,T,d] and ``grad_state`` = (dL/dS_T, dL/dA_T,
     dL/dz^key_T) (each optional, None = zero); ``state`` = the forward's
     optional initial (S0, A0, zk0). Returns ``((dq, dk, dv, du), (dS0, dA0,
     dzk0))``, float32 on the inputs' device. d in {32, 64, 96}.
-    ``check=True`` synchronises and raises on an in-kernel failure.
+    ``out`` may hold the seven result tensors (float32, contiguous, on the
+    inputs' device). CPU inputs run on the current CUDA device with
+    host<->device copies. ``check=True`` synchronises and raises on an
+    in-kernel failure.
     """
+    if q.device.type == "cpu":
+        return _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, check)
     lib = load_library()
     for name, x in (("k", k), ("v", v), ("u", u)):
         if x.shape != q.shape or x.dtype != q.dtype or x.device != q.device:
@@ -259,10 +282,18 @@ def vla_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Ten
         gS = _check_state(gS, (B, H, d, d), dev, "dS_T")
         gA = _check_state(gA, (B, H, d, d), dev, "dA_T")
         gzk = _check_state(gzk, (B, H, d), dev, "dzk_T")
-    outs = [torch.empty((B, H, T, d), dtype=torch.float32, device=dev) for _ in range(4)]
-    dS0 = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
-    dA0 = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
-    dzk0 = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    shapes = [(B, H, T, d)] * 4 + [(B, H, d, d), (B, H, d, d), (B, H, d)]
+    if out is None:
+        res = [torch.empty(sh, dtype=torch.float32, device=dev) for sh in shapes]
+    else:
+        res = list(out)
+        if len(res) != 7:
+            raise ValueError("out must hold (dq, dk, dv, du, dS0, dA0, dzk0)")
+        for x, sh in zip(res, shapes):
+            if (tuple(x.shape) != sh or x.dtype != torch.float32 or x.device != dev or not x.is_contiguous()):
+                raise ValueError(f"out tensors must be contiguous float32 {sh} on {dev}")
+    outs = res[:4]
+    dS0, dA0, dzk0 = res[4:]
     nbytes = int(lib.vla_backward_workspace_bytes(B, H, T, d))
     if nbytes == 0:
         raise ValueError("sizes overflow the backward workspace")

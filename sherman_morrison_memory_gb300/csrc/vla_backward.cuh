@@ -5,342 +5,706 @@
 //
 // One CTA per (b, h), two phases:
 //  1. the forward recurrence, token by token, writing a tape to the workspace:
-//     z_t (eq. 9), alpha^_t and ||a_t|| (eq. 10), e_t (eq. 10), delta_t and
-//     den_t (eq. 11), and S, A every BW_CK tokens;
+//     z_t (eq. 9), alpha^_t and ||a_t|| (eq. 10), e_t (eq. 10), delta_t, den_t
+//     (eq. 11) and ||u_t||^2, ||k_t||^2; S, A and z^key every CK tokens;
 //  2. the reverse sweep t = T-1 .. 0 applying the adjoint of each step of
-//     eq. 9-11 in reverse order (the same order as the fp64 oracle's). S_{t-1}
-//     and A_{t-1} are rebuilt from S_t, A_t by undoing the step's rank-1
-//     update (S_{t-1} = S_t - e alpha^^T, A_{t-1} = A_t + z z^T / delta) and
-//     reset from the checkpoint every BW_CK tokens.
-// S, A and the adjoints dL/dS, dL/dA live in shared memory ([D][D+1] fp32);
-// thread i of a 96-thread group owns row (or column) i of a matrix-vector
-// product.
+//     eq. 9-11 in reverse order. S_{t-1} and A_{t-1} are rebuilt from S_t, A_t
+//     by undoing the step's rank-1 update (S_{t-1} = S_t - e alpha^^T,
+//     A_{t-1} = A_t + z z^T / delta) and reloaded from the checkpoint every CK
+//     tokens.
+//
+// S, A and the adjoints dL/dS, dL/dA stay in registers for the whole kernel:
+// warp w owns rows 8w .. 8w+7 and lane l owns columns l, l+32, .. of each.
+// A row product M x is a lane-local partial sum reduced across the warp by a
+// halving exchange (9 shuffles for 8 rows); a column product M^T x is a
+// warp-local partial sum reduced across warps through shared memory. Dot
+// products of d-vectors are recomputed by every warp (butterfly shuffles)
+// instead of block-wide reductions. Per token the forward phase needs one
+// block barrier and the reverse phase three. Token inputs and the tape are
+// prefetched NBUF - 1 tokens ahead into a shared-memory ring with cp.async.
+//
+// Identities that save a product per reverse step (A is symmetric):
+//   A_t u^ = z / delta,  A_t k^ = alpha^ ||a||,  A_{t-1} g = A_t g + z (z.g) / delta,
+// so the reverse step has two rounds of matrix-vector products, not three.
 
 namespace bw {
 
 constexpr int CK = 64;  // checkpoint interval (tokens)
 
-template <int D>
+template <int D, typename TIn>
 struct BLay {
-    static constexpr int NG = 6;              // 6 groups of D threads for the matrix-vector rounds
-    static constexpr int THREADS = NG * D;    // 576 at d = 96
-    static constexpr int LD = D + 1;          // odd row stride: row and column walks are conflict-free
-    static constexpr int MAT = D * LD;
-    // tape per token: z | alpha | e (D each), then delta, ||a||, den (signed:
-    // negative = the eps floor was taken)
-    static constexpr int TREC = 3 * D + 4;
-    static constexpr int NVEC = 24;           // shared d-vectors
-    static constexpr size_t SMEM = ((size_t)4 * MAT + (size_t)NVEC * D + 64) * 4;
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static constexpr int RW = 8;                // rows per warp
+    static constexpr int NW = D / RW;           // warps
+    static constexpr int THREADS = 32 * NW;     // 384 at d = 96
+    static constexpr int CL = D / 32;           // columns per lane: j = lane + 32 c
+    // tape per token: z | alpha^ | e (D each), then delta, ||a||, den (signed:
+    // negative = the eps floor was taken), ||u||^2, ||k||^2, 3 unused
+    static constexpr int TREC = 3 * D + 8;
+    static constexpr int CREC = 2 * D * D + D;  // checkpoint: S | A | z^key
+    static constexpr int NB1 = 4;               // forward ring depth (prefetch 3 tokens ahead)
+    static constexpr int NB2 = 5;               // reverse ring depth (prefetch 3 tokens ahead, 1 slot in use
+                                                // by the deferred k/u gradients of the previous token)
+    // ring slot (bytes): raw u | k | q (TIn), then v (TIn, forward) or dL/do
+    // (fp32, reverse), then the tape record (reverse)
+    static constexpr int IN_B = D * (int)sizeof(TIn);
+    static constexpr int U = 0, K = IN_B, Q = 2 * IN_B, G = 3 * IN_B, TP = 3 * IN_B + 4 * D;
+    static constexpr int SLOT_B = TP + 4 * TREC;
+    // shared memory (bytes)
+    static constexpr int RING = 0;
+    static constexpr int X1 = RING + NB2 * SLOT_B;    // forward: [2 parities][z | A k^] per row
+    static constexpr int P1 = X1 + 2 * 2 * D * 4;     // reverse round 1 column partials [NW][3][D]
+    static constexpr int C1 = P1 + NW * 3 * D * 4;    // their sums [3][D]
+    static constexpr int R1 = C1 + 3 * D * 4;         // round 1 row products [2 parities][2][D]
+    static constexpr int P2 = R1 + 2 * 2 * D * 4;     // round 2 column partials [NW][D]
+    static constexpr int R2 = P2 + NW * D * 4;        // round 2 row products [2][D]
+    static constexpr int DP = R2 + 2 * D * 4;         // per-warp dot partials [4][NW]
+    static constexpr int DS = DP + 4 * NW * 4;        // their sums [4]
+    static constexpr int RED = DS + 4 * 4;            // [D/32 warps][2] dot partials of the k/u gradients
+    static constexpr int SMEM = RED + 8 * 4;
+    static_assert(D % 32 == 0 && D <= 96, "register tiles hold 8 rows x d/32 columns of four d x d matrices");
+    static_assert(SLOT_B % 16 == 0 && IN_B % 16 == 0, "cp.async chunks");
+    static_assert(3 * IN_B / 16 + D / 4 + TREC / 4 <= THREADS, "one prefetch chunk per thread");
+    static_assert(4 * IN_B <= TP, "forward slot fits");
+    static_assert(NW - 3 * CL == CL, "the warps left over by the column sums are d/32");
 };
-
-// shared vector slots
-enum {
-    V_UH, V_KH, V_PQ, V_PK, V_ZK, V_Z, V_AL, V_E, V_GO, V_O, V_GPQ, V_GE, V_GAL, V_GA, V_GKH, V_GZ, V_GUH, V_T0,
-    V_T1, V_T2, V_T3, V_T4, V_T5, V_T6
-};
-// shared scalars
-enum { X_NU, X_NK, X_DEN, X_DELTA, X_NA, X_R0, X_R1, X_R2, X_R3, X_R4, X_R5, X_R6, X_R7, X_NX };
-
-// block-wide sum of one value per thread (every thread gets the result);
-// `red` holds THREADS/32 floats; callers separate uses with __syncthreads
-template <int NT>
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-    for (int h = 16; h >= 1; h >>= 1) v += __shfl_xor_sync(0xffffffffu, v, h);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) red[w] = v;
-    __syncthreads();
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < NT / 32; ++i) s += red[i];
-    return s;
-}
 
 __device__ __forceinline__ float phi_d(float x) { return x > 0.f ? 1.f : expf(x); }  // d phi / dx
 
+__device__ __forceinline__ float rcpa(float x) {  // 1/x, approximate (1 ulp)
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float inv_norm(float n2) { return fminf(rsqrtf(n2), 1e12f); }  // 1 / max(sqrt(n2), 1e-12)
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// element j of a TIn row held in shared memory, as float
+template <typename TIn>
+__device__ __forceinline__ float lds_in(const unsigned char* base, int j);
+template <>
+__device__ __forceinline__ float lds_in<float>(const unsigned char* base, int j) {
+    return reinterpret_cast<const float*>(base)[j];
+}
+template <>
+__device__ __forceinline__ float lds_in<__nv_bfloat16>(const unsigned char* base, int j) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[j]);
+}
+
+// elements r0 .. r0+7 of a row in shared memory (r0 a multiple of 8): one or
+// two 16-byte broadcast loads
+template <typename TIn>
+__device__ __forceinline__ void lds8(const unsigned char* base, int r0, float (&x)[8]);
+template <>
+__device__ __forceinline__ void lds8<float>(const unsigned char* base, int r0, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(base)[r0 / 4];
+    const float4 b = reinterpret_cast<const float4*>(base)[r0 / 4 + 1];
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void lds8<__nv_bfloat16>(const unsigned char* base, int r0, float (&x)[8]) {
+    const uint4 a = reinterpret_cast<const uint4*>(base)[r0 / 8];
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void lds8f(const float* base, int r0, float (&x)[8]) {
+    lds8<float>(reinterpret_cast<const unsigned char*>(base), r0, x);
+}
+
+// Row sums of a warp's 8 rows: p[r] is this lane's partial sum for row r.
+// Returns the full sum of row (lane >> 2); each row ends in 4 lanes.
+__device__ __forceinline__ float rowsum8(const float (&p)[8]) {
+    const int l = threadIdx.x & 31;
+    const bool b4 = l & 16, b3 = l & 8, b2 = l & 4;
+    float q[4], r[2];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float send = b4 ? p[m] : p[m + 4];
+        const float keep = b4 ? p[m + 4] : p[m];
+        q[m] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const float send = b3 ? q[m] : q[m + 2];
+        const float keep = b3 ? q[m + 2] : q[m];
+        r[m] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b2 ? r[0] : r[1];
+    float s = (b2 ? r[1] : r[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    return s;
+}
+
+// x[c] for the warp-uniform column index c < N, without local memory
+template <int N>
+__device__ __forceinline__ float pick(const float (&x)[N], int c) {
+    float v = x[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i) v = c == i ? x[i] : v;
+    return v;
+}
+
 template <int D, typename TIn>
-__global__ void __launch_bounds__(BLay<D>::THREADS, 1)
+__device__ __forceinline__ void prefetch_fwd(unsigned char* slot, const TIn* gu, const TIn* gk, const TIn* gq,
+                                             const TIn* gv, int t) {
+    using L = BLay<D, TIn>;
+    constexpr int NC = L::IN_B / 16;
+    const int tid = threadIdx.x;
+    if (tid < 4 * NC) {
+        const int part = tid / NC, off = tid - part * NC;
+        const TIn* src = part == 0 ? gu : part == 1 ? gk : part == 2 ? gq : gv;
+        cp_async16(slot + part * L::IN_B + off * 16,
+                   reinterpret_cast<const unsigned char*>(src + (size_t)t * D) + off * 16);
+    }
+}
+
+template <int D, typename TIn>
+__device__ __forceinline__ void prefetch_rev(unsigned char* slot, const TIn* gu, const TIn* gk, const TIn* gq,
+                                             const float* go, const float* tp, int t) {
+    using L = BLay<D, TIn>;
+    constexpr int NC = L::IN_B / 16, NG = D / 4, NR = L::TREC / 4;
+    const int tid = threadIdx.x;
+    if (tid < 3 * NC) {
+        const int part = tid / NC, off = tid - part * NC;
+        const TIn* src = part == 0 ? gu : part == 1 ? gk : gq;
+        cp_async16(slot + part * L::IN_B + off * 16,
+                   reinterpret_cast<const unsigned char*>(src + (size_t)t * D) + off * 16);
+    } else if (tid < 3 * NC + NG) {
+        const int off = tid - 3 * NC;
+        if (go) cp_async16(slot + L::G + off * 16, go + (size_t)t * D + off * 4);
+    } else if (tid < 3 * NC + NG + NR) {
+        const int off = tid - 3 * NC - NG;
+        cp_async16(slot + L::TP + off * 16, tp + (size_t)t * L::TREC + off * 4);
+    }
+}
+
+// dL/dk_t and dL/du_t (column j = 32 jw + lane) from the round-2 products of
+// token t (P2, R2) and its scalars; run by the d/32 warps that the column sums
+// of the next step leave free. Returns false on a non-finite result.
+template <int D, typename TIn>
+__device__ __forceinline__ bool ku_grads(const unsigned char* sl, const float* P2, const float* R2, float* RED,
+                                         int jw, float gzk, float e_ge, float kz, float gdl, float zgz, float az,
+                                         float nac, float dl, float nu, float nk, float* dk, float* du) {
+    using L = BLay<D, TIn>;
+    const int l = threadIdx.x & 31, j = 32 * jw + l;
+    const float* rec = reinterpret_cast<const float*>(sl + L::TP);
+    float st = 0.f;
+#pragma unroll
+    for (int v = 0; v < L::NW; ++v) st += P2[v * D + j];
+    const float aga = R2[j], aw1 = R2[D + j];
+    const float zj = rec[j], alj = rec[D + j];
+    const float kj = lds_in<TIn>(sl + L::K, j);
+    const float iu = inv_norm(nu), ik = inv_norm(nk), rdl = rcpa(dl);
+    const float khj = kj * ik, uhj = lds_in<TIn>(sl + L::U, j) * iu;
+    const float gkh = aga - fmaf(-alj, e_ge, st);                                          // A_t g_a - S_{t-1}^T g_e
+    const float atgz = fmaf(gdl * rdl, zj, -(aw1 + fmaf(aga, kz, alj * nac * az)) * rdl);  // A_t g_z
+    const float zgzf = -zgz * (dl + 1.f) * rdl * rdl;                                      // z . g_z
+    const float guh = fmaf(zj, fmaf(zgzf, rdl, gdl), atgz);                                // A_{t-1} g_z + g_delta z
+    float d2[2] = {uhj * guh, khj * gkh};
+    allreduce<2, 16>(d2);
+    if (l == 0) {
+        RED[2 * jw] = d2[0];
+        RED[2 * jw + 1] = d2[1];
+    }
+    named_bar(1, D);
+    float ugu = 0.f, kgk = 0.f;
+#pragma unroll
+    for (int v = 0; v < L::CL; ++v) {
+        ugu += RED[2 * v];
+        kgk += RED[2 * v + 1];
+    }
+    const float dut = nu < 1e-24f ? guh * 1e12f : fmaf(-uhj, ugu, guh) * iu;
+    const float dkt = fmaf(gzk, phi_d(kj), nk < 1e-24f ? gkh * 1e12f : fmaf(-khj, kgk, gkh) * ik);
+    du[j] = dut;
+    dk[j] = dkt;
+    return isfinite(dut) && isfinite(dkt);
+}
+
+template <int D, typename TIn>
+__global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     vla_backward_kernel(const Params p, const float* dO, const float* dST, const float* dAT, const float* dzkT,
                         float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0, float* dzk0,
                         float* tape, float* ckpt) {
-    using L = BLay<D>;
-    constexpr int NT = L::THREADS, LD = L::LD;
-    extern __shared__ __align__(16) float sh[];
-    float* S = sh;
-    float* A = S + L::MAT;
-    float* gS = A + L::MAT;
-    float* gA = gS + L::MAT;
-    float* vec = gA + L::MAT;
-    float* sx = vec + L::NVEC * D;   // scalars
-    float* red = sx + 16;            // block reductions (NT / 32 <= 32 floats)
-    auto V = [&](int slot) { return vec + slot * D; };
+    using L = BLay<D, TIn>;
+    constexpr int RW = L::RW, CL = L::CL, NW = L::NW, NB1 = L::NB1, NB2 = L::NB2;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ __align__(16) unsigned char smem[];
+    unsigned char* ring = smem + L::RING;
+    float* X1 = reinterpret_cast<float*>(smem + L::X1);
+    float* P1 = reinterpret_cast<float*>(smem + L::P1);
+    float* C1 = reinterpret_cast<float*>(smem + L::C1);
+    float* R1 = reinterpret_cast<float*>(smem + L::R1);
+    float* P2 = reinterpret_cast<float*>(smem + L::P2);
+    float* R2 = reinterpret_cast<float*>(smem + L::R2);
+    float* DP = reinterpret_cast<float*>(smem + L::DP);
+    float* DS = reinterpret_cast<float*>(smem + L::DS);
+    float* RED = reinterpret_cast<float*>(smem + L::RED);
 
-    const int tid = threadIdx.x, grp = tid / D, li = tid - grp * D;
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int r0 = w * RW;           // first row owned by this warp
+    const int rr = r0 + (l >> 2);    // the row whose sums rowsum8 leaves in this lane
     const int bh = blockIdx.x, T = p.T;
-    const size_t hin = (size_t)bh * T * D;
+    const size_t hin = (size_t)bh * T * D, hdd = (size_t)bh * D * D;
     const TIn* gq = static_cast<const TIn*>(p.q) + hin;
     const TIn* gk = static_cast<const TIn*>(p.k) + hin;
     const TIn* gv = static_cast<const TIn*>(p.v) + hin;
     const TIn* gu = static_cast<const TIn*>(p.u) + hin;
+    const float* go_h = dO ? dO + hin : nullptr;
     float* tp = tape + (size_t)bh * T * L::TREC;
-    float* cp = ckpt + (size_t)bh * ((T + CK - 1) / CK + 1) * 2 * D * D;
-    bool nonfinite = false;
+    float* cp = ckpt + (size_t)bh * ((T + CK - 1) / CK + 1) * L::CREC;
+    bool bad = false;
+
+    float S[RW][CL], A[RW][CL], zk[CL];
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            const int i = r0 + r, j = l + 32 * c;
+            A[r][c] = p.A0 ? p.A0[hdd + i * D + j] : (i == j ? p.inv_lambda0 : 0.f);
+            S[r][c] = p.S0 ? p.S0[hdd + i * D + j] : 0.f;
+        }
+#pragma unroll
+    for (int c = 0; c < CL; ++c) zk[c] = p.zk0 ? p.zk0[(size_t)bh * D + l + 32 * c] : 0.f;
 
     // ------------------------------------------------------------------
     // phase 1: forward with tape
     // ------------------------------------------------------------------
-    for (int e = tid; e < D * D; e += NT) {
-        const int i = e / D, j = e - i * D;
-        A[i * LD + j] = p.A0 ? p.A0[(size_t)bh * D * D + e] : (i == j ? p.inv_lambda0 : 0.f);
-        S[i * LD + j] = p.S0 ? p.S0[(size_t)bh * D * D + e] : 0.f;
+    for (int s = 0; s < NB1 - 1; ++s) {
+        if (s < T) prefetch_fwd<D, TIn>(ring + s * L::SLOT_B, gu, gk, gq, gv, s);
+        cp_commit();
     }
-    if (tid < D) V(V_ZK)[tid] = p.zk0 ? p.zk0[(size_t)bh * D + tid] : 0.f;
+    cp_wait<NB1 - 2>();
     __syncthreads();
+    // raw u, k, q of the current token (this lane's columns) and its squared norms
+    float uc[CL], kc[CL], qc[CL], nu = 0.f, nk = 0.f;
+    if (T > 0) {
+        float nn[2] = {0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            uc[c] = lds_in<TIn>(ring + L::U, l + 32 * c);
+            kc[c] = lds_in<TIn>(ring + L::K, l + 32 * c);
+            qc[c] = lds_in<TIn>(ring + L::Q, l + 32 * c);
+            nn[0] = fmaf(uc[c], uc[c], nn[0]);
+            nn[1] = fmaf(kc[c], kc[c], nn[1]);
+        }
+        allreduce<2, 16>(nn);
+        nu = nn[0];
+        nk = nn[1];
+    }
     for (int t = 0; t < T; ++t) {
-        if (t % CK == 0) {
-            float* c = cp + (size_t)(t / CK) * 2 * D * D;
-            for (int e = tid; e < D * D; e += NT) {
-                const int i = e / D, j = e - i * D;
-                c[e] = S[i * LD + j];
-                c[D * D + e] = A[i * LD + j];
+        const unsigned char* sl = ring + (t % NB1) * L::SLOT_B;
+        // the slot of token t-1 is free: every warp passed token t-1's barrier
+        if (t + NB1 - 1 < T)
+            prefetch_fwd<D, TIn>(ring + ((t + NB1 - 1) % NB1) * L::SLOT_B, gu, gk, gq, gv, t + NB1 - 1);
+        cp_commit();
+        if (t % CK == 0) {  // state before token t
+            float* c = cp + (size_t)(t / CK) * L::CREC;
+#pragma unroll
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int cc = 0; cc < CL; ++cc) {
+                    const int e = (r0 + r) * D + l + 32 * cc;
+                    c[e] = S[r][cc];
+                    c[D * D + e] = A[r][cc];
+                }
+            if (w == 0)
+#pragma unroll
+                for (int cc = 0; cc < CL; ++cc) c[2 * D * D + l + 32 * cc] = zk[cc];
+        }
+        const float iu = inv_norm(nu), ik = inv_norm(nk);
+        float uh[CL], kh[CL], pq[CL];
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            uh[c] = uc[c] * iu;
+            kh[c] = kc[c] * ik;
+            pq[c] = phi(qc[c]);
+            zk[c] += phi(kc[c]);  // z^key_t (eq. 11), on raw k
+        }
+        // eq. 9 and 10 products with the states before the token: A u^, A k^, S k^
+        float pa[RW], pk[RW], ps[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            pa[r] = pk[r] = ps[r] = 0.f;
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                pa[r] = fmaf(A[r][c], uh[c], pa[r]);
+                pk[r] = fmaf(A[r][c], kh[c], pk[r]);
+                ps[r] = fmaf(S[r][c], kh[c], ps[r]);
             }
         }
-        // inputs of the token; norms, phi, key sum and den (eq. 11)
-        float nu = 0.f, nk = 0.f, pd = 0.f;
-        if (tid < D) {
-            const float uv = ld_in<TIn>(gu + (size_t)t * D, tid), kv = ld_in<TIn>(gk + (size_t)t * D, tid);
-            const float qv = ld_in<TIn>(gq + (size_t)t * D, tid);
-            nu = uv * uv;
-            nk = kv * kv;
-            const float zk = V(V_ZK)[tid] + phi(kv);
-            V(V_ZK)[tid] = zk;
-            const float pq = phi(qv);
-            V(V_PQ)[tid] = pq;
-            pd = pq * zk;
-            V(V_T0)[tid] = uv;
-            V(V_T1)[tid] = kv;
+        const float za = rowsum8(pa), ka = rowsum8(pk), sk = rowsum8(ps);
+        float* x1 = X1 + (t & 1) * 2 * D;
+        if ((l & 3) == 0) {
+            x1[rr] = za;
+            x1[D + rr] = ka;
         }
-        nu = block_sum<NT>(nu, red);
-        nk = block_sum<NT>(nk, red);
-        pd = block_sum<NT>(pd, red);
-        const float iu = 1.f / fmaxf(sqrtf(nu), 1e-12f), ik = 1.f / fmaxf(sqrtf(nk), 1e-12f);
-        if (tid < D) {
-            V(V_UH)[tid] = V(V_T0)[tid] * iu;
-            V(V_KH)[tid] = V(V_T1)[tid] * ik;
+        const float erow = lds_in<TIn>(sl + L::G, rr) - sk;  // e = v - S_{t-1} k^ for row rr
+        cp_wait<NB1 - 2>();
+        __syncthreads();
+        // delta, z.k^, den, and the next token's squared norms (its slot is complete)
+        const unsigned char* sn = ring + ((t + 1) % NB1) * L::SLOT_B;
+        const bool more = t + 1 < T;
+        float zc[CL], d5[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            zc[c] = x1[l + 32 * c];
+            d5[0] = fmaf(uh[c], zc[c], d5[0]);
+            d5[1] = fmaf(kh[c], zc[c], d5[1]);
+            d5[2] = fmaf(pq[c], zk[c], d5[2]);
+            if (more) {
+                uc[c] = lds_in<TIn>(sn + L::U, l + 32 * c);
+                kc[c] = lds_in<TIn>(sn + L::K, l + 32 * c);
+                qc[c] = lds_in<TIn>(sn + L::Q, l + 32 * c);
+                d5[3] = fmaf(uc[c], uc[c], d5[3]);
+                d5[4] = fmaf(kc[c], kc[c], d5[4]);
+            }
         }
-        __syncthreads();
-        // eq. 9: z = A u^ (rows), e = v - S k^ (rows; S_{t-1})
-        if (grp == 0) {
-            float s = 0.f;
-            for (int j = 0; j < D; ++j) s = fmaf(A[li * LD + j], V(V_UH)[j], s);
-            V(V_Z)[li] = s;
-        } else if (grp == 1) {
-            float s = 0.f;
-            for (int j = 0; j < D; ++j) s = fmaf(S[li * LD + j], V(V_KH)[j], s);
-            V(V_E)[li] = ld_in<TIn>(gv + (size_t)t * D, li) - s;
+        allreduce<5, 16>(d5);
+        const float dl = 1.f + d5[0], kz = d5[1], pd = d5[2];
+        const float rdl = rcpa(dl);
+        // a = A_t k^ = A_{t-1} k^ - z (z.k^) / delta
+        float al[CL], na2 = 0.f;
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            al[c] = fmaf(-zc[c], kz * rdl, x1[D + l + 32 * c]);
+            na2 = fmaf(al[c], al[c], na2);
         }
-        __syncthreads();
-        const float delta = 1.f + block_sum<NT>(tid < D ? V(V_UH)[tid] * V(V_Z)[tid] : 0.f, red);
-        const float rdl = 1.f / delta;
-        for (int e = tid; e < D * D; e += NT) {
-            const int i = e / D, j = e - i * D;
-            A[i * LD + j] = fmaf(-V(V_Z)[i] * rdl, V(V_Z)[j], A[i * LD + j]);
-        }
-        __syncthreads();
-        // eq. 10: a = A_t k^, alpha^ = a / ||a||, S_t = S_{t-1} + e alpha^^T
-        if (grp == 0) {
-            float s = 0.f;
-            for (int j = 0; j < D; ++j) s = fmaf(A[li * LD + j], V(V_KH)[j], s);
-            V(V_T2)[li] = s;
-        }
-        __syncthreads();
-        const float na = sqrtf(block_sum<NT>(tid < D ? V(V_T2)[tid] * V(V_T2)[tid] : 0.f, red));
-        const float ina = 1.f / fmaxf(na, 1e-12f);
-        if (tid < D) V(V_AL)[tid] = V(V_T2)[tid] * ina;
-        __syncthreads();
-        for (int e = tid; e < D * D; e += NT) {
-            const int i = e / D, j = e - i * D;
-            S[i * LD + j] = fmaf(V(V_E)[i], V(V_AL)[j], S[i * LD + j]);
+        allreduce<1, 16>(&na2);
+        const float ina = inv_norm(na2);
+#pragma unroll
+        for (int c = 0; c < CL; ++c) al[c] *= ina;
+        // A_t = A_{t-1} - z z^T / delta;  S_t = S_{t-1} + e alpha^^T
+        float zr[RW];
+        lds8f(x1, r0, zr);
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            const float er = __shfl_sync(FULL, erow, 4 * r);
+            const float zs = -zr[r] * rdl;
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                A[r][c] = fmaf(zs, zc[c], A[r][c]);
+                S[r][c] = fmaf(er, al[c], S[r][c]);
+            }
         }
         // tape
-        float* r = tp + (size_t)t * L::TREC;
-        if (tid < D) {
-            r[tid] = V(V_Z)[tid];
-            r[D + tid] = V(V_AL)[tid];
-            r[2 * D + tid] = V(V_E)[tid];
+        float* rec = tp + (size_t)t * L::TREC;
+        if (w == 0) {
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                rec[l + 32 * c] = zc[c];
+                rec[D + l + 32 * c] = al[c];
+            }
+            if (l == 0) {
+                const float na = sqrtf(na2);
+                rec[3 * D] = dl;
+                rec[3 * D + 1] = na;
+                rec[3 * D + 2] = pd < p.eps ? -p.eps : pd;
+                rec[3 * D + 3] = nu;
+                rec[3 * D + 4] = nk;
+                if (!isfinite(dl) || !isfinite(na) || !isfinite(pd)) bad = true;
+            }
         }
-        if (tid == 0) {
-            r[3 * D] = delta;
-            r[3 * D + 1] = na;
-            r[3 * D + 2] = pd < p.eps ? -p.eps : pd;
-            if (!isfinite(delta) || !isfinite(na) || !isfinite(pd)) nonfinite = true;
-        }
-        __syncthreads();
+        if ((l & 3) == 0) rec[2 * D + rr] = erow;
+        nu = d5[3];
+        nk = d5[4];
     }
 
     // ------------------------------------------------------------------
     // phase 2: reverse sweep
     // ------------------------------------------------------------------
-    for (int e = tid; e < D * D; e += NT) {
-        const int i = e / D, j = e - i * D;
-        const size_t g = (size_t)bh * D * D + e;
-        gS[i * LD + j] = dST ? dST[g] : 0.f;
-        gA[i * LD + j] = dAT ? dAT[g] : 0.f;
+    cp_wait<0>();
+    __syncthreads();  // ring free, tape visible to the whole CTA
+    float gS[RW][CL], gA[RW][CL], gzk[CL];
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            const size_t e = hdd + (r0 + r) * D + l + 32 * c;
+            gS[r][c] = dST ? dST[e] : 0.f;
+            gA[r][c] = dAT ? dAT[e] : 0.f;
+        }
+#pragma unroll
+    for (int c = 0; c < CL; ++c) gzk[c] = dzkT ? dzkT[(size_t)bh * D + l + 32 * c] : 0.f;
+    if (!dO)
+        for (int i = tid; i < NB2 * D; i += L::THREADS)
+            reinterpret_cast<float*>(ring + (i / D) * L::SLOT_B + L::G)[i % D] = 0.f;
+    for (int s = 0; s < 3; ++s) {
+        const int tok = T - 1 - s;
+        if (tok >= 0) prefetch_rev<D, TIn>(ring + (tok % NB2) * L::SLOT_B, gu, gk, gq, go_h, tp, tok);
+        cp_commit();
     }
-    float gzk = 0.f;  // thread tid < D: dL/dz^key_t[tid]
-    if (tid < D) gzk = dzkT ? dzkT[(size_t)bh * D + tid] : 0.f;
+    cp_wait<1>();
     __syncthreads();
+    const bool ku_warp = w >= NW - CL;  // the warps that compute dL/dk, dL/du
+    const int jw = w - (NW - CL);
+    // scalars of the token whose k/u gradients are pending
+    float j_ege = 0.f, j_kz = 0.f, j_gdl = 0.f, j_zgz = 0.f, j_az = 0.f, j_nac = 1.f, j_dl = 1.f, j_nu = 1.f,
+          j_nk = 1.f;
     for (int t = T - 1; t >= 0; --t) {
-        const float* r = tp + (size_t)t * L::TREC;
-        float qv = 0.f, kv = 0.f, uv = 0.f;
-        if (tid < D) {
-            uv = ld_in<TIn>(gu + (size_t)t * D, tid);
-            kv = ld_in<TIn>(gk + (size_t)t * D, tid);
-            qv = ld_in<TIn>(gq + (size_t)t * D, tid);
-            V(V_Z)[tid] = r[tid];
-            V(V_AL)[tid] = r[D + tid];
-            V(V_E)[tid] = r[2 * D + tid];
-            V(V_PQ)[tid] = phi(qv);
-            V(V_GO)[tid] = dO ? dO[((size_t)bh * T + t) * D + tid] : 0.f;
-            V(V_T0)[tid] = uv;
-            V(V_T1)[tid] = kv;
-        }
-        const float delta = r[3 * D], na = r[3 * D + 1], dsg = r[3 * D + 2];
+        const unsigned char* sl = ring + (t % NB2) * L::SLOT_B;
+        const float* rec = reinterpret_cast<const float*>(sl + L::TP);
+        const float* gov = reinterpret_cast<const float*>(sl + L::G);
+        float* r1 = R1 + (t & 1) * 2 * D;
+        const float dl = rec[3 * D], na = rec[3 * D + 1], dsg = rec[3 * D + 2];
+        const float nu = rec[3 * D + 3], nk = rec[3 * D + 4];
         const bool clamped = dsg < 0.f;
-        const float den = clamped ? -dsg : dsg;
-        const float nu = block_sum<NT>(uv * uv, red), nk = block_sum<NT>(kv * kv, red);
-        const float iu = 1.f / fmaxf(sqrtf(nu), 1e-12f), ik = 1.f / fmaxf(sqrtf(nk), 1e-12f);
-        if (tid < D) {
-            V(V_UH)[tid] = uv * iu;
-            V(V_KH)[tid] = kv * ik;
+        const float rden = rcpa(clamped ? -dsg : dsg), rdl = rcpa(dl);
+        const float iu = inv_norm(nu), ik = inv_norm(nk);
+        const bool tiny = na < 1e-12f;
+        const float nac = fmaxf(na, 1e-12f), ina = rcpa(nac);
+        const size_t orow = ((size_t)bh * T + t) * D;
+
+        // this lane's columns
+        float uh[CL], kh[CL], pq[CL], zc[CL], al[CL];
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            const int j = l + 32 * c;
+            uh[c] = lds_in<TIn>(sl + L::U, j) * iu;
+            kh[c] = lds_in<TIn>(sl + L::K, j) * ik;
+            pq[c] = phi(lds_in<TIn>(sl + L::Q, j));
+            zc[c] = rec[j];
+            al[c] = rec[D + j];
         }
-        __syncthreads();
-        // round 1 (gS, gA are the adjoints of S_t, A_t before this token's terms):
-        // o = S_t phi_q / den, S_t^T gO, gS alpha, gS^T e, gA z, gA^T z
+        // round 1 (gS, gA: adjoints of S_t, A_t before this token's terms)
+        //   rows: gS alpha^, gA z;  columns: gS^T e, S_t^T dL/do, gA^T z
         {
-            const float* M;
-            const float* x;
-            bool col;
-            int out;
-            switch (grp) {
-                case 0: M = S; x = V(V_PQ); col = false; out = V_O; break;
-                case 1: M = S; x = V(V_GO); col = true; out = V_GPQ; break;
-                case 2: M = gS; x = V(V_AL); col = false; out = V_GE; break;
-                case 3: M = gS; x = V(V_E); col = true; out = V_GAL; break;
-                case 4: M = gA; x = V(V_Z); col = false; out = V_T2; break;
-                default: M = gA; x = V(V_Z); col = true; out = V_T3; break;
+            float pg[RW], pz[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                pg[r] = pz[r] = 0.f;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    pg[r] = fmaf(gS[r][c], al[c], pg[r]);
+                    pz[r] = fmaf(gA[r][c], zc[c], pz[r]);
+                }
             }
-            float s = 0.f;
-            if (col) {
-                for (int i = 0; i < D; ++i) s = fmaf(M[i * LD + li], x[i], s);
-            } else {
-                for (int j = 0; j < D; ++j) s = fmaf(M[li * LD + j], x[j], s);
+            const float gsal = rowsum8(pg), gaz = rowsum8(pz);
+            if ((l & 3) == 0) {
+                r1[rr] = gsal;
+                r1[D + rr] = gaz;
             }
-            V(out)[li] = s;
         }
-        __syncthreads();
+        // token dots and this warp's share of the dots of the column products:
+        // phi_q.alpha^, dL/do.e, k^.z, phi_q.z, alpha^.z | phi_q.S^T gO, alpha^.gS^T e
+        // (= e.gS alpha^), z.gS^T e, z.gA^T z
+        float d9[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        {
+            float er[RW], gor[RW], zr[RW], qe[CL], qo[CL], qz[CL];
+            lds8f(rec + 2 * D, r0, er);
+            lds8f(gov, r0, gor);
+            lds8f(rec, r0, zr);
+#pragma unroll
+            for (int c = 0; c < CL; ++c) qe[c] = qo[c] = qz[c] = 0.f;
+#pragma unroll
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    qe[c] = fmaf(gS[r][c], er[r], qe[c]);
+                    qo[c] = fmaf(S[r][c], gor[r], qo[c]);
+                    qz[c] = fmaf(gA[r][c], zr[r], qz[c]);
+                }
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                const int j = l + 32 * c;
+                P1[(w * 3 + 0) * D + j] = qe[c];
+                P1[(w * 3 + 1) * D + j] = qo[c];
+                P1[(w * 3 + 2) * D + j] = qz[c];
+                d9[0] = fmaf(pq[c], al[c], d9[0]);
+                d9[1] = fmaf(gov[j], rec[2 * D + j], d9[1]);
+                d9[2] = fmaf(kh[c], zc[c], d9[2]);
+                d9[3] = fmaf(pq[c], zc[c], d9[3]);
+                d9[4] = fmaf(al[c], zc[c], d9[4]);
+                d9[5] = fmaf(pq[c], qo[c], d9[5]);
+                d9[6] = fmaf(al[c], qe[c], d9[6]);
+                d9[7] = fmaf(zc[c], qe[c], d9[7]);
+                d9[8] = fmaf(zc[c], qz[c], d9[8]);
+            }
+        }
+        allreduce<5, 16>(d9);             // token dots: every lane needs them
+        reduce_scatter<4, 16>(d9 + 5, l);  // this warp's shares: one lane per dot writes it
+        {
+            const int x = rs_index<4, 16>(l, 0);
+            if (x >= 0) DP[x * NW + w] = d9[5];
+        }
+        cp_wait<1>();
+        __syncthreads();  // B1 (also publishes token t-1's slot)
+        // the slot of token t+2 is free: prefetch token t-3 into it
+        if (t >= 3) prefetch_rev<D, TIn>(ring + ((t - 3) % NB2) * L::SLOT_B, gu, gk, gq, go_h, tp, t - 3);
+        cp_commit();
+        if (tid < 3 * D) {
+            const int x = tid / D, j = tid - x * D;
+            float s = 0.f;
+#pragma unroll
+            for (int v = 0; v < NW; ++v) s += P1[(v * 3 + x) * D + j];
+            C1[x * D + j] = s;
+        } else {
+            if (w == NW - 1 && l < 4) {
+                float s = 0.f;
+#pragma unroll
+                for (int v = 0; v < NW; ++v) s += DP[l * NW + v];
+                DS[l] = s;
+            }
+            if (t + 1 < T) {  // dL/dk, dL/du of token t+1
+                const bool ok = ku_grads<D, TIn>(ring + ((t + 1) % NB2) * L::SLOT_B, P2, R2, RED, jw, pick<CL>(gzk, jw),
+                                                 j_ege, j_kz, j_gdl, j_zgz, j_az, j_nac, j_dl, j_nu, j_nk,
+                                                 dk + orow + D, du + orow + D);
+                if (!ok) bad = true;
+            }
+        }
+        __syncthreads();  // B2
+
         // scalars of the adjoint step
-        const float go_o = block_sum<NT>(tid < D ? V(V_GO)[tid] * V(V_O)[tid] : 0.f, red) / den;  // gO . o_t
-        const float pq_al = block_sum<NT>(tid < D ? V(V_PQ)[tid] * V(V_AL)[tid] : 0.f, red);
-        const float go_e = block_sum<NT>(tid < D ? V(V_GO)[tid] * V(V_E)[tid] : 0.f, red);
-        const float gden = clamped ? 0.f : -go_o / den;
-        if (tid < D) {
-            // gS_t = gS + gO phi_q^T / den: its products with alpha and e
-            V(V_GE)[tid] = fmaf(V(V_GO)[tid], pq_al / den, V(V_GE)[tid]);                    // g_e = gS_t alpha
-            V(V_GAL)[tid] = fmaf(V(V_PQ)[tid], go_e / den, V(V_GAL)[tid]);                   // g_alpha = gS_t^T e
-            V(V_GPQ)[tid] = fmaf(gden, V(V_ZK)[tid], V(V_GPQ)[tid] / den);                   // g_phiq
-            gzk = fmaf(gden, V(V_PQ)[tid], gzk);
-        }
-        __syncthreads();
-        const float al_gal = block_sum<NT>(tid < D ? V(V_AL)[tid] * V(V_GAL)[tid] : 0.f, red);
-        const float e_ge = block_sum<NT>(tid < D ? V(V_E)[tid] * V(V_GE)[tid] : 0.f, red);
-        const float ina = na < 1e-12f ? 1e12f : 1.f / na;
-        if (tid < D)  // g_a = (g_alpha - alpha (alpha . g_alpha)) / ||a||
-            V(V_GA)[tid] = (na < 1e-12f ? V(V_GAL)[tid] : fmaf(-V(V_AL)[tid], al_gal, V(V_GAL)[tid])) * ina;
-        __syncthreads();
-        // round 2: S_t^T g_e (then S_{t-1}^T g_e = S_t^T g_e - alpha (e . g_e)), A_t^T g_a
-        if (grp == 0) {
-            float s = 0.f;
-            for (int i = 0; i < D; ++i) s = fmaf(S[i * LD + li], V(V_GE)[i], s);
-            V(V_T4)[li] = s;
-        } else if (grp == 1) {
-            float s = 0.f;
-            for (int i = 0; i < D; ++i) s = fmaf(A[i * LD + li], V(V_GA)[i], s);
-            V(V_T5)[li] = s;
-        }
-        __syncthreads();
-        // g_k^ = -S_{t-1}^T g_e + A_t^T g_a; the A adjoint now includes g_a k^^T:
-        // (gA + g_a k^^T) z and its transpose product, z^T gA z
-        const float kz = block_sum<NT>(tid < D ? V(V_KH)[tid] * V(V_Z)[tid] : 0.f, red);
-        const float az = block_sum<NT>(tid < D ? V(V_GA)[tid] * V(V_Z)[tid] : 0.f, red);
-        const float zgz0 = block_sum<NT>(tid < D ? V(V_Z)[tid] * V(V_T2)[tid] : 0.f, red);
-        if (tid < D) {
-            V(V_GKH)[tid] = -fmaf(-V(V_AL)[tid], e_ge, V(V_T4)[tid]) + V(V_T5)[tid];
-            const float gaz = fmaf(V(V_GA)[tid], kz, V(V_T2)[tid]);   // (gA + g_a k^^T) z
-            const float gatz = fmaf(V(V_KH)[tid], az, V(V_T3)[tid]);  // (gA + g_a k^^T)^T z
-            V(V_GZ)[tid] = -(gaz + gatz) / delta;
-        }
-        const float zgz = fmaf(az, kz, zgz0);
-        const float gdelta = zgz / (delta * delta);
-        __syncthreads();
-        if (tid < D) V(V_GZ)[tid] = fmaf(gdelta, V(V_UH)[tid], V(V_GZ)[tid]);
-        __syncthreads();
-        // round 3: A_t^T g_z (A_{t-1}^T g_z = A_t^T g_z + z (z . g_z) / delta)
-        if (grp == 0) {
-            float s = 0.f;
-            for (int i = 0; i < D; ++i) s = fmaf(A[i * LD + li], V(V_GZ)[i], s);
-            V(V_T6)[li] = s;
-        }
-        __syncthreads();
-        const float zgzz = block_sum<NT>(tid < D ? V(V_Z)[tid] * V(V_GZ)[tid] : 0.f, red);
-        if (tid < D) V(V_GUH)[tid] = fmaf(gdelta, V(V_Z)[tid], fmaf(V(V_Z)[tid], zgzz / delta, V(V_T6)[tid]));
-        __syncthreads();
-        // gradients of the token's inputs
-        const float ugu = block_sum<NT>(tid < D ? V(V_UH)[tid] * V(V_GUH)[tid] : 0.f, red);
-        const float kgk = block_sum<NT>(tid < D ? V(V_KH)[tid] * V(V_GKH)[tid] : 0.f, red);
-        if (tid < D) {
-            const size_t o = ((size_t)bh * T + t) * D + tid;
-            const float dut = nu < 1e-24f ? V(V_GUH)[tid] * 1e12f : fmaf(-V(V_UH)[tid], ugu, V(V_GUH)[tid]) * iu;
-            const float dkt = nk < 1e-24f ? V(V_GKH)[tid] * 1e12f : fmaf(-V(V_KH)[tid], kgk, V(V_GKH)[tid]) * ik;
-            du[o] = dut;
-            dk[o] = fmaf(gzk, phi_d(kv), dkt);
-            dq[o] = V(V_GPQ)[tid] * phi_d(qv);
-            dv[o] = V(V_GE)[tid];
-            if (!isfinite(dut) || !isfinite(dk[o]) || !isfinite(dq[o]) || !isfinite(dv[o])) nonfinite = true;
-            // z^key_{t-1} = z^key_t - phi(k_t)
-            V(V_ZK)[tid] -= phi(kv);
-        }
-        // adjoints of S_{t-1}, A_{t-1}; states S_{t-1}, A_{t-1}
-        //   gS += gO phi_q^T / den - g_e k^^T;  gA += g_a k^^T + g_z u^^T
-        //   S_{t-1} = S_t - e alpha^^T;  A_{t-1} = A_t + z z^T / delta
-        const bool reload = (t % CK == 0);
-        const float rden = 1.f / den, rdl = 1.f / delta;
-        const float* c = cp + (size_t)(t / CK) * 2 * D * D;
-        for (int e = tid; e < D * D; e += NT) {
-            const int i = e / D, j = e - i * D;
-            const int x = i * LD + j;
-            gS[x] = fmaf(V(V_GO)[i] * rden, V(V_PQ)[j], fmaf(-V(V_GE)[i], V(V_KH)[j], gS[x]));
-            gA[x] = fmaf(V(V_GA)[i], V(V_KH)[j], fmaf(V(V_GZ)[i], V(V_UH)[j], gA[x]));
-            if (reload) {
-                S[x] = c[e];
-                A[x] = c[D * D + e];
-            } else {
-                S[x] = fmaf(-V(V_E)[i], V(V_AL)[j], S[x]);
-                A[x] = fmaf(V(V_Z)[i] * rdl, V(V_Z)[j], A[x]);
+        const float c1n = d9[0], c2n = d9[1], kz = d9[2];
+        const float c1 = c1n * rden, c2 = c2n * rden;
+        const float s_o = DS[0], s_ae = DS[1], s_ze = DS[2], s_zz = DS[3];
+        const float gden = clamped ? 0.f : -s_o * rden * rden;     // -(dL/do . o) / den
+        const float al_gal = fmaf(c2, c1n, s_ae);                   // alpha^ . g_alpha
+        const float e_ge = fmaf(c1, c2n, s_ae);                     // e . g_e
+        const float galz = fmaf(c2, d9[3], s_ze);                   // g_alpha . z
+        const float az = (tiny ? galz : fmaf(-al_gal, d9[4], galz)) * ina;  // g_a . z
+        const float zgz = fmaf(az, kz, s_zz);                       // z^T (gA + g_a k^^T) z
+        const float gdl = zgz * rdl * rdl;                          // dL/d delta
+        // columns: g_a, w1 = (gA + gA^T) z, g_z, dL/dphi_q
+        float gac[CL], w1c[CL], gzc[CL];
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            const int j = l + 32 * c;
+            const float gal = fmaf(pq[c], c2, C1[j]);
+            gac[c] = (tiny ? gal : fmaf(-al[c], al_gal, gal)) * ina;
+            w1c[c] = r1[D + j] + C1[2 * D + j];
+            // g_z = -((gA + g_a k^^T) z + (gA + g_a k^^T)^T z) / delta + g_delta u^
+            gzc[c] = fmaf(gdl, uh[c], -(w1c[c] + fmaf(gac[c], kz, kh[c] * az)) * rdl);
+            const float gpq = fmaf(gden, zk[c], C1[D + j] * rden);
+            gzk[c] = fmaf(gden, pq[c], gzk[c]);
+            if (w == 0) {
+                const float x = gpq * phi_d(lds_in<TIn>(sl + L::Q, j));
+                dq[orow + j] = x;
+                if (!isfinite(x)) bad = true;
             }
         }
-        __syncthreads();
+        // rows: g_e
+        float ger[RW];
+        {
+            float a8[RW], b8[RW];
+            lds8f(r1, r0, a8);   // gS alpha^
+            lds8f(gov, r0, b8);  // dL/do
+#pragma unroll
+            for (int r = 0; r < RW; ++r) ger[r] = fmaf(b8[r], c1, a8[r]);
+        }
+        if (l < RW) {
+            const float x = pick<RW>(ger, l);
+            dv[orow + r0 + l] = x;
+            if (!isfinite(x)) bad = true;
+        }
+        // round 2: columns S_t^T g_e; rows A_t g_a, A_t w1
+        {
+            float pa[RW], pw[RW], qg[CL];
+#pragma unroll
+            for (int c = 0; c < CL; ++c) qg[c] = 0.f;
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                pa[r] = pw[r] = 0.f;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    qg[c] = fmaf(S[r][c], ger[r], qg[c]);
+                    pa[r] = fmaf(A[r][c], gac[c], pa[r]);
+                    pw[r] = fmaf(A[r][c], w1c[c], pw[r]);
+                }
+            }
+            const float aga = rowsum8(pa), aw1 = rowsum8(pw);
+            if ((l & 3) == 0) {
+                R2[rr] = aga;
+                R2[D + rr] = aw1;
+            }
+#pragma unroll
+            for (int c = 0; c < CL; ++c) P2[w * D + l + 32 * c] = qg[c];
+        }
+        // adjoints of S_{t-1}, A_{t-1}:
+        //   gS += dL/do phi_q^T / den - g_e k^^T;  gA += g_a k^^T + g_z u^^T
+        {
+            float gor[RW];
+            lds8f(gov, r0, gor);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const float gs = gor[r] * rden;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) gS[r][c] = fmaf(gs, pq[c], fmaf(-ger[r], kh[c], gS[r][c]));
+            }
+        }
+        {
+            // this warp's rows of g_a and g_z: rows r0 .. r0+7 are columns held by
+            // lanes (r0 mod 32) .. +7 in slot r0 / 32
+            const int cs = r0 >> 5, lb = r0 & 31;
+            const float ga_s = pick<CL>(gac, cs), gz_s = pick<CL>(gzc, cs);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const float gar = __shfl_sync(FULL, ga_s, lb + r), gzr = __shfl_sync(FULL, gz_s, lb + r);
+#pragma unroll
+                for (int c = 0; c < CL; ++c) gA[r][c] = fmaf(gar, kh[c], fmaf(gzr, uh[c], gA[r][c]));
+            }
+        }
+        // states before the token: S_{t-1} = S_t - e alpha^^T, A_{t-1} = A_t + z z^T / delta,
+        // z^key_{t-1} = z^key_t - phi(k_t); exact copies at checkpoints
+        if (t % CK == 0) {
+            const float* c = cp + (size_t)(t / CK) * L::CREC;
+#pragma unroll
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int cc = 0; cc < CL; ++cc) {
+                    const int e = (r0 + r) * D + l + 32 * cc;
+                    S[r][cc] = c[e];
+                    A[r][cc] = c[D * D + e];
+                }
+#pragma unroll
+            for (int cc = 0; cc < CL; ++cc) zk[cc] = c[2 * D * D + l + 32 * cc];
+        } else {
+            float er[RW], zr[RW];
+            lds8f(rec + 2 * D, r0, er);
+            lds8f(rec, r0, zr);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const float zs = zr[r] * rdl;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    S[r][c] = fmaf(-er[r], al[c], S[r][c]);
+                    A[r][c] = fmaf(zs, zc[c], A[r][c]);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < CL; ++c) zk[c] -= phi(lds_in<TIn>(sl + L::K, l + 32 * c));
+        }
+        j_ege = e_ge, j_kz = kz, j_gdl = gdl, j_zgz = zgz, j_az = az, j_nac = nac, j_dl = dl, j_nu = nu, j_nk = nk;
     }
-    for (int e = tid; e < D * D; e += NT) {
-        const int i = e / D, j = e - i * D;
-        const size_t g = (size_t)bh * D * D + e;
-        if (dS0) dS0[g] = gS[i * LD + j];
-        if (dA0) dA0[g] = gA[i * LD + j];
+    __syncthreads();  // round-2 products of token 0 visible
+    if (T > 0 && ku_warp) {
+        const bool ok = ku_grads<D, TIn>(ring, P2, R2, RED, jw, pick<CL>(gzk, jw), j_ege, j_kz, j_gdl, j_zgz, j_az,
+                                         j_nac, j_dl, j_nu, j_nk, dk + (size_t)bh * T * D, du + (size_t)bh * T * D);
+        if (!ok) bad = true;
     }
-    if (tid < D && dzk0) dzk0[(size_t)bh * D + tid] = gzk;
-    if (nonfinite) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            const size_t e = hdd + (r0 + r) * D + l + 32 * c;
+            if (dS0) dS0[e] = gS[r][c];
+            if (dA0) dA0[e] = gA[r][c];
+        }
+    if (w == 0 && dzk0)
+#pragma unroll
+        for (int c = 0; c < CL; ++c) dzk0[(size_t)bh * D + l + 32 * c] = gzk[c];
+    if (bad) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
 }
 
 }  // namespace bw

@@ -1372,8 +1372,9 @@ bool bw_sizes(int B, int H, int T, int d, BwSizes* out) {
     if (B < 0 || H < 0 || T < 0 || d <= 0) return false;
     const unsigned long long BH = (unsigned long long)B * (unsigned long long)H;
     const unsigned long long nck = (unsigned long long)((T + vla::bw::CK - 1) / vla::bw::CK + 1);
-    const unsigned long long tape = BH * (unsigned long long)T * (unsigned long long)(3 * d + 4) * 4ull;
-    const unsigned long long ck = BH * nck * 2ull * (unsigned long long)d * (unsigned long long)d * 4ull;
+    const unsigned long long tape = BH * (unsigned long long)T * (unsigned long long)(3 * d + 8) * 4ull;
+    const unsigned long long ck =
+        BH * nck * (2ull * (unsigned long long)d * (unsigned long long)d + (unsigned long long)d) * 4ull;
     if (BH > (1ull << 31) || tape > (1ull << 50) || ck > (1ull << 50)) return false;
     auto al = [](unsigned long long x) { return (x + 255ull) / 256ull * 256ull; };
     out->tape = (size_t)al(tape);
@@ -1386,7 +1387,7 @@ template <int D, typename TIn>
 vla_status launch_bw(const vla::Params& p, int BH, const float* dO, const float* dST, const float* dAT,
                      const float* dzkT, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
                      float* dzk0, float* tape, float* ckpt, cudaStream_t s) {
-    using BL = vla::bw::BLay<D>;
+    using BL = vla::bw::BLay<D, TIn>;
     auto kern = vla::bw::vla_backward_kernel<D, TIn>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BL::SMEM) != cudaSuccess)
         return VLA_ERR_CUDA;

@@ -37,6 +37,7 @@ __all__ = [
     "normal",
     "recall",
     "make",
+    "upstream_grad",
     "to_bf16_values",
 ]
 
@@ -161,3 +162,14 @@ def make(w: Workload, B=None, H=None, T=None):
     if w.dtype == "bf16":
         arrs = tuple(to_bf16_values(a) for a in arrs)
     return arrs
+
+
+def upstream_grad(w: Workload, B=None, H=None, T=None, seed_offset=1000):
+    """A seeded upstream gradient dL/do of workload ``w`` for the backward
+    pass: float32 N(0,1) of shape [B, H, T, d], from
+    ``default_rng(w.seed + seed_offset)``."""
+    B = w.B if B is None else B
+    H = w.H if H is None else H
+    T = w.T if T is None else T
+    rng = np.random.default_rng(w.seed + seed_offset)
+    return rng.standard_normal((B, H, T, w.d), dtype=np.float32)

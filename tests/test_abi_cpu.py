@@ -103,10 +103,12 @@ def test_algo_argument_errors(lib, algo, d, status):
 
 
 def test_backward_workspace_bytes(lib):
-    """Status record + tape (3d + 4 floats per head-token) + S, A checkpoints
-    every 64 tokens plus the initial one (2 d^2 floats each), 256-byte aligned."""
-    assert lib.vla_backward_workspace_bytes(1, 1, 64, 32) == 256 + 64 * 100 * 4 + 2 * 2 * 32 * 32 * 4
-    assert lib.vla_backward_workspace_bytes(2, 3, 65, 96) == 256 + (6 * 65 * 292 * 4 + 255) // 256 * 256 + 6 * 3 * 2 * 96 * 96 * 4
+    """Status record + tape (3d + 8 floats per head-token) + S, A, z^key
+    checkpoints every 64 tokens plus the initial one (2 d^2 + d floats each),
+    each part 256-byte aligned."""
+    al = lambda x: (x + 255) // 256 * 256
+    assert lib.vla_backward_workspace_bytes(1, 1, 64, 32) == 256 + al(64 * 104 * 4) + al(2 * (2 * 32 * 32 + 32) * 4)
+    assert lib.vla_backward_workspace_bytes(2, 3, 65, 96) == 256 + al(6 * 65 * 296 * 4) + al(6 * 3 * (2 * 96 * 96 + 96) * 4)
     assert lib.vla_backward_workspace_bytes(1, 1, 0, 64) > 0
     assert lib.vla_backward_workspace_bytes(-1, 1, 4, 64) == 0
     assert lib.vla_backward_workspace_bytes(1 << 30, 1 << 30, 4, 64) == 0
