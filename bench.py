@@ -22,6 +22,7 @@ dL/do; the forward recurrence is recomputed inside the call).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -51,7 +52,9 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
 # sources hash to SOURCE_SHA; otherwise reported as null.
 NCU_TRAFFIC = {"source_sha": "757966978bd67c06", "bytes_per_launch": 402742272 + 175727360}
-NCU_TRAFFIC_BW = {"source_sha": None, "bytes_per_launch": None}
+# the backward kernel's, from a capture of the same workload at B=2 (32 heads; a full launch holds
+# about 2.6 GB on the device) scaled by 4: every byte it moves is per head-token or per head
+NCU_TRAFFIC_BW = {"source_sha": "200d44df5443e982", "bytes_per_launch": 4 * (486493440 + 484519680)}
 
 
 def kernel_source_sha() -> str:
@@ -512,12 +515,16 @@ def main(argv=None):
                     help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96), 1 per-token, 2 chunked")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
                     help="time the forward recurrence (default) or its reverse-mode gradient")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size B (smaller cases for profiler captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from sherman_morrison_memory_gb300 import workloads as W
 
     w = W.WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = dataclasses.replace(w, B=args.batch)
     if args.impl == "reference":
         run_reference(args, w)
     elif args.pass_ == "backward":

@@ -197,7 +197,9 @@ size_t vla_backward_workspace_bytes(int B, int H, int T, int d);
  * it writes dq, dk, dv, du [B,H,T,d] = dL/dq_t ... (fp32) and, where not NULL,
  * dS0, dA0 [B,H,d,d] and dzk0 [B,H,d] = dL/d(initial state). q, k, v, u,
  * dtype, sizes, lambda0, eps and the optional initial state (S0, A0, zk0) are
- * those of the forward call; the forward pass is recomputed inside.
+ * those of the forward call; the forward pass is recomputed inside. A0, when
+ * given, must be symmetric, as every state of the recurrence is (A_t is the
+ * inverse of a symmetric matrix); the kernel uses A_t^T = A_t.
  *
  * Layout and ownership as for vla_forward(); every gradient is fp32,
  * row-major, caller-owned device memory, 16-byte aligned (state pointers
