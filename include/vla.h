@@ -65,17 +65,29 @@ typedef struct {
                                     of 16*T u64 that receives per-token SM clock stamps of head 0
                                     (roles and sub-steps of the per-token kernel); else ignored */
     int algo;                    /* VLA_ALGO_*: which kernel runs the recurrence (0 = automatic) */
+    int fixed_a;                 /* nonzero: the fixed-A variant ("Variational Linear Attention",
+                                    §3.5 ablation): A is held at its initial value (A0, or I/lambda0)
+                                    and eq. 9 is skipped, so alpha^_t = A0 k^_t / ||A0 k^_t||; u is
+                                    not read and may be NULL. Runs on VLA_ALGO_CHUNKED (d <= 96;
+                                    the A team only forms A0 k^) and VLA_ALGO_DECODE; VLA_ALGO_AUTO
+                                    picks the decode kernel for T <= 4 or d = 128, else the chunked
+                                    one; VLA_ALGO_PER_TOKEN returns VLA_ERR_UNSUPPORTED */
 } vla_options;
 
-/* Kernels behind vla_forward_ex() (vla_options.algo). Both compute eq. 9-11
+/* Kernels behind vla_forward_ex() (vla_options.algo). All compute eq. 9-11
  * exactly up to rounding order.
- *   VLA_ALGO_AUTO       chunked tensor-core kernel for d <= 96, per-token kernel for d = 128
+ *   VLA_ALGO_AUTO       decode kernel for T <= 4; otherwise the chunked tensor-core kernel
+ *                       for d <= 96, the per-token kernel for d = 128 (the decode kernel for
+ *                       the fixed-A variant at d = 128)
  *   VLA_ALGO_PER_TOKEN  one token at a time on the FMA pipes (any supported d)
  *   VLA_ALGO_CHUNKED    16 tokens at a time: the Sherman-Morrison steps of a chunk as an
  *                       LDL^T factorisation, the d x d products on the tcgen05 tensor cores
  *                       in 3-term tf32 (fp32 accuracy); d in {32, 64, 96}, else
- *                       VLA_ERR_UNSUPPORTED. Any other value: VLA_ERR_INVALID_ARG. */
-enum { VLA_ALGO_AUTO = 0, VLA_ALGO_PER_TOKEN = 1, VLA_ALGO_CHUNKED = 2 };
+ *                       VLA_ERR_UNSUPPORTED
+ *   VLA_ALGO_DECODE     one token at a time with S and A in registers, laid out to stream
+ *                       the carried state: for decode (T = 1) and short sequences (any d)
+ * Any other value: VLA_ERR_INVALID_ARG. */
+enum { VLA_ALGO_AUTO = 0, VLA_ALGO_PER_TOKEN = 1, VLA_ALGO_CHUNKED = 2, VLA_ALGO_DECODE = 3 };
 
 /* Bytes of device workspace vla_forward() needs (one status record). The
  * workspace must be zero-filled before its first use (cudaMemset or

@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     VLA_ALGO_AUTO,
     VLA_ALGO_PER_TOKEN,
     VLA_ALGO_CHUNKED,
+    VLA_ALGO_DECODE,
     VLAError,
     library_path,
     load_library,

@@ -24,6 +24,7 @@ VLA_ERR_NONFINITE = 5
 VLA_ALGO_AUTO = 0
 VLA_ALGO_PER_TOKEN = 1
 VLA_ALGO_CHUNKED = 2
+VLA_ALGO_DECODE = 3
 
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
@@ -44,7 +45,7 @@ class VLAError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("wait_limit_us", ctypes.c_uint), ("test_stall_producer", ctypes.c_int),
-                ("trace", ctypes.c_void_p), ("algo", ctypes.c_int)]
+                ("trace", ctypes.c_void_p), ("algo", ctypes.c_int), ("fixed_a", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -134,7 +135,7 @@ def _check_state(x, shape, device, name):
 def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tensor,
                 lambda0: float = 0.1, eps: float = 1e-4, state=None, *, out=None, stream=None,
                 check: bool = False, wait_limit_us: int = 0, test_stall_producer: bool = False,
-                algo: int = 0):
+                algo: int = 0, fixed_a: bool = False):
     """VLA forward recurrence (§3.3 eq. 9-11) over all heads.
 
     Returns ``(o, (S, A, zk))``: o [B,H,T,d] float32, S and A [B,H,d,d], zk [B,H,d].
@@ -142,20 +143,28 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
     ``out`` = (o, S, A, zk) preallocated outputs on the inputs' device.
     CPU inputs run on the current CUDA device with host<->device copies.
     ``check=True`` synchronises and raises on an in-kernel failure.
-    ``algo`` selects the kernel: VLA_ALGO_AUTO (0), VLA_ALGO_PER_TOKEN (1) or
-    VLA_ALGO_CHUNKED (2, the tensor-core chunked kernel, d <= 96).
+    ``algo`` selects the kernel: VLA_ALGO_AUTO (0), VLA_ALGO_PER_TOKEN (1),
+    VLA_ALGO_CHUNKED (2, the tensor-core chunked kernel, d <= 96) or
+    VLA_ALGO_DECODE (3, short sequences with a carried state).
+    ``fixed_a=True`` runs the fixed-A variant (§3.5 ablation): A stays at its
+    initial value, u is not read (it may be None).
     """
     if q.device.type == "cpu":
-        return _forward_host(q, k, v, u, lambda0, eps, state, out=out, check=check, algo=algo)
+        return _forward_host(q, k, v, u, lambda0, eps, state, out=out, check=check, algo=algo, fixed_a=fixed_a)
     lib = load_library()
+    if u is None and not fixed_a:
+        raise ValueError("u is required unless fixed_a=True")
     for name, x in (("k", k), ("v", v), ("u", u)):
+        if x is None:
+            continue
         if x.shape != q.shape or x.dtype != q.dtype or x.device != q.device:
             raise ValueError(f"{name} must match q in shape, dtype and device")
     if q.dim() != 4:
         raise ValueError("q, k, v, u must be [B, H, T, d]")
     if q.dtype not in _DTYPES:
         raise ValueError(f"unsupported input dtype {q.dtype} (float32 or bfloat16)")
-    q, k, v, u = (x.contiguous() for x in (q, k, v, u))
+    q, k, v = (x.contiguous() for x in (q, k, v))
+    u = None if u is None else u.contiguous()
     B, H, T, d = q.shape
     dev = q.device
     S0 = A0 = zk0 = None
@@ -177,8 +186,9 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
         args = (_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d,
                 float(lambda0), float(eps), _ptr(S0), _ptr(A0), _ptr(zk0),
                 _ptr(o), _ptr(S), _ptr(A), _ptr(zk), _ptr(ws), ws.numel() * 4, ctypes.c_void_p(sh))
-        if wait_limit_us or test_stall_producer or algo:
-            opts = _Options(int(wait_limit_us), 1 if test_stall_producer else 0, None, int(algo))
+        if wait_limit_us or test_stall_producer or algo or fixed_a:
+            opts = _Options(int(wait_limit_us), 1 if test_stall_producer else 0, None, int(algo),
+                            1 if fixed_a else 0)
             st = lib.vla_forward_ex(*args, ctypes.byref(opts))
         else:
             st = lib.vla_forward(*args)
@@ -191,16 +201,17 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
     return o, (S, A, zk)
 
 
-def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False, algo=0):
+def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False, algo=0, fixed_a=False):
     """Host buffers in, host buffers out: H2D copies, the kernel, D2H copies,
     all on the current stream of the current CUDA device. ``out`` may hold
     preallocated (pinned) host outputs (o, S, A, zk)."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    dq, dk, dv, du = (x.to(dev, non_blocking=True) for x in (q, k, v, u))
+    dq, dk, dv = (x.to(dev, non_blocking=True) for x in (q, k, v))
+    du = None if u is None else u.to(dev, non_blocking=True)
     dstate = None
     if state is not None:
         dstate = tuple(None if x is None else x.to(dev, non_blocking=True) for x in state)
-    o, (S, A, zk) = vla_forward(dq, dk, dv, du, lambda0, eps, dstate, check=check, algo=algo)
+    o, (S, A, zk) = vla_forward(dq, dk, dv, du, lambda0, eps, dstate, check=check, algo=algo, fixed_a=fixed_a)
     pin = q.is_pinned()
     outs = []
     for i, x in enumerate((o, S, A, zk)):

@@ -144,6 +144,7 @@ struct Params {
     unsigned long long wait_ns;
     int stall_producer;
     unsigned long long* trace;
+    int fixed_a;  // the fixed-A variant: A stays A0 and eq. 9 is skipped
 };
 
 // Per-token clock stamps of head 0 for pipeline analysis (-DVLA_TRACE builds only).
@@ -1104,6 +1105,7 @@ __global__ void __launch_bounds__(LA_THREADS) la_state_kernel(const TIn* k, cons
 
 #include "vla_tc.cuh"
 #include "vla_backward.cuh"
+#include "vla_decode.cuh"
 
 }  // namespace vla
 
@@ -1140,8 +1142,31 @@ vla_status launch_tc(const vla::Params& p, int BH, cudaStream_t s) {
 
 // algo: VLA_ALGO_AUTO picks the chunked tensor-core kernel where it exists
 // (d <= 96) and the per-token kernel otherwise.
+template <int D, typename TIn>
+vla_status launch_dec(const vla::Params& p, int BH, bool fixed_a, cudaStream_t s) {
+    using DL = vla::dec::DLay<D>;
+    if (fixed_a)
+        vla::dec::vla_decode_kernel<D, TIn, true><<<BH, DL::THREADS, DL::SMEM, s>>>(p);
+    else
+        vla::dec::vla_decode_kernel<D, TIn, false><<<BH, DL::THREADS, DL::SMEM, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
+}
+
+// sequences up to this length go to the decode kernel under VLA_ALGO_AUTO
+constexpr int kDecodeMaxT = 4;
+
 template <typename TIn>
-vla_status launch_d(int d, int algo, const vla::Params& p, int BH, cudaStream_t s) {
+vla_status launch_d(int d, int algo, bool fixed_a, const vla::Params& p, int BH, cudaStream_t s) {
+    if (algo == VLA_ALGO_DECODE || (algo == VLA_ALGO_AUTO && (p.T <= kDecodeMaxT || (fixed_a && d > 96)))) {
+        switch (d) {
+            case 32: return launch_dec<32, TIn>(p, BH, fixed_a, s);
+            case 64: return launch_dec<64, TIn>(p, BH, fixed_a, s);
+            case 96: return launch_dec<96, TIn>(p, BH, fixed_a, s);
+            case 128: return launch_dec<128, TIn>(p, BH, fixed_a, s);
+            default: return VLA_ERR_UNSUPPORTED;
+        }
+    }
+    if (fixed_a && algo == VLA_ALGO_PER_TOKEN) return VLA_ERR_UNSUPPORTED;
     const bool chunked = algo == VLA_ALGO_CHUNKED || (algo == VLA_ALGO_AUTO && d <= 96);
     if (chunked) {
         switch (d) {
@@ -1199,9 +1224,10 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
         return VLA_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) || workspace_bytes < kWorkspaceBytes) return VLA_ERR_INVALID_ARG;
     if (BH == 0) return VLA_OK;
+    const bool no_u = opts && opts->fixed_a;  // the fixed-A variant does not read u
     if (T > 0) {
-        if (!q || !k || !v || !u || !o) return VLA_ERR_INVALID_ARG;
-        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(u) || !aligned16(o))
+        if (!q || !k || !v || (!u && !no_u) || !o) return VLA_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (u && !aligned16(u)) || !aligned16(o))
             return VLA_ERR_INVALID_ARG;
     }
     if (!S_out || !A_out || !aligned16(S_out) || !aligned16(A_out)) return VLA_ERR_INVALID_ARG;
@@ -1229,14 +1255,19 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
     p.wait_ns = 1000ull * wait_us;
     p.stall_producer = (opts && opts->test_stall_producer) ? 1 : 0;
     p.trace = opts ? opts->trace : nullptr;
+    p.fixed_a = (opts && opts->fixed_a) ? 1 : 0;
+    if (p.fixed_a && !u) p.u = k;  // u is not used; staging reads a valid buffer of the same shape
 
     const int algo = opts ? opts->algo : VLA_ALGO_AUTO;
-    if (algo != VLA_ALGO_AUTO && algo != VLA_ALGO_PER_TOKEN && algo != VLA_ALGO_CHUNKED) return VLA_ERR_INVALID_ARG;
+    const bool fixed_a = opts && opts->fixed_a;
+    if (algo != VLA_ALGO_AUTO && algo != VLA_ALGO_PER_TOKEN && algo != VLA_ALGO_CHUNKED && algo != VLA_ALGO_DECODE)
+        return VLA_ERR_INVALID_ARG;
     if (algo == VLA_ALGO_CHUNKED && d > 96) return VLA_ERR_UNSUPPORTED;
+    if (fixed_a && algo == VLA_ALGO_PER_TOKEN) return VLA_ERR_UNSUPPORTED;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return dtype == VLA_BF16 ? launch_d<__nv_bfloat16>(d, algo, p, (int)BH, s)
-                             : launch_d<float>(d, algo, p, (int)BH, s);
+    return dtype == VLA_BF16 ? launch_d<__nv_bfloat16>(d, algo, fixed_a, p, (int)BH, s)
+                             : launch_d<float>(d, algo, fixed_a, p, (int)BH, s);
 }
 
 vla_status vla_forward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B, int H,

@@ -483,6 +483,9 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     float* zh = x.f(L::OFF_ZH);
     float* zl = x.f(L::OFF_ZL);
     bool bad = false, nonfinite = false;
+    // the fixed-A variant: A stays A_0, the gate is a_t = A_0 k^_t, and the
+    // Sherman-Morrison steps (Grams, LDL^T, update, lo refresh) are skipped
+    const bool fixed = p.fixed_a != 0;
 
     // A_0 = I / lambda0 unless carried in (eq. 9), and its lo part
     if (rw) {
@@ -555,23 +558,25 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 xr[t * XS + i] = v0[t];
                 xr[(C + t) * XS + i] = v1[t];
             }
-            put_row16(zh, i, v0, false);
-            put_row16(zl, i, v0, true);
+            if (!fixed) {
+                put_row16(zh, i, v0, false);
+                put_row16(zl, i, v0, true);
+            }
         }
         named_bar(ID_A, 128);
-        // Guu[s][t] = u^_s . z'_t, Guk[s][t] = u^_s . w_t; warp = (matrix, half of D),
-        // the half-D partials of a warp pair summed through shared memory
-        {
+        if (!fixed) {
+            // Guu[s][t] = u^_s . z'_t, Guk[s][t] = u^_s . w_t; warp = (matrix, half of D),
+            // the half-D partials of a warp pair summed through shared memory
             const int mat = warp & 1, half = warp >> 1;
             float acc[2][4];
             gram16<D, true>(hi, 0, xr + mat * C * XS, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc);
             gram_pair_sum(sm + (mat ? L::SM_GUK : L::SM_GUU), L::MS, L::GSTR, acc, lane, half, 4 + mat,
                           sc + L::SC_IU, false);
+            named_bar(ID_A, 128);
         }
-        named_bar(ID_A, 128);
         if (ta == 0) VLA_TRACE_AT(p, 6, c);
         if (ta == 0) mbar_arrive(x.b.empty_p + s);  // done with the chunk's u, k rows
-        if (warp == 3) {
+        if (warp == 3 && !fixed) {
             // LDL^T of I + Guu by Gaussian elimination of the augmented
             // [I + Guu | Guk]: lane j < C holds column j, lane C + j column j of
             // Guk. delta_t = pivot t (eq. 9's 1 + u^_t . z_t), L[r][t] = the
@@ -629,7 +634,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         // the -M operand first: the state update is issued before the gate,
         // which only the S team needs, is computed
         float y[C], lr[C];
-        if (rw) {
+        if (rw && !fixed) {
             // y = z_i = z'_i L^-T (forward substitution, in place), then y D^-1
 #pragma unroll
             for (int t = 0; t < C; ++t) y[t] = xr[t * XS + i];
@@ -660,7 +665,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         fence_proxy_async_smem();
         named_bar(ID_A, 128);
         // A_{c+1} = A_c - M Z'^T
-        if (ta == 0) {
+        if (ta == 0 && !fixed) {
             VLA_TRACE_AT(p, 8, c);
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, D);
@@ -681,10 +686,12 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             float av[C];
 #pragma unroll
             for (int t = 0; t < C; ++t) {
-                ld_row16(sm + L::SM_XGT + t * L::GSTR, lr);  // X[q][t]
                 float a = xr[(C + t) * XS + i];
+                if (!fixed) {
+                    ld_row16(sm + L::SM_XGT + t * L::GSTR, lr);  // X[q][t]
 #pragma unroll
-                for (int q = 0; q <= t; ++q) a = fmaf(-y[q], lr[q], a);
+                    for (int q = 0; q <= t; ++q) a = fmaf(-y[q], lr[q], a);
+                }
                 av[t] = t < n ? a : 0.f;
                 alr[t * XS + i] = av[t];
             }
@@ -708,11 +715,13 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             __syncwarp();
             if (lane == 0) mbar_arrive(x.b.full_al + b);
         }
-        bad = !mbar_wait(x.b.mma_a, pa, nullptr, p.wait_ns);
-        pa ^= 1;
+        if (!fixed) {
+            bad = !mbar_wait(x.b.mma_a, pa, nullptr, p.wait_ns);
+            pa ^= 1;
+        }
         if (ta == 0) VLA_TRACE_AT(p, 9, c);
         tc_fence_after();
-        if (rw) refresh_lo<D>(tl, L::T_A, L::T_AL);
+        if (rw && !fixed) refresh_lo<D>(tl, L::T_A, L::T_AL);
         if (ta == 0) VLA_TRACE_AT(p, 10, c);
         tc_fence_before();
         if (bar_red_or(ID_A, 128, bad)) {

@@ -89,17 +89,31 @@ def test_status_read_rejects_null(lib):
     assert list(d) == [-1, -1, -1]
 
 
-@pytest.mark.parametrize("algo,d,status", [(3, 64, 1), (-1, 64, 1), (2, 128, 2)])
-def test_algo_argument_errors(lib, algo, d, status):
-    """VLA_ALGO_* outside {0, 1, 2} is an argument error; the chunked kernel
-    reports d = 128 as unsupported. Both are decided before any CUDA call."""
+@pytest.mark.parametrize("algo,d,fixed,status", [
+    (4, 64, 0, 1), (-1, 64, 0, 1), (2, 128, 0, 2),
+    (1, 64, 1, 2), (2, 128, 1, 2),
+])
+def test_algo_argument_errors(lib, algo, d, fixed, status):
+    """VLA_ALGO_* outside {0, 1, 2, 3} is an argument error; the chunked kernel
+    reports d = 128 as unsupported; the fixed-A variant does not run on the
+    per-token kernel. All are decided before any CUDA call."""
     from sherman_morrison_memory_gb300 import _binding
     vp = ctypes.c_void_p
-    opts = _binding._Options(0, 0, None, algo)
+    opts = _binding._Options(0, 0, None, algo, fixed)
     st = lib.vla_forward_ex(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 1, 1, 1, 4, d, ctypes.c_float(0.1),
                             ctypes.c_float(1e-4), None, None, None, vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE),
                             ctypes.c_size_t(256), None, ctypes.byref(opts))
     assert st == status
+
+
+def test_u_may_be_null_only_for_fixed_a(lib):
+    from sherman_morrison_memory_gb300 import _binding
+    vp = ctypes.c_void_p
+    opts = _binding._Options(0, 0, None, 0, 0)
+    st = lib.vla_forward_ex(vp(FAKE), vp(FAKE), vp(FAKE), None, 1, 1, 1, 4, 64, ctypes.c_float(0.1),
+                            ctypes.c_float(1e-4), None, None, None, vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE),
+                            ctypes.c_size_t(256), None, ctypes.byref(opts))
+    assert st == 1
 
 
 def test_backward_workspace_bytes(lib):

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from parity_util import TOL, assert_close, errors, rel_heads, rel_rows, to_dev
-from sherman_morrison_memory_gb300 import (VLA_ALGO_CHUNKED, VLA_ALGO_PER_TOKEN, VLA_ERR_NONFINITE,
+from sherman_morrison_memory_gb300 import (VLA_ALGO_CHUNKED, VLA_ALGO_DECODE, VLA_ALGO_PER_TOKEN, VLA_ERR_NONFINITE,
                                            VLA_ERR_TIMEOUT, VLA_OK, vla_forward, vla_get_last_device_status,
                                            vla_linear_attention_state)
 from sherman_morrison_memory_gb300 import workloads as W
@@ -48,7 +48,7 @@ def _state_ref(state):
     return dict(S0=f(S0), A0=f(A0), zk0=f(zk0))
 
 
-ALGOS = [VLA_ALGO_PER_TOKEN, VLA_ALGO_CHUNKED]
+ALGOS = [VLA_ALGO_PER_TOKEN, VLA_ALGO_CHUNKED, VLA_ALGO_DECODE]
 
 
 def _algo_ok(algo, d):
@@ -150,6 +150,48 @@ def test_decode_one_token_at_a_time(orc, algo):
     assert_close(errors((torch.cat(outs, dim=2), state), ref), what=f"decode algo={algo}")
 
 
+def _spd(B, H, d, seed, scale=10.0):
+    """A symmetric positive definite A0 per head (eigenvalues in (0, scale])."""
+    rng = np.random.default_rng(seed)
+    Q, _ = np.linalg.qr(rng.standard_normal((B, H, d, d)))
+    lam = scale * rng.uniform(0.05, 1.0, size=(B, H, d))
+    A = np.einsum("bhij,bhj,bhkj->bhik", Q, lam, Q)
+    return (0.5 * (A + np.swapaxes(A, -1, -2))).astype(np.float32)
+
+
+@pytest.mark.parametrize("algo", [0, VLA_ALGO_CHUNKED, VLA_ALGO_DECODE])
+@pytest.mark.parametrize("d", [32, 96, 128])
+@pytest.mark.parametrize("a0", ["default", "spd"])
+def test_fixed_a_variant(orc, d, a0, algo):
+    """fixed_a: A stays at A0 (u is not read), i.e. the recurrence with u = 0.
+    Several 16-token chunks and a ragged tail."""
+    if not _algo_ok(algo, d):
+        pytest.skip("the chunked kernel covers d <= 96")
+    T = 16 * 5 + 7
+    q, k, v, u = _inputs(2, 2, T, d, "bf16", seed=31 + d)
+    state = None if a0 == "default" else (None, _spd(2, 2, d, seed=d), None)
+    ref = orc.forward(q, k, v, np.zeros_like(u), **_state_ref(state))
+    for uu in (None, u):  # u is ignored: None or garbage give the same result
+        dev = to_dev([q, k, v], "bf16") + [None if uu is None else to_dev([uu], "bf16")[0]]
+        out = vla_forward(*dev, state=_state_dev(state), check=True, fixed_a=True, algo=algo)
+        assert_close(errors(out, ref), what=f"fixed A d={d} {a0} algo={algo} u={'none' if uu is None else 'given'}")
+        if state is not None:
+            assert torch.equal(out[1][1].cpu(), torch.from_numpy(state[1]))
+
+
+@pytest.mark.parametrize("d", [64, 96, 128])
+@pytest.mark.parametrize("T", [1, 4])
+def test_decode_batch_with_carried_state(orc, d, T):
+    """Decode-shaped calls (1024 heads, one or a few tokens, carried state) on
+    the default kernel choice."""
+    B, H = 64, 16
+    arrs = _inputs(B, H, T, d, "bf16", seed=40 + d + T)
+    warm = orc.forward(*_inputs(B, H, 25, d, "bf16", seed=41 + d))
+    state = (warm.S, warm.A, warm.zk)
+    out, ref = _run(orc, arrs, "bf16", state=state)
+    assert_close(errors(out, ref), what=f"decode batch d={d} T={T}")
+
+
 def test_lambda_and_eps(orc):
     arrs = _inputs(1, 2, 50, 64, "f32", seed=3)
     out, ref = _run(orc, arrs, "f32", lambda0=0.7, eps=0.5)
@@ -206,7 +248,7 @@ def test_linear_attention_state(orc):
     assert rel_heads(S.cpu().numpy(), want) < 1e-4
 
 
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", [VLA_ALGO_PER_TOKEN, VLA_ALGO_CHUNKED])
 def test_timeout_is_reported_and_context_survives(orc, algo):
     """A stalled staging warp makes every consumer's bounded wait run out; the
     call reports VLA_ERR_TIMEOUT and the next call on the same context works."""
