@@ -38,12 +38,14 @@ if ROOT not in sys.path:
 
 METRIC = "VLA head-tokens/sec at d_h=96,T=4096; % of FP32-FMA roofline"
 METRIC_BW = "VLA backward head-tokens/sec at d_h=96,T=4096; % of FP32-FMA roofline"
+METRIC_DEC = "VLA decode head-tokens/sec at d_h=96, T=1, carried state; % of HBM roofline"
 UNIT = "head-tokens/s"
 # algorithmic FP32 work per head-token, in units of d^2 FLOP: the forward is 6 matrix-vector
 # products / rank-1 updates of d x d matrices (2 d^2 FLOP each); the backward recomputes 5 of
 # them (A u^, A k^, S k^ and the rank-1 updates of A and S) and then runs 8 matrix-vector
 # products and 6 rank-1 updates on S, A and their adjoints (19 x 2 d^2)
-FLOP_D2 = {"forward": 12, "backward": 38}
+# (the fixed-A variant skips A u^ and the A update: 8 d^2)
+FLOP_D2 = {"forward": 12, "backward": 38, "fixed_a": 8}
 FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM (sm_103)
 FALLBACK_SM_MAX_MHZ = 2070.0
 FALLBACK_HBM_GBS = 6800.0
@@ -205,12 +207,48 @@ def oracle_time_bw(arrs, gO, w, tokens: int, heads: int):
     return heads * tokens / dt, r["threads"], dt
 
 
+def run_reference_decode(args, w):
+    """The oracle on the decode step: all heads, one token, from the state the
+    oracle reached over the same earlier tokens."""
+    import oracle
+    from sherman_morrison_memory_gb300 import workloads as W
+
+    B, H, T, warm = DECODE_WORKLOAD["B"], DECODE_WORKLOAD["H"], DECODE_WORKLOAD["T"], DECODE_WORKLOAD["warm"]
+    wr = W.Workload("decode", B, H, warm + T, w.d, w.dtype, w.structure, w.lambda0, w.eps, seed=w.seed)
+    arrs = W.make(wr)
+    orc = oracle.load()
+    r0 = orc.forward(*[a[:, :, :warm] for a in arrs], lambda0=w.lambda0, eps=w.eps, want_o=False)
+    sq = [a[:, :, -T:] for a in arrs]
+    total, steps = 0.0, 0
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        r = orc.forward(*sq, lambda0=w.lambda0, eps=w.eps, S0=r0.S, A0=r0.A, zk0=r0.zk)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            total += dt
+            steps += 1
+    value = B * H * T * steps / total
+    line = {
+        "impl": "reference", "metric": METRIC_DEC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"decode: B={B},H={H},T={T},d_h={w.d}, carried state from {warm} earlier tokens"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": r.threads, "kind": "oracle",
+                         "sample": f"one decode step of all {B * H} heads per step (fp64 oracle, OpenMP over heads)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
         return
     from sherman_morrison_memory_gb300 import workloads as W
 
+    if args.pass_ == "decode":
+        run_reference_decode(args, w)
+        return
     arrs = W.make(w)
     heads = w.heads
     bw = args.pass_ == "backward"
@@ -275,8 +313,11 @@ def run_ours(args, w):
     out = (o, S, A, zk)
     stream = torch.cuda.current_stream(dev)
 
+    fa = bool(args.fixed_a)
+    if fa:
+        u = None  # not read by the fixed-A variant
     for _ in range(args.warmup):
-        vla_forward(q, k, v, u, w.lambda0, w.eps, out=out, algo=args.algo)
+        vla_forward(q, k, v, u, w.lambda0, w.eps, out=out, algo=args.algo, fixed_a=fa)
     st, detail = vla_get_last_device_status(dev)
     if st != VLA_OK:
         raise RuntimeError(f"device status {st} {detail} after warm-up")
@@ -291,7 +332,7 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(args.steps):
-            vla_forward(q, k, v, u, w.lambda0, w.eps, out=out, algo=args.algo)
+            vla_forward(q, k, v, u, w.lambda0, w.eps, out=out, algo=args.algo, fixed_a=fa)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world, dev)
@@ -304,14 +345,20 @@ def run_ours(args, w):
     value = aggregate_value(units, world, ms_max / 1e3)
 
     # roofline of the one kernel that a step launches
-    kernel = "vla_tc_kernel" if args.algo == 2 or (args.algo == 0 and d <= 96) else "vla_fused_kernel"
+    if args.algo == 3 or (args.algo == 0 and (T <= 4 or (fa and d > 96))):
+        kernel = "vla_decode_kernel"
+    elif args.algo == 2 or (args.algo == 0 and d <= 96):
+        kernel = "vla_tc_kernel"
+    else:
+        kernel = "vla_fused_kernel"
     peaks = load_peaks()
     sm_max = float(peaks.get("sm_max_mhz", FALLBACK_SM_MAX_MHZ))
     n_sm = props.multi_processor_count
     peak_tflops = n_sm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
-    flops = 12.0 * d * d * units
+    flop_d2 = FLOP_D2["fixed_a" if fa else "forward"]
+    flops = flop_d2 * d * d * units
     achieved = flops / (ms / 1e3) / 1e12
-    in_bytes = 4 * units * d * (2 if w.dtype == "bf16" else 4)
+    in_bytes = (3 if fa else 4) * units * d * (2 if w.dtype == "bf16" else 4)
     out_bytes = units * d * 4 + w.heads * (2 * d * d + d) * 4
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
@@ -321,22 +368,23 @@ def run_ours(args, w):
     # the same metric end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv, hu = (x.cpu().pin_memory() for x in (q, k, v, u))
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        hu = None if u is None else u.cpu().pin_memory()
         hout = tuple(torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in out)
         ksteps = max(3, min(args.steps, args.e2e_steps))
         for _ in range(2):
-            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout, algo=args.algo)
+            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout, algo=args.algo, fixed_a=fa)
         torch.cuda.synchronize(dev)
         barrier(world, dev)
         e0.record(stream)
         for _ in range(ksteps):
-            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout, algo=args.algo)
+            vla_forward(hq, hk, hv, hu, w.lambda0, w.eps, out=hout, algo=args.algo, fixed_a=fa)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world, dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ksteps, world, dev)
         e2e = {"value": aggregate_value(units, world, e2e_ms / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (hq, hk, hv, hu)),
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (hq, hk, hv, hu) if x is not None),
                "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in hout),
                "ms_per_step": e2e_ms, "steps": ksteps}
 
@@ -348,22 +396,26 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, threads, dt = oracle_time(arrs, w, w.T, w.heads)
+        carr = arrs if not fa else (arrs[0], arrs[1], arrs[2], arrs[3] * 0)
+        rate, threads, dt = oracle_time(carr, w, w.T, w.heads)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"the full workload once ({w.heads} heads x {w.T} tokens, fp64, {dt:.1f} s)"}
+               "sample": f"the full workload once ({w.heads} heads x {w.T} tokens, fp64"
+                         f"{', u = 0 for fixed A' if fa else ''}, {dt:.1f} s)"}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": METRIC + ("; fixed-A variant" if fa else ""), "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.describe(), "B": B, "H": H, "T": T, "d_h": d, "input_dtype": w.dtype,
+                       "variant": "fixed A (A = I/lambda0, eq. 9 skipped, u not read)" if fa else "full",
                        "per_rank_heads": w.heads,
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB per step), no flush"},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                          "frac": achieved / peak_tflops, "traffic": traffic,
                          "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FP32 FMA lanes x 2 x {sm_max:.0f} MHz",
-                         "flop_per_head_token": 12 * d * d, "kernel": kernel},
+                         "flop_per_head_token": flop_d2 * d * d, "kernel": kernel},
             "fp32_roofline_pct": 100.0 * achieved / peak_tflops,
             "hbm": {"achieved_gbs": hbm_gbs, "peak_gbs": hbm_peak, "frac": hbm_gbs / hbm_peak,
                     "algorithmic_bytes_per_launch": in_bytes + out_bytes},
@@ -373,6 +425,127 @@ def run_ours(args, w):
             "clocks": clk.summary(),
             "state_norm_fro_mean": {"vla": vla_fro, "linear_attention": la_fro},
             "kernel_source_sha": sha,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+DECODE_WORKLOAD = dict(B=128, H=16, T=1, warm=16)
+
+
+def run_ours_decode(args, w):
+    """One decode step for B*H heads (T = 1) from a carried state that a
+    previous call produced: the state is read and written once per step."""
+    import torch
+    import torch.distributed as dist
+
+    from sherman_morrison_memory_gb300 import VLA_OK, vla_forward, vla_get_last_device_status
+    from sherman_morrison_memory_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    B, H, T = DECODE_WORKLOAD["B"], DECODE_WORKLOAD["H"], DECODE_WORKLOAD["T"]
+    d = w.d
+    wr = W.Workload("decode", B, H, DECODE_WORKLOAD["warm"] + T, d, w.dtype, w.structure, w.lambda0, w.eps,
+                    seed=rank_seed(w.seed, rank))
+    arrs = W.make(wr)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    warm_in = [torch.from_numpy(a[:, :, :-T].copy()).to(dev).to(tdt) for a in arrs]
+    q, k, v, u = (torch.from_numpy(a[:, :, -T:].copy()).to(dev).to(tdt) for a in arrs)
+    _, state = vla_forward(*warm_in, w.lambda0, w.eps, check=True)  # the carried state
+    o = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
+    out = (o, torch.empty_like(state[0]), torch.empty_like(state[1]), torch.empty_like(state[2]))
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        vla_forward(q, k, v, u, w.lambda0, w.eps, state, out=out)
+    st, detail = vla_get_last_device_status(dev)
+    if st != VLA_OK:
+        raise RuntimeError(f"device status {st} {detail} after warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", "") or "")
+    gpu_id = ("GPU-" + gpu_id) if gpu_id and not gpu_id.startswith("GPU-") else (gpu_id or str(local))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id) as clk:
+        barrier(world, dev)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            vla_forward(q, k, v, u, w.lambda0, w.eps, state, out=out)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    st, detail = vla_get_last_device_status(dev)
+    if st != VLA_OK:
+        raise RuntimeError(f"device status {st} {detail} in the timed region")
+    ms_max = max_over_ranks(ms, world, dev)
+    units = B * H * T
+    value = aggregate_value(units, world, ms_max / 1e3)
+    esz = 2 if w.dtype == "bf16" else 4
+    state_bytes = B * H * (2 * d * d + d) * 4
+    step_bytes = 2 * state_bytes + units * d * (4 * esz + 4)
+    peaks = load_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    gbs = step_bytes / (ms / 1e3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        hin = [x.cpu().pin_memory() for x in (q, k, v, u)]
+        hst = tuple(x.cpu().pin_memory() for x in state)
+        hout = tuple(torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in out)
+        ksteps = max(3, min(args.steps, args.e2e_steps))
+        for _ in range(2):
+            vla_forward(*hin, w.lambda0, w.eps, hst, out=hout)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        e0.record(stream)
+        for _ in range(ksteps):
+            vla_forward(*hin, w.lambda0, w.eps, hst, out=hout)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ksteps, world, dev)
+        e2e = {"value": aggregate_value(units, world, e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hin + list(hst)),
+               "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in hout),
+               "ms_per_step": e2e_ms, "steps": ksteps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        orc = oracle.load()
+        sq = [a[:, :, -T:] for a in arrs]
+        hs = [x.cpu().numpy().astype("float64") for x in state]
+        t0 = time.perf_counter()
+        r = orc.forward(*sq, lambda0=w.lambda0, eps=w.eps, S0=hs[0], A0=hs[1], zk0=hs[2])
+        dt = time.perf_counter() - t0
+        cpu = {"value": units / dt, "unit": UNIT, "cores": r.threads, "kind": "oracle",
+               "sample": f"one decode step of all {B * H} heads from the same state (fp64, {dt:.2f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC_DEC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"decode: B={B},H={H},T={T},d_h={d}, {w.dtype} q,k,v,u N(0,1), "
+                                   f"carried fp32 state from {DECODE_WORKLOAD['warm']} earlier tokens",
+                       "pass": "decode", "B": B, "H": H, "T": T, "d_h": d,
+                       "l2": f"state larger than L2 ({state_bytes / 1e6:.0f} MB read and written per step), no flush"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "traffic": None,
+                         "bytes_per_head_token": step_bytes // units, "kernel": "vla_decode_kernel"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "kernel_source_sha": kernel_source_sha(),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -513,8 +686,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--algo", type=int, default=0,
                     help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96), 1 per-token, 2 chunked")
-    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
-                    help="time the forward recurrence (default) or its reverse-mode gradient")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "decode"], default="forward",
+                    help="time the forward recurrence (default), its reverse-mode gradient, or one "
+                         "decode step (T = 1) of 2048 heads from a carried state")
+    ap.add_argument("--fixed-a", action="store_true",
+                    help="forward pass: the fixed-A variant (A held at I/lambda0, eq. 9 skipped)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size B (smaller cases for profiler captures)")
     args = ap.parse_args(argv)
@@ -529,6 +705,8 @@ def main(argv=None):
         run_reference(args, w)
     elif args.pass_ == "backward":
         run_ours_backward(args, w)
+    elif args.pass_ == "decode":
+        run_ours_decode(args, w)
     else:
         run_ours(args, w)
 
