@@ -20,7 +20,7 @@
 // warp-local partial sum reduced across warps through shared memory. Dot
 // products of d-vectors are recomputed by every warp (butterfly shuffles)
 // instead of block-wide reductions. Per token the forward phase needs one
-// block barrier and the reverse phase three. Token inputs and the tape are
+// block barrier and the reverse phase two. Token inputs and the tape are
 // prefetched NBUF - 1 tokens ahead into a shared-memory ring with cp.async.
 //
 // Identities that save a product per reverse step (A is symmetric):

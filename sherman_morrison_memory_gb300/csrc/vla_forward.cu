@@ -1144,11 +1144,18 @@ vla_status launch_tc(const vla::Params& p, int BH, cudaStream_t s) {
 // (d <= 96) and the per-token kernel otherwise.
 template <int D, typename TIn>
 vla_status launch_dec(const vla::Params& p, int BH, bool fixed_a, cudaStream_t s) {
-    using DL = vla::dec::DLay<D>;
-    if (fixed_a)
-        vla::dec::vla_decode_kernel<D, TIn, true><<<BH, DL::THREADS, DL::SMEM, s>>>(p);
-    else
-        vla::dec::vla_decode_kernel<D, TIn, false><<<BH, DL::THREADS, DL::SMEM, s>>>(p);
+    using DL = vla::dec::DLay<D, TIn>;
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+        return VLA_ERR_CUDA;
+    const int grid = BH < n_sm ? BH : n_sm;  // one persistent CTA per SM
+    // bulk copies of the carried state need 16-byte aligned state pointers
+    const int bulk = ((!p.S0 || aligned16(p.S0)) && (!p.A0 || aligned16(p.A0)) && (!p.zk0 || aligned16(p.zk0))) ? 1 : 0;
+    auto kern = fixed_a ? vla::dec::vla_decode_kernel<D, TIn, true> : vla::dec::vla_decode_kernel<D, TIn, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DL::SMEM) != cudaSuccess)
+        return VLA_ERR_CUDA;
+    kern<<<grid, DL::THREADS, DL::SMEM, s>>>(p, BH, bulk);
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
 }
 
