@@ -50,22 +50,42 @@ FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM (sm_103)
 FALLBACK_SM_MAX_MHZ = 2070.0
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch of the default workload's kernel, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
-# sources hash to SOURCE_SHA; otherwise reported as null.
-NCU_TRAFFIC = {"source_sha": "757966978bd67c06", "bytes_per_launch": 402742272 + 175727360}
-# the backward kernel's, from a capture of the same workload at B=2 (32 heads; a full launch holds
-# about 2.6 GB on the device) scaled by 4: every byte it moves is per head-token or per head
-NCU_TRAFFIC_BW = {"source_sha": "200d44df5443e982", "bytes_per_launch": 4 * (486493440 + 484519680)}
+# The source files each kernel is compiled from (besides the launch code).
+KERNEL_FILES = {
+    "vla_tc_kernel": ("vla_tc.cuh", "vla_device.cuh"),
+    "vla_fused_kernel": ("vla_forward.cu", "vla_device.cuh"),
+    "vla_backward_kernel": ("vla_backward.cuh", "vla_device.cuh"),
+    "vla_decode_kernel": ("vla_decode.cuh", "vla_backward.cuh", "vla_device.cuh"),
+}
+
+# DRAM bytes per launch of a bench line's kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum) from one ncu capture of the same command, valid only
+# while that kernel's own sources hash to source_sha; otherwise reported as null.
+NCU_TRAFFIC = {
+    "vla_tc_kernel": {"source_sha": "11be82f602ecb6d5", "bytes_per_launch": 402884864 + 176023808},
+    # from a capture of the same workload at B=2 (32 heads; a full launch holds about 2.6 GB on the
+    # device) scaled by 4: every byte it moves is per head-token or per head
+    "vla_backward_kernel": {"source_sha": "a8e88d58cc249e71", "bytes_per_launch": 4 * (485387008 + 484124672)},
+    "vla_decode_kernel": {"source_sha": "0f39f3063992b248", "bytes_per_launch": 153396992 + 100321024},
+}
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(kernel: str = None) -> str:
+    """Hash of the CUDA sources: of one kernel's own files, or of all of them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sherman_morrison_memory_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = sorted(KERNEL_FILES[kernel]) if kernel else sorted(os.listdir(csrc))
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    t = NCU_TRAFFIC.get(kernel)
+    if t and t["source_sha"] and t["source_sha"] == kernel_source_sha(kernel):
+        return t["bytes_per_launch"]
+    return None
 
 
 def load_peaks() -> dict:
@@ -362,8 +382,8 @@ def run_ours(args, w):
     out_bytes = units * d * 4 + w.heads * (2 * d * d + d) * 4
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
-    sha = kernel_source_sha()
-    traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["source_sha"] == sha else None
+    sha = kernel_source_sha(kernel)
+    traffic = ncu_traffic(kernel)
 
     # the same metric end to end through the public API with host buffers
     e2e = None
@@ -539,13 +559,13 @@ def run_ours_decode(args, w):
                        "pass": "decode", "B": B, "H": H, "T": T, "d_h": d,
                        "l2": f"state larger than L2 ({state_bytes / 1e6:.0f} MB read and written per step), no flush"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": gbs / hbm_peak, "traffic": None,
+                         "frac": gbs / hbm_peak, "traffic": ncu_traffic("vla_decode_kernel"),
                          "bytes_per_head_token": step_bytes // units, "kernel": "vla_decode_kernel"},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
-            "kernel_source_sha": kernel_source_sha(),
+            "kernel_source_sha": kernel_source_sha("vla_decode_kernel"),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -612,8 +632,8 @@ def run_ours_backward(args, w):
     tape_bytes = 2 * units * (3 * d + 8) * 4
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
-    sha = kernel_source_sha()
-    traffic = NCU_TRAFFIC_BW["bytes_per_launch"] if NCU_TRAFFIC_BW["source_sha"] == sha else None
+    sha = kernel_source_sha("vla_backward_kernel")
+    traffic = ncu_traffic("vla_backward_kernel")
 
     e2e = None
     if not args.no_e2e:
