@@ -406,7 +406,8 @@ def run_ours(args, w):
         e2e = {"value": aggregate_value(units, world, e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (hq, hk, hv, hu) if x is not None),
                "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in hout),
-               "ms_per_step": e2e_ms, "steps": ksteps}
+               "ms_per_step": e2e_ms, "steps": ksteps,
+               "path": "vla_forward_host: automatic chunks (about T/4 tokens), H2D on two streams, kernels, D2H overlapped"}
 
     # ||S_T||_F of VLA next to plain cumulative linear attention on the same inputs
     vla_fro = torch.linalg.matrix_norm(S).mean().item()

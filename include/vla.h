@@ -179,6 +179,54 @@ vla_status vla_forward_noalloc(const void* q, const void* k, const void* v, cons
                                float* o, float* S_out, float* A_out, float* zk_out,
                                void* stream, int* device_status);
 
+/*
+ * vla_forward_host -- vla_forward (eq. 9-11 of §3.3, every head) over HOST
+ * buffers, with the host<->device copies overlapped with the computation.
+ *
+ * The recurrence is causal: the state after token t is all that later tokens
+ * need. The call therefore cuts the sequence into chunks of `chunk_tokens`
+ * tokens (0 = automatic: about 4 chunks, multiples of 16 tokens, at least
+ * 256) and runs one vla_forward_ex() launch per chunk over all heads, with
+ * the state (S, A, z^key) carried in the workspace from launch to launch.
+ * While chunk j computes on `stream`, the next chunks' q, k, v, u are copied
+ * in and chunk j-1's o is copied out on streams of the library. The result
+ * equals one vla_forward() over the whole sequence up to rounding order.
+ *
+ *  q, k, v, u   [B, H, T, d] HOST arrays of `dtype` (u may be NULL for the
+ *               fixed-A variant). Page-locked memory (cudaHostAlloc,
+ *               cudaHostRegister) gives the overlap; pageable memory works
+ *               but each copy then waits for the host.
+ *  S0, A0, zk0  HOST initial state as for vla_forward (NULL = defaults).
+ *  o, S_out, A_out, zk_out   HOST outputs as for vla_forward (zk_out may be NULL).
+ *  chunk_tokens tokens per launch, >= 0 (0 = automatic; values above T mean T).
+ *  workspace    device memory of vla_forward_host_workspace_bytes() bytes,
+ *               256-byte aligned, its first vla_workspace_bytes() bytes
+ *               zero-filled before the first use (the status record, read by
+ *               vla_get_last_device_status(workspace, stream)). It holds the
+ *               carried state and three input and three output slots of one chunk.
+ *  stream, opts as for vla_forward_ex (the kernels run on `stream`).
+ *
+ * Asynchronous: returns once everything is enqueued. All work of the call,
+ * copies included, is complete when `stream` reaches the point after the
+ * call (e.g. cudaStreamSynchronize(stream)); until then the host buffers and
+ * the workspace are in use. Copies start only after the work queued on
+ * `stream` before the call. The first call on a device creates three streams
+ * (two for copies in, one for copies out) and fourteen events that live until the
+ * process exits; calls from several
+ * host threads are serialised while they enqueue. Two calls that may overlap
+ * on the GPU need separate workspaces. On an error return nothing the call
+ * enqueued is still copying.
+ */
+size_t vla_forward_host_workspace_bytes(vla_dtype dtype, int B, int H, int T, int d, int chunk_tokens);
+
+vla_status vla_forward_host(const void* q, const void* k, const void* v, const void* u,
+                            vla_dtype dtype, int B, int H, int T, int d,
+                            float lambda0, float eps,
+                            const float* S0, const float* A0, const float* zk0,
+                            float* o, float* S_out, float* A_out, float* zk_out,
+                            int chunk_tokens, void* workspace, size_t workspace_bytes,
+                            void* stream, const vla_options* opts);
+
 /* Static text for a status code. */
 const char* vla_status_string(vla_status s);
 

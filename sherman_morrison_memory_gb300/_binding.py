@@ -86,6 +86,10 @@ def load_library():
         lib.vla_backward.argtypes = ([vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, cf, vp, vp, vp, vp, vp, vp, vp]
                                      + [vp] * 7 + [vp, ctypes.c_size_t, vp])
         lib.vla_backward.restype = ci
+        lib.vla_forward_host_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
+        lib.vla_forward_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.vla_forward_host.argtypes = (fwd_args[:18] + [ci, vp, ctypes.c_size_t, vp, ctypes.POINTER(_Options)])
+        lib.vla_forward_host.restype = ci
         del cp
         _LIB = lib
         return lib
@@ -135,13 +139,16 @@ def _check_state(x, shape, device, name):
 def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tensor,
                 lambda0: float = 0.1, eps: float = 1e-4, state=None, *, out=None, stream=None,
                 check: bool = False, wait_limit_us: int = 0, test_stall_producer: bool = False,
-                algo: int = 0, fixed_a: bool = False):
+                algo: int = 0, fixed_a: bool = False, chunk_tokens: int = 0):
     """VLA forward recurrence (§3.3 eq. 9-11) over all heads.
 
     Returns ``(o, (S, A, zk))``: o [B,H,T,d] float32, S and A [B,H,d,d], zk [B,H,d].
     ``state`` = (S0, A0, zk0), each optional, continues a previous call.
     ``out`` = (o, S, A, zk) preallocated outputs on the inputs' device.
-    CPU inputs run on the current CUDA device with host<->device copies.
+    CPU inputs run on the current CUDA device through vla_forward_host:
+    ``chunk_tokens`` tokens per launch (0 = automatic), the host<->device
+    copies overlapped with the kernels; synchronise the stream before reading
+    page-locked host outputs.
     ``check=True`` synchronises and raises on an in-kernel failure.
     ``algo`` selects the kernel: VLA_ALGO_AUTO (0), VLA_ALGO_PER_TOKEN (1),
     VLA_ALGO_CHUNKED (2, the tensor-core chunked kernel, d <= 96) or
@@ -150,7 +157,8 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
     initial value, u is not read (it may be None).
     """
     if q.device.type == "cpu":
-        return _forward_host(q, k, v, u, lambda0, eps, state, out=out, check=check, algo=algo, fixed_a=fixed_a)
+        return _forward_host(q, k, v, u, lambda0, eps, state, out=out, check=check, algo=algo, fixed_a=fixed_a,
+                             chunk_tokens=chunk_tokens, stream=stream)
     lib = load_library()
     if u is None and not fixed_a:
         raise ValueError("u is required unless fixed_a=True")
@@ -201,24 +209,73 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
     return o, (S, A, zk)
 
 
-def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False, algo=0, fixed_a=False):
-    """Host buffers in, host buffers out: H2D copies, the kernel, D2H copies,
-    all on the current stream of the current CUDA device. ``out`` may hold
-    preallocated (pinned) host outputs (o, S, A, zk)."""
-    dev = torch.device("cuda", torch.cuda.current_device())
-    dq, dk, dv = (x.to(dev, non_blocking=True) for x in (q, k, v))
-    du = None if u is None else u.to(dev, non_blocking=True)
-    dstate = None
+_HOST_WORKSPACES = {}
+
+
+def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False, algo=0, fixed_a=False,
+                  chunk_tokens=0, stream=None):
+    """Host buffers in, host buffers out, through vla_forward_host: the
+    sequence runs in chunks on the current CUDA device, with the copies of
+    chunk j+1's inputs and chunk j-1's outputs overlapped with chunk j's
+    kernel. ``out`` may hold preallocated host outputs (o, S, A, zk); new
+    outputs are page-locked when q is. Like torch's non-blocking copies, the
+    call returns once the work is enqueued: synchronise the stream before
+    reading page-locked outputs (``check=True`` does)."""
+    lib = load_library()
+    if u is None and not fixed_a:
+        raise ValueError("u is required unless fixed_a=True")
+    for name, x in (("k", k), ("v", v), ("u", u)):
+        if x is None:
+            continue
+        if x.shape != q.shape or x.dtype != q.dtype or x.device != q.device:
+            raise ValueError(f"{name} must match q in shape, dtype and device")
+    if q.dim() != 4 or q.dtype not in _DTYPES:
+        raise ValueError("q, k, v, u must be [B, H, T, d] float32 or bfloat16")
+    q, k, v = (x.contiguous() for x in (q, k, v))
+    u = None if u is None else u.contiguous()
+    B, H, T, d = q.shape
+    cpu = torch.device("cpu")
+    S0 = A0 = zk0 = None
     if state is not None:
-        dstate = tuple(None if x is None else x.to(dev, non_blocking=True) for x in state)
-    o, (S, A, zk) = vla_forward(dq, dk, dv, du, lambda0, eps, dstate, check=check, algo=algo, fixed_a=fixed_a)
-    pin = q.is_pinned()
-    outs = []
-    for i, x in enumerate((o, S, A, zk)):
-        h = out[i] if out is not None else torch.empty(x.shape, dtype=x.dtype, pin_memory=pin)
-        h.copy_(x, non_blocking=h.is_pinned())
-        outs.append(h)
-    return outs[0], (outs[1], outs[2], outs[3])
+        S0, A0, zk0 = state
+        S0 = _check_state(S0, (B, H, d, d), cpu, "S0")
+        A0 = _check_state(A0, (B, H, d, d), cpu, "A0")
+        zk0 = _check_state(zk0, (B, H, d), cpu, "zk0")
+    shapes = [(B, H, T, d), (B, H, d, d), (B, H, d, d), (B, H, d)]
+    if out is None:
+        pin = q.is_pinned()
+        res = [torch.empty(sh, dtype=torch.float32, pin_memory=pin) for sh in shapes]
+    else:
+        res = list(out)
+        for x, sh in zip(res, shapes):
+            if (tuple(x.shape) != sh or x.dtype != torch.float32 or x.device.type != "cpu"
+                    or not x.is_contiguous()):
+                raise ValueError(f"out tensors must be contiguous float32 host tensors {sh}")
+    o, S, A, zk = res
+    dev = torch.device("cuda", torch.cuda.current_device())
+    nbytes = int(lib.vla_forward_host_workspace_bytes(_DTYPES[q.dtype], B, H, T, d, int(chunk_tokens)))
+    if nbytes == 0:
+        raise ValueError("unsupported sizes for vla_forward_host")
+    ws = _HOST_WORKSPACES.get(dev.index)
+    if ws is None or ws.numel() * 4 < nbytes:
+        _HOST_WORKSPACES.pop(dev.index, None)
+        ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=dev)
+        _HOST_WORKSPACES[dev.index] = ws
+    with torch.cuda.device(dev):
+        sh = _stream_handle(dev, stream)
+        opts = _Options(0, 0, None, int(algo), 1 if fixed_a else 0)
+        st = lib.vla_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d,
+                                  float(lambda0), float(eps), _ptr(S0), _ptr(A0), _ptr(zk0),
+                                  _ptr(o), _ptr(S), _ptr(A), _ptr(zk), int(chunk_tokens), _ptr(ws),
+                                  ws.numel() * 4, ctypes.c_void_p(sh), ctypes.byref(opts))
+        if st != VLA_OK:
+            raise VLAError(st, "vla_forward_host")
+        if check:
+            detail = (ctypes.c_int * 3)()
+            st = lib.vla_get_last_device_status(_ptr(ws), ctypes.c_void_p(sh), detail)
+            if st != VLA_OK:
+                raise VLAError(st, "vla_forward_host (device)", (detail[0], detail[1], detail[2]))
+    return o, (S, A, zk)
 
 
 def vla_get_last_device_status(device=None, stream=None) -> Tuple[int, tuple]:

@@ -157,3 +157,51 @@ def test_backward_argument_errors(lib, kw, status):
 
 def test_backward_empty_batch_is_a_no_op(lib):
     assert _bw_call(lib, B=0) == 0
+
+
+def _host_call(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, u=FAKE, dtype=1, B=1, H=1, T=4, d=64, lambda0=0.1, eps=1e-4,
+             S0=None, A0=None, zk0=None, o=FAKE, S=FAKE, A=FAKE, zk=None, chunk=0, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    p = lambda n: vp(a[n])
+    return lib.vla_forward_host(p("q"), p("k"), p("v"), p("u"), a["dtype"], a["B"], a["H"], a["T"], a["d"],
+                                a["lambda0"], a["eps"], p("S0"), p("A0"), p("zk0"), p("o"), p("S"), p("A"),
+                                p("zk"), a["chunk"], p("ws"), a["wsb"], None, None)
+
+
+def test_host_workspace_bytes(lib):
+    """Status record, S, A, z^key, three input slots (q, k, v, u of one chunk)
+    and three output slots (o of one chunk), each part 256-byte aligned. The
+    automatic chunk is about T/4 tokens, a multiple of 16, at least 256."""
+    al = lambda x: (x + 255) // 256 * 256
+    def expect(es, BH, T, d, tc):
+        return (256 + 2 * al(BH * d * d * 4) + al(BH * d * 4) + 3 * 4 * al(BH * tc * d * es)
+                + 3 * al(BH * tc * d * 4))
+    assert lib.vla_forward_host_workspace_bytes(1, 8, 16, 4096, 96, 0) == expect(2, 128, 4096, 96, 1024)
+    assert lib.vla_forward_host_workspace_bytes(0, 1, 32, 65536, 128, 0) == expect(4, 32, 65536, 128, 16384)
+    assert lib.vla_forward_host_workspace_bytes(0, 2, 3, 1100, 64, 0) == expect(4, 6, 1100, 64, 288)
+    assert lib.vla_forward_host_workspace_bytes(0, 2, 3, 300, 64, 0) == expect(4, 6, 300, 64, 256)
+    assert lib.vla_forward_host_workspace_bytes(0, 2, 3, 100, 64, 0) == expect(4, 6, 100, 64, 100)
+    assert lib.vla_forward_host_workspace_bytes(1, 2, 3, 300, 32, 64) == expect(2, 6, 300, 32, 64)
+    assert lib.vla_forward_host_workspace_bytes(1, 2, 3, 0, 32, 0) == expect(2, 6, 0, 32, 0)
+    assert lib.vla_forward_host_workspace_bytes(1, 1, 1, 4, 48, 0) == 0
+    assert lib.vla_forward_host_workspace_bytes(1, 1, 1, 4, 64, -1) == 0
+    assert lib.vla_forward_host_workspace_bytes(2, 1, 1, 4, 64, 0) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=48), 2), (dict(d=0), 2),
+    (dict(B=-1), 1), (dict(T=-1), 1), (dict(dtype=3), 1), (dict(chunk=-5), 1),
+    (dict(lambda0=0.0), 1), (dict(eps=float("nan")), 1),
+    (dict(ws=None), 1), (dict(ws=FAKE + 16), 1), (dict(wsb=4096), 1),
+    (dict(q=None), 1), (dict(u=None), 1), (dict(o=None), 1), (dict(S=None), 1), (dict(A=None), 1),
+    (dict(B=1 << 20, H=1 << 12), 1),
+])
+def test_host_argument_errors(lib, kw, status):
+    """vla_forward_host rejects these before any CUDA call or copy."""
+    assert _host_call(lib, **kw) == status
+
+
+def test_host_empty_batch_is_a_no_op(lib):
+    assert _host_call(lib, B=0) == 0
