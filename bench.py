@@ -56,6 +56,7 @@ KERNEL_FILES = {
     "vla_fused_kernel": ("vla_forward.cu", "vla_device.cuh"),
     "vla_backward_kernel": ("vla_backward.cuh", "vla_device.cuh"),
     "vla_decode_kernel": ("vla_decode.cuh", "vla_backward.cuh", "vla_device.cuh"),
+    "vla_tc2_kernel": ("vla_tc2.cuh", "vla_tc.cuh", "vla_device.cuh"),
 }
 
 # DRAM bytes per launch of a bench line's kernel (dram__bytes_read.sum +
@@ -365,8 +366,10 @@ def run_ours(args, w):
     value = aggregate_value(units, world, ms_max / 1e3)
 
     # roofline of the one kernel that a step launches
-    if args.algo == 3 or (args.algo == 0 and (T <= 4 or (fa and d > 96))):
+    if args.algo == 3 or (args.algo == 0 and T <= 4):
         kernel = "vla_decode_kernel"
+    elif args.algo == 4 or (args.algo == 0 and d == 128):
+        kernel = "vla_tc2_kernel"
     elif args.algo == 2 or (args.algo == 0 and d <= 96):
         kernel = "vla_tc_kernel"
     else:
@@ -706,7 +709,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--algo", type=int, default=0,
-                    help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96), 1 per-token, 2 chunked")
+                    help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96, its cluster-pair form "
+                         "for d_h = 128), 1 per-token, 2 chunked, 3 decode, 4 chunked on a cluster pair")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "decode"], default="forward",
                     help="time the forward recurrence (default), its reverse-mode gradient, or one "
                          "decode step (T = 1) of 2048 heads from a carried state")

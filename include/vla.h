@@ -69,16 +69,15 @@ typedef struct {
                                     §3.5 ablation): A is held at its initial value (A0, or I/lambda0)
                                     and eq. 9 is skipped, so alpha^_t = A0 k^_t / ||A0 k^_t||; u is
                                     not read and may be NULL. Runs on VLA_ALGO_CHUNKED (d <= 96;
-                                    the A team only forms A0 k^) and VLA_ALGO_DECODE; VLA_ALGO_AUTO
-                                    picks the decode kernel for T <= 4 or d = 128, else the chunked
-                                    one; VLA_ALGO_PER_TOKEN returns VLA_ERR_UNSUPPORTED */
+                                    the A team only forms A0 k^), VLA_ALGO_CHUNKED_PAIR and
+                                    VLA_ALGO_DECODE; VLA_ALGO_AUTO picks as for the full
+                                    recurrence; VLA_ALGO_PER_TOKEN returns VLA_ERR_UNSUPPORTED */
 } vla_options;
 
 /* Kernels behind vla_forward_ex() (vla_options.algo). All compute eq. 9-11
  * exactly up to rounding order.
  *   VLA_ALGO_AUTO       decode kernel for T <= 4; otherwise the chunked tensor-core kernel
- *                       for d <= 96, the per-token kernel for d = 128 (the decode kernel for
- *                       the fixed-A variant at d = 128)
+ *                       for d <= 96 and the cluster-pair chunked kernel for d = 128
  *   VLA_ALGO_PER_TOKEN  one token at a time on the FMA pipes (any supported d)
  *   VLA_ALGO_CHUNKED    16 tokens at a time: the Sherman-Morrison steps of a chunk as an
  *                       LDL^T factorisation, the d x d products on the tcgen05 tensor cores
@@ -86,8 +85,14 @@ typedef struct {
  *                       VLA_ERR_UNSUPPORTED
  *   VLA_ALGO_DECODE     one token at a time with S and A in registers, laid out to stream
  *                       the carried state: for decode (T = 1) and short sequences (any d)
+ *   VLA_ALGO_CHUNKED_PAIR  the chunked tensor-core recurrence on a cluster of two CTAs per
+ *                       head: one SM runs the A-pass (eq. 9 and the gate of eq. 10) and
+ *                       sends each chunk's gate to the other, which runs the S-pass
+ *                       (eq. 10-11); each state has a whole SM's tensor memory, so d = 128
+ *                       runs too (any supported d)
  * Any other value: VLA_ERR_INVALID_ARG. */
-enum { VLA_ALGO_AUTO = 0, VLA_ALGO_PER_TOKEN = 1, VLA_ALGO_CHUNKED = 2, VLA_ALGO_DECODE = 3 };
+enum { VLA_ALGO_AUTO = 0, VLA_ALGO_PER_TOKEN = 1, VLA_ALGO_CHUNKED = 2, VLA_ALGO_DECODE = 3,
+       VLA_ALGO_CHUNKED_PAIR = 4 };
 
 /* Bytes of device workspace vla_forward() needs (one status record). The
  * workspace must be zero-filled before its first use (cudaMemset or

@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     VLA_ALGO_PER_TOKEN,
     VLA_ALGO_CHUNKED,
     VLA_ALGO_DECODE,
+    VLA_ALGO_CHUNKED_PAIR,
     VLAError,
     library_path,
     load_library,

@@ -25,6 +25,7 @@ VLA_ALGO_AUTO = 0
 VLA_ALGO_PER_TOKEN = 1
 VLA_ALGO_CHUNKED = 2
 VLA_ALGO_DECODE = 3
+VLA_ALGO_CHUNKED_PAIR = 4
 
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
@@ -151,8 +152,10 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
     page-locked host outputs.
     ``check=True`` synchronises and raises on an in-kernel failure.
     ``algo`` selects the kernel: VLA_ALGO_AUTO (0), VLA_ALGO_PER_TOKEN (1),
-    VLA_ALGO_CHUNKED (2, the tensor-core chunked kernel, d <= 96) or
-    VLA_ALGO_DECODE (3, short sequences with a carried state).
+    VLA_ALGO_CHUNKED (2, the tensor-core chunked kernel, d <= 96),
+    VLA_ALGO_DECODE (3, short sequences with a carried state) or
+    VLA_ALGO_CHUNKED_PAIR (4, the chunked kernel on a cluster of two CTAs per
+    head: A-pass and S-pass on separate SMs; any d).
     ``fixed_a=True`` runs the fixed-A variant (§3.5 ablation): A stays at its
     initial value, u is not read (it may be None).
     """

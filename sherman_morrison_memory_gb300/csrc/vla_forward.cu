@@ -1104,6 +1104,7 @@ __global__ void __launch_bounds__(LA_THREADS) la_state_kernel(const TIn* k, cons
 }
 
 #include "vla_tc.cuh"
+#include "vla_tc2.cuh"
 #include "vla_backward.cuh"
 #include "vla_decode.cuh"
 
@@ -1140,8 +1141,19 @@ vla_status launch_tc(const vla::Params& p, int BH, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
 }
 
-// algo: VLA_ALGO_AUTO picks the chunked tensor-core kernel where it exists
-// (d <= 96) and the per-token kernel otherwise.
+// the chunked recurrence on a cluster of two CTAs per head (rank 0 the A-pass,
+// rank 1 the S-pass)
+template <int D, typename TIn>
+vla_status launch_tc2(const vla::Params& p, int BH, cudaStream_t s) {
+    using LY = vla::tc2::Lay2<D, TIn>;
+    auto kern = vla::vla_tc2_kernel<D, TIn>;
+    if ((long long)BH * 2 > 2147483647LL) return VLA_ERR_INVALID_ARG;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::SMEM_LAUNCH) != cudaSuccess)
+        return VLA_ERR_CUDA;
+    kern<<<2 * BH, vla::tc2::THREADS, LY::SMEM_LAUNCH, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
+}
+
 template <int D, typename TIn>
 vla_status launch_dec(const vla::Params& p, int BH, bool fixed_a, cudaStream_t s) {
     using DL = vla::dec::DLay<D, TIn>;
@@ -1162,9 +1174,12 @@ vla_status launch_dec(const vla::Params& p, int BH, bool fixed_a, cudaStream_t s
 // sequences up to this length go to the decode kernel under VLA_ALGO_AUTO
 constexpr int kDecodeMaxT = 4;
 
+// algo: VLA_ALGO_AUTO picks the decode kernel for short sequences, the
+// single-CTA chunked tensor-core kernel for d <= 96 and the cluster-pair
+// chunked kernel for d = 128.
 template <typename TIn>
 vla_status launch_d(int d, int algo, bool fixed_a, const vla::Params& p, int BH, cudaStream_t s) {
-    if (algo == VLA_ALGO_DECODE || (algo == VLA_ALGO_AUTO && (p.T <= kDecodeMaxT || (fixed_a && d > 96)))) {
+    if (algo == VLA_ALGO_DECODE || (algo == VLA_ALGO_AUTO && p.T <= kDecodeMaxT)) {
         switch (d) {
             case 32: return launch_dec<32, TIn>(p, BH, fixed_a, s);
             case 64: return launch_dec<64, TIn>(p, BH, fixed_a, s);
@@ -1174,6 +1189,15 @@ vla_status launch_d(int d, int algo, bool fixed_a, const vla::Params& p, int BH,
         }
     }
     if (fixed_a && algo == VLA_ALGO_PER_TOKEN) return VLA_ERR_UNSUPPORTED;
+    if (algo == VLA_ALGO_CHUNKED_PAIR || (algo == VLA_ALGO_AUTO && d == 128)) {
+        switch (d) {
+            case 32: return launch_tc2<32, TIn>(p, BH, s);
+            case 64: return launch_tc2<64, TIn>(p, BH, s);
+            case 96: return launch_tc2<96, TIn>(p, BH, s);
+            case 128: return launch_tc2<128, TIn>(p, BH, s);
+            default: return VLA_ERR_UNSUPPORTED;
+        }
+    }
     const bool chunked = algo == VLA_ALGO_CHUNKED || (algo == VLA_ALGO_AUTO && d <= 96);
     if (chunked) {
         switch (d) {
@@ -1267,7 +1291,8 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
 
     const int algo = opts ? opts->algo : VLA_ALGO_AUTO;
     const bool fixed_a = opts && opts->fixed_a;
-    if (algo != VLA_ALGO_AUTO && algo != VLA_ALGO_PER_TOKEN && algo != VLA_ALGO_CHUNKED && algo != VLA_ALGO_DECODE)
+    if (algo != VLA_ALGO_AUTO && algo != VLA_ALGO_PER_TOKEN && algo != VLA_ALGO_CHUNKED && algo != VLA_ALGO_DECODE &&
+        algo != VLA_ALGO_CHUNKED_PAIR)
         return VLA_ERR_INVALID_ARG;
     if (algo == VLA_ALGO_CHUNKED && d > 96) return VLA_ERR_UNSUPPORTED;
     if (fixed_a && algo == VLA_ALGO_PER_TOKEN) return VLA_ERR_UNSUPPORTED;
