@@ -718,6 +718,8 @@ def main(argv=None):
                     help="forward pass: the fixed-A variant (A held at I/lambda0, eq. 9 skipped)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size B (smaller cases for profiler captures)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's sequence length T (smaller cases for profiler captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -726,6 +728,8 @@ def main(argv=None):
     w = W.WORKLOADS[args.workload]
     if args.batch > 0:
         w = dataclasses.replace(w, B=args.batch)
+    if args.tokens > 0:
+        w = dataclasses.replace(w, T=args.tokens)
     if args.impl == "reference":
         run_reference(args, w)
     elif args.pass_ == "backward":

@@ -203,6 +203,11 @@ vla_status vla_forward_noalloc(const void* q, const void* k, const void* v, cons
  *               but each copy then waits for the host.
  *  S0, A0, zk0  HOST initial state as for vla_forward (NULL = defaults).
  *  o, S_out, A_out, zk_out   HOST outputs as for vla_forward (zk_out may be NULL).
+ *               If o is page-locked and mapped into the device's address space
+ *               (cudaHostGetDevicePointer succeeds, as for cudaHostAlloc memory)
+ *               and 16-byte aligned, the kernels write o straight into it and
+ *               only the final state is copied out; otherwise o is copied out
+ *               chunk by chunk.
  *  chunk_tokens tokens per launch, >= 0 (0 = automatic; values above T mean T).
  *  workspace    device memory of vla_forward_host_workspace_bytes() bytes,
  *               256-byte aligned, its first vla_workspace_bytes() bytes

@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(DLay<D, TIn>::THREADS, 1) vla_decode_kernel(co
             // o_t = S_t phi / den = (S_{t-1} phi + e (alpha^ . phi)) / den
             const float orow = fmaf(erow, d2[1] * ina, sphi) / den;
             if ((l & 3) == 0) {
-                p.o[((size_t)bh * T + t) * D + rr] = orow;
+                p.o[(size_t)bh * p.o_stride + (size_t)t * D + rr] = orow;
                 if (!isfinite(orow)) bad = true;
             }
             if (l == 0 && w == 0 && (!isfinite(dl) || !isfinite(d2[0]) || !isfinite(pd))) bad = true;

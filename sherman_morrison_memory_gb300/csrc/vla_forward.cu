@@ -35,6 +35,7 @@
 
 #include "vla.h"
 #include "vla_device.cuh"
+#include "vla_internal.h"
 
 namespace vla {
 
@@ -134,6 +135,7 @@ struct Params {
     const float* A0;
     const float* zk0;
     float* o;
+    size_t o_stride;  // elements from one head's o rows to the next (T * d when o is [B, H, T, d])
     float* S_out;
     float* A_out;
     float* zk_out;
@@ -888,7 +890,7 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
                 s[r][c] = S0 ? f2(S0[(size_t)(row0 + r) * D + col0 + 2 * c], S0[(size_t)(row0 + r) * D + col0 + 2 * c + 1])
                              : f2(0.f, 0.f);
     }
-    float* o = p.o + (size_t)bh * p.T * D;
+    float* o = p.o + (size_t)bh * p.o_stride;
 
     bool abort = false, nonfinite = false;
     int t = 0;
@@ -1244,6 +1246,16 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
                           int H, int T, int d, float lambda0, float eps, const float* S0, const float* A0,
                           const float* zk0, float* o, float* S_out, float* A_out, float* zk_out,
                           void* workspace, size_t workspace_bytes, void* stream, const vla_options* opts) {
+    return vla_impl::forward(q, k, v, u, dtype, B, H, T, d, lambda0, eps, S0, A0, zk0, o, S_out, A_out, zk_out,
+                             workspace, workspace_bytes, stream, opts, 0);
+}
+
+}  // extern "C"
+
+vla_status vla_impl::forward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B,
+                             int H, int T, int d, float lambda0, float eps, const float* S0, const float* A0,
+                             const float* zk0, float* o, float* S_out, float* A_out, float* zk_out, void* workspace,
+                             size_t workspace_bytes, void* stream, const vla_options* opts, size_t o_head_stride) {
     if (B < 0 || H < 0 || T < 0) return VLA_ERR_INVALID_ARG;
     if (dtype != VLA_F32 && dtype != VLA_BF16) return VLA_ERR_INVALID_ARG;
     if (d != 32 && d != 64 && d != 96 && d != 128) return VLA_ERR_UNSUPPORTED;
@@ -1254,6 +1266,8 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
     if ((unsigned long long)BH * (unsigned long long)T * (unsigned long long)d > (1ULL << 60))
         return VLA_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) || workspace_bytes < kWorkspaceBytes) return VLA_ERR_INVALID_ARG;
+    if (o_head_stride == 0) o_head_stride = (size_t)T * d;
+    if (o_head_stride < (size_t)T * d || (o_head_stride * sizeof(float)) % 16 != 0) return VLA_ERR_INVALID_ARG;
     if (BH == 0) return VLA_OK;
     const bool no_u = opts && opts->fixed_a;  // the fixed-A variant does not read u
     if (T > 0) {
@@ -1275,6 +1289,7 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
     p.A0 = A0;
     p.zk0 = zk0;
     p.o = o;
+    p.o_stride = o_head_stride;
     p.S_out = S_out;
     p.A_out = A_out;
     p.zk_out = zk_out;
@@ -1301,6 +1316,8 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
     return dtype == VLA_BF16 ? launch_d<__nv_bfloat16>(d, algo, fixed_a, p, (int)BH, s)
                              : launch_d<float>(d, algo, fixed_a, p, (int)BH, s);
 }
+
+extern "C" {
 
 vla_status vla_forward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B, int H,
                        int T, int d, float lambda0, float eps, const float* S0, const float* A0,

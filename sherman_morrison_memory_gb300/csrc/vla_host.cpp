@@ -14,13 +14,11 @@
 //   caller's  the kernel of chunk j on input slot j mod 3 -> output slot j mod 3
 //   copy-out  D2H of chunk j's o into the host array, then the final state
 //
-// so copies in both directions run while the kernels compute. Events order
-// slot reuse: the copy into an input slot waits for the kernel that read it
-// three chunks earlier, and a kernel waits for the D2H that drained its
-// output slot three chunks earlier. The caller's stream waits for the last
-// copy-out before the call's work counts as done. Three slots rather than two
-// keep the link busy while a kernel waits for a slot (measured on the d = 96,
-// T = 4096 workload: 3.0 ms per call against 3.7 ms with two slots).
+// When the host o is page-locked and mapped into the device's address space
+// (cudaHostGetDevicePointer succeeds, e.g. cudaHostAlloc memory), the kernels
+// write o straight into it (plain stores, rows of head h at h * T * d) and
+// only the final state is copied out: o then crosses the link while the
+// kernels run, in the direction the input copies do not use.
 //
 // Host code only (no kernels): compiled as its own translation unit.
 #include <cuda_runtime.h>
@@ -30,6 +28,7 @@
 #include <mutex>
 
 #include "vla.h"
+#include "vla_internal.h"
 
 namespace {
 
@@ -73,29 +72,51 @@ vla_status pipe_for(int dev, Pipe** out) {
     return VLA_OK;
 }
 
-// Workspace layout: status record | S | A | z^key | kSlots input slots (q, k,
-// v, u of one chunk, compact [B*H, Tc, d]) | kSlots output slots (o, [B*H, Tc, d] fp32).
+// Chunks: tc tokens each, or with the automatic choice a first and a last
+// chunk of ra = tc / 4 tokens around chunks of tc: the copy of the first
+// chunk, which nothing overlaps, and the launch of the last one, after the
+// last copy, are then short. Workspace layout: status record | S | A | z^key |
+// kSlots input slots (q, k, v, u of one chunk, compact [B*H, n, d]) | kSlots
+// output slots (o, [B*H, n, d] fp32), sized for tc tokens.
 struct Plan {
-    int tc = 0, nchunks = 0;
+    int T = 0, tc = 0, ra = 0, nchunks = 0;
     size_t es = 0, status = 0, S = 0, A = 0, zk = 0, in_arr = 0, in_slot[kSlots] = {}, out_slot[kSlots] = {},
            total = 0;
+    // first token and length of chunk j
+    long long start(int j) const {
+        if (ra == 0 || j == 0) return (long long)j * tc;
+        if (j == nchunks - 1) return (long long)T - ra;
+        return ra + (long long)(j - 1) * tc;
+    }
+    int len(int j) const {
+        if (T == 0) return 0;
+        if (ra > 0 && (j == 0 || j == nchunks - 1)) return ra;
+        const long long end = (ra > 0) ? (long long)T - ra : (long long)T;
+        const long long n = end - start(j);
+        return (int)(n < tc ? n : tc);
+    }
 };
 
 bool make_plan(vla_dtype dtype, long long BH, int T, int d, int chunk_tokens, Plan* pl) {
     if (BH < 0 || T < 0 || chunk_tokens < 0) return false;
+    pl->T = T;
     if (T == 0) {
         pl->tc = 0;
         pl->nchunks = 1;  // one launch with T = 0 writes the initial state out
     } else {
-        int tc = chunk_tokens;
-        if (tc == 0) {  // about 4 chunks, multiples of 16 tokens, at least 256 tokens each
+        int tc = chunk_tokens, ra = 0;
+        if (tc == 0) {  // about T/4 tokens, a multiple of 16, at least 256; short first and last chunks
             long long c = ((long long)T + 3) / 4;
             c = (c + 15) / 16 * 16;
             tc = (int)(c < 256 ? 256 : c);
+            ra = tc / 4 / 16 * 16;
+            if ((long long)T < 2LL * ra + tc) ra = 0;  // too short to gain from the ramps
         }
         if (tc > T) tc = T;
         pl->tc = tc;
-        pl->nchunks = (int)(((long long)T + tc - 1) / tc);
+        pl->ra = ra;
+        const long long mid = (long long)T - 2LL * ra;
+        pl->nchunks = (int)((mid + tc - 1) / tc) + (ra > 0 ? 2 : 0);
     }
     pl->es = dtype == VLA_BF16 ? 2 : 4;
     const size_t bh = (size_t)BH, dd = (size_t)d;
@@ -172,6 +193,15 @@ vla_status vla_forward_host(const void* q, const void* k, const void* v, const v
     const size_t bh = (size_t)BH, dd = (size_t)d, es = pl.es;
     const size_t state_bytes = bh * dd * dd * 4;
     const void* hin[4] = {q, k, v, no_u ? nullptr : u};
+    // device alias of the host o, if it is page-locked and mapped
+    float* od = nullptr;
+    if (T > 0) {
+        void* dp = nullptr;
+        if (cudaHostGetDevicePointer(&dp, o, 0) == cudaSuccess && dp && !(reinterpret_cast<uintptr_t>(dp) & 15u))
+            od = static_cast<float*>(dp);
+        else
+            (void)cudaGetLastError();  // pageable memory: clear the error, copy o out instead
+    }
 
     // Leave the internal streams drained on an error, so that no copy touches
     // the caller's buffers after the call has returned.
@@ -191,7 +221,7 @@ vla_status vla_forward_host(const void* q, const void* k, const void* v, const v
         (zk0 && !ok(cudaMemcpyAsync(dZ, zk0, bh * dd * 4, cudaMemcpyHostToDevice, P->in[0]))))
         return fail(VLA_ERR_CUDA);
 
-    auto chunk_len = [&](int j) { return T == 0 ? 0 : (j + 1 < pl.nchunks ? pl.tc : T - j * pl.tc); };
+    auto chunk_len = [&](int j) { return pl.len(j); };
     // H2D of chunk j into input slot j mod kSlots, compact [B*H, n, d]; array a
     // on copy-in stream a mod 2
     auto h2d = [&](int j) -> bool {
@@ -201,7 +231,7 @@ vla_status vla_forward_host(const void* q, const void* k, const void* v, const v
         const size_t row = (size_t)n * dd * es;
         for (int a = 0; a < 4; ++a) {
             if (!hin[a] || n == 0) continue;
-            const char* src = static_cast<const char*>(hin[a]) + (size_t)j * pl.tc * dd * es;
+            const char* src = static_cast<const char*>(hin[a]) + (size_t)pl.start(j) * dd * es;
             if (!ok(cudaMemcpy2DAsync(ws + pl.in_slot[slot] + a * pl.in_arr, row, src, (size_t)T * dd * es, row, bh,
                                       cudaMemcpyHostToDevice, P->in[a & 1])))
                 return false;
@@ -216,22 +246,24 @@ vla_status vla_forward_host(const void* q, const void* k, const void* v, const v
         const int slot = j % kSlots, n = chunk_len(j);
         if (!ok(cudaStreamWaitEvent(cs, P->h2d[slot][0], 0)) || !ok(cudaStreamWaitEvent(cs, P->h2d[slot][1], 0)))
             return fail(VLA_ERR_CUDA);
-        if (j >= kSlots && !ok(cudaStreamWaitEvent(cs, P->d2h[slot], 0))) return fail(VLA_ERR_CUDA);
+        if (!od && j >= kSlots && !ok(cudaStreamWaitEvent(cs, P->d2h[slot], 0))) return fail(VLA_ERR_CUDA);
         const bool first = j == 0;
         char* in = ws + pl.in_slot[slot];
-        float* dO = reinterpret_cast<float*>(ws + pl.out_slot[slot]);
         const bool has = n > 0;
-        st = vla_forward_ex(has ? in : nullptr, has ? in + pl.in_arr : nullptr, has ? in + 2 * pl.in_arr : nullptr,
-                            (has && hin[3]) ? in + 3 * pl.in_arr : nullptr, dtype, B, H, n, d, lambda0, eps,
-                            (first && !S0) ? nullptr : dS, (first && !A0) ? nullptr : dA,
-                            (first && !zk0) ? nullptr : dZ, has ? dO : nullptr, dS, dA, dZ, ws + pl.status,
-                            vla_workspace_bytes(), stream, opts);
+        // o of the chunk: straight into the mapped host array (row pitch T * d), or an output slot
+        float* dO = od ? od + (size_t)pl.start(j) * dd : reinterpret_cast<float*>(ws + pl.out_slot[slot]);
+        st = vla_impl::forward(has ? in : nullptr, has ? in + pl.in_arr : nullptr,
+                               has ? in + 2 * pl.in_arr : nullptr, (has && hin[3]) ? in + 3 * pl.in_arr : nullptr,
+                               dtype, B, H, n, d, lambda0, eps, (first && !S0) ? nullptr : dS,
+                               (first && !A0) ? nullptr : dA, (first && !zk0) ? nullptr : dZ, has ? dO : nullptr, dS,
+                               dA, dZ, ws + pl.status, vla_workspace_bytes(), stream, opts,
+                               od ? (size_t)T * dd : 0);
         if (st != VLA_OK) return fail(st);
         if (!ok(cudaEventRecord(P->kern[slot], cs))) return fail(VLA_ERR_CUDA);
-        if (has) {
+        if (has && !od) {
             const size_t row = (size_t)n * dd * 4;
             if (!ok(cudaStreamWaitEvent(P->out, P->kern[slot], 0)) ||
-                !ok(cudaMemcpy2DAsync(o + (size_t)j * pl.tc * dd, (size_t)T * dd * 4, dO, row, row, bh,
+                !ok(cudaMemcpy2DAsync(o + (size_t)pl.start(j) * dd, (size_t)T * dd * 4, dO, row, row, bh,
                                       cudaMemcpyDeviceToHost, P->out)) ||
                 !ok(cudaEventRecord(P->d2h[slot], P->out)))
                 return fail(VLA_ERR_CUDA);

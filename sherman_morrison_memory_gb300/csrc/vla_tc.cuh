@@ -766,7 +766,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     float* eh = x.f(L::OFF_EH);
     float* el = x.f(L::OFF_EL);
     const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * T * D;
-    float* go = p.o + (size_t)bh * T * D;
+    float* go = p.o + (size_t)bh * p.o_stride;
     bool bad = false, nonfinite = false;
 
     // S_0 = 0 unless carried in, and its lo part

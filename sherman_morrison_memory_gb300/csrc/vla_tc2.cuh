@@ -43,6 +43,10 @@ constexpr int THREADS = 32 * 12;
 constexpr int NT_A = 160, NT_S = 128;        // threads of the rank-0 / rank-1 team barrier
 constexpr int ID_T = 1, ID_ST = 3;           // team and staging named barriers (4, 5: Gram pairs)
 constexpr int FACTOR_WARP = 4;
+// warps that issue the d x 2C chunk products (one thread each, into their own
+// accumulator): issuing a tcgen05.mma costs a thread about 100 clocks at
+// N = 2C, so the K steps are spread over four issuers
+constexpr int NISS = 4;
 // one CTA per SM: a second CTA's tensor-memory request could otherwise wait
 // for a CTA whose cluster peer waits for it
 constexpr size_t MIN_SMEM = 116 * 1024;
@@ -107,6 +111,26 @@ __device__ __noinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, const 
     return false;
 }
 
+// row i of the chunk products summed over the NISS accumulators: columns
+// [0, C) into a, [C, 2C) into b (this warp's TMEM lanes)
+__device__ __forceinline__ void ld_products(uint32_t tp, float (&a)[16], float (&b)[16]) {
+    tc_ld16(tp, a);
+    tc_ld16(tp + C, b);
+    tc_wait_ld();
+#pragma unroll 1
+    for (int q = 1; q < NISS; ++q) {
+        float x[16], y[16];
+        tc_ld16(tp + q * 2 * C, x);
+        tc_ld16(tp + q * 2 * C + C, y);
+        tc_wait_ld();
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            a[t] += x[t];
+            b[t] += y[t];
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // layout (the same offsets in both ranks, so that the mailbox and the
 // barriers of the peer are found by mapa)
@@ -129,10 +153,10 @@ struct Lay2 {
     static constexpr int SCR_STRIDE = D + 4;
     static constexpr int GSTR = C + 4;
     static constexpr int XS = D + 4;
-    // tensor memory of each rank: state | its lo part | chunk products (even
-    // and odd K steps in two accumulators of 2C columns)
-    static constexpr uint32_t T_X = 0, T_XL = D, T_P = 2 * D, T_P2 = 2 * D + 2 * C;
-    static constexpr uint32_t TNEED = 2 * D + 4 * C;
+    // tensor memory of each rank: state | its lo part | chunk products (K
+    // step ks in accumulator ks mod NISS, 2C columns each)
+    static constexpr uint32_t T_X = 0, T_XL = D, T_P = 2 * D;
+    static constexpr uint32_t TNEED = 2 * D + NISS * 2 * C;
     static constexpr uint32_t TCOLS = TNEED <= 128 ? 128 : (TNEED <= 256 ? 256 : 512);
     static_assert(TNEED <= 512, "TMEM columns");
     // mailbox buffer sizes (bytes)
@@ -184,7 +208,7 @@ struct Bars2 {
     uint64_t* full_al;   // [2] rank 1: mailbox buffer filled by rank 0 (tx bytes)
     uint64_t* empty_al;  // [2] rank 0: rank 1 done with the mailbox buffer
     uint64_t* mma_x;     // state update committed
-    uint64_t* mma_p;     // chunk products issued by two warps (count 2)
+    uint64_t* mma_p;     // chunk products issued by NISS warps (count NISS)
 };
 
 template <int D, typename TIn>
@@ -372,7 +396,7 @@ __device__ __forceinline__ void stage2(const Params& p, const Ctx2<D, TIn>& x, i
             x.abort_both(rank);
             // let copies already in flight land before the CTA can exit
             for (int cc = c; cc < issued; ++cc)
-                (void)mbar_wait(x.b.full_r + cc % L::NRAW, (cc / L::NRAW) & 1, nullptr, p.wait_ns);
+                    (void)mbar_wait(x.b.full_r + cc % L::NRAW, (cc / L::NRAW) & 1, nullptr, p.wait_ns);
         }
         return;
     }
@@ -448,16 +472,16 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         const float* hi = x.hi(s);
         const float* sc = x.sc(s);
         // [Z' | W] = A_c [u | k]^T (rows u, k of the chunk; scaled by 1/||.|| below);
-        // warps 0 and 1 issue the even and odd K steps into separate accumulators
-        if (lane == 0 && warp < 2) {
+        // warp q < NISS issues the K steps ks = q mod NISS into accumulator q
+        if (lane == 0 && warp < NISS) {
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, 2 * C);
             const uint32_t bh0 = smem_u32(hi), bl0 = smem_u32(x.lo(s));
+            const uint32_t dst = tm + L::T_P + warp * 2 * C;
 #pragma unroll 1
-            for (int ks = warp; ks < D / 8; ks += 2) {
-                const uint32_t dst = tm + ((ks & 1) ? L::T_P2 : L::T_P);
+            for (int ks = warp; ks < D / 8; ks += NISS) {
                 const uint64_t bd = tc_sdesc(bh0 + ks * 256, 128, L::SBO_D);
-                tc_mma_ts(dst, tm + L::T_X + 8 * ks, bd, id, ks > 1);
+                tc_mma_ts(dst, tm + L::T_X + 8 * ks, bd, id, ks >= NISS);
                 tc_mma_ts(dst, tm + L::T_XL + 8 * ks, bd, id, 1);
                 if constexpr (L::F32IN)
                     tc_mma_ts(dst, tm + L::T_X + 8 * ks, tc_sdesc(bl0 + ks * 256, 128, L::SBO_D), id, 1);
@@ -467,16 +491,12 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         bool ok = mbar_wait(x.b.mma_p, c & 1, nullptr, p.wait_ns);
         tc_fence_after();
         if (rw) {
-            float v0[16], v1[16], v2[16], v3[16];
-            tc_ld16(tl + L::T_P, v0);
-            tc_ld16(tl + L::T_P + C, v1);
-            tc_ld16(tl + L::T_P2, v2);
-            tc_ld16(tl + L::T_P2 + C, v3);
-            tc_wait_ld();
+            float v0[16], v1[16];
+            ld_products(tl + L::T_P, v0, v1);
 #pragma unroll
             for (int t = 0; t < C; ++t) {
-                v0[t] = (v0[t] + v2[t]) * sc[L::SC_IU + t];  // z'_t = A_c u^_t
-                v1[t] = (v1[t] + v3[t]) * sc[L::SC_IK + t];  // w_t = A_c k^_t
+                v0[t] *= sc[L::SC_IU + t];  // z'_t = A_c u^_t
+                v1[t] *= sc[L::SC_IK + t];  // w_t = A_c k^_t
                 xr[t * XS + i] = v0[t];
                 xr[(C + t) * XS + i] = v1[t];
             }
@@ -696,7 +716,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
     float* eh = x.f(L::OFF_EH);
     float* el = x.f(L::OFF_EL);
     const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * T * D;
-    float* go = p.o + (size_t)bh * T * D;
+    float* go = p.o + (size_t)bh * p.o_stride;
     const uint32_t r_empty_al = peer_addr(x.b.empty_al, 0u);
     bool bad = false, nonfinite = false;
     int recv = 0;
@@ -744,17 +764,18 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         const float* hi = x.hi(s);
         const float* sc = x.sc(s);
         const float* alr = x.f(L::OFF_AL) + (size_t)b * C * XS;
-        // [S_c k | S_c phi] (rows k, phi of the chunk)
-        if (lane == 0 && warp < 2) {
+        // [S_c k | S_c phi] (rows k, phi of the chunk); warp q < NISS issues the
+        // K steps ks = q mod NISS into accumulator q
+        if (lane == 0 && warp < NISS) {
             tc_fence_after();
             const uint32_t id32 = tc_idesc_tf32(128, 2 * C), id16 = tc_idesc_tf32(128, C);
             const uint32_t bh0 = smem_u32(hi), bl0 = smem_u32(x.lo(s));
+            const uint32_t dst = tm + L::T_P + warp * 2 * C;
 #pragma unroll 1
-            for (int ks = warp; ks < D / 8; ks += 2) {
-                const uint32_t dst = tm + ((ks & 1) ? L::T_P2 : L::T_P);
+            for (int ks = warp; ks < D / 8; ks += NISS) {
                 const uint64_t bd = tc_sdesc(bh0 + ks * 256, 128, L::SBO_D);
                 const uint64_t bld = tc_sdesc(bl0 + ks * 256, 128, L::SBO_D);
-                tc_mma_ts(dst, tm + L::T_X + 8 * ks, bd, id32, ks > 1);
+                tc_mma_ts(dst, tm + L::T_X + 8 * ks, bd, id32, ks >= NISS);
                 tc_mma_ts(dst, tm + L::T_XL + 8 * ks, bd, id32, 1);
                 if constexpr (L::F32IN)
                     tc_mma_ts(dst, tm + L::T_X + 8 * ks, bld, id32, 1);
@@ -767,17 +788,9 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         tc_fence_after();
         float sk[C], sq[C];
         if (rw) {
-            float v0[16], v1[16], v2[16], v3[16];
-            tc_ld16(tl + L::T_P, v0);
-            tc_ld16(tl + L::T_P + C, v1);
-            tc_ld16(tl + L::T_P2, v2);
-            tc_ld16(tl + L::T_P2 + C, v3);
-            tc_wait_ld();
+            ld_products(tl + L::T_P, sk, sq);
 #pragma unroll
-            for (int t = 0; t < C; ++t) {
-                sk[t] = (v0[t] + v2[t]) * sc[L::SC_IK + t];  // S_c k^_t
-                sq[t] = v1[t] + v3[t];                        // S_c phi_t
-            }
+            for (int t = 0; t < C; ++t) sk[t] *= sc[L::SC_IK + t];  // S_c k^_t; sq = S_c phi_t
         }
         // Lk[t][s] = k^_t . a_s, Lq[t][s] = phi_t . a_s; warp = (matrix, half of D)
         {
@@ -914,7 +927,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc2::THREADS, 1) vla
             mbar_init(x.b.empty_al + s, 1);
         }
         mbar_init(x.b.mma_x, 1);
-        mbar_init(x.b.mma_p, 2);
+        mbar_init(x.b.mma_p, tc2::NISS);
         *x.abort = 0;
         *x.n_sent = 0;
         *x.n_recv = 0;

@@ -65,10 +65,11 @@ def test_chunks_match_oracle(orc, d, dtype, T, chunk, algo):
     _agree(out, _dev_run(arrs, dtype, algo=algo))
 
 
-def test_automatic_chunks_long_sequence(orc):
-    # T = 2048 -> 4 automatic chunks of 512 tokens
+@pytest.mark.parametrize("pin", [True, False])
+def test_automatic_chunks_long_sequence(orc, pin):
+    # T = 2048 -> automatic chunks of 128, 512, 512, 512, 256, 128 tokens
     arrs = _inputs(1, 4, 2048, 96, "bf16", seed=21)
-    out = vla_forward(*_host(arrs, "bf16"), check=True)
+    out = vla_forward(*_host(arrs, "bf16", pin=pin), check=True)
     assert_close(errors(out, orc.forward(*arrs)), what="automatic chunks")
     _agree(out, _dev_run(arrs, "bf16"))
 
@@ -133,3 +134,16 @@ def test_back_to_back_calls_share_workspace(orc):
     assert_close(errors(oa, orc.forward(*arrs_a)), what="first of two calls")
     assert_close(errors(ob, orc.forward(*arrs_b)), what="second of two calls")
     assert TOL == 2e-3
+
+
+@pytest.mark.parametrize("pin_in,pin_out", [(True, True), (True, False), (False, True), (False, False)])
+def test_output_written_in_place_or_copied(orc, pin_in, pin_out):
+    """Page-locked (mapped) host o is written by the kernels directly; pageable
+    o is copied out chunk by chunk. Both give the same result."""
+    B, H, T, d = 1, 3, 170, 64
+    arrs = _inputs(B, H, T, d, "bf16", seed=27)
+    shapes = [(B, H, T, d), (B, H, d, d), (B, H, d, d), (B, H, d)]
+    out = tuple(torch.full(sh, float("nan"), dtype=torch.float32, pin_memory=pin_out) for sh in shapes)
+    res = vla_forward(*_host(arrs, "bf16", pin=pin_in), out=out, chunk_tokens=48, check=True)
+    assert all(r is x for r, x in zip((res[0],) + tuple(res[1]), out))
+    assert_close(errors(res, orc.forward(*arrs)), what=f"pin_in={pin_in} pin_out={pin_out}")
