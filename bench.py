@@ -60,14 +60,22 @@ KERNEL_FILES = {
 }
 
 # DRAM bytes per launch of a bench line's kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum) from one ncu capture of the same command, valid only
-# while that kernel's own sources hash to source_sha; otherwise reported as null.
+# dram__bytes_write.sum) from one ncu capture, valid only for the workload it
+# was taken on (B, H, T, d, input dtype) and while that kernel's own sources
+# hash to source_sha; otherwise reported as null.
 NCU_TRAFFIC = {
-    "vla_tc_kernel": {"source_sha": "11be82f602ecb6d5", "bytes_per_launch": 402884864 + 176023808},
+    "vla_tc_kernel": {"source_sha": "11814d239cfbf5fe", "workload": (8, 16, 4096, 96, "bf16"),
+                      "bytes_per_launch": 402789120 + 176162048},
+    # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
+    # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
+    "vla_tc2_kernel": {"source_sha": "ded3216552f411a1", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (268562432 + 108441344 - 4227072) + 4227072},
     # from a capture of the same workload at B=2 (32 heads; a full launch holds about 2.6 GB on the
     # device) scaled by 4: every byte it moves is per head-token or per head
-    "vla_backward_kernel": {"source_sha": "a8e88d58cc249e71", "bytes_per_launch": 4 * (485387008 + 484124672)},
-    "vla_decode_kernel": {"source_sha": "0f39f3063992b248", "bytes_per_launch": 153396992 + 100321024},
+    "vla_backward_kernel": {"source_sha": "a8e88d58cc249e71", "workload": (8, 16, 4096, 96, "bf16"),
+                            "bytes_per_launch": 4 * (485387008 + 484124672)},
+    "vla_decode_kernel": {"source_sha": "0f39f3063992b248", "workload": (128, 16, 1, 96, "bf16"),
+                          "bytes_per_launch": 153396992 + 100321024},
 }
 
 
@@ -82,11 +90,14 @@ def kernel_source_sha(kernel: str = None) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
+def ncu_traffic(kernel: str, workload=None):
+    """Captured DRAM bytes per launch of `kernel` on `workload` = (B, H, T, d, dtype), or None."""
     t = NCU_TRAFFIC.get(kernel)
-    if t and t["source_sha"] and t["source_sha"] == kernel_source_sha(kernel):
-        return t["bytes_per_launch"]
-    return None
+    if not t or t["source_sha"] != kernel_source_sha(kernel):
+        return None
+    if workload is not None and tuple(workload) != t["workload"]:
+        return None
+    return t["bytes_per_launch"]
 
 
 def load_peaks() -> dict:
@@ -386,7 +397,7 @@ def run_ours(args, w):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
     sha = kernel_source_sha(kernel)
-    traffic = ncu_traffic(kernel)
+    traffic = ncu_traffic(kernel, (B, H, T, d, w.dtype))
 
     # the same metric end to end through the public API with host buffers
     e2e = None
@@ -563,7 +574,7 @@ def run_ours_decode(args, w):
                        "pass": "decode", "B": B, "H": H, "T": T, "d_h": d,
                        "l2": f"state larger than L2 ({state_bytes / 1e6:.0f} MB read and written per step), no flush"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": gbs / hbm_peak, "traffic": ncu_traffic("vla_decode_kernel"),
+                         "frac": gbs / hbm_peak, "traffic": ncu_traffic("vla_decode_kernel", (B, H, T, d, w.dtype)),
                          "bytes_per_head_token": step_bytes // units, "kernel": "vla_decode_kernel"},
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -637,7 +648,7 @@ def run_ours_backward(args, w):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
     sha = kernel_source_sha("vla_backward_kernel")
-    traffic = ncu_traffic("vla_backward_kernel")
+    traffic = ncu_traffic("vla_backward_kernel", (w.B, w.H, w.T, w.d, w.dtype))
 
     e2e = None
     if not args.no_e2e:
