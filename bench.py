@@ -74,8 +74,8 @@ NCU_TRAFFIC = {
     # device) scaled by 4: every byte it moves is per head-token or per head
     "vla_backward_kernel": {"source_sha": "a8e88d58cc249e71", "workload": (8, 16, 4096, 96, "bf16"),
                             "bytes_per_launch": 4 * (485387008 + 484124672)},
-    "vla_decode_kernel": {"source_sha": "0f39f3063992b248", "workload": (128, 16, 1, 96, "bf16"),
-                          "bytes_per_launch": 153396992 + 100321024},
+    "vla_decode_kernel": {"source_sha": "1184df56e9dcd781", "workload": (128, 16, 1, 96, "bf16"),
+                          "bytes_per_launch": 153394688 + 100198656},
 }
 
 
