@@ -136,6 +136,44 @@ struct Ctx {
 // and adds the sums of the warps before it. The raw u, k rows and phi(q)
 // pass through a row-major scratch into the K-major operand tiles.
 // ---------------------------------------------------------------------------
+// The S rows' v loads leave their values unconverted in registers: a bf16 ->
+// fp32 conversion (or a select) right after a global load would make the
+// thread wait for the load there, at the top of the chunk, instead of where
+// the residual first uses it.
+template <typename TIn>
+struct RawIn;
+template <>
+struct RawIn<float> {
+    using type = float;
+};
+template <>
+struct RawIn<__nv_bfloat16> {
+    using type = unsigned short;
+};
+__device__ __forceinline__ float raw_f32(float x) { return x; }
+__device__ __forceinline__ float raw_f32(unsigned short x) { return __uint_as_float((uint32_t)x << 16); }
+
+// rows t < n of column i of a chunk of v (row stride D), unconverted; rows >= n are zero
+template <int D, typename TIn>
+__device__ __forceinline__ void load_v_raw(const TIn* vrow, int i, int n, typename RawIn<TIn>::type (&vr)[16]) {
+    using R = typename RawIn<TIn>::type;
+    const R* p = reinterpret_cast<const R*>(vrow) + i;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        vr[t] = R(0);
+        if (t < n) vr[t] = p[(size_t)t * D];
+    }
+}
+
+// prefetch the n rows of a chunk of v into L2 (one 128-byte line per staging
+// thread; a chunk of v is at most 16 x 128 x 4 bytes = 64 lines)
+template <int D, typename TIn>
+__device__ __forceinline__ void prefetch_v_l2(const TIn* vrow, int n, int tid) {
+    const int bytes = n * D * (int)sizeof(TIn);
+    if (tid * 128 < bytes)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const unsigned char*>(vrow) + tid * 128));
+}
+
 __device__ __forceinline__ float phi_bf(float x) {  // ELU + 1, branch-free; NaN stays NaN
     const float e = __expf(x);
     return x > 0.f ? x + 1.f : e;
@@ -149,6 +187,7 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
     const TIn* gq = static_cast<const TIn*>(p.q) + (size_t)bh * T * D;
     const TIn* gk = static_cast<const TIn*>(p.k) + (size_t)bh * T * D;
     const TIn* gu = static_cast<const TIn*>(p.u) + (size_t)bh * T * D;
+    const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * T * D;
     float zk[E];  // z^key before the chunk (identical in every staging warp)
 #pragma unroll
     for (int m = 0; m < E; ++m) zk[m] = p.zk0 ? p.zk0[(size_t)bh * D + lane + 32 * m] : 0.f;
@@ -179,6 +218,8 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
             bad = true;
             break;
         }
+        // the S rows read this chunk's v from global memory a few chunks from now
+        prefetch_v_l2<D, TIn>(gv + (size_t)c * C * D, n, sw * 32 + lane);
         const TIn* rq = reinterpret_cast<const TIn*>(x.raw(rs));
         const TIn* rk = reinterpret_cast<const TIn*>(x.raw(rs) + L::RAW_T);
         const TIn* ru = reinterpret_cast<const TIn*>(x.raw(rs) + 2 * L::RAW_T);
@@ -798,10 +839,8 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     for (; c < nch; ++c) {
         const int s = c % L::NP, n = min(C, T - c * C), b = c & 1;
         float vv[C];
-        if (rw) {
-#pragma unroll
-            for (int t = 0; t < C; ++t) vv[t] = t < n ? ld_in<TIn>(gv + (size_t)(c * C + t) * D, i) : 0.f;
-        }
+        typename RawIn<TIn>::type vr[C];
+        if (rw) load_v_raw<D, TIn>(gv + (size_t)c * C * D, i, n, vr);
         bad = !mbar_wait(x.b.full_p + s, (c / L::NP) & 1, x.abort, p.wait_ns) ||
               !mbar_wait(x.b.full_al + b, (c >> 1) & 1, x.abort, p.wait_ns);
         if (bar_red_or(ID_S, 128, bad || *x.abort != 0)) {
@@ -868,7 +907,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             ld_row16(sm + L::SM_LAA + b * C, nr);
 #pragma unroll
             for (int t = 0; t < C; ++t) {
-                vv[t] -= sk[t];
+                vv[t] = raw_f32(vr[t]) - sk[t];
                 nr[t] = rsqrtf(fmaxf(nr[t], 1e-24f));
             }
 #pragma unroll

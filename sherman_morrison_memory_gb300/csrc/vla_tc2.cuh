@@ -249,6 +249,7 @@ __device__ __forceinline__ void stage2(const Params& p, const Ctx2<D, TIn>& x, i
     const int T = p.T, nch = (T + C - 1) / C;
     const TIn* g0 = static_cast<const TIn*>(RANK0 ? p.u : p.q) + (size_t)bh * T * D;
     const TIn* gk = static_cast<const TIn*>(p.k) + (size_t)bh * T * D;
+    const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * T * D;
     float zk[E];  // z^key before the chunk (rank 1; identical in every staging warp)
 #pragma unroll
     for (int m = 0; m < E; ++m) zk[m] = (!RANK0 && p.zk0) ? p.zk0[(size_t)bh * D + lane + 32 * m] : 0.f;
@@ -278,6 +279,8 @@ __device__ __forceinline__ void stage2(const Params& p, const Ctx2<D, TIn>& x, i
             bad = true;
             break;
         }
+        // rank 1's S rows read this chunk's v from global memory a few chunks from now
+        if constexpr (!RANK0) tc::prefetch_v_l2<D, TIn>(gv + (size_t)c * C * D, n, sw * 32 + lane);
         const TIn* r0 = reinterpret_cast<const TIn*>(x.raw(rs));
         const TIn* rk = reinterpret_cast<const TIn*>(x.raw(rs) + L::RAW_T);
         float fq[TW][E], pk[TW][E], red[TW][3];
@@ -750,10 +753,8 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
     for (; c < nch; ++c) {
         const int s = c % L::NP, n = min(C, T - c * C), b = c & 1;
         float vv[C];
-        if (rw) {
-#pragma unroll
-            for (int t = 0; t < C; ++t) vv[t] = t < n ? ld_in<TIn>(gv + (size_t)(c * C + t) * D, i) : 0.f;
-        }
+        typename tc::RawIn<TIn>::type vr[C];
+        if (rw) tc::load_v_raw<D, TIn>(gv + (size_t)c * C * D, i, n, vr);
         bad = !mbar_wait(x.b.full_p + s, (c / L::NP) & 1, x.abort, p.wait_ns) ||
               !mbar_wait_cl(x.b.full_al + b, (c >> 1) & 1, x.abort, p.wait_ns);
         if (bar_red_or(ID_T, NT_S, bad || *x.abort != 0)) {
@@ -810,7 +811,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             tc::ld_row16(x.f(L::OFF_LAA) + b * C, nr);
 #pragma unroll
             for (int t = 0; t < C; ++t) {
-                vv[t] -= sk[t];
+                vv[t] = tc::raw_f32(vr[t]) - sk[t];
                 nr[t] = rsqrtf(fmaxf(nr[t], 1e-24f));
             }
 #pragma unroll
