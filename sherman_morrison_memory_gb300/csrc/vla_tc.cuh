@@ -391,9 +391,11 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ uint32_t tf32_hi_bits(float x) { return __float_as_uint(x) & 0xFFFFE000u; }
 __device__ __forceinline__ uint32_t tf32_lo_bits(float x) { return __float_as_uint(tf32_lo(x)); }
 
+// a_exact: every a value is exact in tf32 (raw bf16 inputs), so its lo part is
+// zero and the lo(a) x hi(b) term is skipped.
 template <int D, bool A_CM>
 __device__ __forceinline__ void gram16(const float* a, int as, const float* b, int bs, int k0, int k1, int lane,
-                                       float (&acc)[2][4]) {
+                                       float (&acc)[2][4], bool a_exact = false) {
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll
     for (int n = 0; n < 2; ++n)
@@ -421,13 +423,13 @@ __device__ __forceinline__ void gram16(const float* a, int as, const float* b, i
         }
         const uint32_t ah0 = tf32_hi_bits(av[0]), ah1 = tf32_hi_bits(av[1]), ah2 = tf32_hi_bits(av[2]),
                        ah3 = tf32_hi_bits(av[3]);
-        const uint32_t al0 = tf32_lo_bits(av[0]), al1 = tf32_lo_bits(av[1]), al2 = tf32_lo_bits(av[2]),
-                       al3 = tf32_lo_bits(av[3]);
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
             const uint32_t bh0 = tf32_hi_bits(bv[n][0]), bh1 = tf32_hi_bits(bv[n][1]);
             mma_tf32(acc[n], ah0, ah1, ah2, ah3, tf32_lo_bits(bv[n][0]), tf32_lo_bits(bv[n][1]));
-            mma_tf32(acc[n], al0, al1, al2, al3, bh0, bh1);
+            if (!a_exact)
+                mma_tf32(acc[n], tf32_lo_bits(av[0]), tf32_lo_bits(av[1]), tf32_lo_bits(av[2]), tf32_lo_bits(av[3]),
+                         bh0, bh1);
             mma_tf32(acc[n], ah0, ah1, ah2, ah3, bh0, bh1);
         }
     }
@@ -610,7 +612,8 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             // the half-D partials of a warp pair summed through shared memory
             const int mat = warp & 1, half = warp >> 1;
             float acc[2][4];
-            gram16<D, true>(hi, 0, xr + mat * C * XS, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc);
+            gram16<D, true>(hi, 0, xr + mat * C * XS, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc,
+                            !L::F32IN);
             gram_pair_sum(sm + (mat ? L::SM_GUK : L::SM_GUU), L::MS, L::GSTR, acc, lane, half, 4 + mat,
                           sc + L::SC_IU, false);
             named_bar(ID_A, 128);
@@ -892,7 +895,8 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         {
             const int mat = wq & 1, half = wq >> 1;
             float acc[2][4];
-            gram16<D, true>(hi + (mat ? 32 : 16) * D, 0, alr, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc);
+            gram16<D, true>(hi + (mat ? 32 : 16) * D, 0, alr, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc,
+                            !L::F32IN && mat == 0);
             if (mat)
                 gram_pair_sum(sm + L::SM_LQ, L::MS, L::GSTR, acc, lane, half, 6 + mat, nullptr, false);
             else

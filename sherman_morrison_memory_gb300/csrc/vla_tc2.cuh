@@ -514,7 +514,8 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             if (warp < 4) {
                 const int mat = warp & 1, half = warp >> 1;
                 float acc[2][4];
-                tc::gram16<D, true>(hi, 0, xr + mat * C * XS, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc);
+                tc::gram16<D, true>(hi, 0, xr + mat * C * XS, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc,
+                                    !L::F32IN);
                 tc::gram_pair_sum(sm + (mat ? L::SM_GUK : L::SM_GUU), L::MS, L::GSTR, acc, lane, half, 4 + mat,
                                   sc + L::SC_IU, false);
             }
@@ -797,7 +798,8 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         {
             const int mat = warp & 1, half = warp >> 1;
             float acc[2][4];
-            tc::gram16<D, true>(hi + (mat ? C : 0) * D, 0, alr, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc);
+            tc::gram16<D, true>(hi + (mat ? C : 0) * D, 0, alr, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc,
+                                !L::F32IN && mat == 0);
             if (mat)
                 tc::gram_pair_sum(sm + L::SM_LQ, L::MS, L::GSTR, acc, lane, half, 4 + mat, nullptr, false);
             else
