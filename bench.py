@@ -64,12 +64,12 @@ KERNEL_FILES = {
 # was taken on (B, H, T, d, input dtype) and while that kernel's own sources
 # hash to source_sha; otherwise reported as null.
 NCU_TRAFFIC = {
-    "vla_tc_kernel": {"source_sha": "11814d239cfbf5fe", "workload": (8, 16, 4096, 96, "bf16"),
-                      "bytes_per_launch": 402789120 + 176162048},
+    "vla_tc_kernel": {"source_sha": "cd59003580031efb", "workload": (8, 16, 4096, 96, "bf16"),
+                      "bytes_per_launch": 403204864 + 175723520},
     # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
-    "vla_tc2_kernel": {"source_sha": "ded3216552f411a1", "workload": (1, 32, 65536, 128, "bf16"),
-                       "bytes_per_launch": 8 * (268562432 + 108441344 - 4227072) + 4227072},
+    "vla_tc2_kernel": {"source_sha": "111b7a2bfcc953fa", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (269610240 + 108268288 - 4227072) + 4227072},
     # from a capture of the same workload at B=2 (32 heads; a full launch holds about 2.6 GB on the
     # device) scaled by 4: every byte it moves is per head-token or per head
     "vla_backward_kernel": {"source_sha": "a8e88d58cc249e71", "workload": (8, 16, 4096, 96, "bf16"),
