@@ -252,7 +252,8 @@ vla_status vla_linear_attention_state(const void* k, const void* v, vla_dtype dt
 /* Bytes of device workspace vla_backward() needs for (B, H, T, d): one status
  * record, a per-token tape of the forward pass (z_t, alpha^_t, e_t, delta_t,
  * ||A_t k^_t||, den_t, ||u_t||^2, ||k_t||^2: 3d + 8 floats per head-token) and
- * S, A, z^key checkpoints every 64 tokens (2 d^2 + d floats each). 0 if the
+ * S, A, z^key checkpoints every 64 tokens (2 d^2 + d floats each), and the
+ * forward's final S, A, z^key (2 d^2 + d floats per head). 0 if the
  * sizes overflow. */
 size_t vla_backward_workspace_bytes(int B, int H, int T, int d);
 

@@ -236,7 +236,7 @@ template <int D, typename TIn>
 __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     vla_backward_kernel(const Params p, const float* dO, const float* dST, const float* dAT, const float* dzkT,
                         float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0, float* dzk0,
-                        float* tape, float* ckpt) {
+                        float* tape, float* ckpt, const float* fin) {
     using L = BLay<D, TIn>;
     constexpr int RW = L::RW, CL = L::CL, NW = L::NW, NB1 = L::NB1, NB2 = L::NB2;
     constexpr unsigned FULL = 0xffffffffu;
@@ -279,8 +279,24 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     for (int c = 0; c < CL; ++c) zk[c] = p.zk0 ? p.zk0[(size_t)bh * D + l + 32 * c] : 0.f;
 
     // ------------------------------------------------------------------
-    // phase 1: forward with tape
+    // phase 1: forward with tape. When `fin` is given, the chunked forward
+    // kernel has already written the tape and the checkpoints, and `fin`
+    // holds its final S [B*H, d, d] | A [B*H, d, d] | z^key [B*H, d].
     // ------------------------------------------------------------------
+    if (fin) {
+        const size_t BH = gridDim.x;
+#pragma unroll
+        for (int r = 0; r < RW; ++r)
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                const size_t e = hdd + (size_t)(r0 + r) * D + l + 32 * c;
+                S[r][c] = fin[e];
+                A[r][c] = fin[BH * D * D + e];
+            }
+#pragma unroll
+        for (int c = 0; c < CL; ++c) zk[c] = fin[2 * BH * D * D + (size_t)bh * D + l + 32 * c];
+    }
+    if (!fin) {
     for (int s = 0; s < NB1 - 1; ++s) {
         if (s < T) prefetch_fwd<D, TIn>(ring + s * L::SLOT_B, gu, gk, gq, gv, s);
         cp_commit();
@@ -420,6 +436,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
         nu = d5[3];
         nk = d5[4];
     }
+    }  // !fin
 
     // ------------------------------------------------------------------
     // phase 2: reverse sweep

@@ -147,6 +147,8 @@ struct Params {
     int stall_producer;
     unsigned long long* trace;
     int fixed_a;  // the fixed-A variant: A stays A0 and eq. 9 is skipped
+    float* tape;  // chunked kernel with TAPE (the backward pass's forward): per-token records
+    float* ckpt;  //   and the states before every 64th token; else null
 };
 
 // Per-token clock stamps of head 0 for pipeline analysis (-DVLA_TRACE builds only).
@@ -1280,7 +1282,7 @@ vla_status vla_impl::forward(const void* q, const void* k, const void* v, const 
         (zk_out && !aligned4(zk_out)))
         return VLA_ERR_INVALID_ARG;
 
-    vla::Params p;
+    vla::Params p{};
     p.q = q;
     p.k = k;
     p.v = v;
@@ -1445,7 +1447,7 @@ vla_status vla_linear_attention_state(const void* k, const void* v, vla_dtype dt
 namespace {
 
 struct BwSizes {
-    size_t tape, ckpt, total;
+    size_t tape, ckpt, fin, total;
 };
 
 bool bw_sizes(int B, int H, int T, int d, BwSizes* out) {
@@ -1457,32 +1459,59 @@ bool bw_sizes(int B, int H, int T, int d, BwSizes* out) {
         BH * nck * (2ull * (unsigned long long)d * (unsigned long long)d + (unsigned long long)d) * 4ull;
     if (BH > (1ull << 31) || tape > (1ull << 50) || ck > (1ull << 50)) return false;
     auto al = [](unsigned long long x) { return (x + 255ull) / 256ull * 256ull; };
+    const unsigned long long fin = BH * (2ull * (unsigned long long)d * (unsigned long long)d + (unsigned long long)d) * 4ull;
     out->tape = (size_t)al(tape);
     out->ckpt = (size_t)al(ck);
-    out->total = kWorkspaceBytes + out->tape + out->ckpt;
+    out->fin = (size_t)al(fin);
+    out->total = kWorkspaceBytes + out->tape + out->ckpt + out->fin;
     return true;
 }
 
 template <int D, typename TIn>
 vla_status launch_bw(const vla::Params& p, int BH, const float* dO, const float* dST, const float* dAT,
                      const float* dzkT, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
-                     float* dzk0, float* tape, float* ckpt, cudaStream_t s) {
+                     float* dzk0, float* tape, float* ckpt, float* fin, cudaStream_t s) {
     using BL = vla::bw::BLay<D, TIn>;
+    using TL = vla::tc::Lay<D, TIn>;
+    const float* fin_used = nullptr;
+    if (p.T > 0) {
+        // the forward on the chunked tensor-core kernel, writing the tape, the
+        // checkpoints and the final state (o goes to dq, which the reverse sweep
+        // overwrites)
+        vla::Params pf = p;
+        pf.o = dq;
+        pf.o_stride = (size_t)p.T * D;
+        pf.S_out = fin;
+        pf.A_out = fin + (size_t)BH * D * D;
+        pf.zk_out = fin + 2 * (size_t)BH * D * D;
+        pf.tape = tape;
+        pf.ckpt = ckpt;
+        auto fk = vla::vla_tc_kernel<D, TIn, true>;
+        if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TL::SMEM) != cudaSuccess)
+            return VLA_ERR_CUDA;
+        fk<<<BH, vla::tc::THREADS, TL::SMEM, s>>>(pf);
+        if (cudaGetLastError() != cudaSuccess) return VLA_ERR_CUDA;
+        fin_used = fin;
+    }
     auto kern = vla::bw::vla_backward_kernel<D, TIn>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BL::SMEM) != cudaSuccess)
         return VLA_ERR_CUDA;
-    kern<<<BH, BL::THREADS, BL::SMEM, s>>>(p, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt);
+    kern<<<BH, BL::THREADS, BL::SMEM, s>>>(p, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt,
+                                           fin_used);
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
 }
 
 template <typename TIn>
 vla_status launch_bw_d(int d, const vla::Params& p, int BH, const float* dO, const float* dST, const float* dAT,
                        const float* dzkT, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
-                       float* dzk0, float* tape, float* ckpt, cudaStream_t s) {
+                       float* dzk0, float* tape, float* ckpt, float* fin, cudaStream_t s) {
     switch (d) {
-        case 32: return launch_bw<32, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, s);
-        case 64: return launch_bw<64, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, s);
-        case 96: return launch_bw<96, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, s);
+        case 32:
+            return launch_bw<32, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin, s);
+        case 64:
+            return launch_bw<64, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin, s);
+        case 96:
+            return launch_bw<96, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin, s);
         default: return VLA_ERR_UNSUPPORTED;
     }
 }
@@ -1538,11 +1567,12 @@ vla_status vla_backward(const void* q, const void* k, const void* v, const void*
     unsigned char* w = static_cast<unsigned char*>(workspace);
     float* tape = reinterpret_cast<float*>(w + kWorkspaceBytes);
     float* ckpt = reinterpret_cast<float*>(w + kWorkspaceBytes + z.tape);
+    float* fin = reinterpret_cast<float*>(w + kWorkspaceBytes + z.tape + z.ckpt);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == VLA_BF16 ? launch_bw_d<__nv_bfloat16>(d, p, (int)BH, dO, dS_T, dA_T, dzk_T, dq, dk, dv, du, dS0,
-                                                          dA0, dzk0, tape, ckpt, s)
+                                                          dA0, dzk0, tape, ckpt, fin, s)
                              : launch_bw_d<float>(d, p, (int)BH, dO, dS_T, dA_T, dzk_T, dq, dk, dv, du, dS0, dA0,
-                                                  dzk0, tape, ckpt, s);
+                                                  dzk0, tape, ckpt, fin, s);
 }
 
 }  // extern "C"

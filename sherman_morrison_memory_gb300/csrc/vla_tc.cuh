@@ -179,7 +179,35 @@ __device__ __forceinline__ float phi_bf(float x) {  // ELU + 1, branch-free; NaN
     return x > 0.f ? x + 1.f : e;
 }
 
-template <int D, typename TIn>
+// record of token t of head bh in the backward pass's tape, and the checkpoint
+// slot of the state before token 64 k (layouts of vla_backward.cuh)
+template <int D>
+__device__ __forceinline__ float* tape_rec(const Params& p, int bh, int t) {
+    return p.tape + ((size_t)bh * p.T + t) * (size_t)(3 * D + 8);
+}
+template <int D>
+__device__ __forceinline__ float* ckpt_slot(const Params& p, int bh, int k) {
+    return p.ckpt + ((size_t)bh * ((p.T + 63) / 64 + 1) + k) * (size_t)(2 * D * D + D);
+}
+// row i (this thread's TMEM lane) of a d x d state in TMEM columns [col, col + D) to dst[0..D)
+template <int D>
+__device__ __forceinline__ void tmem_row_out(uint32_t lanebase, uint32_t col, float* dst) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+        tc_ld16(lanebase + col + c0, v);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    }
+}
+
+// TAPE (the backward pass's forward): also write, per token, the record the
+// reverse sweep reads (z_t, alpha^_t, e_t, delta_t, ||a_t||, den_t with the
+// sign of the eps floor, ||u_t||^2, ||k_t||^2: 3d + 8 floats) to p.tape, and
+// the state before every 64th token (S, A, z^key) to p.ckpt.
+template <int D, typename TIn, bool TAPE>
 __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, int bh, int sw, int lane) {
     using L = Lay<D, TIn>;
     constexpr int E = D / 32, TW = C / NSTAGE;
@@ -220,6 +248,11 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
         }
         // the S rows read this chunk's v from global memory a few chunks from now
         prefetch_v_l2<D, TIn>(gv + (size_t)c * C * D, n, sw * 32 + lane);
+        if (TAPE && (c & 3) == 0 && sw == 0) {  // z^key before token 16 c (= 64 (c / 4))
+            float* ck = ckpt_slot<D>(p, bh, c >> 2) + 2 * D * D;
+#pragma unroll
+            for (int m = 0; m < E; ++m) ck[lane + 32 * m] = zk[m];
+        }
         const TIn* rq = reinterpret_cast<const TIn*>(x.raw(rs));
         const TIn* rk = reinterpret_cast<const TIn*>(x.raw(rs) + L::RAW_T);
         const TIn* ru = reinterpret_cast<const TIn*>(x.raw(rs) + 2 * L::RAW_T);
@@ -282,6 +315,12 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
             sc[L::SC_IU + t] = t < n ? rsqrtf(fmaxf(r0, 1e-24f)) : 0.f;
             sc[L::SC_IK + t] = t < n ? rsqrtf(fmaxf(r1, 1e-24f)) : 0.f;
             sc[L::SC_RDEN + t] = t < n ? __frcp_rn(fmaxf(r2, p.eps)) : 1.f;  // 1 / den
+            if (TAPE && t < n) {
+                float* rec = tape_rec<D>(p, bh, c * C + t) + 3 * D;
+                rec[2] = r2 < p.eps ? -p.eps : r2;  // den, negative where the eps floor is taken
+                rec[3] = r0;                         // ||u_t||^2
+                rec[4] = r1;                         // ||k_t||^2
+            }
         }
         named_bar(ID_ST, 32 * NSTAGE);
         // scratch rows -> operand tiles, one 8-row group per unit: lane =
@@ -509,7 +548,7 @@ __device__ __forceinline__ void refresh_lo(uint32_t lanebase, uint32_t col, uint
 // one chunk at a time. Thread i < D of the row warps owns row i of A (TMEM
 // lane i) and of every d x C intermediate.
 // ---------------------------------------------------------------------------
-template <int D, typename TIn>
+template <int D, typename TIn, bool TAPE>
 __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int warp, int lane) {
     using L = Lay<D, TIn>;
     constexpr int XS = L::XS;
@@ -565,6 +604,10 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             break;
         }
         if (ta == 0) VLA_TRACE_AT(p, 4, c);
+        if (TAPE && (c & 3) == 0 && rw) {  // A before token 16 c
+            tc_fence_after();
+            tmem_row_out<D>(tl, L::T_A, ckpt_slot<D>(p, bh, c >> 2) + D * D + (size_t)i * D);
+        }
         const float* hi = x.hi(s);
         const float* sc = x.sc(s);
         // [Z' | W] = A_c [u | k]^T (rows u, k of the chunk; scaled by 1/||.|| below);
@@ -620,6 +663,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         }
         if (ta == 0) VLA_TRACE_AT(p, 6, c);
         if (ta == 0) mbar_arrive(x.b.empty_p + s);  // done with the chunk's u, k rows
+        float mypiv = 1.f;  // delta of token `lane` (warp 3, taped)
         if (warp == 3 && !fixed) {
             // LDL^T of I + Guu by Gaussian elimination of the augmented
             // [I + Guu | Guk]: lane j < C holds column j, lane C + j column j of
@@ -637,6 +681,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 const float piv = __shfl_sync(0xffffffffu, col[t], t);
                 const float rdt = rcp_approx(piv);
                 if (lane == t) myrd = rdt;
+                if (TAPE && lane == t) mypiv = piv;
                 if (!(piv > 0.f) || !isfinite(rdt)) nonfinite = true;
                 // eliminate below pivot t in the columns not yet factored (M
                 // columns j > t, every Guk column); a factored column j keeps
@@ -687,6 +732,11 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 ld_row16(sm + L::SM_LMT + r * L::GSTR, lr);  // L[t][r], t > r
 #pragma unroll
                 for (int t = r + 1; t < C; ++t) y[t] = fmaf(-lr[t], y[r], y[t]);
+            }
+            if (TAPE) {  // z_t = A_{t-1} u^_t of eq. 9
+#pragma unroll
+                for (int t = 0; t < C; ++t)
+                    if (t < n) tape_rec<D>(p, bh, c * C + t)[i] = y[t];
             }
             ld_row16(sm + L::SM_RD, lr);
 #pragma unroll
@@ -755,6 +805,11 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                     acc = __ffma2_rn(f2(a.z, a.w), f2(a.z, a.w), acc);
                 }
                 sm[L::SM_LAA + b * C + lane] = acc.x + acc.y;
+                if (TAPE && lane < n) {
+                    float* rec = tape_rec<D>(p, bh, c * C + lane) + 3 * D;
+                    rec[0] = mypiv;                      // delta_t = 1 + u^_t . z_t
+                    rec[1] = sqrtf(acc.x + acc.y);       // ||a_t||
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(x.b.full_al + b);
@@ -796,7 +851,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
 // S team (warps 4-7): residual writes and readout of eq. 10-11 for the chunk
 // the A team published. Thread i < D of the row warps owns row i of S.
 // ---------------------------------------------------------------------------
-template <int D, typename TIn>
+template <int D, typename TIn, bool TAPE>
 __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int warp, int lane) {
     using L = Lay<D, TIn>;
     constexpr int XS = L::XS;
@@ -853,6 +908,10 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         const float* hi = x.hi(s);
         const float* sc = x.sc(s);
         if (ts == 0) VLA_TRACE_AT(p, 11, c);
+        if (TAPE && (c & 3) == 0 && rw) {  // S before token 16 c
+            tc_fence_after();
+            tmem_row_out<D>(tl, L::T_S, ckpt_slot<D>(p, bh, c >> 2) + (size_t)i * D);
+        }
         const float* alr = x.f(L::OFF_AL) + (size_t)b * C * XS;
         // [S_c k | S_c phi] (rows k, phi of the chunk)
         if (lane == 0 && wq < 2) {
@@ -924,6 +983,15 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 }
             }
             if (ts == 0) VLA_TRACE_AT(p, 0, c);
+            if (TAPE) {  // alpha^_t = a_t / ||a_t|| and e_t = e'_t ||a_t|| (eq. 10)
+#pragma unroll
+                for (int t = 0; t < C; ++t)
+                    if (t < n) {
+                        float* rec = tape_rec<D>(p, bh, c * C + t);
+                        rec[D + i] = alr[t * XS + i] * nr[t];
+                        rec[2 * D + i] = vv[t] / nr[t];
+                    }
+            }
             // o_t = (S_c phi_t + sum_{s<=t} e_s (alpha^_s . phi_t)) / den_t = S_t phi_t / den_t (eq. 11)
             ld_row16(sc + L::SC_RDEN, nr);
 #pragma unroll
@@ -997,7 +1065,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
 
 }  // namespace tc
 
-template <int D, typename TIn>
+template <int D, typename TIn, bool TAPE = false>
 __global__ void __launch_bounds__(tc::THREADS, 1) vla_tc_kernel(const Params p) {
     using L = tc::Lay<D, TIn>;
     static_assert(D % 32 == 0 && D <= 96, "row warps of a team fit in warps 0-2 / 4-6");
@@ -1040,11 +1108,11 @@ __global__ void __launch_bounds__(tc::THREADS, 1) vla_tc_kernel(const Params p) 
     __syncthreads();
     tc_fence_after();
     if (warp < 4)
-        tc::tc_a_team<D, TIn>(p, x, bh, warp, lane);
+        tc::tc_a_team<D, TIn, TAPE>(p, x, bh, warp, lane);
     else if (warp < 8)
-        tc::tc_s_team<D, TIn>(p, x, bh, warp, lane);
+        tc::tc_s_team<D, TIn, TAPE>(p, x, bh, warp, lane);
     else
-        tc::tc_stage<D, TIn>(p, x, bh, warp - 8, lane);
+        tc::tc_stage<D, TIn, TAPE>(p, x, bh, warp - 8, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -118,11 +118,15 @@ def test_u_may_be_null_only_for_fixed_a(lib):
 
 def test_backward_workspace_bytes(lib):
     """Status record + tape (3d + 8 floats per head-token) + S, A, z^key
-    checkpoints every 64 tokens plus the initial one (2 d^2 + d floats each),
-    each part 256-byte aligned."""
+    checkpoints every 64 tokens plus one more slot (2 d^2 + d floats each) +
+    the forward's final S, A, z^key (2 d^2 + d floats per head), each part
+    256-byte aligned."""
     al = lambda x: (x + 255) // 256 * 256
-    assert lib.vla_backward_workspace_bytes(1, 1, 64, 32) == 256 + al(64 * 104 * 4) + al(2 * (2 * 32 * 32 + 32) * 4)
-    assert lib.vla_backward_workspace_bytes(2, 3, 65, 96) == 256 + al(6 * 65 * 296 * 4) + al(6 * 3 * (2 * 96 * 96 + 96) * 4)
+    assert lib.vla_backward_workspace_bytes(1, 1, 64, 32) == (256 + al(64 * 104 * 4) + al(2 * (2 * 32 * 32 + 32) * 4)
+                                                             + al((2 * 32 * 32 + 32) * 4))
+    assert lib.vla_backward_workspace_bytes(2, 3, 65, 96) == (256 + al(6 * 65 * 296 * 4)
+                                                             + al(6 * 3 * (2 * 96 * 96 + 96) * 4)
+                                                             + al(6 * (2 * 96 * 96 + 96) * 4))
     assert lib.vla_backward_workspace_bytes(1, 1, 0, 64) > 0
     assert lib.vla_backward_workspace_bytes(-1, 1, 4, 64) == 0
     assert lib.vla_backward_workspace_bytes(1 << 30, 1 << 30, 4, 64) == 0
