@@ -40,6 +40,7 @@ constexpr int C = 16;           // tokens per chunk
 constexpr int NSTAGE = 4;        // staging warps
 constexpr int THREADS = 32 * (8 + NSTAGE);
 constexpr int ID_A = 1, ID_S = 2, ID_ST = 3;  // named barriers of the A team, S team, staging warps
+constexpr int ID_M = 9;  // A-team rows (arrive) -> warp 3 (sync): -M of a chunk is in place
 
 template <int D, typename TIn>
 struct Lay {
@@ -543,6 +544,11 @@ __device__ __forceinline__ void refresh_lo(uint32_t lanebase, uint32_t col, uint
     tc_wait_st();
 }
 
+// arrive at named barrier `id` (of `nthreads`) without waiting for it
+__device__ __forceinline__ void bar_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // A team (warps 0-3): Sherman-Morrison steps of eq. 9 and the gate of eq. 10,
 // one chunk at a time. Thread i < D of the row warps owns row i of A (TMEM
@@ -757,9 +763,13 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             put_row16(pl, i, mv, true);
         }
         fence_proxy_async_smem();
-        named_bar(ID_A, 128);
-        // A_{c+1} = A_c - M Z'^T
-        if (ta == 0 && !fixed) {
+        // A_{c+1} = A_c - M Z'^T, issued by warp 3 (not a row warp for d <= 96) once
+        // the rows have -M in place; the rows go on to the gate without waiting
+        if (warp < 3)
+            bar_arrive(ID_M, 128);
+        else
+            named_bar(ID_M, 128);
+        if (warp == 3 && lane == 0 && !fixed) {
             VLA_TRACE_AT(p, 8, c);
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, D);
