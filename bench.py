@@ -64,8 +64,8 @@ KERNEL_FILES = {
 # was taken on (B, H, T, d, input dtype) and while that kernel's own sources
 # hash to source_sha; otherwise reported as null.
 NCU_TRAFFIC = {
-    "vla_tc_kernel": {"source_sha": "cd59003580031efb", "workload": (8, 16, 4096, 96, "bf16"),
-                      "bytes_per_launch": 403204864 + 175723520},
+    "vla_tc_kernel": {"source_sha": "7b3cdff138d6bc99", "workload": (8, 16, 4096, 96, "bf16"),
+                      "bytes_per_launch": 403343360 + 176027392},
     # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
     "vla_tc2_kernel": {"source_sha": "111b7a2bfcc953fa", "workload": (1, 32, 65536, 128, "bf16"),
