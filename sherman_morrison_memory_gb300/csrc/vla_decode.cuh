@@ -13,7 +13,9 @@
 // (A u^, A k^, S k^, S phi(q), with the states before the token), a
 // warp-shuffle halving exchange for the row sums, one block barrier to share
 // z and A k^, then scalars by warp butterflies and the rank-1 updates in
-// registers. The readout uses S_t phi = S_{t-1} phi + e (alpha^ . phi).
+// registers. The readout uses S_t phi = S_{t-1} phi + e (alpha^ . phi). For
+// d <= 96 the finished head's S and A go back through shared memory and two
+// bulk copies, which overlap the next head's work.
 
 namespace dec {
 
@@ -33,7 +35,11 @@ struct DLay {
     static constexpr int IZ = IA + D * D * 4;
     static constexpr int IU = IZ + D * 4;
     static constexpr int IK = IU + IN_B, IQ = IK + IN_B, IV = IQ + IN_B;
-    static constexpr int SMEM = IV + IN_B;
+    // the finished head's S | A, written out by two bulk copies (when both
+    // areas fit: d <= 96; larger d stores from registers)
+    static constexpr int OS = (IV + IN_B + 127) / 128 * 128, OA = OS + D * D * 4;
+    static constexpr bool BULK_OUT = OA + D * D * 4 <= 227 * 1024;
+    static constexpr int SMEM = BULK_OUT ? OA + D * D * 4 : IV + IN_B;
     static_assert(D % 32 == 0 && D <= 128, "register tiles hold 8 rows x d/32 columns of S and A");
     static_assert(IS % 16 == 0 && IN_B % 16 == 0, "bulk copy alignment");
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -65,6 +71,19 @@ __device__ __forceinline__ float rowsum8(const float (&p)[8]) {
 }
 
 __device__ __forceinline__ float inv_norm(float n2) { return fminf(rsqrtf(n2), 1e12f); }  // 1 / max(sqrt(n2), 1e-12)
+
+// bulk copy shared -> global (both addresses 16-byte aligned, size a multiple
+// of 16), tracked by this thread's bulk async-groups
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk copies have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's bulk copies are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Thread 0: bulk copies of head h's carried state and first-token inputs into
 // the IN area, completing on `bar`. Every copied pointer is 16-byte aligned
@@ -133,7 +152,10 @@ __global__ void __launch_bounds__(DLay<D, TIn>::THREADS, 1) vla_decode_kernel(co
         if (bulk) {
             const bool timed_out = !mbar_wait(bar, it & 1, nullptr, p.wait_ns);
             if (__syncthreads_or(timed_out)) {
-                if (tid == 0) record_failure(p.status, BIT_TIMEOUT, ROLE_S, bh, 0);
+                if (tid == 0) {
+                    record_failure(p.status, BIT_TIMEOUT, ROLE_S, bh, 0);
+                    if (L::BULK_OUT) bulk_wait_all();  // earlier heads' stores leave shared memory first
+                }
                 return;
             }
 #pragma unroll
@@ -295,20 +317,47 @@ __global__ void __launch_bounds__(DLay<D, TIn>::THREADS, 1) vla_decode_kernel(co
             nu = d5[3];
             nk = d5[4];
         }
-#pragma unroll
-        for (int r = 0; r < RW; ++r)
-#pragma unroll
-            for (int c = 0; c < CL; ++c) {
-                const size_t e = hdd + (size_t)(r0 + r) * D + l + 32 * c;
-                p.S_out[e] = S[r][c];
-                p.A_out[e] = A[r][c];
+        if constexpr (L::BULK_OUT) {
+            // the state through shared memory and two bulk copies: the previous
+            // head's copies have read the OUT area before it is rewritten
+            float* oS = reinterpret_cast<float*>(sm + L::OS);
+            float* oA = reinterpret_cast<float*>(sm + L::OA);
+            if (it > 0) {
+                if (tid == 0) bulk_wait_read();
+                __syncthreads();
             }
+#pragma unroll
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    const int e = (r0 + r) * D + l + 32 * c;
+                    oS[e] = S[r][c];
+                    oA[e] = A[r][c];
+                }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                bulk_s2g(p.S_out + hdd, oS, D * D * 4);
+                bulk_s2g(p.A_out + hdd, oA, D * D * 4);
+                bulk_commit();
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    const size_t e = hdd + (size_t)(r0 + r) * D + l + 32 * c;
+                    p.S_out[e] = S[r][c];
+                    p.A_out[e] = A[r][c];
+                }
+        }
         if (w == 0 && p.zk_out)
 #pragma unroll
             for (int c = 0; c < CL; ++c) p.zk_out[(size_t)bh * D + l + 32 * c] = zk[c];
         if (bad) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
         bad = false;
     }
+    if (L::BULK_OUT && tid == 0) bulk_wait_all();
 }
 
 }  // namespace dec
