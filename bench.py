@@ -68,15 +68,15 @@ NCU_TRAFFIC = {
                       "bytes_per_launch": 403343360 + 176027392},
     # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
-    "vla_tc2_kernel": {"source_sha": "111b7a2bfcc953fa", "workload": (1, 32, 65536, 128, "bf16"),
-                       "bytes_per_launch": 8 * (269610240 + 108268288 - 4227072) + 4227072},
+    "vla_tc2_kernel": {"source_sha": "aeb9ce62cb15937b", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (268578304 + 108794112 - 4227072) + 4227072},
     # the reverse sweep (the step's dominant kernel, after the taped chunked forward), from a capture of
     # the same workload at B=2 (32 heads; a full step holds about 2.8 GB on the device) scaled by 4:
     # every byte it moves is per head-token or per head
     "vla_backward_kernel": {"source_sha": "59d6bc9c070fdaa3", "workload": (8, 16, 4096, 96, "bf16"),
                             "bytes_per_launch": 4 * (435487488 + 177234688)},
-    "vla_decode_kernel": {"source_sha": "1184df56e9dcd781", "workload": (128, 16, 1, 96, "bf16"),
-                          "bytes_per_launch": 153394688 + 100198656},
+    "vla_decode_kernel": {"source_sha": "25e3bf6ab2367048", "workload": (128, 16, 1, 96, "bf16"),
+                          "bytes_per_launch": 153395456 + 98124544},
 }
 
 
