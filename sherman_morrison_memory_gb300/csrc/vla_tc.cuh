@@ -30,9 +30,9 @@
 // vectors are MMA operands in shared memory.
 //
 // Warps: 0-3 A team (row warps own TMEM lane quarters, warp 3 also factors
-// I + Guu), 4-7 S team (row warps), 8-11 staging (TMA bulk copies of q, k, u;
-// phi, norms, z^key, den, operand tiles). The A team runs up to two chunks
-// ahead of the S team. All waits are bounded.
+// I + Guu), 4-7 S team (row warps; 6-7 form the gate), 8-11 staging (TMA bulk
+// copies of q, k, u; phi, norms, z^key, den, operand tiles). The A team runs up
+// to two chunks ahead of the S team's gate. All waits are bounded.
 
 namespace tc {
 
@@ -41,6 +41,7 @@ constexpr int NSTAGE = 4;        // staging warps
 constexpr int THREADS = 32 * (8 + NSTAGE);
 constexpr int ID_A = 1, ID_S = 2, ID_ST = 3;  // named barriers of the A team, S team, staging warps
 constexpr int ID_M = 9;  // A-team rows (arrive) -> warp 3 (sync): -M of a chunk is in place
+constexpr int ID_G = 8;  // S-team warps 6 and 7: the chunk's gate rows are in place
 
 template <int D, typename TIn>
 struct Lay {
@@ -86,17 +87,22 @@ struct Lay {
     static constexpr size_t OFF_ZL = OFF_ZH + (size_t)D * C * 4;
     static constexpr size_t OFF_EH = OFF_ZL + (size_t)D * C * 4;            // E hi/lo, 128 x C
     static constexpr size_t OFF_EL = OFF_EH + 128 * C * 4;
-    static constexpr size_t OFF_AL = OFF_EL + 128 * C * 4;                  // a rows [2][C x XS]
-    static constexpr size_t OFF_GH = OFF_AL + (size_t)2 * C * XS * 4;      // a^T hi/lo [2][D x C]
-    static constexpr size_t OFF_GL = OFF_GH + (size_t)2 * D * C * 4;
-    static constexpr size_t OFF_SM = OFF_GL + (size_t)2 * D * C * 4;       // small matrices
+    // the gate of a chunk, formed by the S team: a rows [C x XS], a^T hi/lo [D x C]
+    static constexpr size_t OFF_AL = OFF_EL + 128 * C * 4;
+    static constexpr size_t OFF_GH = OFF_AL + (size_t)C * XS * 4;
+    static constexpr size_t OFF_GL = OFF_GH + (size_t)D * C * 4;
+    // what the A team hands the S team for a chunk's gate, two buffers each:
+    // w rows [C x D], y rows (z / delta) [C x D], X [C x GSTR]
+    static constexpr size_t OFF_WP = OFF_GL + (size_t)D * C * 4;
+    static constexpr size_t OFF_YP = OFF_WP + (size_t)2 * C * D * 4;
+    static constexpr size_t OFF_XP = OFF_YP + (size_t)2 * C * D * 4;
+    static constexpr size_t OFF_SM = OFF_XP + (size_t)2 * C * GSTR * 4;    // small matrices
     // small matrices: Guu, Guk (two partial sums each, over the halves of
-    // D), L, L^T, X^T (X = L^-1 Guk), Lk^T, Lq (two partials each),
-    // 1/delta, ||a||^2 of the two a buffers
+    // D), L, L^T, Lk^T, Lq (two partials each), 1/delta, ||a||^2
     static constexpr int MS = C * GSTR;
-    static constexpr int SM_GUU = 0, SM_GUK = 2 * MS, SM_LM = 4 * MS, SM_LMT = 5 * MS, SM_XGT = 6 * MS,
-                         SM_LKT = 7 * MS, SM_LQ = 9 * MS, SM_RD = 11 * MS, SM_LAA = SM_RD + C;
-    static constexpr size_t SMEM = al(OFF_SM + (size_t)(11 * MS + 3 * C) * 4);
+    static constexpr int SM_GUU = 0, SM_GUK = 2 * MS, SM_LM = 4 * MS, SM_LMT = 5 * MS, SM_LKT = 6 * MS,
+                         SM_LQ = 8 * MS, SM_RD = 10 * MS, SM_LAA = SM_RD + C;
+    static constexpr size_t SMEM = al(OFF_SM + (size_t)(10 * MS + 2 * C) * 4);
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(RAW_T % 16 == 0 && (D * sizeof(TIn)) % 16 == 0, "bulk-copy granularity");
 };
@@ -105,8 +111,8 @@ struct Bars {
     uint64_t* full_r;    // [NRAW] raw chunk landed
     uint64_t* full_p;    // [NP] prepared chunk published
     uint64_t* empty_p;   // [NP] released by both teams (count 2)
-    uint64_t* full_al;   // [2] A team published a rows / a^T operands of a chunk
-    uint64_t* empty_al;  // [2] S team done with them
+    uint64_t* full_al;   // [2] A team published w, z / delta and X of a chunk
+    uint64_t* empty_al;  // [2] S team has formed the chunk's gate from them
     uint64_t* mma_a;     // A-team tcgen05 commits (state update)
     uint64_t* mma_s;     // S-team tcgen05 commits (state update)
     uint64_t* mma_xa;    // [A u | A k] issued by two A warps (count 2)
@@ -550,9 +556,9 @@ __device__ __forceinline__ void bar_arrive(int id, int nthreads) {
 }
 
 // ---------------------------------------------------------------------------
-// A team (warps 0-3): Sherman-Morrison steps of eq. 9 and the gate of eq. 10,
-// one chunk at a time. Thread i < D of the row warps owns row i of A (TMEM
-// lane i) and of every d x C intermediate.
+// A team (warps 0-3): Sherman-Morrison steps of eq. 9 and what the gate of
+// eq. 10 is formed from, one chunk at a time. Thread i < D of the row warps
+// owns row i of A (TMEM lane i) and of every d x C intermediate.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn, bool TAPE>
 __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int warp, int lane) {
@@ -605,6 +611,8 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     for (; c < nch; ++c) {
         const int s = c % L::NP, n = min(C, T - c * C), b = c & 1;
         bad = !mbar_wait(x.b.full_p + s, (c / L::NP) & 1, x.abort, p.wait_ns);
+        // the S team has formed the gate of chunk c - 2 from the hand-over buffers
+        if (c >= 2 && !bad) bad = !mbar_wait(x.b.empty_al + b, ((c >> 1) & 1) ^ 1, x.abort, p.wait_ns);
         if (bar_red_or(ID_A, 128, bad || *x.abort != 0)) {
             bad = true;
             break;
@@ -636,6 +644,8 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         bool ok = mbar_wait(x.b.mma_xa, c & 1, nullptr, p.wait_ns);
         if (ta == 0) VLA_TRACE_AT(p, 5, c);
         tc_fence_after();
+        float* wp = x.f(L::OFF_WP) + (size_t)b * C * D;
+        float* yp = x.f(L::OFF_YP) + (size_t)b * C * D;
         if (rw) {
             float v0[16], v1[16], v2[16], v3[16];
             tc_ld16(tl + L::T_XA, v0);
@@ -649,6 +659,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 v1[t] = (v1[t] + v3[t]) * sc[L::SC_IK + t];  // w_t = A_c k^_t
                 xr[t * XS + i] = v0[t];
                 xr[(C + t) * XS + i] = v1[t];
+                wp[t * D + i] = v1[t];
             }
             if (!fixed) {
                 put_row16(zh, i, v0, false);
@@ -710,24 +721,17 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                     sm[L::SM_LMT + j * L::GSTR + r] = l;
                 }
             } else {
+                float* xp = x.f(L::OFF_XP) + (size_t)b * C * L::GSTR;  // X for the S team's gate
 #pragma unroll
-                for (int r = 0; r < C; ++r) sm[L::SM_XGT + j * L::GSTR + r] = col[r];
+                for (int r = 0; r < C; ++r) xp[r * L::GSTR + j] = col[r];
             }
             if (lane == 0) VLA_TRACE_AT(p, 1, c);
-        } else if (c >= 2) {
-            // the S team is done with the a buffers of chunk c - 2
-            ok = ok && mbar_wait(x.b.empty_al + b, ((c >> 1) & 1) ^ 1, x.abort, p.wait_ns);
         }
         if (bar_red_or(ID_A, 128, !ok || *x.abort != 0)) {
             bad = true;
             break;
         }
         if (ta == 0) VLA_TRACE_AT(p, 7, c);
-        float* alr = x.f(L::OFF_AL) + (size_t)b * C * XS;
-        float* gh = x.f(L::OFF_GH) + (size_t)b * D * C;
-        float* gl = x.f(L::OFF_GL) + (size_t)b * D * C;
-        // the -M operand first: the state update is issued before the gate,
-        // which only the S team needs, is computed
         float y[C], lr[C];
         if (rw && !fixed) {
             // y = z_i = z'_i L^-T (forward substitution, in place), then y D^-1
@@ -746,7 +750,10 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             }
             ld_row16(sm + L::SM_RD, lr);
 #pragma unroll
-            for (int t = 0; t < C; ++t) y[t] *= lr[t];
+            for (int t = 0; t < C; ++t) {
+                y[t] *= lr[t];
+                yp[t * D + i] = y[t];  // z_t / delta_t for the S team's gate
+            }
             // m_i = (z_i D^-1) L^-1 (backward substitution); the operand is -m_i
             float mv[C];
 #pragma unroll
@@ -764,65 +771,31 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         }
         fence_proxy_async_smem();
         // A_{c+1} = A_c - M Z'^T, issued by warp 3 (not a row warp for d <= 96) once
-        // the rows have -M in place; the rows go on to the gate without waiting
+        // the rows have -M and z / delta in place; then the chunk's hand-over
+        // buffers go to the S team, which forms the gate (eq. 10) off this chain
         if (warp < 3)
             bar_arrive(ID_M, 128);
         else
             named_bar(ID_M, 128);
-        if (warp == 3 && lane == 0 && !fixed) {
-            VLA_TRACE_AT(p, 8, c);
-            tc_fence_after();
-            const uint32_t id = tc_idesc_tf32(128, D);
-#pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks) {
-                const uint64_t ah = tc_sdesc(smem_u32(ph) + ks * 256, 128, L::SBO_C);
-                const uint64_t alo = tc_sdesc(smem_u32(pl) + ks * 256, 128, L::SBO_C);
-                const uint64_t bhd = tc_sdesc(smem_u32(zh) + ks * 256, 128, L::SBO_C);
-                const uint64_t bld = tc_sdesc(smem_u32(zl) + ks * 256, 128, L::SBO_C);
-                tc_mma_ss(tm + L::T_A, ah, bhd, id, 1);
-                tc_mma_ss(tm + L::T_A, ah, bld, id, 1);
-                tc_mma_ss(tm + L::T_A, alo, bhd, id, 1);
-            }
-            tc_commit(x.b.mma_a);
-        }
-        if (rw) {
-            // a_t = A_t k^_t = w_t - sum_{s<=t} z_s (z_s . k^_t) / delta_s (eq. 10)
-            float av[C];
-#pragma unroll
-            for (int t = 0; t < C; ++t) {
-                float a = xr[(C + t) * XS + i];
-                if (!fixed) {
-                    ld_row16(sm + L::SM_XGT + t * L::GSTR, lr);  // X[q][t]
-#pragma unroll
-                    for (int q = 0; q <= t; ++q) a = fmaf(-y[q], lr[q], a);
-                }
-                av[t] = t < n ? a : 0.f;
-                alr[t * XS + i] = av[t];
-            }
-            put_row16(gh, i, av, false);
-            put_row16(gl, i, av, true);
-        }
-        fence_proxy_async_smem();
-        named_bar(ID_A, 128);
         if (warp == 3) {
-            // ||a_t||^2 for the S team, then publish the chunk's a buffers
-            if (lane < C) {
-                float2 acc = f2(0.f, 0.f);
-#pragma unroll 8
-                for (int k4 = 0; k4 < D / 4; ++k4) {
-                    const float4 a = ld4(alr + lane * XS + 4 * k4);
-                    acc = __ffma2_rn(f2(a.x, a.y), f2(a.x, a.y), acc);
-                    acc = __ffma2_rn(f2(a.z, a.w), f2(a.z, a.w), acc);
+            if (lane == 0 && !fixed) {
+                VLA_TRACE_AT(p, 8, c);
+                tc_fence_after();
+                const uint32_t id = tc_idesc_tf32(128, D);
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const uint64_t ah = tc_sdesc(smem_u32(ph) + ks * 256, 128, L::SBO_C);
+                    const uint64_t alo = tc_sdesc(smem_u32(pl) + ks * 256, 128, L::SBO_C);
+                    const uint64_t bhd = tc_sdesc(smem_u32(zh) + ks * 256, 128, L::SBO_C);
+                    const uint64_t bld = tc_sdesc(smem_u32(zl) + ks * 256, 128, L::SBO_C);
+                    tc_mma_ss(tm + L::T_A, ah, bhd, id, 1);
+                    tc_mma_ss(tm + L::T_A, ah, bld, id, 1);
+                    tc_mma_ss(tm + L::T_A, alo, bhd, id, 1);
                 }
-                sm[L::SM_LAA + b * C + lane] = acc.x + acc.y;
-                if (TAPE && lane < n) {
-                    float* rec = tape_rec<D>(p, bh, c * C + lane) + 3 * D;
-                    rec[0] = mypiv;                      // delta_t = 1 + u^_t . z_t
-                    rec[1] = sqrtf(acc.x + acc.y);       // ||a_t||
-                }
+                tc_commit(x.b.mma_a);
             }
-            __syncwarp();
             if (lane == 0) mbar_arrive(x.b.full_al + b);
+            if (TAPE && lane < n) tape_rec<D>(p, bh, c * C + lane)[3 * D] = mypiv;  // delta_t = 1 + u^_t . z_t
         }
         if (!fixed) {
             bad = !mbar_wait(x.b.mma_a, pa, nullptr, p.wait_ns);
@@ -858,8 +831,8 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
 }
 
 // ---------------------------------------------------------------------------
-// S team (warps 4-7): residual writes and readout of eq. 10-11 for the chunk
-// the A team published. Thread i < D of the row warps owns row i of S.
+// S team (warps 4-7): the gate, residual writes and readout of eq. 10-11 for
+// the chunk the A team published. Thread i < D of the row warps owns row i of S.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn, bool TAPE>
 __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int warp, int lane) {
@@ -874,6 +847,10 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     float* sm = x.sm();
     float* eh = x.f(L::OFF_EH);
     float* el = x.f(L::OFF_EL);
+    float* alr = x.f(L::OFF_AL);
+    float* gh = x.f(L::OFF_GH);
+    float* gl = x.f(L::OFF_GL);
+    const bool fixed = p.fixed_a != 0;
     const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * T * D;
     float* go = p.o + (size_t)bh * p.o_stride;
     bool bad = false, nonfinite = false;
@@ -922,7 +899,6 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             tc_fence_after();
             tmem_row_out<D>(tl, L::T_S, ckpt_slot<D>(p, bh, c >> 2) + (size_t)i * D);
         }
-        const float* alr = x.f(L::OFF_AL) + (size_t)b * C * XS;
         // [S_c k | S_c phi] (rows k, phi of the chunk)
         if (lane == 0 && wq < 2) {
             tc_fence_after();
@@ -943,6 +919,68 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             }
             tc_commit(x.b.mma_xs);
         }
+        // while warps 4 and 5 issue the products (about 100 clocks per MMA),
+        // warps 6 and 7 form the gate a_t = A_t k^_t = w_t - sum_{q<=t}
+        // (z_q / delta_q) X[q][t] (eq. 10; a_t = A_0 k^_t with A fixed), zero
+        // past the end of the sequence, from the A team's hand-over buffers:
+        // thread g of the two warps takes rows g and g + 64
+        if (wq >= 2) {
+            const float* wp = x.f(L::OFF_WP) + (size_t)b * C * D;
+            const float* yp = x.f(L::OFF_YP) + (size_t)b * C * D;
+            const float* xp = x.f(L::OFF_XP) + (size_t)b * C * L::GSTR;
+#pragma unroll 1
+            for (int r = ts - 64; r < D; r += 64) {
+                float lr[C], av[C];
+#pragma unroll
+                for (int t = 0; t < C; ++t) av[t] = wp[t * D + r];
+                if (!fixed) {
+                    // q outermost: the 16 sums advance side by side, each in
+                    // ascending q
+#pragma unroll
+                    for (int q = 0; q < C; ++q) {
+                        const float yq = yp[q * D + r];
+                        ld_row16(xp + q * L::GSTR, lr);  // X[q][t]
+#pragma unroll
+                        for (int t = q; t < C; ++t) av[t] = fmaf(-yq, lr[t], av[t]);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    av[t] = t < n ? av[t] : 0.f;
+                    alr[t * XS + r] = av[t];
+                }
+                put_row16(gh, r, av, false);
+                put_row16(gl, r, av, true);
+            }
+        }
+        if (wq >= 2) {
+            named_bar(ID_G, 64);
+            if (wq == 3 && lane < C) {
+                // ||a_t||^2
+                float2 acc = f2(0.f, 0.f);
+#pragma unroll 8
+                for (int k4 = 0; k4 < D / 4; ++k4) {
+                    const float4 a = ld4(alr + lane * XS + 4 * k4);
+                    acc = __ffma2_rn(f2(a.x, a.y), f2(a.x, a.y), acc);
+                    acc = __ffma2_rn(f2(a.z, a.w), f2(a.z, a.w), acc);
+                }
+                sm[L::SM_LAA + lane] = acc.x + acc.y;
+                if (TAPE && lane < n) tape_rec<D>(p, bh, c * C + lane)[3 * D + 1] = sqrtf(acc.x + acc.y);  // ||a_t||
+            }
+        }
+        named_bar(ID_S, 128);
+        if (ts == 0) mbar_arrive(x.b.empty_al + b);  // the hand-over buffers are free
+        // Lk[t][s] = k^_t . a_s, Lq[t][s] = phi_t . a_s; warp = (matrix, half of D)
+        {
+            const int mat = wq & 1, half = wq >> 1;
+            float acc[2][4];
+            gram16<D, true>(hi + (mat ? 32 : 16) * D, 0, alr, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc,
+                            !L::F32IN && mat == 0);
+            if (mat)
+                gram_pair_sum(sm + L::SM_LQ, L::MS, L::GSTR, acc, lane, half, 6 + mat, nullptr, false);
+            else
+                gram_pair_sum(sm + L::SM_LKT, L::MS, L::GSTR, acc, lane, half, 6 + mat, sc + L::SC_IK, true);
+        }
         bool ok = mbar_wait(x.b.mma_xs, c & 1, nullptr, p.wait_ns);
         if (ts == 0) VLA_TRACE_AT(p, 12, c);
         tc_fence_after();
@@ -960,24 +998,13 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 sq[t] = v1[t] + v3[t];                        // S_c phi_t
             }
         }
-        // Lk[t][s] = k^_t . a_s, Lq[t][s] = phi_t . a_s; warp = (matrix, half of D)
-        {
-            const int mat = wq & 1, half = wq >> 1;
-            float acc[2][4];
-            gram16<D, true>(hi + (mat ? 32 : 16) * D, 0, alr, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc,
-                            !L::F32IN && mat == 0);
-            if (mat)
-                gram_pair_sum(sm + L::SM_LQ, L::MS, L::GSTR, acc, lane, half, 6 + mat, nullptr, false);
-            else
-                gram_pair_sum(sm + L::SM_LKT, L::MS, L::GSTR, acc, lane, half, 6 + mat, sc + L::SC_IK, true);
-        }
         named_bar(ID_S, 128);
         if (ts == 0) VLA_TRACE_AT(p, 13, c);
         if (rw) {
             float lr[C], nr[C];
             // e_t = v_t - S_c k^_t - sum_{s<t} (k^_t . alpha^_s) e_s, kept (in place)
             // as e'_t = e_t / ||a_t||
-            ld_row16(sm + L::SM_LAA + b * C, nr);
+            ld_row16(sm + L::SM_LAA, nr);
 #pragma unroll
             for (int t = 0; t < C; ++t) {
                 vv[t] = raw_f32(vr[t]) - sk[t];
@@ -1027,8 +1054,6 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             mbar_arrive(x.b.empty_p + s);  // done with the chunk's k, phi rows and den
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, D);
-            const float* gh = x.f(L::OFF_GH) + (size_t)b * D * C;
-            const float* gl = x.f(L::OFF_GL) + (size_t)b * D * C;
 #pragma unroll
             for (int ks = 0; ks < C / 8; ++ks) {
                 const uint64_t ah = tc_sdesc(smem_u32(eh) + ks * 256, 128, L::SBO_C);
@@ -1046,7 +1071,6 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         ps ^= 1;
         if (ts == 0) VLA_TRACE_AT(p, 15, c);
         tc_fence_after();
-        if (ts == 0) mbar_arrive(x.b.empty_al + b);
         if (rw) refresh_lo<D>(tl, L::T_S, L::T_SL);
         tc_fence_before();
         if (bar_red_or(ID_S, 128, !ok)) {
