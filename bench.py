@@ -64,12 +64,12 @@ KERNEL_FILES = {
 # was taken on (B, H, T, d, input dtype) and while that kernel's own sources
 # hash to source_sha; otherwise reported as null.
 NCU_TRAFFIC = {
-    "vla_tc_kernel": {"source_sha": "d60249ad5432539a", "workload": (8, 16, 4096, 96, "bf16"),
-                      "bytes_per_launch": 402924800 + 176285184},
+    "vla_tc_kernel": {"source_sha": "14ab9db29a5b1786", "workload": (8, 16, 4096, 96, "bf16"),
+                      "bytes_per_launch": 402762240 + 176187136},
     # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
-    "vla_tc2_kernel": {"source_sha": "7e8b3a0e584c88cf", "workload": (1, 32, 65536, 128, "bf16"),
-                       "bytes_per_launch": 8 * (269107712 + 108425728 - 4227072) + 4227072},
+    "vla_tc2_kernel": {"source_sha": "0f583c6ba916b9fc", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (268582912 + 108756224 - 4227072) + 4227072},
     # the reverse sweep (the step's dominant kernel, after the taped chunked forward), from a capture of
     # the same workload at B=2 (32 heads; a full step holds about 2.8 GB on the device) scaled by 4:
     # every byte it moves is per head-token or per head

@@ -43,6 +43,16 @@ constexpr int ID_A = 1, ID_S = 2, ID_ST = 3;  // named barriers of the A team, S
 constexpr int ID_M = 9;  // A-team rows (arrive) -> warp 3 (sync): -M of a chunk is in place
 constexpr int ID_G = 8;  // S-team warps 6 and 7: the chunk's gate rows are in place
 
+// true on one lane of a converged warp (elect.sync). Issuing tcgen05 work
+// from a warp-uniform branch through it, with operands the compiler can prove
+// warp-uniform (warp index and TMEM base broadcast from lane 0), keeps them
+// out of a per-lane path.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
 template <int D, typename TIn>
 struct Lay {
     static constexpr bool F32IN = sizeof(TIn) == 4;
@@ -567,7 +577,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     const int ta = threadIdx.x;
     const bool rw = warp < L::NRW;
     const int i = ta;
-    const uint32_t tm = *x.tmem_base;
+    const uint32_t tm = __shfl_sync(0xffffffffu, *x.tmem_base, 0);
     const uint32_t tl = tm + ((uint32_t)(32 * warp) << 16);
     const int T = p.T, nch = (T + C - 1) / C;
     float* sm = x.sm();
@@ -626,7 +636,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         const float* sc = x.sc(s);
         // [Z' | W] = A_c [u | k]^T (rows u, k of the chunk; scaled by 1/||.|| below);
         // warps 0 and 1 issue the even and odd K steps into separate accumulators
-        if (lane == 0 && warp < 2) {
+        if (warp < 2 && elect_one()) {
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, 2 * C);
             const uint32_t bh0 = smem_u32(hi), bl0 = smem_u32(x.lo(s));
@@ -778,7 +788,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         else
             named_bar(ID_M, 128);
         if (warp == 3) {
-            if (lane == 0 && !fixed) {
+            if (!fixed && elect_one()) {
                 VLA_TRACE_AT(p, 8, c);
                 tc_fence_after();
                 const uint32_t id = tc_idesc_tf32(128, D);
@@ -841,7 +851,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     const int ts = threadIdx.x - 128, wq = warp - 4;
     const bool rw = wq < L::NRW;
     const int i = ts;
-    const uint32_t tm = *x.tmem_base;
+    const uint32_t tm = __shfl_sync(0xffffffffu, *x.tmem_base, 0);
     const uint32_t tl = tm + ((uint32_t)(32 * wq) << 16);
     const int T = p.T, nch = (T + C - 1) / C;
     float* sm = x.sm();
@@ -900,7 +910,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             tmem_row_out<D>(tl, L::T_S, ckpt_slot<D>(p, bh, c >> 2) + (size_t)i * D);
         }
         // [S_c k | S_c phi] (rows k, phi of the chunk)
-        if (lane == 0 && wq < 2) {
+        if (wq < 2 && elect_one()) {
             tc_fence_after();
             const uint32_t id32 = tc_idesc_tf32(128, 2 * C), id16 = tc_idesc_tf32(128, C);
             const uint32_t bh0 = smem_u32(hi) + 2 * L::SBO_D;
@@ -1050,7 +1060,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         fence_proxy_async_smem();
         named_bar(ID_S, 128);
         // S_{c+1} = S_c + E' A (rows a_t, columns scaled into E')
-        if (ts == 0) {
+        if (wq == 0 && elect_one()) {
             mbar_arrive(x.b.empty_p + s);  // done with the chunk's k, phi rows and den
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, D);
@@ -1118,7 +1128,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1) vla_tc_kernel(const Params p) 
     x.b.mma_xs = x.b.mma_xa + 1;
     x.abort = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
     x.tmem_base = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC + 8);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
     if (threadIdx.x == 0) {
         for (int r = 0; r < L::NRAW; ++r) mbar_init(x.b.full_r + r, 1);

@@ -422,7 +422,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
     const int ta = threadIdx.x;
     const bool rw = warp < L::NRW;
     const int i = ta;
-    const uint32_t tm = *x.tmem_base;
+    const uint32_t tm = __shfl_sync(0xffffffffu, *x.tmem_base, 0);
     const uint32_t tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);
     const int T = p.T, nch = (T + C - 1) / C;
     float* sm = x.sm();
@@ -476,7 +476,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         const float* sc = x.sc(s);
         // [Z' | W] = A_c [u | k]^T (rows u, k of the chunk; scaled by 1/||.|| below);
         // warp q < NISS issues the K steps ks = q mod NISS into accumulator q
-        if (lane == 0 && warp < NISS) {
+        if (warp < NISS && tc::elect_one()) {
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, 2 * C);
             const uint32_t bh0 = smem_u32(hi), bl0 = smem_u32(x.lo(s));
@@ -607,7 +607,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         fence_proxy_async_smem();
         named_bar(ID_T, NT_A);
         // A_{c+1} = A_c - M Z'^T
-        if (ta == 0 && !fixed) {
+        if (warp == 0 && !fixed && tc::elect_one()) {
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, D);
 #pragma unroll
@@ -713,7 +713,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
     const int ts = threadIdx.x;
     const bool rw = warp < L::NRW;
     const int i = ts;
-    const uint32_t tm = *x.tmem_base;
+    const uint32_t tm = __shfl_sync(0xffffffffu, *x.tmem_base, 0);
     const uint32_t tl = tm + ((uint32_t)(32 * warp) << 16);
     const int T = p.T, nch = (T + C - 1) / C;
     float* sm = x.sm();
@@ -768,7 +768,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         const float* alr = x.f(L::OFF_AL) + (size_t)b * C * XS;
         // [S_c k | S_c phi] (rows k, phi of the chunk); warp q < NISS issues the
         // K steps ks = q mod NISS into accumulator q
-        if (lane == 0 && warp < NISS) {
+        if (warp < NISS && tc::elect_one()) {
             tc_fence_after();
             const uint32_t id32 = tc_idesc_tf32(128, 2 * C), id16 = tc_idesc_tf32(128, C);
             const uint32_t bh0 = smem_u32(hi), bl0 = smem_u32(x.lo(s));
@@ -845,7 +845,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         fence_proxy_async_smem();
         named_bar(ID_T, NT_S);
         // S_{c+1} = S_c + E' A (rows a_t from the mailbox, columns scaled into E')
-        if (ts == 0) {
+        if (warp == 0 && tc::elect_one()) {
             mbar_arrive(x.b.empty_p + s);  // done with the chunk's k, phi rows and den
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, D);
@@ -916,7 +916,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc2::THREADS, 1) vla
     x.tmem_base = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC + 4);
     x.n_sent = reinterpret_cast<int*>(smem + L::OFF_MISC + 8);
     x.n_recv = reinterpret_cast<int*>(smem + L::OFF_MISC + 12);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
     const uint32_t rank = tc2::cluster_rank();
     const int bh = blockIdx.x >> 1;
     if (threadIdx.x == 0) {
