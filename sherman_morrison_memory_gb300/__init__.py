@@ -40,6 +40,7 @@ from ._binding import (  # noqa: F401
 
 __all__ = [
     "vla_forward",
+    "vla_backward",
     "vla_get_last_device_status",
     "vla_linear_attention_state",
     "vla_status_string",
