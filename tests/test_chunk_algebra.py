@@ -132,6 +132,23 @@ def test_chunked_form_matches_per_token_loop(orc, chunk, state):
             assert _rel(x, ref) < 1e-10, (name, h, _rel(x, ref))
 
 
+@pytest.mark.parametrize("case", ["u_zero", "one_partial_chunk"])
+def test_degenerate_cases(orc, case):
+    """u = 0 (the unit guard gives u^ = 0: delta_t = 1, A never moves, the
+    fixed-A variant) and a sequence shorter than one chunk."""
+    BH, T, d = 2, (40 if case == "u_zero" else 5), 24
+    (q, k, v, u), _ = _inputs(31, BH, T, d)
+    if case == "u_zero":
+        u = np.zeros_like(u)
+    o_r, S_r, A_r, zk_r = orc.forward_f64(q, k, v, u, 0.1, 1e-4)
+    for h in range(BH):
+        o, S, A, zk = chunked_forward(q[h], k[h], v[h], u[h], 0.1, 1e-4, 16)
+        for name, x, ref in (("o", o, o_r[h]), ("S", S, S_r[h]), ("A", A, A_r[h]), ("zk", zk, zk_r[h])):
+            assert _rel(x, ref) < 1e-10, (case, name, h, _rel(x, ref))
+    if case == "u_zero":
+        assert np.array_equal(A_r[0], np.eye(d) / 0.1)
+
+
 def test_ldl_pivots_are_the_sherman_morrison_denominators(orc):
     """The pivots of I + U^ A_c U^T are the delta_t = 1 + u^_t . A_{t-1} u^_t
     of eq. 9 that the per-token loop forms one at a time."""
