@@ -101,6 +101,48 @@ def ncu_traffic(kernel: str, workload=None):
     return t["bytes_per_launch"]
 
 
+def kernel_for(algo: int, T: int, d: int) -> str:
+    """The kernel one vla_forward call launches (the choice VLA_ALGO_AUTO makes)."""
+    if algo == 3 or (algo == 0 and T <= 4):
+        return "vla_decode_kernel"
+    if algo == 4 or (algo == 0 and d == 128):
+        return "vla_tc2_kernel"
+    if algo == 2 or (algo == 0 and d <= 96):
+        return "vla_tc_kernel"
+    return "vla_fused_kernel"
+
+
+def measure_ffma_peak(dev, n_sm: int, iters: int = 100000, reps: int = 3) -> dict:
+    """FP32 FMA throughput of this GPU, measured now: the library's probe
+    (include/vla_probe.h: 8 independent FMA chains per thread, 4 CTAs x 256
+    threads per SM), scalar and packed, best of `reps` timed launches each,
+    CUDA events on the launching stream. The roofline's denominator."""
+    import torch
+
+    from sherman_morrison_memory_gb300 import _binding
+
+    blocks, threads = 4 * n_sm, 256
+    sink = torch.empty(blocks * threads, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {"blocks": blocks, "threads": threads, "iters": iters}
+    for packed in (False, True):
+        flop = _binding.vla_probe_ffma(blocks, threads, iters, packed, sink)  # warm-up
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            _binding.vla_probe_ffma(blocks, threads, iters, packed, sink)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        out["packed_tflops" if packed else "scalar_tflops"] = flop / (best / 1e3) / 1e12
+        out["packed_ms" if packed else "scalar_ms"] = best
+    out["tflops"] = max(out["scalar_tflops"], out["packed_tflops"])
+    return out
+
+
 def load_peaks() -> dict:
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -377,19 +419,15 @@ def run_ours(args, w):
     units = w.head_tokens
     value = aggregate_value(units, world, ms_max / 1e3)
 
-    # roofline of the one kernel that a step launches
-    if args.algo == 3 or (args.algo == 0 and T <= 4):
-        kernel = "vla_decode_kernel"
-    elif args.algo == 4 or (args.algo == 0 and d == 128):
-        kernel = "vla_tc2_kernel"
-    elif args.algo == 2 or (args.algo == 0 and d <= 96):
-        kernel = "vla_tc_kernel"
-    else:
-        kernel = "vla_fused_kernel"
+    # roofline of the one kernel that a step launches, against the FP32 FMA
+    # peak measured by the probe in this run (the nominal figure beside it)
+    kernel = kernel_for(args.algo, T, d)
     peaks = load_peaks()
     sm_max = float(peaks.get("sm_max_mhz", FALLBACK_SM_MAX_MHZ))
     n_sm = props.multi_processor_count
-    peak_tflops = n_sm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    nominal_tflops = n_sm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    probe = measure_ffma_peak(dev, n_sm)
+    peak_tflops = probe["tflops"]
     flop_d2 = FLOP_D2["fixed_a" if fa else "forward"]
     flops = flop_d2 * d * d * units
     achieved = flops / (ms / 1e3) / 1e12
@@ -430,6 +468,11 @@ def run_ours(args, w):
     la_fro = torch.linalg.matrix_norm(S_la).mean().item()
     torch.cuda.synchronize(dev)
 
+    # the other workloads, each timed in this run (the headline stays the one above)
+    configs = None
+    if world == 1 and not args.no_configs and not fa and args.algo == 0 and args.batch == 0 and args.tokens == 0:
+        configs = time_workloads([i for i in sorted(W.WORKLOADS) if i != args.workload], dev, peak_tflops)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         carr = arrs if not fa else (arrs[0], arrs[1], arrs[2], arrs[3] * 0)
@@ -450,9 +493,19 @@ def run_ours(args, w):
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB per step), no flush"},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                          "frac": achieved / peak_tflops, "traffic": traffic,
-                         "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FP32 FMA lanes x 2 x {sm_max:.0f} MHz",
+                         "peak_basis": "measured in this run: FFMA probe (include/vla_probe.h), best of scalar "
+                                       f"{probe['scalar_tflops']:.1f} and packed {probe['packed_tflops']:.1f} TFLOP/s "
+                                       f"on {probe['blocks']} CTAs x {probe['threads']} threads",
+                         "peak_nominal": nominal_tflops,
+                         "peak_nominal_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FP32 FMA lanes x 2 x {sm_max:.0f} MHz",
+                         "frac_of_nominal": achieved / nominal_tflops,
+                         "achieved_basis": "nominal FLOP (12 d^2 per head-token, the FP32 FMA work of the "
+                                           "recurrence) / kernel time; the kernel runs its d x d products on the "
+                                           "tensor cores in 3-term tf32",
                          "flop_per_head_token": flop_d2 * d * d, "kernel": kernel},
             "fp32_roofline_pct": 100.0 * achieved / peak_tflops,
+            "ffma_probe": probe,
+            "configs": configs,
             "hbm": {"achieved_gbs": hbm_gbs, "peak_gbs": hbm_peak, "frac": hbm_gbs / hbm_peak,
                     "algorithmic_bytes_per_launch": in_bytes + out_bytes},
             "cpu_baseline": cpu,
@@ -465,6 +518,61 @@ def run_ours(args, w):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def time_workloads(ids, dev, peak_tflops: float, steps: int = 20, warmup: int = 3) -> dict:
+    """Each workload in `ids` timed in this run with the default kernel
+    choice: `warmup` untimed calls, then `steps` calls between CUDA events on
+    the launching stream. Inputs of workloads up to 1 GB are the seeded numpy
+    draws of workloads.make (the ones the parity tests use); larger ones are
+    drawn on the device (torch generator, seed 0, the same N(0,1) bf16
+    distribution) to keep the run short. The kernels' timing does not depend
+    on the values."""
+    import torch
+
+    from sherman_morrison_memory_gb300 import VLA_OK, vla_forward, vla_get_last_device_status
+    from sherman_morrison_memory_gb300 import workloads as W
+
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for wid in ids:
+        w = W.WORKLOADS[wid]
+        B, H, T, d = w.B, w.H, w.T, w.d
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        in_bytes = 4 * w.head_tokens * d * (2 if w.dtype == "bf16" else 4)
+        if in_bytes <= (1 << 30):
+            src = "workloads.make (numpy, seeded)"
+            q, k, v, u = (torch.from_numpy(a).to(dev).to(tdt) for a in W.make(w))
+        else:
+            src = "device draw (torch generator, seed 0)"
+            g = torch.Generator(device=dev)
+            g.manual_seed(0)
+            q, k, v, u = (torch.randn((B, H, T, d), generator=g, device=dev, dtype=torch.float32).to(tdt)
+                          for _ in range(4))
+        o = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
+        S = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+        res = (o, S, torch.empty_like(S), torch.empty((B, H, d), dtype=torch.float32, device=dev))
+        for _ in range(warmup):
+            vla_forward(q, k, v, u, w.lambda0, w.eps, out=res)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(steps):
+            vla_forward(q, k, v, u, w.lambda0, w.eps, out=res)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        st, detail = vla_get_last_device_status(dev)
+        if st != VLA_OK:
+            raise RuntimeError(f"workload {wid}: device status {st} {detail}")
+        ms = e0.elapsed_time(e1) / steps
+        tflops = FLOP_D2["forward"] * d * d * w.head_tokens / (ms / 1e3) / 1e12
+        out[str(wid)] = {"workload": w.describe(), "kernel": kernel_for(0, T, d), "ms_per_step": ms,
+                         "head_tokens_per_s": w.head_tokens / (ms / 1e3), "achieved_tflops": tflops,
+                         "fp32_roofline_frac": tflops / peak_tflops, "steps": steps, "warmup": warmup,
+                         "inputs": src}
+        del q, k, v, u, o, S, res
+        torch.cuda.empty_cache()
+    return out
 
 
 DECODE_WORKLOAD = dict(B=128, H=16, T=1, warm=16)
@@ -720,6 +828,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other workloads (the `configs` object of the forward line)")
     ap.add_argument("--algo", type=int, default=0,
                     help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96, its cluster-pair form "
                          "for d_h = 128), 1 per-token, 2 chunked, 3 decode, 4 chunked on a cluster pair")

@@ -94,10 +94,15 @@ typedef struct {
 enum { VLA_ALGO_AUTO = 0, VLA_ALGO_PER_TOKEN = 1, VLA_ALGO_CHUNKED = 2, VLA_ALGO_DECODE = 3,
        VLA_ALGO_CHUNKED_PAIR = 4 };
 
-/* Bytes of device workspace vla_forward() needs (one status record). The
- * workspace must be zero-filled before its first use (cudaMemset or
- * vla_workspace_reset); vla_get_last_device_status() clears it again. */
-size_t vla_workspace_bytes(void);
+/* Bytes of device workspace vla_forward() needs for a call over B x H heads
+ * of T tokens at head dimension d: 256 bytes, which hold the status record
+ * (16 bytes, the rest reserved). The kernels
+ * keep every intermediate of the recurrence on chip (registers, shared and
+ * tensor memory), so the size is the same for every valid shape; it is 0 for
+ * negative sizes or a d outside {32, 64, 96, 128}. The workspace must be
+ * zero-filled before its first use (cudaMemset or vla_workspace_reset);
+ * vla_get_last_device_status() clears it again. */
+size_t vla_workspace_bytes(int B, int H, int T, int d);
 
 /* Zero the status record in `workspace` (asynchronous on `stream`). */
 vla_status vla_workspace_reset(void* workspace, void* stream);
@@ -119,7 +124,7 @@ vla_status vla_workspace_reset(void* workspace, void* stream);
  *  o            [B, H, T, d] float32 output, 16-byte aligned (NULL only if T == 0).
  *  S_out, A_out [B, H, d, d] float32 final state, 16-byte aligned, required.
  *  zk_out       [B, H, d] float32 final z^key, or NULL to skip.
- *  workspace    >= vla_workspace_bytes() bytes of zero-filled device memory,
+ *  workspace    >= vla_workspace_bytes(B, H, T, d) bytes of zero-filled device memory,
  *               16-byte aligned; holds the device status record.
  *  stream       cudaStream_t as void*.
  *
@@ -166,16 +171,21 @@ vla_status vla_get_last_device_status(void* workspace, void* stream, int* detail
  * file-scope __device__ array of the library (256 bytes, held by every device
  * that loads the library until the process exits). The first call on a device
  * looks up that array's device address (cudaGetSymbolAddress) with the device
- * current; make that first call before any stream capture. Every call clears
- * the record before its launch, so a call starts from a zero status. All calls
- * share the one record: calls that overlap on the GPU (different streams, no
- * ordering) race on it and their statuses are unreliable. The call allocates
- * nothing (no cudaMalloc, cudaFree or allocating library routine). It returns
- * VLA_ERR_UNSUPPORTED if the status record the kernel needs does not fit in the
- * array. Arguments are as for vla_forward, without workspace; if
- * `device_status` is not NULL the call synchronises `stream` after the launch
- * and stores there the device-side status (VLA_OK, VLA_ERR_TIMEOUT or
- * VLA_ERR_NONFINITE); otherwise it returns as soon as the work is enqueued.
+ * current and keeps it for the life of the process; make that first call
+ * before any stream capture. cudaDeviceReset() (or anything else that tears
+ * down the device's primary context) makes the kept address stale: this entry
+ * point is not supported after such a reset. Every call clears the record
+ * before its launch, so a call starts from a zero status. All calls share the
+ * one record: calls that overlap on the GPU (different streams, no ordering)
+ * race on it and their statuses are unreliable. The call allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine). It returns
+ * VLA_ERR_UNSUPPORTED if the status record that vla_workspace_bytes(B, H, T, d)
+ * asks for does not fit in the array. Arguments are as for vla_forward,
+ * without workspace; if `device_status` is not NULL the call synchronises
+ * `stream` after the launch and stores there the device-side status (VLA_OK,
+ * VLA_ERR_TIMEOUT or VLA_ERR_NONFINITE); otherwise it returns as soon as the
+ * work is enqueued. When the call itself returns an error, nothing was
+ * launched and `device_status` (if not NULL) receives that same error.
  */
 vla_status vla_forward_noalloc(const void* q, const void* k, const void* v, const void* u,
                                vla_dtype dtype, int B, int H, int T, int d,
@@ -210,7 +220,7 @@ vla_status vla_forward_noalloc(const void* q, const void* k, const void* v, cons
  *               chunk by chunk.
  *  chunk_tokens tokens per launch, >= 0 (0 = automatic; values above T mean T).
  *  workspace    device memory of vla_forward_host_workspace_bytes() bytes,
- *               256-byte aligned, its first vla_workspace_bytes() bytes
+ *               256-byte aligned, its first vla_workspace_bytes(B, H, T, d) bytes
  *               zero-filled before the first use (the status record, read by
  *               vla_get_last_device_status(workspace, stream)). It holds the
  *               carried state and three input and three output slots of one chunk.

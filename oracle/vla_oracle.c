@@ -20,7 +20,7 @@
  * with A_0 = lambda0^{-1} I (lambda0 = 0.1 gives A_0 = 10 I, §3.2) and the
  * penalty directions u_t and the keys used unit-normalised (§3.2, §3.3).
  *
- * Readings of points the paper leaves open (each is listed in the design doc):
+ * Readings of points the paper leaves open (the design notes list each one):
  *  - u_t and k_t are op inputs and are normalised inside the op:
  *    x^ = x / max(||x||, 1e-12); the same guard is used for alpha^.
  *  - phi is applied to the raw (un-normalised) q_t and k_t.

@@ -72,7 +72,7 @@ def load_library():
         lib.vla_forward.restype = ci
         lib.vla_forward_ex.argtypes = fwd_args + [ctypes.POINTER(_Options)]
         lib.vla_forward_ex.restype = ci
-        lib.vla_workspace_bytes.argtypes = []
+        lib.vla_workspace_bytes.argtypes = [ci, ci, ci, ci]
         lib.vla_workspace_bytes.restype = ctypes.c_size_t
         lib.vla_workspace_reset.argtypes = [vp, vp]
         lib.vla_workspace_reset.restype = ci
@@ -91,6 +91,12 @@ def load_library():
         lib.vla_forward_host_workspace_bytes.restype = ctypes.c_size_t
         lib.vla_forward_host.argtypes = (fwd_args[:18] + [ci, vp, ctypes.c_size_t, vp, ctypes.POINTER(_Options)])
         lib.vla_forward_host.restype = ci
+        lib.vla_forward_noalloc.argtypes = fwd_args[:18] + [vp, ctypes.POINTER(ci)]
+        lib.vla_forward_noalloc.restype = ci
+        lib.vla_probe_ffma.argtypes = [ci, ci, ci, ci, vp, vp]
+        lib.vla_probe_ffma.restype = ci
+        lib.vla_probe_ffma_flop.argtypes = [ci, ci, ci, ci]
+        lib.vla_probe_ffma_flop.restype = ctypes.c_double
         del cp
         _LIB = lib
         return lib
@@ -103,8 +109,22 @@ def vla_status_string(status: int) -> str:
         return f"status {status}"
 
 
-def vla_workspace_bytes() -> int:
-    return int(load_library().vla_workspace_bytes())
+def vla_workspace_bytes(B: int = 1, H: int = 1, T: int = 1, d: int = 32) -> int:
+    """Device workspace bytes vla_forward needs for B x H heads of T tokens at head dimension d."""
+    return int(load_library().vla_workspace_bytes(int(B), int(H), int(T), int(d)))
+
+
+def vla_probe_ffma(blocks: int, threads: int, iters: int, packed: bool, sink: torch.Tensor, stream=None) -> float:
+    """Enqueue the FP32 FMA throughput probe (include/vla_probe.h) on the
+    current stream of sink's device; returns the FLOP the call performs."""
+    lib = load_library()
+    if sink.dtype != torch.float32 or not sink.is_cuda or sink.numel() < blocks * threads:
+        raise ValueError("sink must be a CUDA float32 tensor of at least blocks * threads elements")
+    st = lib.vla_probe_ffma(int(blocks), int(threads), int(iters), int(bool(packed)), _ptr(sink),
+                            ctypes.c_void_p(_stream_handle(sink.device, stream)))
+    if st != VLA_OK:
+        raise VLAError(st, "vla_probe_ffma")
+    return float(lib.vla_probe_ffma_flop(int(blocks), int(threads), int(iters), int(bool(packed))))
 
 
 def _stream_handle(device: torch.device, stream=None) -> int:
@@ -113,12 +133,18 @@ def _stream_handle(device: torch.device, stream=None) -> int:
     return int(stream.cuda_stream)
 
 
-def _workspace(device: torch.device) -> torch.Tensor:
+def _workspace(device: torch.device, nbytes: int = 0) -> torch.Tensor:
+    """The device's status workspace (shared by the calls on it, so that the
+    status is sticky until vla_get_last_device_status reads it), grown to at
+    least `nbytes` bytes (default: what a call at any supported shape needs)."""
     idx = device.index if device.index is not None else torch.cuda.current_device()
+    nbytes = max(int(nbytes), vla_workspace_bytes())
     ws = _WORKSPACES.get(idx)
-    if ws is None:
-        nbytes = vla_workspace_bytes()
-        ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=torch.device("cuda", idx))
+    if ws is None or ws.numel() * 4 < nbytes:
+        grown = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=torch.device("cuda", idx))
+        if ws is not None:
+            grown[:ws.numel()].copy_(ws)
+        ws = grown
         _WORKSPACES[idx] = ws
     return ws
 
@@ -191,7 +217,7 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
         zk = torch.empty((B, H, d), dtype=torch.float32, device=dev)
     else:
         o, S, A, zk = out
-    ws = _workspace(dev)
+    ws = _workspace(dev, vla_workspace_bytes(B, H, T, d))
     with torch.cuda.device(dev):
         sh = _stream_handle(dev, stream)
         args = (_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d,

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD_DIR, "libvla_gb300.so")
-SOURCES = [os.path.join(CSRC, "vla_forward.cu"), os.path.join(CSRC, "vla_host.cpp")]
+SOURCES = [os.path.join(CSRC, "vla_forward.cu"), os.path.join(CSRC, "vla_host.cpp"), os.path.join(CSRC, "vla_probe.cu")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

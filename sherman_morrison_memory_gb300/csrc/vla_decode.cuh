@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(DLay<D, TIn>::THREADS, 1) vla_decode_kernel(co
             fence_mbar_init();
         }
         __syncthreads();
-        if (tid == 0 && (int)blockIdx.x < BH) issue_head<D, TIn, FIXED>(p, sm, bar, blockIdx.x);
+        // test hook: copy nothing, so that the wait below runs out
+        if (tid == 0 && (int)blockIdx.x < BH && !p.stall_producer) issue_head<D, TIn, FIXED>(p, sm, bar, blockIdx.x);
     }
     int it = 0;
     for (int bh = blockIdx.x; bh < BH; bh += gridDim.x, ++it) {
@@ -154,6 +155,9 @@ __global__ void __launch_bounds__(DLay<D, TIn>::THREADS, 1) vla_decode_kernel(co
             if (__syncthreads_or(timed_out)) {
                 if (tid == 0) {
                     record_failure(p.status, BIT_TIMEOUT, ROLE_S, bh, 0);
+                    // the copies issue_head started for this head may still be in
+                    // flight: let them land (bounded wait) before the CTA can exit
+                    (void)mbar_wait(bar, it & 1, nullptr, p.wait_ns);
                     if (L::BULK_OUT) bulk_wait_all();  // earlier heads' stores leave shared memory first
                 }
                 return;

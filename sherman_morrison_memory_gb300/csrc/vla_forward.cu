@@ -159,7 +159,15 @@ struct Params {
     } while (0)
 // sub-step stamps of one thread (rows 5.. of the trace buffer)
 #define VLA_TRACE_PT(p, row, t) VLA_TRACE_AT(p, row, t)
+// stamp from the CTAs for which `cond` holds (e.g. both CTAs of head 0's cluster)
+#define VLA_TRACE_IF(p, cond, row, t)                                                   \
+    do {                                                                                \
+        if ((p).trace && (cond)) (p).trace[(size_t)(row) * (p).T + (t)] = clock64();   \
+    } while (0)
 #else
+#define VLA_TRACE_IF(p, cond, row, t) \
+    do {                              \
+    } while (0)
 #define VLA_TRACE_AT(p, role, t) \
     do {                         \
     } while (0)
@@ -1234,7 +1242,11 @@ void launch_la(int d, const TIn* k, const TIn* v, int T, float* S, int BH, cudaS
 
 extern "C" {
 
-size_t vla_workspace_bytes(void) { return kWorkspaceBytes; }
+size_t vla_workspace_bytes(int B, int H, int T, int d) {
+    if (B < 0 || H < 0 || T < 0) return 0;
+    if (d != 32 && d != 64 && d != 96 && d != 128) return 0;
+    return kWorkspaceBytes;
+}
 
 vla_status vla_workspace_reset(void* workspace, void* stream) {
     if (!workspace || !aligned16(workspace)) return VLA_ERR_INVALID_ARG;
@@ -1386,24 +1398,30 @@ vla_status vla_forward_noalloc(const void* q, const void* k, const void* v, cons
                                int H, int T, int d, float lambda0, float eps, const float* S0, const float* A0,
                                const float* zk0, float* o, float* S_out, float* A_out, float* zk_out,
                                void* stream, int* device_status) {
-    if (device_status) *device_status = VLA_OK;
+    // a call that returns an error has no device-side status of its own: report the error there too
+    auto fail = [device_status](vla_status e) {
+        if (device_status) *device_status = e;
+        return e;
+    };
     // arguments that need no device are rejected before the one-time set-up
-    if (B < 0 || H < 0 || T < 0) return VLA_ERR_INVALID_ARG;
-    if (dtype != VLA_F32 && dtype != VLA_BF16) return VLA_ERR_INVALID_ARG;
-    if (d != 32 && d != 64 && d != 96 && d != 128) return VLA_ERR_UNSUPPORTED;
-    if (vla_workspace_bytes() > kNoAllocScratchBytes) return VLA_ERR_UNSUPPORTED;
+    if (B < 0 || H < 0 || T < 0) return fail(VLA_ERR_INVALID_ARG);
+    if (dtype != VLA_F32 && dtype != VLA_BF16) return fail(VLA_ERR_INVALID_ARG);
+    if (d != 32 && d != 64 && d != 96 && d != 128) return fail(VLA_ERR_UNSUPPORTED);
+    // the sizes' status record must fit the static array
+    if (vla_workspace_bytes(B, H, T, d) > kNoAllocScratchBytes) return fail(VLA_ERR_UNSUPPORTED);
     void* scratch = nullptr;
     vla_status st = noalloc_scratch(&scratch);
-    if (st != VLA_OK) return st;
+    if (st != VLA_OK) return fail(st);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the record must start at zero: the previous call's contents stay in the array
-    if (cudaMemsetAsync(scratch, 0, sizeof(vla::DeviceStatus), s) != cudaSuccess) return VLA_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, sizeof(vla::DeviceStatus), s) != cudaSuccess) return fail(VLA_ERR_CUDA);
     st = vla_forward_ex(q, k, v, u, dtype, B, H, T, d, lambda0, eps, S0, A0, zk0, o, S_out, A_out, zk_out, scratch,
                         kNoAllocScratchBytes, stream, nullptr);
-    if (st != VLA_OK || !device_status) return st;
+    if (st != VLA_OK) return fail(st);
+    if (!device_status) return VLA_OK;
     vla::DeviceStatus h;
-    if (cudaMemcpyAsync(&h, scratch, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return VLA_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return VLA_ERR_CUDA;
+    if (cudaMemcpyAsync(&h, scratch, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return fail(VLA_ERR_CUDA);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return fail(VLA_ERR_CUDA);
     *device_status = h.bits == 0 ? VLA_OK : ((h.bits & vla::BIT_TIMEOUT) ? VLA_ERR_TIMEOUT : VLA_ERR_NONFINITE);
     return VLA_OK;
 }

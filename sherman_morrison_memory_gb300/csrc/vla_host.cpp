@@ -80,8 +80,8 @@ vla_status pipe_for(int dev, Pipe** out) {
 // output slots (o, [B*H, n, d] fp32), sized for tc tokens.
 struct Plan {
     int T = 0, tc = 0, ra = 0, nchunks = 0;
-    size_t es = 0, status = 0, S = 0, A = 0, zk = 0, in_arr = 0, in_slot[kSlots] = {}, out_slot[kSlots] = {},
-           total = 0;
+    size_t es = 0, status = 0, status_bytes = 0, S = 0, A = 0, zk = 0, in_arr = 0, in_slot[kSlots] = {},
+           out_slot[kSlots] = {}, total = 0;
     // first token and length of chunk j
     long long start(int j) const {
         if (ra == 0 || j == 0) return (long long)j * tc;
@@ -120,7 +120,11 @@ bool make_plan(vla_dtype dtype, long long BH, int T, int d, int chunk_tokens, Pl
     }
     pl->es = dtype == VLA_BF16 ? 2 : 4;
     const size_t bh = (size_t)BH, dd = (size_t)d;
-    size_t off = round_up(vla_workspace_bytes());
+    // the status record that every launch of the call shares (its size does not
+    // depend on the batch and head counts)
+    pl->status_bytes = vla_workspace_bytes(1, 1, T, d);
+    if (pl->status_bytes == 0) return false;
+    size_t off = round_up(pl->status_bytes);
     pl->status = 0;
     pl->S = off;
     off += round_up(bh * dd * dd * 4);
@@ -256,7 +260,7 @@ vla_status vla_forward_host(const void* q, const void* k, const void* v, const v
                                has ? in + 2 * pl.in_arr : nullptr, (has && hin[3]) ? in + 3 * pl.in_arr : nullptr,
                                dtype, B, H, n, d, lambda0, eps, (first && !S0) ? nullptr : dS,
                                (first && !A0) ? nullptr : dA, (first && !zk0) ? nullptr : dZ, has ? dO : nullptr, dS,
-                               dA, dZ, ws + pl.status, vla_workspace_bytes(), stream, opts,
+                               dA, dZ, ws + pl.status, pl.status_bytes, stream, opts,
                                od ? (size_t)T * dd : 0);
         if (st != VLA_OK) return fail(st);
         if (!ok(cudaEventRecord(P->kern[slot], cs))) return fail(VLA_ERR_CUDA);

@@ -37,6 +37,11 @@
 
 namespace tc2 {
 
+// -DVLA_TRACE builds: per-chunk clock stamps of head 0's cluster, stamp k of
+// chunk c at trace[row][k * nch + c] (row 4: rank 0, row 5: rank 1)
+#define TC2_STAMP(p, row, k, c, nch) \
+    VLA_TRACE_IF(p, blockIdx.x < 2 && threadIdx.x == 0, row, (k) * (nch) + (c))
+
 constexpr int C = tc::C;
 constexpr int NSTAGE = 4;
 constexpr int THREADS = 32 * 12;
@@ -472,6 +477,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             bad = true;
             break;
         }
+        TC2_STAMP(p, 4, 0, c, nch);
         const float* hi = x.hi(s);
         const float* sc = x.sc(s);
         // [Z' | W] = A_c [u | k]^T (rows u, k of the chunk; scaled by 1/||.|| below);
@@ -492,6 +498,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             tc_commit(x.b.mma_p);
         }
         bool ok = mbar_wait(x.b.mma_p, c & 1, nullptr, p.wait_ns);
+        TC2_STAMP(p, 4, 1, c, nch);
         tc_fence_after();
         if (rw) {
             float v0[16], v1[16];
@@ -509,6 +516,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             }
         }
         named_bar(ID_T, NT_A);
+        TC2_STAMP(p, 4, 2, c, nch);
         if (!fixed) {
             // Guu[s][t] = u^_s . z'_t, Guk[s][t] = u^_s . w_t; warps 0-3 = (matrix, half of D)
             if (warp < 4) {
@@ -521,6 +529,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             }
             named_bar(ID_T, NT_A);
         }
+        TC2_STAMP(p, 4, 3, c, nch);
         if (ta == 0) mbar_arrive(x.b.empty_p + s);  // done with the chunk's u, k rows
         if (warp == FACTOR_WARP && !fixed) {
             // LDL^T of I + Guu by Gaussian elimination of the augmented
@@ -570,6 +579,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             bad = true;
             break;
         }
+        TC2_STAMP(p, 4, 4, c, nch);
         float* alr = x.f(L::OFF_AL) + (size_t)b * C * XS;
         float* gh = x.f(L::OFF_GH) + (size_t)b * D * C;
         float* gl = x.f(L::OFF_GL) + (size_t)b * D * C;
@@ -606,6 +616,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         }
         fence_proxy_async_smem();
         named_bar(ID_T, NT_A);
+        TC2_STAMP(p, 4, 5, c, nch);
         // A_{c+1} = A_c - M Z'^T
         if (warp == 0 && !fixed && tc::elect_one()) {
             tc_fence_after();
@@ -641,6 +652,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         }
         fence_proxy_async_smem();
         named_bar(ID_T, NT_A);
+        TC2_STAMP(p, 4, 6, c, nch);
         if (warp == FACTOR_WARP) {
             // ||a_t||^2 for rank 1, then the chunk's gate into rank 1's mailbox
             if (lane < C) {
@@ -669,6 +681,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             bad = !mbar_wait(x.b.mma_x, pa, nullptr, p.wait_ns);
             pa ^= 1;
         }
+        TC2_STAMP(p, 4, 7, c, nch);
         tc_fence_after();
         if (rw && !fixed) tc::refresh_lo<D>(tl, L::T_X, L::T_XL);
         tc_fence_before();
@@ -677,6 +690,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             ++c;
             break;
         }
+        TC2_STAMP(p, 4, 8, c, nch);
     }
     if (warp == FACTOR_WARP && lane == 0) {
         *x.n_sent = sent;
@@ -756,12 +770,14 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         float vv[C];
         typename tc::RawIn<TIn>::type vr[C];
         if (rw) tc::load_v_raw<D, TIn>(gv + (size_t)c * C * D, i, n, vr);
+        TC2_STAMP(p, 5, 0, c, nch);
         bad = !mbar_wait(x.b.full_p + s, (c / L::NP) & 1, x.abort, p.wait_ns) ||
               !mbar_wait_cl(x.b.full_al + b, (c >> 1) & 1, x.abort, p.wait_ns);
         if (bar_red_or(ID_T, NT_S, bad || *x.abort != 0)) {
             bad = true;
             break;
         }
+        TC2_STAMP(p, 5, 1, c, nch);
         recv = c + 1;
         const float* hi = x.hi(s);
         const float* sc = x.sc(s);
@@ -787,6 +803,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             tc_commit(x.b.mma_p);
         }
         bool ok = mbar_wait(x.b.mma_p, c & 1, nullptr, p.wait_ns);
+        TC2_STAMP(p, 5, 2, c, nch);
         tc_fence_after();
         float sk[C], sq[C];
         if (rw) {
@@ -794,6 +811,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
 #pragma unroll
             for (int t = 0; t < C; ++t) sk[t] *= sc[L::SC_IK + t];  // S_c k^_t; sq = S_c phi_t
         }
+        TC2_STAMP(p, 5, 3, c, nch);
         // Lk[t][s] = k^_t . a_s, Lq[t][s] = phi_t . a_s; warp = (matrix, half of D)
         {
             const int mat = warp & 1, half = warp >> 1;
@@ -806,6 +824,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
                 tc::gram_pair_sum(sm + L::SM_LKT, L::MS, L::GSTR, acc, lane, half, 4 + mat, sc + L::SC_IK, true);
         }
         named_bar(ID_T, NT_S);
+        TC2_STAMP(p, 5, 4, c, nch);
         if (rw) {
             float lr[C], nr[C];
             // e_t = v_t - S_c k^_t - sum_{s<t} (k^_t . alpha^_s) e_s, kept (in place)
@@ -825,6 +844,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
                     for (int t = r + 1; t < C; ++t) vv[t] = fmaf(-lr[t], vv[r], vv[t]);
                 }
             }
+            TC2_STAMP(p, 5, 5, c, nch);
             // o_t = (S_c phi_t + sum_{s<=t} e_s (alpha^_s . phi_t)) / den_t = S_t phi_t / den_t (eq. 11)
             tc::ld_row16(sc + L::SC_RDEN, nr);
 #pragma unroll
@@ -844,6 +864,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         }
         fence_proxy_async_smem();
         named_bar(ID_T, NT_S);
+        TC2_STAMP(p, 5, 6, c, nch);
         // S_{c+1} = S_c + E' A (rows a_t from the mailbox, columns scaled into E')
         if (warp == 0 && tc::elect_one()) {
             mbar_arrive(x.b.empty_p + s);  // done with the chunk's k, phi rows and den
@@ -864,6 +885,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             tc_commit(x.b.mma_x);
         }
         ok = mbar_wait(x.b.mma_x, ps, nullptr, p.wait_ns) && ok;
+        TC2_STAMP(p, 5, 7, c, nch);
         ps ^= 1;
         tc_fence_after();
         if (ts == 0) mbar_arrive_peer(r_empty_al + 8u * b);  // mailbox buffer b back to rank 0
@@ -874,6 +896,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             ++c;
             break;
         }
+        TC2_STAMP(p, 5, 8, c, nch);
     }
     if (ts == 0) *x.n_recv = recv;
     if (bad) {

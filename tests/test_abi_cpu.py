@@ -1,6 +1,8 @@
 """The C ABI without a GPU: the library loads, exports every entry point that
-include/vla.h declares, and rejects bad arguments before any CUDA work."""
+the headers under include/ declare, and rejects bad arguments before any CUDA
+work."""
 import ctypes
+import glob
 import os
 import re
 
@@ -8,6 +10,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "vla.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -19,10 +22,12 @@ def lib():
     return _binding.load_library()
 
 
-def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(vla_[a-z_]+)\s*\(", text)))
+def declared_functions(headers=None):
+    names = set()
+    for h in headers or HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(vla_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_entry_points():
@@ -33,14 +38,45 @@ def test_header_declares_entry_points():
 
 
 def test_exports_every_declared_symbol(lib):
+    assert len(HEADERS) >= 2
     for name in declared_functions():
-        assert hasattr(lib, name), f"{name} declared in vla.h but not exported"
+        assert hasattr(lib, name), f"{name} declared under include/ but not exported"
+    assert "vla_probe_ffma" in declared_functions() and "vla_forward_noalloc" in declared_functions()
+
+
+def test_probe_arguments(lib):
+    """The FFMA probe's FLOP count and its argument checks (no launch)."""
+    assert lib.vla_probe_ffma_flop(152, 256, 1000, 0) == 2.0 * 32 * 1000 * 152 * 256
+    assert lib.vla_probe_ffma_flop(152, 256, 1000, 1) == 2.0 * 32 * 1000 * 152 * 256
+    for bad in ((0, 256, 10), (1, 48, 10), (1, 2048, 10), (1, 256, 0)):
+        assert lib.vla_probe_ffma_flop(*bad, 0) == 0.0
+        assert lib.vla_probe_ffma(*bad, 0, ctypes.c_void_p(FAKE), None) == 1
+    assert lib.vla_probe_ffma(1, 32, 1, 0, None, None) == 1
+    assert lib.vla_probe_ffma(1, 32, 1, 0, ctypes.c_void_p(FAKE + 2), None) == 1
+
+
+def test_noalloc_rejects_before_any_device_work(lib):
+    """Argument errors of the no-allocation entry point come back before it
+    touches a device, and its device-status output carries the same error."""
+    vp = ctypes.c_void_p
+    for (dtype, B, d, want) in ((1, 1, 48, 2), (7, 1, 64, 1), (1, -1, 64, 1)):
+        st = ctypes.c_int(-7)
+        r = lib.vla_forward_noalloc(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), dtype, B, 1, 4, d, 0.1, 1e-4,
+                                    None, None, None, vp(FAKE), vp(FAKE), vp(FAKE), None, None, ctypes.byref(st))
+        assert r == want and st.value == want
 
 
 def test_status_strings(lib):
     for s in range(6):
         assert lib.vla_status_string(s)
-    assert lib.vla_workspace_bytes() >= 16
+
+
+def test_workspace_bytes(lib):
+    """The status record's 256 bytes for every valid shape; 0 for invalid sizes."""
+    for shape in ((1, 1, 1, 32), (8, 16, 4096, 96), (1, 32, 65536, 128), (64, 8, 1024, 64), (1, 1, 0, 64)):
+        assert lib.vla_workspace_bytes(*shape) == 256
+    for shape in ((-1, 1, 4, 64), (1, -1, 4, 64), (1, 1, -4, 64), (1, 1, 4, 48), (1, 1, 4, 0)):
+        assert lib.vla_workspace_bytes(*shape) == 0
 
 
 FAKE = 1 << 20  # an aligned non-null address that the validation paths never dereference

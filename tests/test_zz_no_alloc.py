@@ -4,9 +4,9 @@ vla_forward_noalloc is for callers that cannot allocate device memory (a
 device budget already reserved in full by another runtime, loops that must not
 call the allocator, callers without an allocator): its status record lives in
 a static device array instead of a caller-provided workspace. Two calls in a
-row must each match vla_forward within the parity tolerance, and the second
-call must start from a cleared status even though the first one left an error
-in the shared record.
+row must each match vla_forward within the parity tolerance (and the fp64
+oracle, directly), and the second call must start from a cleared status even
+though the first one left an error in the shared record.
 """
 import ctypes
 
@@ -14,7 +14,8 @@ import numpy as np
 import pytest
 import torch
 
-from parity_util import TOL, rel_heads, rel_rows
+import oracle
+from parity_util import TOL, assert_close, errors, rel_heads, rel_rows
 from sherman_morrison_memory_gb300 import VLA_ERR_NONFINITE, VLA_OK, _binding, vla_forward
 from sherman_morrison_memory_gb300 import workloads as W
 
@@ -46,10 +47,14 @@ def _call_noalloc(lib, q, k, v, u):
     return st, status.value, (o, S, A, zk)
 
 
-def _inputs(seed, dtype="bf16", B=2, H=3, T=77, d=96):
+def _host_inputs(seed, dtype="bf16", B=2, H=3, T=77, d=96):
     arrs = W.normal(B, H, T, d, seed=seed)
+    return [W.to_bf16_values(a) if dtype == "bf16" else a for a in arrs]
+
+
+def _inputs(seed, dtype="bf16", B=2, H=3, T=77, d=96):
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    return [torch.from_numpy(W.to_bf16_values(a) if dtype == "bf16" else a).cuda().to(tdt) for a in arrs]
+    return [torch.from_numpy(a).cuda().to(tdt) for a in _host_inputs(seed, dtype, B, H, T, d)]
 
 
 def _close(a, b):
@@ -61,6 +66,7 @@ def _close(a, b):
 
 def test_noalloc_matches_vla_forward_twice():
     lib = _lib()
+    orc = oracle.load()
     torch.cuda.synchronize()
     for seed, dtype, d in ((31, "bf16", 96), (32, "f32", 64)):
         q, k, v, u = _inputs(seed, dtype, d=d)
@@ -68,6 +74,10 @@ def test_noalloc_matches_vla_forward_twice():
         st, dev_st, out = _call_noalloc(lib, q, k, v, u)
         assert st == VLA_OK and dev_st == VLA_OK, (st, dev_st)
         _close(out, (ref_o, ref_S, ref_A, ref_zk))
+        # and directly against the fp64 oracle on the same input bits
+        fp64 = orc.forward(*_host_inputs(seed, dtype, d=d), lambda0=0.1, eps=1e-4)
+        o, S, A, zk = out
+        assert_close(errors((o, (S, A, zk)), fp64), what=f"noalloc vs oracle d={d} {dtype}")
 
 
 def test_noalloc_status_is_cleared_between_calls():
