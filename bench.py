@@ -57,6 +57,7 @@ KERNEL_FILES = {
     "vla_backward_kernel": ("vla_backward.cuh", "vla_device.cuh"),
     "vla_decode_kernel": ("vla_decode.cuh", "vla_backward.cuh", "vla_device.cuh"),
     "vla_tc2_kernel": ("vla_tc2.cuh", "vla_tc.cuh", "vla_device.cuh"),
+    "vla_tc3_kernel": ("vla_tc3.cuh", "vla_tc2.cuh", "vla_tc.cuh", "vla_device.cuh"),
 }
 
 # DRAM bytes per launch of a bench line's kernel (dram__bytes_read.sum +
@@ -105,6 +106,8 @@ def kernel_for(algo: int, T: int, d: int) -> str:
     """The kernel one vla_forward call launches (the choice VLA_ALGO_AUTO makes)."""
     if algo == 3 or (algo == 0 and T <= 4):
         return "vla_decode_kernel"
+    if algo == 5:
+        return "vla_tc3_kernel"
     if algo == 4 or (algo == 0 and d == 128):
         return "vla_tc2_kernel"
     if algo == 2 or (algo == 0 and d <= 96):
@@ -831,8 +834,9 @@ def main(argv=None):
     ap.add_argument("--no-configs", action="store_true",
                     help="skip timing the other workloads (the `configs` object of the forward line)")
     ap.add_argument("--algo", type=int, default=0,
-                    help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96, its cluster-pair form "
-                         "for d_h = 128), 1 per-token, 2 chunked, 3 decode, 4 chunked on a cluster pair")
+                    help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96, its cluster forms "
+                         "for d_h = 128), 1 per-token, 2 chunked, 3 decode, 4 chunked on a cluster pair, "
+                         "5 chunked on a cluster with S's rows split")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "decode"], default="forward",
                     help="time the forward recurrence (default), its reverse-mode gradient, or one "
                          "decode step (T = 1) of 2048 heads from a carried state")

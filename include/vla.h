@@ -90,9 +90,16 @@ typedef struct {
  *                       sends each chunk's gate to the other, which runs the S-pass
  *                       (eq. 10-11); each state has a whole SM's tensor memory, so d = 128
  *                       runs too (any supported d)
+ *   VLA_ALGO_CHUNKED_ROWS  the chunked tensor-core recurrence on a cluster of 1 + NS CTAs
+ *                       per head, the rows of S split over NS of them (the residual write
+ *                       of eq. 10 acts on each row of S on its own): rank 0 runs the A-pass
+ *                       and sends each chunk's gate to every S rank through distributed
+ *                       shared memory; NS = 1 for d <= 64, 2 for d = 96 and 128 (any
+ *                       supported d). Uses 1 + NS SMs per head, so that fewer heads than
+ *                       SMs keep more of the chip busy
  * Any other value: VLA_ERR_INVALID_ARG. */
 enum { VLA_ALGO_AUTO = 0, VLA_ALGO_PER_TOKEN = 1, VLA_ALGO_CHUNKED = 2, VLA_ALGO_DECODE = 3,
-       VLA_ALGO_CHUNKED_PAIR = 4 };
+       VLA_ALGO_CHUNKED_PAIR = 4, VLA_ALGO_CHUNKED_ROWS = 5 };
 
 /* Bytes of device workspace vla_forward() needs for a call over B x H heads
  * of T tokens at head dimension d: 256 bytes, which hold the status record

@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     VLA_ALGO_CHUNKED,
     VLA_ALGO_DECODE,
     VLA_ALGO_CHUNKED_PAIR,
+    VLA_ALGO_CHUNKED_ROWS,
     VLAError,
     library_path,
     load_library,

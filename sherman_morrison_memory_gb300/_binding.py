@@ -26,6 +26,7 @@ VLA_ALGO_PER_TOKEN = 1
 VLA_ALGO_CHUNKED = 2
 VLA_ALGO_DECODE = 3
 VLA_ALGO_CHUNKED_PAIR = 4
+VLA_ALGO_CHUNKED_ROWS = 5
 
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 

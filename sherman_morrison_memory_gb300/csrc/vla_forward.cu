@@ -1117,6 +1117,7 @@ __global__ void __launch_bounds__(LA_THREADS) la_state_kernel(const TIn* k, cons
 
 #include "vla_tc.cuh"
 #include "vla_tc2.cuh"
+#include "vla_tc3.cuh"
 #include "vla_backward.cuh"
 #include "vla_decode.cuh"
 
@@ -1166,6 +1167,31 @@ vla_status launch_tc2(const vla::Params& p, int BH, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
 }
 
+// the chunked recurrence on a cluster of 1 + NS CTAs per head: rank 0 the
+// A-pass, ranks 1..NS the rows of S split in NS equal blocks
+template <int D, typename TIn, int NS>
+vla_status launch_tc3(const vla::Params& p, int BH, cudaStream_t s) {
+    using LY = vla::tc3::Lay3<D, TIn, NS>;
+    auto kern = vla::vla_tc3_kernel<D, TIn, NS>;
+    if ((long long)BH * (1 + NS) > 2147483647LL) return VLA_ERR_INVALID_ARG;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::SMEM_LAUNCH) != cudaSuccess)
+        return VLA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((1 + NS) * BH), 1, 1);
+    cfg.blockDim = dim3(vla::tc3::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = LY::SMEM_LAUNCH;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1 + NS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return VLA_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
+}
+
 template <int D, typename TIn>
 vla_status launch_dec(const vla::Params& p, int BH, bool fixed_a, cudaStream_t s) {
     using DL = vla::dec::DLay<D, TIn>;
@@ -1201,6 +1227,16 @@ vla_status launch_d(int d, int algo, bool fixed_a, const vla::Params& p, int BH,
         }
     }
     if (fixed_a && algo == VLA_ALGO_PER_TOKEN) return VLA_ERR_UNSUPPORTED;
+    if (algo == VLA_ALGO_CHUNKED_ROWS) {
+        // S's rows on one CTA up to d = 64, on two CTAs above
+        switch (d) {
+            case 32: return launch_tc3<32, TIn, 1>(p, BH, s);
+            case 64: return launch_tc3<64, TIn, 1>(p, BH, s);
+            case 96: return launch_tc3<96, TIn, 2>(p, BH, s);
+            case 128: return launch_tc3<128, TIn, 2>(p, BH, s);
+            default: return VLA_ERR_UNSUPPORTED;
+        }
+    }
     if (algo == VLA_ALGO_CHUNKED_PAIR || (algo == VLA_ALGO_AUTO && d == 128)) {
         switch (d) {
             case 32: return launch_tc2<32, TIn>(p, BH, s);
@@ -1321,7 +1357,7 @@ vla_status vla_impl::forward(const void* q, const void* k, const void* v, const 
     const int algo = opts ? opts->algo : VLA_ALGO_AUTO;
     const bool fixed_a = opts && opts->fixed_a;
     if (algo != VLA_ALGO_AUTO && algo != VLA_ALGO_PER_TOKEN && algo != VLA_ALGO_CHUNKED && algo != VLA_ALGO_DECODE &&
-        algo != VLA_ALGO_CHUNKED_PAIR)
+        algo != VLA_ALGO_CHUNKED_PAIR && algo != VLA_ALGO_CHUNKED_ROWS)
         return VLA_ERR_INVALID_ARG;
     if (algo == VLA_ALGO_CHUNKED && d > 96) return VLA_ERR_UNSUPPORTED;
     if (fixed_a && algo == VLA_ALGO_PER_TOKEN) return VLA_ERR_UNSUPPORTED;

@@ -233,7 +233,7 @@ struct Ctx2 {
     __device__ float* f(size_t off) const { return reinterpret_cast<float*>(base + off); }
     __device__ float* sm() const { return f(L::OFF_SM); }
     // raise the abort flag here and in the peer CTA
-    __device__ void abort_both(uint32_t rank) const {
+    __device__ void abort_peers(uint32_t rank) const {
         *abort = 1;
         st_peer_u32(peer_addr((const void*)abort, rank ^ 1u), 1u);
     }
@@ -241,15 +241,18 @@ struct Ctx2 {
 
 // ---------------------------------------------------------------------------
 // staging warps (4) of either rank: per chunk, TMA bulk copies of two raw
-// tensors (rank 0: u, k; rank 1: q, k); warp w handles tokens 4w..4w+3.
-// Rank 0: 1/||u||, 1/||k|| and the u | k operand tiles. Rank 1: phi(q),
-// 1/||k||, z^key += phi(k) and den = max(phi(q) . z^key, eps) (eq. 11), the
-// k | phi operand tiles.
+// tensors (A side: u, k; S side: q, k); warp w handles tokens 4w..4w+3.
+// A side (RANK0): 1/||u||, 1/||k|| and the u | k operand tiles. S side:
+// phi(q), 1/||k||, z^key += phi(k) and den = max(phi(q) . z^key, eps)
+// (eq. 11), the k | phi operand tiles; `write_zk`: this CTA writes the final
+// z^key. X is the cluster kernel's context (its layout X::L has the fields
+// used here; x.abort_peers(rank) raises the abort flag of every CTA of the
+// cluster).
 // ---------------------------------------------------------------------------
-template <int D, typename TIn, bool RANK0>
-__device__ __forceinline__ void stage2(const Params& p, const Ctx2<D, TIn>& x, int bh, int sw, int lane,
-                                       uint32_t rank) {
-    using L = Lay2<D, TIn>;
+template <int D, typename TIn, bool RANK0, typename X>
+__device__ __forceinline__ void stage2(const Params& p, const X& x, int bh, int sw, int lane, uint32_t rank,
+                                       bool write_zk = true) {
+    using L = typename X::L;
     constexpr int E = D / 32, TW = C / NSTAGE;
     const int T = p.T, nch = (T + C - 1) / C;
     const TIn* g0 = static_cast<const TIn*>(RANK0 ? p.u : p.q) + (size_t)bh * T * D;
@@ -401,14 +404,14 @@ __device__ __forceinline__ void stage2(const Params& p, const Ctx2<D, TIn>& x, i
     if (bad) {
         if (leader) {
             record_failure(p.status, BIT_TIMEOUT, ROLE_STAGE, bh, c * C);
-            x.abort_both(rank);
+            x.abort_peers(rank);
             // let copies already in flight land before the CTA can exit
             for (int cc = c; cc < issued; ++cc)
                     (void)mbar_wait(x.b.full_r + cc % L::NRAW, (cc / L::NRAW) & 1, nullptr, p.wait_ns);
         }
         return;
     }
-    if (!RANK0 && p.zk_out && sw == 0) {
+    if (!RANK0 && write_zk && p.zk_out && sw == 0) {
 #pragma unroll
         for (int m = 0; m < E; ++m) p.zk_out[(size_t)bh * D + lane + 32 * m] = zk[m];
     }
@@ -699,7 +702,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
     if (bad) {
         if (ta == 0) {
             record_failure(p.status, BIT_TIMEOUT, ROLE_A, bh, c * C);
-            x.abort_both(rank);
+            x.abort_peers(rank);
         }
     } else if (rw) {
         float* Ao = p.A_out + ((size_t)bh * D + i) * D;
@@ -902,7 +905,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
     if (bad) {
         if (ts == 0) {
             record_failure(p.status, BIT_TIMEOUT, ROLE_S, bh, c * C);
-            x.abort_both(rank);
+            x.abort_peers(rank);
         }
     } else if (rw) {
         float* So = p.S_out + ((size_t)bh * D + i) * D;

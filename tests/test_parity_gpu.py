@@ -13,8 +13,8 @@ import torch
 
 import oracle
 from parity_util import TOL, assert_close, errors, rel_heads, rel_rows, to_dev
-from sherman_morrison_memory_gb300 import (VLA_ALGO_CHUNKED, VLA_ALGO_CHUNKED_PAIR, VLA_ALGO_DECODE,
-                                           VLA_ALGO_PER_TOKEN, VLA_ERR_NONFINITE,
+from sherman_morrison_memory_gb300 import (VLA_ALGO_CHUNKED, VLA_ALGO_CHUNKED_PAIR, VLA_ALGO_CHUNKED_ROWS,
+                                           VLA_ALGO_DECODE, VLA_ALGO_PER_TOKEN, VLA_ERR_NONFINITE,
                                            VLA_ERR_TIMEOUT, VLA_OK, vla_forward, vla_get_last_device_status,
                                            vla_linear_attention_state)
 from sherman_morrison_memory_gb300 import workloads as W
@@ -49,7 +49,7 @@ def _state_ref(state):
     return dict(S0=f(S0), A0=f(A0), zk0=f(zk0))
 
 
-ALGOS = [VLA_ALGO_PER_TOKEN, VLA_ALGO_CHUNKED, VLA_ALGO_DECODE, VLA_ALGO_CHUNKED_PAIR]
+ALGOS = [VLA_ALGO_PER_TOKEN, VLA_ALGO_CHUNKED, VLA_ALGO_DECODE, VLA_ALGO_CHUNKED_PAIR, VLA_ALGO_CHUNKED_ROWS]
 
 
 def _algo_ok(algo, d):
@@ -85,11 +85,12 @@ def test_small_bf16(orc, d, algo):
 
 
 @pytest.mark.parametrize("d", [32, 64, 96, 128])
-@pytest.mark.parametrize("other", [VLA_ALGO_CHUNKED, VLA_ALGO_CHUNKED_PAIR])
+@pytest.mark.parametrize("other", [VLA_ALGO_CHUNKED, VLA_ALGO_CHUNKED_PAIR, VLA_ALGO_CHUNKED_ROWS])
 def test_kernels_agree(orc, d, other):
-    """Per-token and chunked kernels (one CTA, or a cluster pair per head) on
-    the same inputs: many 16-token chunks plus a ragged tail; each within
-    tolerance of the oracle and of each other."""
+    """Per-token and chunked kernels (one CTA, a cluster pair, or a cluster
+    with S's rows split, per head) on the same inputs: many 16-token chunks
+    plus a ragged tail; each within tolerance of the oracle and of each
+    other."""
     if not _algo_ok(other, d):
         pytest.skip("the chunked kernel covers d <= 96")
     arrs = _inputs(2, 3, 16 * 23 + 5, d, "bf16", seed=70 + d)
@@ -103,12 +104,14 @@ def test_kernels_agree(orc, d, other):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_pair_kernel_more_heads_than_sms(orc, dtype):
-    """The cluster-pair kernel with more clusters than fit at once (2 CTAs per
-    head, 192 heads): several waves of clusters, every head checked."""
-    arrs = _inputs(4, 48, 16 * 6 + 3, 64, dtype, seed=123)
-    out, ref = _run(orc, arrs, dtype, algo=VLA_ALGO_CHUNKED_PAIR)
-    assert_close(errors(out, ref), what=f"pair kernel, 192 heads, {dtype}")
+@pytest.mark.parametrize("algo,d", [(VLA_ALGO_CHUNKED_PAIR, 64), (VLA_ALGO_CHUNKED_ROWS, 64),
+                                    (VLA_ALGO_CHUNKED_ROWS, 96)])
+def test_cluster_kernels_more_heads_than_sms(orc, dtype, algo, d):
+    """The cluster kernels with more clusters than fit at once (2 or 3 CTAs
+    per head, 192 heads): several waves of clusters, every head checked."""
+    arrs = _inputs(4, 48, 16 * 6 + 3, d, dtype, seed=123)
+    out, ref = _run(orc, arrs, dtype, algo=algo)
+    assert_close(errors(out, ref), what=f"cluster kernel algo={algo}, 192 heads, d={d}, {dtype}")
 
 
 @pytest.mark.parametrize("d", [32, 96])
@@ -173,7 +176,7 @@ def _spd(B, H, d, seed, scale=10.0):
     return (0.5 * (A + np.swapaxes(A, -1, -2))).astype(np.float32)
 
 
-@pytest.mark.parametrize("algo", [0, VLA_ALGO_CHUNKED, VLA_ALGO_DECODE, VLA_ALGO_CHUNKED_PAIR])
+@pytest.mark.parametrize("algo", [0, VLA_ALGO_CHUNKED, VLA_ALGO_DECODE, VLA_ALGO_CHUNKED_PAIR, VLA_ALGO_CHUNKED_ROWS])
 @pytest.mark.parametrize("d", [32, 96, 128])
 @pytest.mark.parametrize("a0", ["default", "spd"])
 def test_fixed_a_variant(orc, d, a0, algo):
@@ -262,7 +265,8 @@ def test_linear_attention_state(orc):
     assert rel_heads(S.cpu().numpy(), want) < 1e-4
 
 
-@pytest.mark.parametrize("algo", [VLA_ALGO_PER_TOKEN, VLA_ALGO_CHUNKED, VLA_ALGO_CHUNKED_PAIR, VLA_ALGO_DECODE])
+@pytest.mark.parametrize("algo", [VLA_ALGO_PER_TOKEN, VLA_ALGO_CHUNKED, VLA_ALGO_CHUNKED_PAIR, VLA_ALGO_DECODE,
+                                  VLA_ALGO_CHUNKED_ROWS])
 def test_timeout_is_reported_and_context_survives(orc, algo):
     """A stalled producer (the staging warps; on the decode kernel, the bulk
     copies of a head's state and inputs) makes every consumer's bounded wait
