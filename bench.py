@@ -102,11 +102,12 @@ def ncu_traffic(kernel: str, workload=None):
     return t["bytes_per_launch"]
 
 
-def kernel_for(algo: int, T: int, d: int) -> str:
-    """The kernel one vla_forward call launches (the choice VLA_ALGO_AUTO makes)."""
+def kernel_for(algo: int, T: int, d: int, heads: int = 1 << 30, n_sm: int = 152) -> str:
+    """The kernel one vla_forward call launches (the choice VLA_ALGO_AUTO makes
+    for `heads` = B * H heads on `n_sm` SMs)."""
     if algo == 3 or (algo == 0 and T <= 4):
         return "vla_decode_kernel"
-    if algo == 5:
+    if algo == 5 or (algo == 0 and d >= 96 and 3 * heads <= n_sm):
         return "vla_tc3_kernel"
     if algo == 4 or (algo == 0 and d == 128):
         return "vla_tc2_kernel"
@@ -424,7 +425,7 @@ def run_ours(args, w):
 
     # roofline of the one kernel that a step launches, against the FP32 FMA
     # peak measured by the probe in this run (the nominal figure beside it)
-    kernel = kernel_for(args.algo, T, d)
+    kernel = kernel_for(args.algo, T, d, w.heads, props.multi_processor_count)
     peaks = load_peaks()
     sm_max = float(peaks.get("sm_max_mhz", FALLBACK_SM_MAX_MHZ))
     n_sm = props.multi_processor_count
@@ -569,7 +570,8 @@ def time_workloads(ids, dev, peak_tflops: float, steps: int = 20, warmup: int = 
             raise RuntimeError(f"workload {wid}: device status {st} {detail}")
         ms = e0.elapsed_time(e1) / steps
         tflops = FLOP_D2["forward"] * d * d * w.head_tokens / (ms / 1e3) / 1e12
-        out[str(wid)] = {"workload": w.describe(), "kernel": kernel_for(0, T, d), "ms_per_step": ms,
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        out[str(wid)] = {"workload": w.describe(), "kernel": kernel_for(0, T, d, w.heads, n_sm), "ms_per_step": ms,
                          "head_tokens_per_s": w.head_tokens / (ms / 1e3), "achieved_tflops": tflops,
                          "fp32_roofline_frac": tflops / peak_tflops, "steps": steps, "warmup": warmup,
                          "inputs": src}

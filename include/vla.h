@@ -76,8 +76,10 @@ typedef struct {
 
 /* Kernels behind vla_forward_ex() (vla_options.algo). All compute eq. 9-11
  * exactly up to rounding order.
- *   VLA_ALGO_AUTO       decode kernel for T <= 4; otherwise the chunked tensor-core kernel
- *                       for d <= 96 and the cluster-pair chunked kernel for d = 128
+ *   VLA_ALGO_AUTO       decode kernel for T <= 4; for d = 96 and 128 with 3 * B * H at most
+ *                       the device's SM count, VLA_ALGO_CHUNKED_ROWS (its clusters all run
+ *                       at once); otherwise the chunked tensor-core kernel for d <= 96 and
+ *                       the cluster-pair chunked kernel for d = 128
  *   VLA_ALGO_PER_TOKEN  one token at a time on the FMA pipes (any supported d)
  *   VLA_ALGO_CHUNKED    16 tokens at a time: the Sherman-Morrison steps of a chunk as an
  *                       LDL^T factorisation, the d x d products on the tcgen05 tensor cores

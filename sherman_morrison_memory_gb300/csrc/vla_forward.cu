@@ -1212,7 +1212,17 @@ vla_status launch_dec(const vla::Params& p, int BH, bool fixed_a, cudaStream_t s
 // sequences up to this length go to the decode kernel under VLA_ALGO_AUTO
 constexpr int kDecodeMaxT = 4;
 
-// algo: VLA_ALGO_AUTO picks the decode kernel for short sequences, the
+// SMs of the current device (0 if the query fails)
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// algo: VLA_ALGO_AUTO picks the decode kernel for short sequences; for
+// d = 96 and 128 the row-split cluster kernel (3 CTAs per head) when all of
+// its clusters fit on the SMs at once, measured faster there; otherwise the
 // single-CTA chunked tensor-core kernel for d <= 96 and the cluster-pair
 // chunked kernel for d = 128.
 template <typename TIn>
@@ -1227,6 +1237,7 @@ vla_status launch_d(int d, int algo, bool fixed_a, const vla::Params& p, int BH,
         }
     }
     if (fixed_a && algo == VLA_ALGO_PER_TOKEN) return VLA_ERR_UNSUPPORTED;
+    if (algo == VLA_ALGO_AUTO && d >= 96 && 3LL * BH <= (long long)sm_count()) algo = VLA_ALGO_CHUNKED_ROWS;
     if (algo == VLA_ALGO_CHUNKED_ROWS) {
         // S's rows on one CTA up to d = 64, on two CTAs above
         switch (d) {

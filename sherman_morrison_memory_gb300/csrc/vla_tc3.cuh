@@ -26,9 +26,8 @@
 // and w + 4): in rank 0, the product columns, the gate sums and the lo
 // refresh of A; in an S rank, the products (S k for the solve, S phi for the
 // readout), the lo refresh, and the readout, which runs beside the update.
-// In an S rank the warps that own no rows form the chunk's 16 x 16 Gram
-// matrices as soon as the gate arrives, while the row warps read the
-// products, which are issued before the gate arrives.
+// In an S rank the chunk's products are issued before the gate arrives, and
+// all eight warps form the chunk's 16 x 16 Gram matrices once it has.
 //
 // Every wait is bounded; a role that gives up raises the abort flag of every
 // CTA of the cluster.
@@ -44,6 +43,14 @@ using tc2::mbar_wait_cl;
 using tc2::peer_addr;
 using tc2::st_peer_u32;
 
+// arm a peer's barrier for `bytes` of bulk copies (one arrival), with relaxed
+// ordering: the data reach the peer through the copies, whose completion the
+// peer's wait observes, so this thread's earlier writes need no release
+__device__ __forceinline__ void mbar_expect_tx_peer_relaxed(uint32_t rbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(rbar), "r"(bytes)
+                 : "memory");
+}
+
 // -DVLA_TRACE builds: per-chunk clock stamps of head 0's cluster, stamp k of
 // chunk c at trace[row][k * nch + c] (row 4 + rank)
 #define TC3_STAMP(p, rank, k, c, nch) \
@@ -56,7 +63,7 @@ constexpr int C = tc::C;
 constexpr int NSTAGE = 4;
 constexpr int THREADS = 32 * 12;
 constexpr int NTEAM = 256;  // team warps 0-7
-// named barriers: 1 team, 3 staging, 4-5 Gram pairs (S ranks), 8-11 row hand-offs
+// named barriers: 1 team, 3 staging, 8-11 row hand-offs
 constexpr int ID_T = 1, ID_ST = 3, ID_Y = 8, ID_M = 9, ID_E = 10, ID_EM = 11;
 constexpr int FACTOR_WARP = 4;
 constexpr int NISS = 4;  // warps that issue the d x 2C chunk products, one accumulator each
@@ -106,9 +113,9 @@ struct Lay3 {
     static constexpr size_t OFF_GL = OFF_GH + 2 * (size_t)MB_G;             // a^T lo [2][D x C]
     static constexpr size_t OFF_LAA = OFF_GL + 2 * (size_t)MB_G;            // ||a||^2 [2][C] (S ranks)
     static constexpr size_t OFF_SM = al(OFF_LAA + 2 * (size_t)MB_LAA);
-    // small matrices, rank 0: Guu, Guk, L, L^T, X^T, 1/delta; S ranks: Lk^T, Lq (two partials each)
+    // small matrices, rank 0: Guu, Guk, L, L^T, X = L^-1 Guk, 1/delta; S ranks: Lk^T, Lq (two partials each)
     static constexpr int MS = C * GSTR;
-    static constexpr int SM_GUU = 0, SM_GUK = MS, SM_LM = 2 * MS, SM_LMT = 3 * MS, SM_XGT = 4 * MS,
+    static constexpr int SM_GUU = 0, SM_GUK = MS, SM_LM = 2 * MS, SM_LMT = 3 * MS, SM_X = 4 * MS,
                          SM_RD = 5 * MS, SM_LKT = 0, SM_LQ = 2 * MS;
     static constexpr size_t OFF_U = al(OFF_SM + (size_t)(5 * MS + C) * 4);
     // rank 0: xr (z' | w rows, then y = z / delta | w) [2C x XS], -M hi / lo
@@ -120,10 +127,11 @@ struct Lay3 {
     static constexpr size_t OFF_ZL = OFF_ZH + (size_t)D * C * 4;
     static constexpr size_t OFF_GP = OFF_ZL + (size_t)D * C * 4;
     static constexpr size_t END_A = OFF_GP + (size_t)2 * 3 * 256 * 4;
-    // S ranks: E' hi / lo [128 x C]
+    // S ranks: E' hi / lo [128 x C], Gram partials of quarters 1..3 [2][3][32 x 8]
     static constexpr size_t OFF_EH = OFF_U;
     static constexpr size_t OFF_EL = OFF_EH + 128 * C * 4;
-    static constexpr size_t END_S = OFF_EL + 128 * C * 4;
+    static constexpr size_t OFF_GPS = OFF_EL + 128 * C * 4;
+    static constexpr size_t END_S = OFF_GPS + (size_t)2 * 3 * 256 * 4;
     static constexpr size_t SMEM = al(END_A > END_S ? END_A : END_S);
     static constexpr size_t SMEM_LAUNCH = SMEM > MIN_SMEM ? SMEM : MIN_SMEM;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -211,42 +219,34 @@ __device__ __forceinline__ void refresh_cols(uint32_t lanebase, uint32_t col, ui
     tc_wait_st();
 }
 
-// 4 gate values of row i (tokens 4g..4g+3) into the row-major a rows and the K-major hi / lo tiles
-__device__ __forceinline__ void put_gate4(float* alr, int xs, float* gh, float* gl, int i, int g, const float (&av)[4]) {
+// a_t[i] = w_t[i] - sum_{q<=t} y_q[i] X[q][t] (eq. 10, a_t = A_t k^_t) for the
+// 16 tokens of row i, q outermost so that the 16 sums advance side by side;
+// tokens t >= n are zero
+__device__ __forceinline__ void gate16(const float* xr, int xs, const float* xm, int gstr, int i, int n, bool fixed,
+                                       const float (&y)[C], float (&av)[C]) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) alr[(4 * g + j) * xs + i] = av[j];
-    *reinterpret_cast<float4*>(gh + cm_off(i, 4 * g, C)) = make_float4(av[0], av[1], av[2], av[3]);
-    *reinterpret_cast<float4*>(gl + cm_off(i, 4 * g, C)) =
-        make_float4(tf32_lo(av[0]), tf32_lo(av[1]), tf32_lo(av[2]), tf32_lo(av[3]));
-}
-
-// a_t[i] = w_t[i] - sum_{q<=t} y_q[i] X[q][t] (eq. 10, a_t = A_t k^_t) for the 4 tokens of group G
-template <int G, int D>
-__device__ __forceinline__ void gate_group(const float* xr, int xs, const float* xgt, int gstr, int i, int n,
-                                           bool fixed, const float (&y)[C], float (&av)[4]) {
+    for (int t = 0; t < C; ++t) av[t] = xr[(C + t) * xs + i];  // w_t
+    if (!fixed) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int t = 4 * G + j;
-        float a = xr[(C + t) * xs + i];
-        if (!fixed) {
+        for (int q = 0; q < C; ++q) {
             float lr[C];
-            tc::ld_row16(xgt + t * gstr, lr);  // X[q][t]
+            tc::ld_row16(xm + q * gstr, lr);  // X[q][t]
 #pragma unroll
-            for (int q = 0; q < C; ++q)
-                if (q <= 4 * G + j) a = fmaf(-y[q], lr[q], a);
+            for (int t = q; t < C; ++t) av[t] = fmaf(-y[q], lr[t], av[t]);
         }
-        av[j] = t < n ? a : 0.f;
     }
+#pragma unroll
+    for (int t = 0; t < C; ++t) av[t] = t < n ? av[t] : 0.f;
 }
 
 // ---------------------------------------------------------------------------
 // rank 0, team warps 0-7: Sherman-Morrison steps of eq. 9 and the gate of
 // eq. 10, one chunk at a time (the arithmetic of tc::tc_a_team). Row i < D is
 // owned by thread i of warps 0-3 ("primary": z' columns, the substitutions,
-// the -M row, gate tokens 0-3 and 12-15, lo refresh of columns [0, D/2))
-// and by thread i of warps 4-7 ("helper": w columns, gate tokens 4-11, lo
-// refresh of columns [D/2, D)). Warp 4 also factors I + Guu and sends the
-// gate to the S ranks.
+// the -M row, lo refresh of columns [0, D/2)) and by thread i of warps 4-7
+// ("helper": w columns, the gate row, lo refresh of columns [D/2, D)); the
+// helper forms the gate while the primary runs the backward substitution.
+// Warp 4 also factors I + Guu and sends the gate to the S ranks.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn, int NS>
 __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int warp, int lane) {
@@ -415,7 +415,7 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
                 }
             } else {
 #pragma unroll
-                for (int r = 0; r < C; ++r) sm[L::SM_XGT + j * L::GSTR + r] = col[r];
+                for (int r = 0; r < C; ++r) sm[L::SM_X + r * L::GSTR + j] = col[r];  // X[r][j]
             }
         } else if (c >= 2) {
             // every S rank is done with mailbox buffer b (chunk c - 2), so its
@@ -434,12 +434,12 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
         // bytes now (the phase completes when the bulk copies below land), so
         // that the send after the gate only issues the copies
         if (warp == FACTOR_WARP && lane < NS)
-            mbar_expect_tx_peer(peer_addr(x.b.full_al + b, (uint32_t)lane + 1u), L::MB_BYTES);
+            mbar_expect_tx_peer_relaxed(peer_addr(x.b.full_al + b, (uint32_t)lane + 1u), L::MB_BYTES);
         float y[C];
         if (prim) {
             if (!fixed) {
                 // y = z_i = z'_i L^-T (forward substitution, in place), then y D^-1;
-                // published in xr rows 0..C-1 for the helper's gate tokens
+                // published in xr rows 0..C-1 for the helper's gate row
                 float lr[C];
 #pragma unroll
                 for (int t = 0; t < C; ++t) y[t] = xr[t * XS + i];
@@ -494,24 +494,18 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
                 tc_commit(x.b.mma_x);
             }
             TC3_STAMP(p, 0, 10, c, nch);
-            // gate tokens 0-3 (the helper forms 4-15 while the substitution runs here)
-            float av[4];
-            gate_group<0, D>(xr, XS, sm + L::SM_XGT, L::GSTR, i, n, fixed, y, av);
-            put_gate4(alr, XS, gh, gl, i, 0, av);
-            TC3_STAMP(p, 0, 11, c, nch);
         } else if (help) {
             named_bar(ID_Y, 64 * NRW);
             TC3_STAMP_T(p, 0, 12, c, nch, 128);
-            // gate tokens 4-15, with y from xr
+            // the gate row, with y = z / delta from xr
 #pragma unroll
             for (int t = 0; t < C; ++t) y[t] = !fixed ? xr[t * XS + i] : 0.f;
-            float av[4];
-            gate_group<1, D>(xr, XS, sm + L::SM_XGT, L::GSTR, i, n, fixed, y, av);
-            put_gate4(alr, XS, gh, gl, i, 1, av);
-            gate_group<2, D>(xr, XS, sm + L::SM_XGT, L::GSTR, i, n, fixed, y, av);
-            put_gate4(alr, XS, gh, gl, i, 2, av);
-            gate_group<3, D>(xr, XS, sm + L::SM_XGT, L::GSTR, i, n, fixed, y, av);
-            put_gate4(alr, XS, gh, gl, i, 3, av);
+            float av[C];
+            gate16(xr, XS, sm + L::SM_X, L::GSTR, i, n, fixed, y, av);
+#pragma unroll
+            for (int t = 0; t < C; ++t) alr[t * XS + i] = av[t];
+            tc::put_row16(gh, i, av, false);
+            tc::put_row16(gl, i, av, true);
             TC3_STAMP_T(p, 0, 13, c, nch, 128);
         }
         fence_proxy_async_smem();
@@ -578,8 +572,9 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
 // Row i is owned by thread i of warp i / 32 ("primary": S k^ columns, the
 // unit-triangular solve, the E' row, lo refresh of columns [0, D/2)) and of
 // warp 4 + i / 32 ("helper": S phi columns, the readout o_t, lo refresh of
-// columns [D/2, D)). Warps 2, 3, 6, 7 own no rows and form the chunk's Gram
-// matrices Lk, Lq as soon as the gate arrives.
+// columns [D/2, D)). The chunk's products are issued before the gate
+// arrives; once it has arrived, all eight warps form the Gram matrices Lk, Lq
+// (the row warps have read their products by then).
 // ---------------------------------------------------------------------------
 template <int D, typename TIn, int NS>
 __device__ void s_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int warp, int lane, uint32_t rank) {
@@ -669,21 +664,9 @@ __device__ void s_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
             }
             tc_commit(x.b.mma_p);
         }
-        bool ok;
+        bool ok = true;
         float sk[C], sq[C];
-        if (gram) {
-            // Lk[t][s] = k^_t . a_s, Lq[t][s] = phi_t . a_s; warp = (matrix, half of D)
-            ok = mbar_wait_cl(x.b.full_al + b, (c >> 1) & 1, x.abort, p.wait_ns);
-            const int mat = warp & 1, half = warp >> 2;
-            float acc[2][4];
-            tc::gram16<D, true>(hi + (mat ? C : 0) * D, 0, alr, XS, half * (D / 2), (half + 1) * (D / 2), lane, acc,
-                                !L::F32IN && mat == 0);
-            if (mat)
-                tc::gram_pair_sum(sm + L::SM_LQ, L::MS, L::GSTR, acc, lane, half, 4 + mat, nullptr, false);
-            else
-                tc::gram_pair_sum(sm + L::SM_LKT, L::MS, L::GSTR, acc, lane, half, 4 + mat, sc + L::SC_IK, true);
-            TC3_STAMP_T(p, rank, 7, c, nch, 64);
-        } else {
+        if (!gram) {
             ok = mbar_wait(x.b.mma_p, c & 1, nullptr, p.wait_ns);
             TC3_STAMP(p, rank, 8, c, nch);
             tc_fence_after();
@@ -694,19 +677,54 @@ __device__ void s_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
             } else if (help_w) {
                 ld_prod_cols(tl + L::T_P, C, sq);  // S_c phi_t
             }
-            ok = mbar_wait_cl(x.b.full_al + b, (c >> 1) & 1, x.abort, p.wait_ns) && ok;
-            TC3_STAMP(p, rank, 9, c, nch);
+        }
+        ok = mbar_wait_cl(x.b.full_al + b, (c >> 1) & 1, x.abort, p.wait_ns) && ok;
+        TC3_STAMP(p, rank, 9, c, nch);
+        {
+            // Lk[t][s] = k^_t . a_s, Lq[t][s] = phi_t . a_s on all eight warps
+            // (matrix, quarter of D); quarters 1-3 leave their partial sums,
+            // warps 0-1 add them (a failed wait leaves garbage here, which the
+            // vote below discards)
+            const int mat = warp & 1, qtr = warp >> 1;
+            float acc[2][4];
+            tc::gram16<D, true>(hi + (mat ? C : 0) * D, 0, alr, XS, qtr * (D / 4), (qtr + 1) * (D / 4), lane, acc,
+                                !L::F32IN && mat == 0);
+            float* part = x.f(L::OFF_GPS) + (size_t)(mat * 3) * 256 + lane * 8;
+            if (qtr > 0) {
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+                    *reinterpret_cast<float4*>(part + (qtr - 1) * 256 + 4 * m) =
+                        make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+            }
             if (warp == 4 && lane < C) {
-                // ||a_t||^2 from the gate rows that just arrived
-                float2 acc = f2(0.f, 0.f);
+                // ||a_t||^2 from the gate rows that arrived
+                float2 a2 = f2(0.f, 0.f);
 #pragma unroll 8
                 for (int k4 = 0; k4 < D / 4; ++k4) {
                     const float4 a = ld4(alr + lane * XS + 4 * k4);
-                    acc = __ffma2_rn(f2(a.x, a.y), f2(a.x, a.y), acc);
-                    acc = __ffma2_rn(f2(a.z, a.w), f2(a.z, a.w), acc);
+                    a2 = __ffma2_rn(f2(a.x, a.y), f2(a.x, a.y), a2);
+                    a2 = __ffma2_rn(f2(a.z, a.w), f2(a.z, a.w), a2);
                 }
-                x.f(L::OFF_LAA)[b * C + lane] = acc.x + acc.y;
+                x.f(L::OFF_LAA)[b * C + lane] = a2.x + a2.y;
             }
+            named_bar(ID_T, NTEAM);
+            if (qtr == 0) {
+#pragma unroll
+                for (int k = 0; k < 3; ++k)
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const float4 o = ld4(part + k * 256 + 4 * m);
+                        acc[m][0] += o.x;
+                        acc[m][1] += o.y;
+                        acc[m][2] += o.z;
+                        acc[m][3] += o.w;
+                    }
+                if (mat)
+                    tc::put_gram16(sm + L::SM_LQ, L::GSTR, acc, lane, nullptr, false);
+                else
+                    tc::put_gram16(sm + L::SM_LKT, L::GSTR, acc, lane, sc + L::SC_IK, true);
+            }
+            TC3_STAMP_T(p, rank, 7, c, nch, 64);
         }
         if (bar_red_or(ID_T, NTEAM, !ok || *x.abort != 0)) {
             bad = true;

@@ -126,11 +126,11 @@ def test_status_read_rejects_null(lib):
 
 
 @pytest.mark.parametrize("algo,d,fixed,status", [
-    (5, 64, 0, 1), (-1, 64, 0, 1), (2, 128, 0, 2),
+    (6, 64, 0, 1), (-1, 64, 0, 1), (2, 128, 0, 2),
     (1, 64, 1, 2), (2, 128, 1, 2),
 ])
 def test_algo_argument_errors(lib, algo, d, fixed, status):
-    """VLA_ALGO_* outside {0, 1, 2, 3, 4} is an argument error; the chunked kernel
+    """VLA_ALGO_* outside {0, ..., 5} is an argument error; the chunked kernel
     reports d = 128 as unsupported; the fixed-A variant does not run on the
     per-token kernel. All are decided before any CUDA call."""
     from sherman_morrison_memory_gb300 import _binding
