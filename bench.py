@@ -71,6 +71,9 @@ NCU_TRAFFIC = {
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
     "vla_tc2_kernel": {"source_sha": "0f583c6ba916b9fc", "workload": (1, 32, 65536, 128, "bf16"),
                        "bytes_per_launch": 8 * (268582912 + 108756224 - 4227072) + 4227072},
+    # the same T = 8192 capture scheme for the row-split cluster kernel
+    "vla_tc3_kernel": {"source_sha": "b553fa72074aaf94", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (268692736 + 108980224 - 4227072) + 4227072},
     # the reverse sweep (the step's dominant kernel, after the taped chunked forward), from a capture of
     # the same workload at B=2 (32 heads; a full step holds about 2.8 GB on the device) scaled by 4:
     # every byte it moves is per head-token or per head
