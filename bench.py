@@ -107,9 +107,12 @@ def ncu_traffic(kernel: str, workload=None):
 
 def kernel_for(algo: int, T: int, d: int, heads: int = 1 << 30, n_sm: int = 152) -> str:
     """The kernel one vla_forward call launches (the choice VLA_ALGO_AUTO makes
-    for `heads` = B * H heads on `n_sm` SMs)."""
+    for `heads` = B * H heads on `n_sm` SMs); for the segmented path, the
+    chunked kernel that its three side-by-side runs use."""
     if algo == 3 or (algo == 0 and T <= 4):
         return "vla_decode_kernel"
+    if algo == 6 or (algo == 0 and d <= 96 and T >= 1024 and 3 * heads <= n_sm):
+        return "vla_tc_kernel"
     if algo == 5 or (algo == 0 and d >= 96 and 3 * heads <= n_sm):
         return "vla_tc3_kernel"
     if algo == 4 or (algo == 0 and d == 128):
@@ -840,8 +843,9 @@ def main(argv=None):
                     help="skip timing the other workloads (the `configs` object of the forward line)")
     ap.add_argument("--algo", type=int, default=0,
                     help="kernel: 0 automatic (chunked tensor-core kernel for d_h <= 96, its cluster forms "
-                         "for d_h = 128), 1 per-token, 2 chunked, 3 decode, 4 chunked on a cluster pair, "
-                         "5 chunked on a cluster with S's rows split")
+                         "for d_h = 128, the segmented path for few heads of long sequences), 1 per-token, "
+                         "2 chunked, 3 decode, 4 chunked on a cluster pair, 5 chunked on a cluster with S's "
+                         "rows split, 6 the sequence's two halves side by side")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "decode"], default="forward",
                     help="time the forward recurrence (default), its reverse-mode gradient, or one "
                          "decode step (T = 1) of 2048 heads from a carried state")

@@ -76,9 +76,10 @@ typedef struct {
 
 /* Kernels behind vla_forward_ex() (vla_options.algo). All compute eq. 9-11
  * exactly up to rounding order.
- *   VLA_ALGO_AUTO       decode kernel for T <= 4; for d = 96 and 128 with 3 * B * H at most
- *                       the device's SM count, VLA_ALGO_CHUNKED_ROWS (its clusters all run
- *                       at once); otherwise the chunked tensor-core kernel for d <= 96 and
+ *   VLA_ALGO_AUTO       decode kernel for T <= 4; with 3 * B * H at most the device's SM
+ *                       count: VLA_ALGO_SEGMENTED for d <= 96 and T >= 1024 when the
+ *                       workspace holds its buffers, else VLA_ALGO_CHUNKED_ROWS for d = 96
+ *                       and 128; otherwise the chunked tensor-core kernel for d <= 96 and
  *                       the cluster-pair chunked kernel for d = 128
  *   VLA_ALGO_PER_TOKEN  one token at a time on the FMA pipes (any supported d)
  *   VLA_ALGO_CHUNKED    16 tokens at a time: the Sherman-Morrison steps of a chunk as an
@@ -99,19 +100,36 @@ typedef struct {
  *                       shared memory; NS = 1 for d <= 64, 2 for d = 96 and 128 (any
  *                       supported d). Uses 1 + NS SMs per head, so that fewer heads than
  *                       SMs keep more of the chip busy
+ *   VLA_ALGO_SEGMENTED  the sequence cut in two halves that run side by side (d <= 96,
+ *                       T >= 32): A and z^key at the cut from the first half's prefix sums
+ *                       of u^ u^^T (§3.2) and phi(k); the second half from S = 0 and, for the
+ *                       transition, from S = I with v = 0 (eq. 12's composition); then
+ *                       S_T = S_cut Pi_T + G_T and o_t += S_cut Pi_t phi_t / den_t. Three
+ *                       chunked CTAs per head. Needs the larger workspace that
+ *                       vla_workspace_bytes() reports (else VLA_ERR_INVALID_ARG)
  * Any other value: VLA_ERR_INVALID_ARG. */
 enum { VLA_ALGO_AUTO = 0, VLA_ALGO_PER_TOKEN = 1, VLA_ALGO_CHUNKED = 2, VLA_ALGO_DECODE = 3,
-       VLA_ALGO_CHUNKED_PAIR = 4, VLA_ALGO_CHUNKED_ROWS = 5 };
+       VLA_ALGO_CHUNKED_PAIR = 4, VLA_ALGO_CHUNKED_ROWS = 5, VLA_ALGO_SEGMENTED = 6 };
 
 /* Bytes of device workspace vla_forward() needs for a call over B x H heads
- * of T tokens at head dimension d: 256 bytes, which hold the status record
- * (16 bytes, the rest reserved). The kernels
- * keep every intermediate of the recurrence on chip (registers, shared and
- * tensor memory), so the size is the same for every valid shape; it is 0 for
- * negative sizes or a d outside {32, 64, 96, 128}. The workspace must be
- * zero-filled before its first use (cudaMemset or vla_workspace_reset);
- * vla_get_last_device_status() clears it again. */
+ * of T tokens at head dimension d, with the kernel that VLA_ALGO_AUTO picks on
+ * the current device (152 SMs assumed when no device answers). 256 bytes
+ * (the status record: 16 bytes, the rest reserved) for every shape whose
+ * kernel keeps all intermediates on chip. Where the segmented path serves the
+ * shape (d <= 96, T >= 1024, 3 * B * H <= the SM count) it also holds that
+ * path's buffers: per head a few d x d states and d-vectors plus T/2 x d
+ * floats. A call given only 256 bytes keeps to the other kernels. 0 for
+ * negative sizes or a d outside {32, 64, 96, 128}. The first 256 bytes must
+ * be zero-filled before the first use (cudaMemset or vla_workspace_reset);
+ * vla_get_last_device_status() clears them again. */
 size_t vla_workspace_bytes(int B, int H, int T, int d);
+
+/* The same for a given kernel choice `algo` (VLA_ALGO_*): what
+ * vla_forward_ex() with that vla_options.algo needs. VLA_ALGO_AUTO gives
+ * vla_workspace_bytes(); VLA_ALGO_SEGMENTED its buffers (0 where it does not
+ * run: d = 128 or T < 32); every other kernel 256. 0 for invalid sizes or an
+ * unknown algo. */
+size_t vla_workspace_bytes_ex(int B, int H, int T, int d, int algo);
 
 /* Zero the status record in `workspace` (asynchronous on `stream`). */
 vla_status vla_workspace_reset(void* workspace, void* stream);
@@ -133,8 +151,10 @@ vla_status vla_workspace_reset(void* workspace, void* stream);
  *  o            [B, H, T, d] float32 output, 16-byte aligned (NULL only if T == 0).
  *  S_out, A_out [B, H, d, d] float32 final state, 16-byte aligned, required.
  *  zk_out       [B, H, d] float32 final z^key, or NULL to skip.
- *  workspace    >= vla_workspace_bytes(B, H, T, d) bytes of zero-filled device memory,
- *               16-byte aligned; holds the device status record.
+ *  workspace    device memory, its first 256 bytes zero-filled (the device status
+ *               record), 16-byte aligned; 256 bytes suffice for every kernel but the
+ *               segmented path, which needs vla_workspace_bytes(B, H, T, d) bytes and
+ *               256-byte alignment.
  *  stream       cudaStream_t as void*.
  *
  * Inputs and outputs must not overlap (S0/S_out, A0/A_out, zk0/zk_out may be

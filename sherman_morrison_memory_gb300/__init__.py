@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     VLA_ALGO_DECODE,
     VLA_ALGO_CHUNKED_PAIR,
     VLA_ALGO_CHUNKED_ROWS,
+    VLA_ALGO_SEGMENTED,
     VLAError,
     library_path,
     load_library,

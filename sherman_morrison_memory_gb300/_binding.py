@@ -27,6 +27,7 @@ VLA_ALGO_CHUNKED = 2
 VLA_ALGO_DECODE = 3
 VLA_ALGO_CHUNKED_PAIR = 4
 VLA_ALGO_CHUNKED_ROWS = 5
+VLA_ALGO_SEGMENTED = 6
 
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
@@ -74,6 +75,8 @@ def load_library():
         lib.vla_forward_ex.argtypes = fwd_args + [ctypes.POINTER(_Options)]
         lib.vla_forward_ex.restype = ci
         lib.vla_workspace_bytes.argtypes = [ci, ci, ci, ci]
+        lib.vla_workspace_bytes_ex.argtypes = [ci, ci, ci, ci, ci]
+        lib.vla_workspace_bytes_ex.restype = ctypes.c_size_t
         lib.vla_workspace_bytes.restype = ctypes.c_size_t
         lib.vla_workspace_reset.argtypes = [vp, vp]
         lib.vla_workspace_reset.restype = ci
@@ -180,9 +183,12 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
     ``check=True`` synchronises and raises on an in-kernel failure.
     ``algo`` selects the kernel: VLA_ALGO_AUTO (0), VLA_ALGO_PER_TOKEN (1),
     VLA_ALGO_CHUNKED (2, the tensor-core chunked kernel, d <= 96),
-    VLA_ALGO_DECODE (3, short sequences with a carried state) or
+    VLA_ALGO_DECODE (3, short sequences with a carried state),
     VLA_ALGO_CHUNKED_PAIR (4, the chunked kernel on a cluster of two CTAs per
-    head: A-pass and S-pass on separate SMs; any d).
+    head: A-pass and S-pass on separate SMs; any d), VLA_ALGO_CHUNKED_ROWS (5,
+    a cluster of 1 + NS CTAs per head with S's rows split over NS of them) or
+    VLA_ALGO_SEGMENTED (6, the sequence's two halves side by side; d <= 96,
+    T >= 32). The workspace is sized for the choice (vla_workspace_bytes_ex).
     ``fixed_a=True`` runs the fixed-A variant (§3.5 ablation): A stays at its
     initial value, u is not read (it may be None).
     """
@@ -218,7 +224,7 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
         zk = torch.empty((B, H, d), dtype=torch.float32, device=dev)
     else:
         o, S, A, zk = out
-    ws = _workspace(dev, vla_workspace_bytes(B, H, T, d))
+    ws = _workspace(dev, int(load_library().vla_workspace_bytes_ex(B, H, T, d, int(algo))))
     with torch.cuda.device(dev):
         sh = _stream_handle(dev, stream)
         args = (_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d,

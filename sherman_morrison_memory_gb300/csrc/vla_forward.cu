@@ -149,6 +149,11 @@ struct Params {
     int fixed_a;  // the fixed-A variant: A stays A0 and eq. 9 is skipped
     float* tape;  // chunked kernel with TAPE (the backward pass's forward): per-token records
     float* ckpt;  //   and the states before every 64th token; else null
+    // read by the single-CTA chunked kernel only (the segmented path runs it on
+    // parts of the sequence); zero-filled fields give the plain layout
+    size_t in_stride;  // elements from one head's q, k, v, u rows to the next (0: T * d)
+    int s0_shared;     // nonzero: every head starts from the same S0 (one d x d matrix)
+    int v_zero;        // nonzero: v is taken as zero and not read
 };
 
 // Per-token clock stamps of head 0 for pipeline analysis (-DVLA_TRACE builds only).
@@ -1118,6 +1123,7 @@ __global__ void __launch_bounds__(LA_THREADS) la_state_kernel(const TIn* k, cons
 #include "vla_tc.cuh"
 #include "vla_tc2.cuh"
 #include "vla_tc3.cuh"
+#include "vla_seg.cuh"
 #include "vla_backward.cuh"
 #include "vla_decode.cuh"
 
@@ -1132,6 +1138,7 @@ constexpr size_t kWorkspaceBytes = 256;
 constexpr unsigned kDefaultWaitUs = 2000000u;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 template <int D, typename TIn>
@@ -1211,6 +1218,9 @@ vla_status launch_dec(const vla::Params& p, int BH, bool fixed_a, cudaStream_t s
 
 // sequences up to this length go to the decode kernel under VLA_ALGO_AUTO
 constexpr int kDecodeMaxT = 4;
+// VLA_ALGO_AUTO takes the segmented path from this length on (d <= 96, heads
+// that fit on the SMs three CTAs each, and a workspace that holds its buffers)
+constexpr int kSegMinT = 1024;
 
 // SMs of the current device (0 if the query fails)
 int sm_count() {
@@ -1218,6 +1228,205 @@ int sm_count() {
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
     return n;
+}
+
+// The segmented path's buffers in the workspace, after the status record:
+// the prefix partial sums, the state at the cut (A, z^key), the identity the
+// transition starts from, the three groups' final states (the first half's
+// S = S_L; the second half's G_T and Pi_T; scratch for the state outputs the
+// combine does not read) and Pi_t phi_t / den_t for the second half's tokens.
+struct SegPlan {
+    int L0 = 0, L1 = 0;
+    size_t dpart = 0, zpart = 0, A_cut = 0, zk_cut = 0, ident = 0, G0 = 0, A_s0 = 0, zk_s0 = 0, G1 = 0, F1 = 0,
+           A_s2 = 0, zk_s2 = 0, fphi = 0, total = 0;
+};
+
+bool seg_plan(long long BH, int T, int d, SegPlan* sp) {
+    if (BH <= 0 || T < 32 || (d != 32 && d != 64 && d != 96)) return false;
+    sp->L0 = T / 2 / 16 * 16;
+    sp->L1 = T - sp->L0;
+    const size_t bh = (size_t)BH, dd = (size_t)d * d, dv = (size_t)d;
+    auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+    size_t off = al(kWorkspaceBytes);
+    auto take = [&](size_t floats) {
+        const size_t at = off;
+        off += al(floats * 4);
+        return at;
+    };
+    sp->dpart = take(bh * vla::seg::NSPLIT * dd);
+    sp->zpart = take(bh * vla::seg::NSPLIT * dv);
+    sp->A_cut = take(bh * dd);
+    sp->zk_cut = take(bh * dv);
+    sp->ident = take(dd);
+    sp->G0 = take(bh * dd);
+    sp->A_s0 = take(bh * dd);
+    sp->zk_s0 = take(bh * dv);
+    sp->G1 = take(bh * dd);
+    sp->F1 = take(bh * dd);
+    sp->A_s2 = take(bh * dd);
+    sp->zk_s2 = take(bh * dv);
+    sp->fphi = take(bh * (size_t)sp->L1 * dv);
+    sp->total = off;
+    return true;
+}
+
+// the segmented path would serve these sizes under VLA_ALGO_AUTO on a device with n_sm SMs
+bool seg_auto(long long BH, int T, int d, int n_sm) { return d <= 96 && T >= kSegMinT && 3LL * BH <= (long long)n_sm; }
+
+// Side streams and events of the segmented path, created on a device's first
+// use and kept until the process exits; a call holds the lock while it
+// enqueues, so that concurrent calls do not share an event in flight.
+constexpr int kSegMaxDevices = 64;
+struct SegFork {
+    bool ready = false;
+    cudaStream_t side[2] = {};
+    cudaEvent_t start = nullptr, cut = nullptr, done[2] = {};
+};
+std::mutex g_seg_mutex;
+SegFork g_seg[kSegMaxDevices];
+
+vla_status seg_fork_for(SegFork** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSegMaxDevices) return VLA_ERR_CUDA;
+    SegFork& F = g_seg[dev];
+    if (!F.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&F.side[0], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&F.side[1], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&F.start, ef) != cudaSuccess || cudaEventCreateWithFlags(&F.cut, ef) != cudaSuccess ||
+            cudaEventCreateWithFlags(&F.done[0], ef) != cudaSuccess ||
+            cudaEventCreateWithFlags(&F.done[1], ef) != cudaSuccess)
+            return VLA_ERR_CUDA;
+        F.ready = true;
+    }
+    *out = &F;
+    return VLA_OK;
+}
+
+// The two-segment form (vla_seg.cuh) as a fork and join on `s`: the first
+// half starts at once on a side stream; the prefix sums and the inverse at
+// the cut run on `s`, then the second half's transition on the other side
+// stream and its run from S = 0 on `s`; `s` waits for both side streams and
+// runs the combine. Every launch is the single-CTA chunked kernel or a small
+// kernel of vla_seg.cuh.
+template <int D, typename TIn>
+vla_status launch_seg(const vla::Params& p, int BH, unsigned char* ws, const SegPlan& sp, cudaStream_t s) {
+    using LY = vla::tc::Lay<D, TIn>;
+    const int T = p.T;
+    auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    const size_t hs = (size_t)T * D;
+    auto tk = vla::vla_tc_kernel<D, TIn>;
+    auto pk = vla::seg::vla_seg_prefix_kernel<D, TIn>;
+    auto ik = vla::seg::vla_seg_invert_kernel<D>;
+    auto ck = vla::seg::vla_seg_combine_kernel<D>;
+    constexpr int p_smem = vla::seg::prefix_smem<D>();
+    constexpr int i_smem = (D * (D + 1) + 4 * D) * 4;
+    constexpr int c_smem = vla::seg::combine_smem<D>();
+    if (cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem) != cudaSuccess ||
+        cudaFuncSetAttribute(ik, cudaFuncAttributeMaxDynamicSharedMemorySize, i_smem) != cudaSuccess ||
+        cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, c_smem) != cudaSuccess)
+        return VLA_ERR_CUDA;
+    // the three runs of the chunked kernel
+    vla::Params g0 = p;  // first half, from the given state
+    g0.T = sp.L0;
+    g0.in_stride = hs;
+    g0.S_out = F(sp.G0);
+    g0.A_out = F(sp.A_s0);
+    g0.zk_out = F(sp.zk_s0);
+    vla::Params g1 = p;  // second half from S = 0, A and z^key at the cut
+    g1.T = sp.L1;
+    g1.in_stride = hs;
+    g1.q = static_cast<const TIn*>(p.q) + (size_t)sp.L0 * D;
+    g1.k = static_cast<const TIn*>(p.k) + (size_t)sp.L0 * D;
+    g1.v = static_cast<const TIn*>(p.v) + (size_t)sp.L0 * D;
+    g1.u = static_cast<const TIn*>(p.u) + (size_t)sp.L0 * D;
+    g1.o = p.o + (size_t)sp.L0 * D;
+    g1.S0 = nullptr;
+    g1.A0 = F(sp.A_cut);
+    g1.zk0 = F(sp.zk_cut);
+    g1.S_out = F(sp.G1);
+    vla::Params g2 = g1;  // the transition: second half from S = I with v = 0
+    g2.v_zero = 1;
+    g2.S0 = F(sp.ident);
+    g2.s0_shared = 1;
+    g2.o = F(sp.fphi);
+    g2.o_stride = (size_t)sp.L1 * D;
+    g2.S_out = F(sp.F1);
+    g2.A_out = F(sp.A_s2);
+    g2.zk_out = F(sp.zk_s2);
+    vla::seg::PrefixParams pp{};
+    pp.u = p.u;
+    pp.k = p.k;
+    pp.in_stride = hs;
+    pp.L = sp.L0;
+    pp.fixed_a = p.fixed_a;
+    pp.dpart = F(sp.dpart);
+    pp.zpart = F(sp.zpart);
+    vla::seg::InvertParams ip{};
+    ip.dpart = F(sp.dpart);
+    ip.zpart = F(sp.zpart);
+    ip.A0 = p.A0;
+    ip.zk0 = p.zk0;
+    ip.lambda0 = 1.0f / p.inv_lambda0;
+    ip.inv_lambda0 = p.inv_lambda0;
+    ip.fixed_a = p.fixed_a;
+    ip.A_cut = F(sp.A_cut);
+    ip.zk_cut = F(sp.zk_cut);
+    ip.ident = F(sp.ident);
+    ip.status = p.status;
+    vla::seg::CombineParams cp{};
+    cp.G0 = F(sp.G0);
+    cp.F1 = F(sp.F1);
+    cp.G1 = F(sp.G1);
+    cp.fphi = F(sp.fphi);
+    cp.o = p.o + (size_t)sp.L0 * D;
+    cp.o_stride = p.o_stride;
+    cp.L1 = sp.L1;
+    cp.S_out = p.S_out;
+    const int ntile = (sp.L1 + vla::seg::OT - 1) / vla::seg::OT;
+
+    std::lock_guard<std::mutex> lock(g_seg_mutex);
+    SegFork* fk = nullptr;
+    if (seg_fork_for(&fk) != VLA_OK) return VLA_ERR_CUDA;
+    bool ok = cudaEventRecord(fk->start, s) == cudaSuccess &&
+              cudaStreamWaitEvent(fk->side[0], fk->start, 0) == cudaSuccess;
+    if (ok) {
+        tk<<<BH, vla::tc::THREADS, LY::SMEM, fk->side[0]>>>(g0);
+        ok = cudaGetLastError() == cudaSuccess;
+    }
+    // the side stream joins `s` below whatever happened, so that nothing of
+    // this call is left running unordered with the caller's later work
+    const bool side0 = ok;
+    if (ok) {
+        pk<<<BH * vla::seg::NSPLIT, vla::seg::THREADS, p_smem, s>>>(pp);
+        ik<<<BH, vla::seg::THREADS, i_smem, s>>>(ip);
+        ok = cudaGetLastError() == cudaSuccess && cudaEventRecord(fk->cut, s) == cudaSuccess &&
+             cudaStreamWaitEvent(fk->side[1], fk->cut, 0) == cudaSuccess;
+    }
+    const bool side1 = ok;
+    if (ok) {
+        tk<<<BH, vla::tc::THREADS, LY::SMEM, fk->side[1]>>>(g2);
+        tk<<<BH, vla::tc::THREADS, LY::SMEM, s>>>(g1);
+        ok = cudaGetLastError() == cudaSuccess;
+    }
+    if (side0) ok = cudaEventRecord(fk->done[0], fk->side[0]) == cudaSuccess &&
+                    cudaStreamWaitEvent(s, fk->done[0], 0) == cudaSuccess && ok;
+    if (side1) ok = cudaEventRecord(fk->done[1], fk->side[1]) == cudaSuccess &&
+                    cudaStreamWaitEvent(s, fk->done[1], 0) == cudaSuccess && ok;
+    if (!ok) return VLA_ERR_CUDA;
+    ck<<<dim3(BH, ntile + 1), vla::seg::THREADS, c_smem, s>>>(cp);
+    return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
+}
+
+template <typename TIn>
+vla_status launch_seg_d(int d, const vla::Params& p, int BH, unsigned char* ws, const SegPlan& sp, cudaStream_t s) {
+    switch (d) {
+        case 32: return launch_seg<32, TIn>(p, BH, ws, sp, s);
+        case 64: return launch_seg<64, TIn>(p, BH, ws, sp, s);
+        case 96: return launch_seg<96, TIn>(p, BH, ws, sp, s);
+        default: return VLA_ERR_UNSUPPORTED;
+    }
 }
 
 // algo: VLA_ALGO_AUTO picks the decode kernel for short sequences; for
@@ -1292,7 +1501,24 @@ extern "C" {
 size_t vla_workspace_bytes(int B, int H, int T, int d) {
     if (B < 0 || H < 0 || T < 0) return 0;
     if (d != 32 && d != 64 && d != 96 && d != 128) return 0;
+    const long long BH = (long long)B * H;
+    if (BH > 2147483647LL) return 0;
+    // the segmented path's buffers, where VLA_ALGO_AUTO would take it (the
+    // current device's SM count; 152 when no device answers)
+    int n_sm = sm_count();
+    if (n_sm <= 0) n_sm = 152;
+    SegPlan sp;
+    if (seg_auto(BH, T, d, n_sm) && seg_plan(BH, T, d, &sp)) return sp.total;
     return kWorkspaceBytes;
+}
+
+size_t vla_workspace_bytes_ex(int B, int H, int T, int d, int algo) {
+    if (algo == VLA_ALGO_AUTO) return vla_workspace_bytes(B, H, T, d);
+    if (algo < VLA_ALGO_AUTO || algo > VLA_ALGO_SEGMENTED) return 0;
+    if (vla_workspace_bytes(B, H, T, d) == 0) return 0;
+    if (algo != VLA_ALGO_SEGMENTED) return kWorkspaceBytes;
+    SegPlan sp;
+    return seg_plan((long long)B * H, T, d, &sp) ? sp.total : 0;
 }
 
 vla_status vla_workspace_reset(void* workspace, void* stream) {
@@ -1312,6 +1538,8 @@ vla_status vla_forward_ex(const void* q, const void* k, const void* v, const voi
 }
 
 }  // extern "C"
+
+size_t vla_impl::status_bytes() { return kWorkspaceBytes; }
 
 vla_status vla_impl::forward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B,
                              int H, int T, int d, float lambda0, float eps, const float* S0, const float* A0,
@@ -1368,12 +1596,30 @@ vla_status vla_impl::forward(const void* q, const void* k, const void* v, const 
     const int algo = opts ? opts->algo : VLA_ALGO_AUTO;
     const bool fixed_a = opts && opts->fixed_a;
     if (algo != VLA_ALGO_AUTO && algo != VLA_ALGO_PER_TOKEN && algo != VLA_ALGO_CHUNKED && algo != VLA_ALGO_DECODE &&
-        algo != VLA_ALGO_CHUNKED_PAIR && algo != VLA_ALGO_CHUNKED_ROWS)
+        algo != VLA_ALGO_CHUNKED_PAIR && algo != VLA_ALGO_CHUNKED_ROWS && algo != VLA_ALGO_SEGMENTED)
         return VLA_ERR_INVALID_ARG;
-    if (algo == VLA_ALGO_CHUNKED && d > 96) return VLA_ERR_UNSUPPORTED;
+    if ((algo == VLA_ALGO_CHUNKED || algo == VLA_ALGO_SEGMENTED) && d > 96) return VLA_ERR_UNSUPPORTED;
     if (fixed_a && algo == VLA_ALGO_PER_TOKEN) return VLA_ERR_UNSUPPORTED;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the segmented path: asked for, or chosen for few heads of a long sequence
+    // when the workspace holds its buffers (with the status record alone,
+    // VLA_ALGO_AUTO keeps to the other kernels)
+    SegPlan sp;
+    bool seg = false;
+    if (algo == VLA_ALGO_SEGMENTED) {
+        if (!seg_plan(BH, T, d, &sp) || workspace_bytes < sp.total) return VLA_ERR_INVALID_ARG;
+        seg = true;
+    } else if (algo == VLA_ALGO_AUTO && T > kDecodeMaxT && seg_auto(BH, T, d, sm_count()) &&
+               seg_plan(BH, T, d, &sp) && workspace_bytes >= sp.total) {
+        seg = true;
+    }
+    if (seg) {
+        if (!aligned256(workspace)) return VLA_ERR_INVALID_ARG;
+        unsigned char* ws = static_cast<unsigned char*>(workspace);
+        return dtype == VLA_BF16 ? launch_seg_d<__nv_bfloat16>(d, p, (int)BH, ws, sp, s)
+                                 : launch_seg_d<float>(d, p, (int)BH, ws, sp, s);
+    }
     return dtype == VLA_BF16 ? launch_d<__nv_bfloat16>(d, algo, fixed_a, p, (int)BH, s)
                              : launch_d<float>(d, algo, fixed_a, p, (int)BH, s);
 }
@@ -1454,8 +1700,10 @@ vla_status vla_forward_noalloc(const void* q, const void* k, const void* v, cons
     if (B < 0 || H < 0 || T < 0) return fail(VLA_ERR_INVALID_ARG);
     if (dtype != VLA_F32 && dtype != VLA_BF16) return fail(VLA_ERR_INVALID_ARG);
     if (d != 32 && d != 64 && d != 96 && d != 128) return fail(VLA_ERR_UNSUPPORTED);
-    // the sizes' status record must fit the static array
-    if (vla_workspace_bytes(B, H, T, d) > kNoAllocScratchBytes) return fail(VLA_ERR_UNSUPPORTED);
+    // the status record, all the workspace this entry point gives the kernels,
+    // must fit the static array (with no more than that, the automatic kernel
+    // choice never takes the segmented path, which needs more)
+    if (vla_impl::status_bytes() > kNoAllocScratchBytes) return fail(VLA_ERR_UNSUPPORTED);
     void* scratch = nullptr;
     vla_status st = noalloc_scratch(&scratch);
     if (st != VLA_OK) return fail(st);

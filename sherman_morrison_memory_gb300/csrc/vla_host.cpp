@@ -120,10 +120,10 @@ bool make_plan(vla_dtype dtype, long long BH, int T, int d, int chunk_tokens, Pl
     }
     pl->es = dtype == VLA_BF16 ? 2 : 4;
     const size_t bh = (size_t)BH, dd = (size_t)d;
-    // the status record that every launch of the call shares (its size does not
-    // depend on the batch and head counts)
-    pl->status_bytes = vla_workspace_bytes(1, 1, T, d);
-    if (pl->status_bytes == 0) return false;
+    // the status record that every launch of the call shares (the launches
+    // then keep to the kernels that need no more workspace than that)
+    if (vla_workspace_bytes(1, 1, T, d) == 0) return false;
+    pl->status_bytes = vla_impl::status_bytes();
     size_t off = round_up(pl->status_bytes);
     pl->status = 0;
     pl->S = off;

@@ -17,4 +17,8 @@ vla_status forward(const void* q, const void* k, const void* v, const void* u, v
                    float* S_out, float* A_out, float* zk_out, void* workspace, size_t workspace_bytes, void* stream,
                    const vla_options* opts, size_t o_head_stride);
 
+// Bytes of workspace every kernel choice needs at any valid shape (the status
+// record): with only this much, VLA_ALGO_AUTO never takes the segmented path.
+size_t status_bytes();
+
 }  // namespace vla_impl

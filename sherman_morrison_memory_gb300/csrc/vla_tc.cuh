@@ -229,10 +229,11 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
     using L = Lay<D, TIn>;
     constexpr int E = D / 32, TW = C / NSTAGE;
     const int T = p.T, nch = (T + C - 1) / C;
-    const TIn* gq = static_cast<const TIn*>(p.q) + (size_t)bh * T * D;
-    const TIn* gk = static_cast<const TIn*>(p.k) + (size_t)bh * T * D;
-    const TIn* gu = static_cast<const TIn*>(p.u) + (size_t)bh * T * D;
-    const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * T * D;
+    const size_t hs = p.in_stride ? p.in_stride : (size_t)T * D;
+    const TIn* gq = static_cast<const TIn*>(p.q) + (size_t)bh * hs;
+    const TIn* gk = static_cast<const TIn*>(p.k) + (size_t)bh * hs;
+    const TIn* gu = static_cast<const TIn*>(p.u) + (size_t)bh * hs;
+    const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * hs;
     float zk[E];  // z^key before the chunk (identical in every staging warp)
 #pragma unroll
     for (int m = 0; m < E; ++m) zk[m] = p.zk0 ? p.zk0[(size_t)bh * D + lane + 32 * m] : 0.f;
@@ -264,7 +265,7 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
             break;
         }
         // the S rows read this chunk's v from global memory a few chunks from now
-        prefetch_v_l2<D, TIn>(gv + (size_t)c * C * D, n, sw * 32 + lane);
+        if (!p.v_zero) prefetch_v_l2<D, TIn>(gv + (size_t)c * C * D, n, sw * 32 + lane);
         if (TAPE && (c & 3) == 0 && sw == 0) {  // z^key before token 16 c (= 64 (c / 4))
             float* ck = ckpt_slot<D>(p, bh, c >> 2) + 2 * D * D;
 #pragma unroll
@@ -861,13 +862,13 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     float* gh = x.f(L::OFF_GH);
     float* gl = x.f(L::OFF_GL);
     const bool fixed = p.fixed_a != 0;
-    const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * T * D;
+    const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * (p.in_stride ? p.in_stride : (size_t)T * D);
     float* go = p.o + (size_t)bh * p.o_stride;
     bool bad = false, nonfinite = false;
 
     // S_0 = 0 unless carried in, and its lo part
     if (rw) {
-        const float* S0 = p.S0 ? p.S0 + ((size_t)bh * D + i) * D : nullptr;
+        const float* S0 = p.S0 ? p.S0 + ((p.s0_shared ? 0 : (size_t)bh * D) + i) * D : nullptr;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 16) {
             float v[16], w[16];
@@ -895,7 +896,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         const int s = c % L::NP, n = min(C, T - c * C), b = c & 1;
         float vv[C];
         typename RawIn<TIn>::type vr[C];
-        if (rw) load_v_raw<D, TIn>(gv + (size_t)c * C * D, i, n, vr);
+        if (rw) load_v_raw<D, TIn>(gv + (size_t)c * C * D, i, p.v_zero ? 0 : n, vr);  // zeros when v is taken as 0
         bad = !mbar_wait(x.b.full_p + s, (c / L::NP) & 1, x.abort, p.wait_ns) ||
               !mbar_wait(x.b.full_al + b, (c >> 1) & 1, x.abort, p.wait_ns);
         if (bar_red_or(ID_S, 128, bad || *x.abort != 0)) {
@@ -1109,8 +1110,9 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
 
 }  // namespace tc
 
-template <int D, typename TIn, bool TAPE = false>
-__global__ void __launch_bounds__(tc::THREADS, 1) vla_tc_kernel(const Params p) {
+// one head (bh) of the chunked kernel on this CTA
+template <int D, typename TIn, bool TAPE>
+__device__ __forceinline__ void tc_head(const Params& p, int bh) {
     using L = tc::Lay<D, TIn>;
     static_assert(D % 32 == 0 && D <= 96, "row warps of a team fit in warps 0-2 / 4-6");
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -1129,7 +1131,6 @@ __global__ void __launch_bounds__(tc::THREADS, 1) vla_tc_kernel(const Params p) 
     x.abort = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
     x.tmem_base = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC + 8);
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
     if (threadIdx.x == 0) {
         for (int r = 0; r < L::NRAW; ++r) mbar_init(x.b.full_r + r, 1);
         for (int s = 0; s < L::NP; ++s) {
@@ -1161,4 +1162,9 @@ __global__ void __launch_bounds__(tc::THREADS, 1) vla_tc_kernel(const Params p) 
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tc_dealloc(*x.tmem_base, L::TCOLS);
+}
+
+template <int D, typename TIn, bool TAPE = false>
+__global__ void __launch_bounds__(tc::THREADS, 1) vla_tc_kernel(const Params p) {
+    tc_head<D, TIn, TAPE>(p, blockIdx.x);
 }

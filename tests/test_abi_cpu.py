@@ -79,6 +79,27 @@ def test_workspace_bytes(lib):
         assert lib.vla_workspace_bytes(*shape) == 0
 
 
+def test_segmented_workspace_bytes(lib):
+    """The segmented path's buffers: reported for few heads of a long sequence
+    at d <= 96 (no device here: 152 SMs assumed), per algo on request."""
+    al = lambda x: (x + 255) // 256 * 256
+    B, H, T, d = 4, 8, 4096, 64
+    BH, L1 = B * H, T - T // 2 // 16 * 16
+    expect = (256 + al(BH * 16 * d * d * 4) + al(BH * 16 * d * 4) + al(BH * d * d * 4) + al(BH * d * 4)
+              + al(d * d * 4) + 5 * al(BH * d * d * 4) + 2 * al(BH * d * 4) + al(BH * L1 * d * 4))
+    # (the plan: prefix partials over 16 slices of the first half, the cut's A and z^key, the
+    #  identity, then S_L, A and z^key scratch, G_T, Pi_T, A and z^key scratch of the
+    #  transition, Pi_t phi_t / den_t)
+    assert lib.vla_workspace_bytes_ex(B, H, T, d, 6) == expect
+    assert lib.vla_workspace_bytes(B, H, T, d) == expect          # few heads, long sequence: segmented
+    assert lib.vla_workspace_bytes(B, H, 1000, d) == 256          # shorter than the automatic choice's limit
+    assert lib.vla_workspace_bytes(8, 16, 4096, 96) == 256        # more heads than fit three CTAs each
+    assert lib.vla_workspace_bytes_ex(B, H, T, d, 2) == 256
+    assert lib.vla_workspace_bytes_ex(1, 32, 65536, 128, 6) == 0  # d = 128 has no segmented path
+    assert lib.vla_workspace_bytes_ex(1, 1, 31, 64, 6) == 0       # too short to cut
+    assert lib.vla_workspace_bytes_ex(B, H, T, d, 7) == 0
+
+
 FAKE = 1 << 20  # an aligned non-null address that the validation paths never dereference
 
 
@@ -126,11 +147,13 @@ def test_status_read_rejects_null(lib):
 
 
 @pytest.mark.parametrize("algo,d,fixed,status", [
-    (6, 64, 0, 1), (-1, 64, 0, 1), (2, 128, 0, 2),
-    (1, 64, 1, 2), (2, 128, 1, 2),
+    (7, 64, 0, 1), (-1, 64, 0, 1), (2, 128, 0, 2),
+    (1, 64, 1, 2), (2, 128, 1, 2), (6, 128, 0, 2), (6, 64, 0, 1),
 ])
 def test_algo_argument_errors(lib, algo, d, fixed, status):
-    """VLA_ALGO_* outside {0, ..., 5} is an argument error; the chunked kernel
+    """VLA_ALGO_* outside {0, ..., 6} is an argument error; the chunked kernel
+    and the segmented path report d = 128 as unsupported; the segmented path
+    with a 256-byte workspace (or T < 32) is an argument error; the
     reports d = 128 as unsupported; the fixed-A variant does not run on the
     per-token kernel. All are decided before any CUDA call."""
     from sherman_morrison_memory_gb300 import _binding

@@ -14,7 +14,7 @@ import torch
 import oracle
 from parity_util import TOL, assert_close, errors, rel_heads, rel_rows, to_dev
 from sherman_morrison_memory_gb300 import (VLA_ALGO_CHUNKED, VLA_ALGO_CHUNKED_PAIR, VLA_ALGO_CHUNKED_ROWS,
-                                           VLA_ALGO_DECODE, VLA_ALGO_PER_TOKEN, VLA_ERR_NONFINITE,
+                                           VLA_ALGO_DECODE, VLA_ALGO_PER_TOKEN, VLA_ALGO_SEGMENTED, VLA_ERR_NONFINITE,
                                            VLA_ERR_TIMEOUT, VLA_OK, vla_forward, vla_get_last_device_status,
                                            vla_linear_attention_state)
 from sherman_morrison_memory_gb300 import workloads as W
@@ -112,6 +112,49 @@ def test_cluster_kernels_more_heads_than_sms(orc, dtype, algo, d):
     arrs = _inputs(4, 48, 16 * 6 + 3, d, dtype, seed=123)
     out, ref = _run(orc, arrs, dtype, algo=algo)
     assert_close(errors(out, ref), what=f"cluster kernel algo={algo}, 192 heads, d={d}, {dtype}")
+
+
+@pytest.mark.parametrize("d", [32, 64, 96])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [32, 16 * 9 + 5, 300])
+def test_segmented_path(orc, d, dtype, T):
+    """The sequence's two halves side by side (A and z^key at the cut from
+    prefix sums, the second half from S = 0 and its transition from S = I):
+    cuts inside and at the edge of 16-token chunks, ragged tails."""
+    arrs = _inputs(2, 3, T, d, dtype, seed=500 + d + T)
+    out, ref = _run(orc, arrs, dtype, algo=VLA_ALGO_SEGMENTED)
+    assert_close(errors(out, ref), what=f"segmented d={d} T={T} {dtype}")
+
+
+@pytest.mark.parametrize("d", [32, 64, 96])
+@pytest.mark.parametrize("case", ["carried", "fixed_a", "fixed_a_spd"])
+def test_segmented_path_state_and_fixed_a(orc, d, case):
+    """With a carried S0, A0 (inverted at the cut, then the prefix added) and
+    z^key0; and the fixed-A variant, where the cut's A is A0 itself."""
+    T = 16 * 11 + 7
+    q, k, v, u = _inputs(2, 2, T, d, "bf16", seed=600 + d)
+    if case == "carried":
+        warm = orc.forward(*_inputs(2, 2, 40, d, "bf16", seed=601 + d))
+        state = (warm.S, warm.A, warm.zk)
+        out, ref = _run(orc, (q, k, v, u), "bf16", state=state, algo=VLA_ALGO_SEGMENTED)
+    else:
+        state = None if case == "fixed_a" else (None, _spd(2, 2, d, seed=d), None)
+        ref = orc.forward(q, k, v, np.zeros_like(u), **_state_ref(state))
+        out = vla_forward(*to_dev([q, k, v, u], "bf16"), state=_state_dev(state), check=True, fixed_a=True,
+                          algo=VLA_ALGO_SEGMENTED)
+    assert_close(errors(out, ref), what=f"segmented d={d} {case}")
+
+
+def test_segmented_path_is_automatic_for_few_heads(orc):
+    """Few heads of a long sequence take the segmented path under
+    VLA_ALGO_AUTO: the binding sizes its workspace, and the result is the
+    oracle's."""
+    from sherman_morrison_memory_gb300 import vla_workspace_bytes
+    B, H, T, d = 2, 4, 1100, 64
+    assert vla_workspace_bytes(B, H, T, d) > 256
+    arrs = _inputs(B, H, T, d, "bf16", seed=77)
+    out, ref = _run(orc, arrs, "bf16")
+    assert_close(errors(out, ref), what="automatic segmented path")
 
 
 @pytest.mark.parametrize("d", [32, 96])
