@@ -31,6 +31,7 @@
 #include <stdint.h>
 
 #include <cmath>
+#include <algorithm>
 #include <mutex>
 
 #include "vla.h"
@@ -1361,11 +1362,17 @@ vla_status launch_seg(const vla::Params& p, int BH, unsigned char* ws, const Seg
     pp.in_stride = hs;
     pp.L = sp.L0;
     pp.fixed_a = p.fixed_a;
+    // one wave of prefix CTAs beside the first half's BH CTAs, 16 tokens at least per CTA
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pk, vla::seg::THREADS, p_smem) != cudaSuccess) return VLA_ERR_CUDA;
+    const int free_slots = std::max(1, sm_count() - BH) * std::max(occ, 1);
+    pp.nsplit = std::max(1, std::min({vla::seg::NSPLIT, free_slots / BH, sp.L0 / 16}));
     pp.dpart = F(sp.dpart);
     pp.zpart = F(sp.zpart);
     vla::seg::InvertParams ip{};
     ip.dpart = F(sp.dpart);
     ip.zpart = F(sp.zpart);
+    ip.nsplit = pp.nsplit;
     ip.A0 = p.A0;
     ip.zk0 = p.zk0;
     ip.lambda0 = 1.0f / p.inv_lambda0;
@@ -1399,7 +1406,7 @@ vla_status launch_seg(const vla::Params& p, int BH, unsigned char* ws, const Seg
     // this call is left running unordered with the caller's later work
     const bool side0 = ok;
     if (ok) {
-        pk<<<BH * vla::seg::NSPLIT, vla::seg::THREADS, p_smem, s>>>(pp);
+        pk<<<BH * pp.nsplit, vla::seg::THREADS, p_smem, s>>>(pp);
         ik<<<BH, vla::seg::THREADS, i_smem, s>>>(ip);
         ok = cudaGetLastError() == cudaSuccess && cudaEventRecord(fk->cut, s) == cudaSuccess &&
              cudaStreamWaitEvent(fk->side[1], fk->cut, 0) == cudaSuccess;
