@@ -55,6 +55,9 @@ KERNEL_FILES = {
     "vla_tc_kernel": ("vla_tc.cuh", "vla_device.cuh"),
     "vla_fused_kernel": ("vla_forward.cu", "vla_device.cuh"),
     "vla_backward_kernel": ("vla_backward.cuh", "vla_device.cuh"),
+    # the split reverse sweep (d = 128): its S side, its A side
+    "vla_backward_s_kernel": ("vla_backward_split.cuh", "vla_backward.cuh", "vla_device.cuh"),
+    "vla_backward_a_kernel": ("vla_backward_split.cuh", "vla_backward.cuh", "vla_device.cuh"),
     "vla_decode_kernel": ("vla_decode.cuh", "vla_backward.cuh", "vla_device.cuh"),
     "vla_tc2_kernel": ("vla_tc2.cuh", "vla_tc.cuh", "vla_device.cuh"),
     "vla_tc3_kernel": ("vla_tc3.cuh", "vla_tc2.cuh", "vla_tc.cuh", "vla_device.cuh"),
@@ -758,7 +761,9 @@ def run_ours_backward(args, w):
     peaks = load_peaks()
     sm_max = float(peaks.get("sm_max_mhz", FALLBACK_SM_MAX_MHZ))
     n_sm = props.multi_processor_count
-    peak_tflops = n_sm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    nominal_tflops = n_sm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    probe = measure_ffma_peak(dev, n_sm)
+    peak_tflops = probe["tflops"]
     flops = FLOP_D2["backward"] * d * d * units
     achieved = flops / (ms / 1e3) / 1e12
     esz = 2 if w.dtype == "bf16" else 4
@@ -767,8 +772,12 @@ def run_ours_backward(args, w):
     tape_bytes = 2 * units * (3 * d + 8) * 4
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
-    sha = kernel_source_sha("vla_backward_kernel")
-    traffic = ncu_traffic("vla_backward_kernel", (w.B, w.H, w.T, w.d, w.dtype))
+    # d <= 96: the taped chunked forward and the single-kernel reverse sweep;
+    # d = 128: the taped per-token forward and the two sweeps of the split form
+    kernel = "vla_backward_kernel" if d <= 96 else "vla_backward_s_kernel"
+    launches_per_step = 2 if d <= 96 else 3
+    sha = kernel_source_sha(kernel)
+    traffic = ncu_traffic(kernel, (w.B, w.H, w.T, w.d, w.dtype))
 
     e2e = None
     if not args.no_e2e:
@@ -812,15 +821,17 @@ def run_ours_backward(args, w):
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB per step), no flush"},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                          "frac": achieved / peak_tflops, "traffic": traffic,
-                         "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FP32 FMA lanes x 2 x {sm_max:.0f} MHz",
-                         "flop_per_head_token": FLOP_D2["backward"] * d * d, "kernel": "vla_backward_kernel"},
+                         "peak_basis": "measured: the FFMA probe in this run (packed FP32 FMA), of measured",
+                         "peak_nominal": nominal_tflops, "frac_of_nominal": achieved / nominal_tflops,
+                         "ffma_probe": probe,
+                         "flop_per_head_token": FLOP_D2["backward"] * d * d, "kernel": kernel},
             "fp32_roofline_pct": 100.0 * achieved / peak_tflops,
             "hbm": {"achieved_gbs": hbm_gbs, "peak_gbs": hbm_peak, "frac": hbm_gbs / hbm_peak,
                     "algorithmic_bytes_per_launch": in_bytes + out_bytes,
                     "tape_bytes_per_launch": tape_bytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
             "kernel_source_sha": sha,
         }

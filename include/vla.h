@@ -316,11 +316,13 @@ size_t vla_backward_workspace_bytes(int B, int H, int T, int d);
  * 4-byte). workspace: device memory of vla_backward_workspace_bytes() bytes,
  * 16-byte aligned, its first 16 bytes zero-filled (status record, read by
  * vla_get_last_device_status). Asynchronous on `stream`.
+ * For d <= 96 the reverse sweep is one kernel per head holding S, A and their
+ * adjoints; for d = 128, where those four d x d matrices do not fit one SM,
+ * it is the split sweep of vla_backward_split().
  * Errors: VLA_ERR_INVALID_ARG as for vla_forward() (including a workspace
- * smaller than required); VLA_ERR_UNSUPPORTED for d = 128 (the state and its
- * adjoint do not fit the kernel's shared memory) or any other d outside
- * {32, 64, 96}; VLA_ERR_NONFINITE is recorded on the device when a gradient
- * or an intermediate is NaN/Inf. */
+ * smaller than required); VLA_ERR_UNSUPPORTED for d outside
+ * {32, 64, 96, 128}; VLA_ERR_NONFINITE is recorded on the device when a
+ * gradient or an intermediate is NaN/Inf. */
 vla_status vla_backward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype,
                         int B, int H, int T, int d, float lambda0, float eps,
                         const float* S0, const float* A0, const float* zk0,
@@ -328,6 +330,23 @@ vla_status vla_backward(const void* q, const void* k, const void* v, const void*
                         float* dq, float* dk, float* dv, float* du,
                         float* dS0, float* dA0, float* dzk0,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* vla_backward() with the reverse sweep split by state, for any supported d
+ * (the path d = 128 always takes). The adjoint recursion of S (eq. 10, 11)
+ * needs nothing from the A side, and the A side (eq. 9, 10) needs only the
+ * gate's gradient g_a = (g_alpha - alpha^ (alpha^ . g_alpha)) / ||A_t k^_t||
+ * per token from it. So one kernel sweeps t = T-1 .. 0 with S and its adjoint,
+ * writing dq, dv, the S part of dk and g_a (into the workspace's tape); a
+ * second sweeps with A and its adjoint, writing du and adding the A part of
+ * dk. Same arguments, workspace size, results (to rounding) and errors as
+ * vla_backward(). */
+vla_status vla_backward_split(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype,
+                              int B, int H, int T, int d, float lambda0, float eps,
+                              const float* S0, const float* A0, const float* zk0,
+                              const float* dO, const float* dS_T, const float* dA_T, const float* dzk_T,
+                              float* dq, float* dk, float* dv, float* du,
+                              float* dS0, float* dA0, float* dzk0,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -91,6 +91,8 @@ def load_library():
         lib.vla_backward.argtypes = ([vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, cf, vp, vp, vp, vp, vp, vp, vp]
                                      + [vp] * 7 + [vp, ctypes.c_size_t, vp])
         lib.vla_backward.restype = ci
+        lib.vla_backward_split.argtypes = lib.vla_backward.argtypes
+        lib.vla_backward_split.restype = ci
         lib.vla_forward_host_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
         lib.vla_forward_host_workspace_bytes.restype = ctypes.c_size_t
         lib.vla_forward_host.argtypes = (fwd_args[:18] + [ci, vp, ctypes.c_size_t, vp, ctypes.POINTER(_Options)])
@@ -330,7 +332,7 @@ def vla_get_last_device_status(device=None, stream=None) -> Tuple[int, tuple]:
 _BW_WORKSPACES = {}
 
 
-def _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, check):
+def _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, check, split):
     """Host buffers in, host buffers out: H2D copies, the kernel, D2H copies,
     all on the current stream of the current CUDA device."""
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -338,7 +340,7 @@ def _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, che
     dq_, dk_, dv_, du_ = (to(x) for x in (q, k, v, u))
     dstate = None if state is None else tuple(to(x) for x in state)
     dgs = None if grad_state is None else tuple(to(x) for x in grad_state)
-    grads, dst = vla_backward(dq_, dk_, dv_, du_, lambda0, eps, dstate, to(grad_o), dgs, check=check)
+    grads, dst = vla_backward(dq_, dk_, dv_, du_, lambda0, eps, dstate, to(grad_o), dgs, check=check, split=split)
     pin = q.is_pinned()
     outs = []
     for i, x in enumerate(grads + dst):
@@ -350,20 +352,22 @@ def _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, che
 
 def vla_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tensor,
                  lambda0: float = 0.1, eps: float = 1e-4, state=None, grad_o=None, grad_state=None, *,
-                 out=None, stream=None, check: bool = False):
+                 out=None, stream=None, check: bool = False, split: bool = False):
     """Gradient of a scalar loss through vla_forward (reverse mode, §3.3 eq. 9-11).
 
     ``grad_o`` = dL/do [B,H,T,d] and ``grad_state`` = (dL/dS_T, dL/dA_T,
     dL/dz^key_T) (each optional, None = zero); ``state`` = the forward's
     optional initial (S0, A0, zk0). Returns ``((dq, dk, dv, du), (dS0, dA0,
-    dzk0))``, float32 on the inputs' device. d in {32, 64, 96}.
+    dzk0))``, float32 on the inputs' device. d in {32, 64, 96, 128}.
+    ``split=True`` runs the reverse sweep as two kernels, one per state
+    (vla_backward_split; the path d = 128 always takes).
     ``out`` may hold the seven result tensors (float32, contiguous, on the
     inputs' device). CPU inputs run on the current CUDA device with
     host<->device copies. ``check=True`` synchronises and raises on an
     in-kernel failure.
     """
     if q.device.type == "cpu":
-        return _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, check)
+        return _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, check, split)
     lib = load_library()
     for name, x in (("k", k), ("v", v), ("u", u)):
         if x.shape != q.shape or x.dtype != q.dtype or x.device != q.device:
@@ -408,12 +412,12 @@ def vla_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Ten
         _BW_WORKSPACES[idx] = ws
     with torch.cuda.device(dev):
         sh = _stream_handle(dev, stream)
-        st = lib.vla_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d, float(lambda0),
-                              float(eps), _ptr(S0), _ptr(A0), _ptr(zk0), _ptr(gO), _ptr(gS), _ptr(gA), _ptr(gzk),
-                              *(_ptr(x) for x in outs), _ptr(dS0), _ptr(dA0), _ptr(dzk0), _ptr(ws),
-                              ws.numel() * 4, ctypes.c_void_p(sh))
+        fn = lib.vla_backward_split if split else lib.vla_backward
+        st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d, float(lambda0), float(eps),
+                _ptr(S0), _ptr(A0), _ptr(zk0), _ptr(gO), _ptr(gS), _ptr(gA), _ptr(gzk), *(_ptr(x) for x in outs),
+                _ptr(dS0), _ptr(dA0), _ptr(dzk0), _ptr(ws), ws.numel() * 4, ctypes.c_void_p(sh))
     if st != VLA_OK:
-        raise VLAError(st, "vla_backward")
+        raise VLAError(st, "vla_backward_split" if split else "vla_backward")
     if check:
         detail = (ctypes.c_int * 3)()
         with torch.cuda.device(dev):

@@ -61,7 +61,7 @@ struct BLay {
     static constexpr int DS = DP + 4 * NW * 4;        // their sums [4]
     static constexpr int RED = DS + 4 * 4;            // [D/32 warps][2] dot partials of the k/u gradients
     static constexpr int SMEM = RED + 8 * 4;
-    static_assert(D % 32 == 0 && D <= 96, "register tiles hold 8 rows x d/32 columns of four d x d matrices");
+    static_assert(D % 32 == 0 && D <= 128, "register tiles hold 8 rows x d/32 columns of each d x d matrix");
     static_assert(SLOT_B % 16 == 0 && IN_B % 16 == 0, "cp.async chunks");
     static_assert(3 * IN_B / 16 + D / 4 + TREC / 4 <= THREADS, "one prefetch chunk per thread");
     static_assert(4 * IN_B <= TP, "forward slot fits");
@@ -232,12 +232,16 @@ __device__ __forceinline__ bool ku_grads(const unsigned char* sl, const float* P
     return isfinite(dut) && isfinite(dkt);
 }
 
-template <int D, typename TIn>
+// MODE 0: both phases (four d x d matrices in registers: d <= 96).
+// MODE 1: phase 1 alone, writing the tape, the checkpoints and the final S, A,
+// z^key to `fin`; the split reverse sweep (vla_backward_split.cuh) follows.
+template <int D, typename TIn, int MODE = 0>
 __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     vla_backward_kernel(const Params p, const float* dO, const float* dST, const float* dAT, const float* dzkT,
                         float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0, float* dzk0,
                         float* tape, float* ckpt, const float* fin) {
     using L = BLay<D, TIn>;
+    static_assert(MODE == 1 || D <= 96, "the single-kernel sweep holds four d x d matrices");
     constexpr int RW = L::RW, CL = L::CL, NW = L::NW, NB1 = L::NB1, NB2 = L::NB2;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     // kernel has already written the tape and the checkpoints, and `fin`
     // holds its final S [B*H, d, d] | A [B*H, d, d] | z^key [B*H, d].
     // ------------------------------------------------------------------
-    if (fin) {
+    if (MODE == 0 && fin) {
         const size_t BH = gridDim.x;
 #pragma unroll
         for (int r = 0; r < RW; ++r)
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < CL; ++c) zk[c] = fin[2 * BH * D * D + (size_t)bh * D + l + 32 * c];
     }
-    if (!fin) {
+    if (MODE == 1 || !fin) {
     for (int s = 0; s < NB1 - 1; ++s) {
         if (s < T) prefetch_fwd<D, TIn>(ring + s * L::SLOT_B, gu, gk, gq, gv, s);
         cp_commit();
@@ -438,6 +442,25 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     }
     }  // !fin
 
+    if constexpr (MODE == 1) {
+        // the forward's final state for the split reverse sweep
+        float* fo = const_cast<float*>(fin);
+        const size_t BH = gridDim.x;
+#pragma unroll
+        for (int r = 0; r < RW; ++r)
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                const size_t e = hdd + (size_t)(r0 + r) * D + l + 32 * c;
+                fo[e] = S[r][c];
+                fo[BH * D * D + e] = A[r][c];
+            }
+        if (w == 0)
+#pragma unroll
+            for (int c = 0; c < CL; ++c) fo[2 * BH * D * D + (size_t)bh * D + l + 32 * c] = zk[c];
+        cp_wait<0>();
+        if (bad) record_failure(p.status, BIT_NONFINITE, ROLE_A, bh, -1);
+        return;
+    } else {
     // ------------------------------------------------------------------
     // phase 2: reverse sweep
     // ------------------------------------------------------------------
@@ -722,6 +745,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < CL; ++c) dzk0[(size_t)bh * D + l + 32 * c] = gzk[c];
     if (bad) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
+    }  // MODE 0
 }
 
 }  // namespace bw

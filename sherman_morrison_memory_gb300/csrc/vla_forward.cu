@@ -1126,6 +1126,7 @@ __global__ void __launch_bounds__(LA_THREADS) la_state_kernel(const TIn* k, cons
 #include "vla_tc3.cuh"
 #include "vla_seg.cuh"
 #include "vla_backward.cuh"
+#include "vla_backward_split.cuh"
 #include "vla_decode.cuh"
 
 }  // namespace vla
@@ -1787,17 +1788,15 @@ bool bw_sizes(int B, int H, int T, int d, BwSizes* out) {
     return true;
 }
 
+// The forward pass that the reverse sweep replays, writing the tape, the
+// checkpoints and the final state to `fin`: the chunked tensor-core kernel for
+// d <= 96 (its o goes to dq, which the reverse sweep overwrites), the per-token
+// phase of the backward kernel for d = 128.
 template <int D, typename TIn>
-vla_status launch_bw(const vla::Params& p, int BH, const float* dO, const float* dST, const float* dAT,
-                     const float* dzkT, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
-                     float* dzk0, float* tape, float* ckpt, float* fin, cudaStream_t s) {
-    using BL = vla::bw::BLay<D, TIn>;
-    using TL = vla::tc::Lay<D, TIn>;
-    const float* fin_used = nullptr;
-    if (p.T > 0) {
-        // the forward on the chunked tensor-core kernel, writing the tape, the
-        // checkpoints and the final state (o goes to dq, which the reverse sweep
-        // overwrites)
+vla_status launch_bw_forward(const vla::Params& p, int BH, float* dq, float* tape, float* ckpt, float* fin,
+                             cudaStream_t s) {
+    if constexpr (D <= 96) {
+        using TL = vla::tc::Lay<D, TIn>;
         vla::Params pf = p;
         pf.o = dq;
         pf.o_stride = (size_t)p.T * D;
@@ -1810,50 +1809,78 @@ vla_status launch_bw(const vla::Params& p, int BH, const float* dO, const float*
         if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TL::SMEM) != cudaSuccess)
             return VLA_ERR_CUDA;
         fk<<<BH, vla::tc::THREADS, TL::SMEM, s>>>(pf);
-        if (cudaGetLastError() != cudaSuccess) return VLA_ERR_CUDA;
-        fin_used = fin;
+    } else {
+        using BL = vla::bw::BLay<D, TIn>;
+        auto fk = vla::bw::vla_backward_kernel<D, TIn, 1>;
+        if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BL::SMEM) != cudaSuccess)
+            return VLA_ERR_CUDA;
+        fk<<<BH, BL::THREADS, BL::SMEM, s>>>(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                             nullptr, nullptr, nullptr, nullptr, tape, ckpt, fin);
     }
-    auto kern = vla::bw::vla_backward_kernel<D, TIn>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BL::SMEM) != cudaSuccess)
+    return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
+}
+
+template <int D, typename TIn>
+vla_status launch_bw(const vla::Params& p, int BH, const float* dO, const float* dST, const float* dAT,
+                     const float* dzkT, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
+                     float* dzk0, float* tape, float* ckpt, float* fin, bool split, cudaStream_t s) {
+    if (p.T > 0) {
+        const vla_status st = launch_bw_forward<D, TIn>(p, BH, dq, tape, ckpt, fin, s);
+        if (st != VLA_OK) return st;
+    }
+    if constexpr (D <= 96) {
+        if (!split) {
+            using BL = vla::bw::BLay<D, TIn>;
+            auto kern = vla::bw::vla_backward_kernel<D, TIn>;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BL::SMEM) != cudaSuccess)
+                return VLA_ERR_CUDA;
+            kern<<<BH, BL::THREADS, BL::SMEM, s>>>(p, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt,
+                                                   p.T > 0 ? fin : nullptr);
+            return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
+        }
+    }
+    // the split sweep: the S side, then the A side (vla_backward_split.cuh)
+    using SL = vla::bw::SLay<D, TIn>;
+    using AL = vla::bw::ALay<D, TIn>;
+    auto sk = vla::bw::vla_backward_s_kernel<D, TIn>;
+    auto ak = vla::bw::vla_backward_a_kernel<D, TIn>;
+    if (cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(ak, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AL::SMEM) != cudaSuccess)
         return VLA_ERR_CUDA;
-    kern<<<BH, BL::THREADS, BL::SMEM, s>>>(p, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt,
-                                           fin_used);
+    sk<<<BH, SL::THREADS, SL::SMEM, s>>>(p, dO, dST, dzkT, dq, dk, dv, dS0, dzk0, tape, ckpt, fin);
+    ak<<<BH, AL::THREADS, AL::SMEM, s>>>(p, dAT, dk, du, dA0, tape, ckpt, fin);
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
 }
 
 template <typename TIn>
 vla_status launch_bw_d(int d, const vla::Params& p, int BH, const float* dO, const float* dST, const float* dAT,
                        const float* dzkT, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
-                       float* dzk0, float* tape, float* ckpt, float* fin, cudaStream_t s) {
+                       float* dzk0, float* tape, float* ckpt, float* fin, bool split, cudaStream_t s) {
     switch (d) {
         case 32:
-            return launch_bw<32, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin, s);
+            return launch_bw<32, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin,
+                                      split, s);
         case 64:
-            return launch_bw<64, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin, s);
+            return launch_bw<64, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin,
+                                      split, s);
         case 96:
-            return launch_bw<96, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin, s);
+            return launch_bw<96, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin,
+                                      split, s);
+        case 128:
+            return launch_bw<128, TIn>(p, BH, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0, tape, ckpt, fin,
+                                       true, s);
         default: return VLA_ERR_UNSUPPORTED;
     }
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t vla_backward_workspace_bytes(int B, int H, int T, int d) {
-    BwSizes z;
-    return bw_sizes(B, H, T, d, &z) ? z.total : 0;
-}
-
-vla_status vla_backward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B,
-                        int H, int T, int d, float lambda0, float eps, const float* S0, const float* A0,
-                        const float* zk0, const float* dO, const float* dS_T, const float* dA_T,
-                        const float* dzk_T, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
-                        float* dzk0, void* workspace, size_t workspace_bytes, void* stream) {
+vla_status backward_impl(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B, int H,
+                         int T, int d, float lambda0, float eps, const float* S0, const float* A0, const float* zk0,
+                         const float* dO, const float* dS_T, const float* dA_T, const float* dzk_T, float* dq,
+                         float* dk, float* dv, float* du, float* dS0, float* dA0, float* dzk0, void* workspace,
+                         size_t workspace_bytes, void* stream, bool split) {
     if (B < 0 || H < 0 || T < 0) return VLA_ERR_INVALID_ARG;
     if (dtype != VLA_F32 && dtype != VLA_BF16) return VLA_ERR_INVALID_ARG;
     if (d != 32 && d != 64 && d != 96 && d != 128) return VLA_ERR_UNSUPPORTED;
-    if (d == 128) return VLA_ERR_UNSUPPORTED;
     if (!(lambda0 > 0.f) || !std::isfinite(lambda0)) return VLA_ERR_INVALID_ARG;
     if (!(eps > 0.f) || !std::isfinite(eps)) return VLA_ERR_INVALID_ARG;
     BwSizes z;
@@ -1890,9 +1917,36 @@ vla_status vla_backward(const void* q, const void* k, const void* v, const void*
     float* fin = reinterpret_cast<float*>(w + kWorkspaceBytes + z.tape + z.ckpt);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == VLA_BF16 ? launch_bw_d<__nv_bfloat16>(d, p, (int)BH, dO, dS_T, dA_T, dzk_T, dq, dk, dv, du, dS0,
-                                                          dA0, dzk0, tape, ckpt, fin, s)
+                                                          dA0, dzk0, tape, ckpt, fin, split, s)
                              : launch_bw_d<float>(d, p, (int)BH, dO, dS_T, dA_T, dzk_T, dq, dk, dv, du, dS0, dA0,
-                                                  dzk0, tape, ckpt, fin, s);
+                                                  dzk0, tape, ckpt, fin, split, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t vla_backward_workspace_bytes(int B, int H, int T, int d) {
+    BwSizes z;
+    return bw_sizes(B, H, T, d, &z) ? z.total : 0;
+}
+
+vla_status vla_backward(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B,
+                        int H, int T, int d, float lambda0, float eps, const float* S0, const float* A0,
+                        const float* zk0, const float* dO, const float* dS_T, const float* dA_T,
+                        const float* dzk_T, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
+                        float* dzk0, void* workspace, size_t workspace_bytes, void* stream) {
+    return backward_impl(q, k, v, u, dtype, B, H, T, d, lambda0, eps, S0, A0, zk0, dO, dS_T, dA_T, dzk_T, dq, dk, dv,
+                         du, dS0, dA0, dzk0, workspace, workspace_bytes, stream, false);
+}
+
+vla_status vla_backward_split(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B,
+                              int H, int T, int d, float lambda0, float eps, const float* S0, const float* A0,
+                              const float* zk0, const float* dO, const float* dS_T, const float* dA_T,
+                              const float* dzk_T, float* dq, float* dk, float* dv, float* du, float* dS0,
+                              float* dA0, float* dzk0, void* workspace, size_t workspace_bytes, void* stream) {
+    return backward_impl(q, k, v, u, dtype, B, H, T, d, lambda0, eps, S0, A0, zk0, dO, dS_T, dA_T, dzk_T, dq, dk, dv,
+                         du, dS0, dA0, dzk0, workspace, workspace_bytes, stream, true);
 }
 
 }  // extern "C"

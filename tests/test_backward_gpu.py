@@ -2,9 +2,10 @@
 fp64 oracle's reverse-mode gradient.
 
 Cases span several 64-token checkpoint segments and a ragged tail, every
-supported head dimension, both input dtypes, with and without an initial
-state, each upstream seed alone, T = 0, and sampled heads of the d = 96,
-T = 4096 workload. Tolerance: 2e-3 relative (parity_util.TOL), per token
+supported head dimension (d = 128 through the split reverse sweep, which is
+also checked at d <= 96 against the oracle and the single-kernel sweep), both
+input dtypes, with and without an initial state, each upstream seed alone,
+T = 0, and sampled heads of the d = 96, T = 4096 workload. Tolerance: 2e-3 relative (parity_util.TOL), per token
 (rows of dq, dk, dv, du) and per head (dS0, dA0, dzk0), as for the forward.
 """
 import numpy as np
@@ -13,7 +14,7 @@ import torch
 
 import oracle
 from parity_util import assert_close, rel_heads, rel_rows
-from sherman_morrison_memory_gb300 import (VLA_ERR_NONFINITE, VLA_ERR_UNSUPPORTED, VLA_OK, VLAError,
+from sherman_morrison_memory_gb300 import (VLA_ERR_NONFINITE, VLA_OK, VLAError,
                                            vla_backward, vla_get_last_device_status)
 from sherman_morrison_memory_gb300 import workloads as W
 
@@ -57,11 +58,12 @@ def _f64(x):
     return None if x is None else np.asarray(x, dtype=np.float64)
 
 
-def _run(orc, arrs, dtype, gO, gst, state=None, lambda0=0.1, eps=1e-4):
+def _run(orc, arrs, dtype, gO, gst, state=None, lambda0=0.1, eps=1e-4, split=False):
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     q, k, v, u = (_dev(a, tdt) for a in arrs)
     grads, dstate = vla_backward(q, k, v, u, lambda0, eps, None if state is None else tuple(_dev(x) for x in state),
-                                 _dev(gO), None if gst is None else tuple(_dev(x) for x in gst), check=True)
+                                 _dev(gO), None if gst is None else tuple(_dev(x) for x in gst), check=True,
+                                 split=split)
     st = (None, None, None) if state is None else tuple(_f64(x) for x in state)
     gs = (None, None, None) if gst is None else tuple(_f64(x) for x in gst)
     ref = orc.backward(*(_f64(a) for a in arrs), lambda0, eps, *st, _f64(gO), *gs)
@@ -115,12 +117,13 @@ def test_long_sequence_bf16(orc):
     assert_close(_errors(*_run(orc, arrs, "bf16", gO, gst)), what="backward T=1000")
 
 
-def test_zero_tokens_passes_state_gradient_through(orc):
+@pytest.mark.parametrize("d,split", [(64, False), (64, True), (128, False)])
+def test_zero_tokens_passes_state_gradient_through(orc, d, split):
     """T = 0: the forward is the identity on the state, so dState0 = dState_T."""
-    B, H, d = 1, 3, 64
+    B, H = 1, 3
     arrs = tuple(np.zeros((B, H, 0, d), np.float32) for _ in range(4))
     _, gst = _seeds(B, H, 0, d, seed=8, with_o=False)
-    grads, dstate, ref = _run(orc, arrs, "f32", None, gst)
+    grads, dstate, ref = _run(orc, arrs, "f32", None, gst, split=split)
     assert all(g.shape == (B, H, 0, d) for g in grads)
     for got, want in zip(dstate, gst):
         np.testing.assert_array_equal(got.cpu().numpy(), want)
@@ -173,8 +176,62 @@ def test_nonfinite_then_clean_call_succeeds(orc):
     assert_close(_errors(*_run(orc, arrs, "f32", gO, None)), what="backward after a non-finite call")
 
 
-def test_d128_is_unsupported():
-    x = torch.zeros((1, 1, 4, 128), device="cuda")
+@pytest.mark.parametrize("T", [1, 37, 129])
+def test_d128_small_f32(orc, T):
+    """d = 128: the per-token forward with tape, then the split reverse sweep."""
+    B, H, d = 1, 2, 128
+    arrs = _inputs(B, H, T, d, "f32", seed=20 + T)
+    gO, gst = _seeds(B, H, T, d, seed=20 + T)
+    assert_close(_errors(*_run(orc, arrs, "f32", gO, gst)), what=f"backward d=128 T={T}")
+
+
+def test_d128_bf16_with_initial_state(orc):
+    B, H, T, d = 2, 2, 150, 128
+    arrs = _inputs(B, H, T, d, "bf16", seed=24)
+    gO, gst = _seeds(B, H, T, d, seed=24)
+    state = _warm_state(orc, B, H, d, seed=25)
+    assert_close(_errors(*_run(orc, arrs, "bf16", gO, gst, state=state)), what="backward d=128 bf16 state")
+
+
+def test_d128_long_sequence_bf16(orc):
+    """Many 64-token checkpoint segments at d = 128."""
+    B, H, T, d = 1, 2, 1000, 128
+    arrs = _inputs(B, H, T, d, "bf16", seed=26)
+    gO, gst = _seeds(B, H, T, d, seed=26)
+    assert_close(_errors(*_run(orc, arrs, "bf16", gO, gst)), what="backward d=128 T=1000")
+
+
+@pytest.mark.parametrize("d", [32, 64, 96])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_split_sweep(orc, d, dtype):
+    """The split reverse sweep (S side, then A side) at the head dimensions the
+    single-kernel sweep also covers: both match the oracle, and each other."""
+    B, H, T = 1, 3, 129
+    arrs = _inputs(B, H, T, d, dtype, seed=30 + d)
+    gO, gst = _seeds(B, H, T, d, seed=30 + d)
+    state = _warm_state(orc, B, H, d, seed=31 + d)
+    g_split, s_split, ref = _run(orc, arrs, dtype, gO, gst, state=state, split=True)
+    assert_close(_errors(g_split, s_split, ref), what=f"split backward d={d} {dtype}")
+    g_one, s_one, _ = _run(orc, arrs, dtype, gO, gst, state=state)
+    for a, b in zip(g_split, g_one):
+        assert rel_rows(a.cpu().numpy(), b.cpu().numpy().astype(np.float64)) <= 2e-3
+    for a, b in zip(s_split, s_one):
+        assert rel_heads(a.cpu().numpy(), b.cpu().numpy().astype(np.float64)) <= 2e-3
+
+
+def test_split_single_upstream_seeds(orc):
+    """Only dL/do, then only the state seeds, through the split sweep."""
+    B, H, T, d = 1, 2, 70, 128
+    arrs = _inputs(B, H, T, d, "f32", seed=40)
+    for with_o in (True, False):
+        gO, gst = _seeds(B, H, T, d, seed=40, with_o=with_o, with_state=not with_o)
+        assert_close(_errors(*_run(orc, arrs, "f32", gO, gst)), what=f"backward d=128 seeds o={with_o}")
+
+
+def test_split_nonfinite_input_is_reported():
+    arrs = [np.array(a) for a in _inputs(1, 1, 40, 128, "f32", seed=41)]
+    arrs[1][0, 0, 9, 5] = np.nan
+    gO, _ = _seeds(1, 1, 40, 128, seed=41, with_state=False)
     with pytest.raises(VLAError) as ei:
-        vla_backward(x, x, x, x, 0.1, 1e-4, None, x)
-    assert ei.value.status == VLA_ERR_UNSUPPORTED
+        vla_backward(*(_dev(a) for a in arrs), 0.1, 1e-4, None, _dev(gO), check=True)
+    assert ei.value.status == VLA_ERR_NONFINITE

@@ -157,6 +157,31 @@ def test_segmented_path_is_automatic_for_few_heads(orc):
     assert_close(errors(out, ref), what="automatic segmented path")
 
 
+@pytest.mark.parametrize("noise", [0.1, 0.01])
+def test_segmented_path_ill_conditioned(orc, noise):
+    """u concentrated on 8 directions plus small noise, so that the penalty
+    M at the cut is ill-conditioned (8 eigenvalues near L/8, the rest near
+    lambda0 + L noise^2 / 8). The cut's A comes from an fp32 inverse of M
+    there; the result must stay within the tolerance, as the sequential
+    chunked kernel's does on the same inputs."""
+    B, H, T, d = 1, 2, 2048, 64
+    q, k, v, _ = _inputs(B, H, T, d, "f32", seed=91)
+    rng = np.random.default_rng(92)
+    pool = rng.standard_normal((B, H, 8, d)).astype(np.float32)
+    idx = rng.integers(0, 8, size=(B, H, T))
+    u = (np.take_along_axis(pool, idx[..., None], axis=2)
+         + noise * rng.standard_normal((B, H, T, d))).astype(np.float32)
+    L = T // 2
+    uh = u[0, 0, :L].astype(np.float64)
+    uh /= np.linalg.norm(uh, axis=1, keepdims=True)
+    cond = np.linalg.cond(0.1 * np.eye(d) + uh.T @ uh)
+    seg, ref = _run(orc, (q, k, v, u), "f32", algo=VLA_ALGO_SEGMENTED)
+    seq, _ = _run(orc, (q, k, v, u), "f32", algo=VLA_ALGO_CHUNKED)
+    e_seq = errors(seq, ref)
+    assert_close(errors(seg, ref), what=f"segmented, cond(M_L) = {cond:.3g} (sequential kernel: "
+                 f"o {e_seq['o']:.2e}, A {e_seq['A']:.2e})")
+
+
 @pytest.mark.parametrize("d", [32, 96])
 def test_zero_tokens_returns_initial_state(orc, d):
     arrs = _inputs(1, 2, 0, d, "f32", seed=1)
