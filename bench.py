@@ -68,22 +68,22 @@ KERNEL_FILES = {
 # was taken on (B, H, T, d, input dtype) and while that kernel's own sources
 # hash to source_sha; otherwise reported as null.
 NCU_TRAFFIC = {
-    "vla_tc_kernel": {"source_sha": "14ab9db29a5b1786", "workload": (8, 16, 4096, 96, "bf16"),
-                      "bytes_per_launch": 402762240 + 176187136},
+    "vla_tc_kernel": {"source_sha": "c26cfcf131e87f0a", "workload": (8, 16, 4096, 96, "bf16"),
+                      "bytes_per_launch": 403085056 + 176358912},
     # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
-    "vla_tc2_kernel": {"source_sha": "0f583c6ba916b9fc", "workload": (1, 32, 65536, 128, "bf16"),
-                       "bytes_per_launch": 8 * (268582912 + 108756224 - 4227072) + 4227072},
-    # the same T = 8192 capture scheme for the row-split cluster kernel
-    "vla_tc3_kernel": {"source_sha": "b553fa72074aaf94", "workload": (1, 32, 65536, 128, "bf16"),
-                       "bytes_per_launch": 8 * (268692736 + 108980224 - 4227072) + 4227072},
+    "vla_tc3_kernel": {"source_sha": "e06afcbbcbab820a", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (268755968 + 108874240 - 4227072) + 4227072},
     # the reverse sweep (the step's dominant kernel, after the taped chunked forward), from a capture of
     # the same workload at B=2 (32 heads; a full step holds about 2.8 GB on the device) scaled by 4:
     # every byte it moves is per head-token or per head
-    "vla_backward_kernel": {"source_sha": "59d6bc9c070fdaa3", "workload": (8, 16, 4096, 96, "bf16"),
-                            "bytes_per_launch": 4 * (435487488 + 177234688)},
-    "vla_decode_kernel": {"source_sha": "25e3bf6ab2367048", "workload": (128, 16, 1, 96, "bf16"),
-                          "bytes_per_launch": 153395456 + 98124544},
+    "vla_backward_kernel": {"source_sha": "8018c1c77adde7f7", "workload": (8, 16, 4096, 96, "bf16"),
+                            "bytes_per_launch": 4 * (437382144 + 177710592)},
+    # the S side of the split reverse sweep (d = 128), on the long-context workload cut to 4096 tokens
+    "vla_backward_s_kernel": {"source_sha": "6e16ee37bd9eeff9", "workload": (1, 32, 4096, 128, "bf16"),
+                              "bytes_per_launch": 478849792 + 237614592},
+    "vla_decode_kernel": {"source_sha": "21f293567c108430", "workload": (128, 16, 1, 96, "bf16"),
+                          "bytes_per_launch": 153430784 + 98220800},
 }
 
 

@@ -154,7 +154,7 @@ struct Params {
     // parts of the sequence); zero-filled fields give the plain layout
     size_t in_stride;  // elements from one head's q, k, v, u rows to the next (0: T * d)
     int s0_shared;     // nonzero: every head starts from the same S0 (one d x d matrix)
-    int v_zero;        // nonzero: v is taken as zero and not read
+    int v_shared;      // nonzero: every head reads the same v rows (at p.v)
 };
 
 // Per-token clock stamps of head 0 for pipeline analysis (-DVLA_TRACE builds only).
@@ -1236,16 +1236,30 @@ int sm_count() {
 // the prefix partial sums, the state at the cut (A, z^key), the identity the
 // transition starts from, the three groups' final states (the first half's
 // S = S_L; the second half's G_T and Pi_T; scratch for the state outputs the
-// combine does not read) and Pi_t phi_t / den_t for the second half's tokens.
+// combine does not read), Pi_t phi_t / den_t for the second half's tokens and
+// the zero rows that the transition reads as its v.
 struct SegPlan {
     int L0 = 0, L1 = 0;
     size_t dpart = 0, zpart = 0, A_cut = 0, zk_cut = 0, ident = 0, G0 = 0, A_s0 = 0, zk_s0 = 0, G1 = 0, F1 = 0,
-           A_s2 = 0, zk_s2 = 0, fphi = 0, total = 0;
+           A_s2 = 0, zk_s2 = 0, fphi = 0, vzero = 0, total = 0;
 };
+
+// Tokens of the first segment. The second half's two runs start only after
+// the prefix sums and the inverse at the cut, the first half at once, so the
+// cut sits past T / 2 by about (prefix + inverse time) / (2 x the chunked
+// kernel's time per token): delta = alpha_d T + gamma_d tokens, fitted to the
+// measured best cut on GB300 (T = 4096 and 16384; d = 64: 0.545 T and 0.52 T,
+// d = 96: 0.56 T at T = 4096). A multiple of 16, one chunk at least each side.
+int seg_cut(int T, int d) {
+    const double alpha = d == 96 ? 0.0218 : d == 64 ? 0.0117 : 0.003;
+    const double gamma = d == 96 ? 157.0 : d == 64 ? 136.0 : 100.0;
+    const int L0 = (int)(0.5 * T + alpha * T + gamma) / 16 * 16;
+    return std::max(16, std::min(L0, (T - 1) / 16 * 16));
+}
 
 bool seg_plan(long long BH, int T, int d, SegPlan* sp) {
     if (BH <= 0 || T < 32 || (d != 32 && d != 64 && d != 96)) return false;
-    sp->L0 = T / 2 / 16 * 16;
+    sp->L0 = seg_cut(T, d);
     sp->L1 = T - sp->L0;
     const size_t bh = (size_t)BH, dd = (size_t)d * d, dv = (size_t)d;
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -1268,6 +1282,7 @@ bool seg_plan(long long BH, int T, int d, SegPlan* sp) {
     sp->A_s2 = take(bh * dd);
     sp->zk_s2 = take(bh * dv);
     sp->fphi = take(bh * (size_t)sp->L1 * dv);
+    sp->vzero = take((size_t)sp->L1 * dv);
     sp->total = off;
     return true;
 }
@@ -1348,8 +1363,9 @@ vla_status launch_seg(const vla::Params& p, int BH, unsigned char* ws, const Seg
     g1.A0 = F(sp.A_cut);
     g1.zk0 = F(sp.zk_cut);
     g1.S_out = F(sp.G1);
-    vla::Params g2 = g1;  // the transition: second half from S = I with v = 0
-    g2.v_zero = 1;
+    vla::Params g2 = g1;  // the transition: second half from S = I with v = 0 (zero rows shared by every head)
+    g2.v = ws + sp.vzero;
+    g2.v_shared = 1;
     g2.S0 = F(sp.ident);
     g2.s0_shared = 1;
     g2.o = F(sp.fphi);
@@ -1398,7 +1414,8 @@ vla_status launch_seg(const vla::Params& p, int BH, unsigned char* ws, const Seg
     SegFork* fk = nullptr;
     if (seg_fork_for(&fk) != VLA_OK) return VLA_ERR_CUDA;
     bool ok = cudaEventRecord(fk->start, s) == cudaSuccess &&
-              cudaStreamWaitEvent(fk->side[0], fk->start, 0) == cudaSuccess;
+              cudaStreamWaitEvent(fk->side[0], fk->start, 0) == cudaSuccess &&
+              cudaMemsetAsync(ws + sp.vzero, 0, (size_t)sp.L1 * D * sizeof(TIn), s) == cudaSuccess;
     if (ok) {
         tk<<<BH, vla::tc::THREADS, LY::SMEM, fk->side[0]>>>(g0);
         ok = cudaGetLastError() == cudaSuccess;

@@ -233,7 +233,7 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
     const TIn* gq = static_cast<const TIn*>(p.q) + (size_t)bh * hs;
     const TIn* gk = static_cast<const TIn*>(p.k) + (size_t)bh * hs;
     const TIn* gu = static_cast<const TIn*>(p.u) + (size_t)bh * hs;
-    const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * hs;
+    const TIn* gv = static_cast<const TIn*>(p.v) + (p.v_shared ? 0 : (size_t)bh * hs);
     float zk[E];  // z^key before the chunk (identical in every staging warp)
 #pragma unroll
     for (int m = 0; m < E; ++m) zk[m] = p.zk0 ? p.zk0[(size_t)bh * D + lane + 32 * m] : 0.f;
@@ -265,7 +265,7 @@ __device__ __forceinline__ void tc_stage(const Params& p, const Ctx<D, TIn>& x, 
             break;
         }
         // the S rows read this chunk's v from global memory a few chunks from now
-        if (!p.v_zero) prefetch_v_l2<D, TIn>(gv + (size_t)c * C * D, n, sw * 32 + lane);
+        prefetch_v_l2<D, TIn>(gv + (size_t)c * C * D, n, sw * 32 + lane);
         if (TAPE && (c & 3) == 0 && sw == 0) {  // z^key before token 16 c (= 64 (c / 4))
             float* ck = ckpt_slot<D>(p, bh, c >> 2) + 2 * D * D;
 #pragma unroll
@@ -862,7 +862,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     float* gh = x.f(L::OFF_GH);
     float* gl = x.f(L::OFF_GL);
     const bool fixed = p.fixed_a != 0;
-    const TIn* gv = static_cast<const TIn*>(p.v) + (size_t)bh * (p.in_stride ? p.in_stride : (size_t)T * D);
+    const TIn* gv = static_cast<const TIn*>(p.v) + (p.v_shared ? 0 : (size_t)bh * (p.in_stride ? p.in_stride : (size_t)T * D));
     float* go = p.o + (size_t)bh * p.o_stride;
     bool bad = false, nonfinite = false;
 
@@ -896,7 +896,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         const int s = c % L::NP, n = min(C, T - c * C), b = c & 1;
         float vv[C];
         typename RawIn<TIn>::type vr[C];
-        if (rw) load_v_raw<D, TIn>(gv + (size_t)c * C * D, i, p.v_zero ? 0 : n, vr);  // zeros when v is taken as 0
+        if (rw) load_v_raw<D, TIn>(gv + (size_t)c * C * D, i, n, vr);
         bad = !mbar_wait(x.b.full_p + s, (c / L::NP) & 1, x.abort, p.wait_ns) ||
               !mbar_wait(x.b.full_al + b, (c >> 1) & 1, x.abort, p.wait_ns);
         if (bar_red_or(ID_S, 128, bad || *x.abort != 0)) {

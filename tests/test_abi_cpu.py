@@ -84,12 +84,13 @@ def test_segmented_workspace_bytes(lib):
     at d <= 96 (no device here: 152 SMs assumed), per algo on request."""
     al = lambda x: (x + 255) // 256 * 256
     B, H, T, d = 4, 8, 4096, 64
-    BH, L1 = B * H, T - T // 2 // 16 * 16
+    # the cut: past T / 2 by 0.0117 T + 136 tokens at d = 64, rounded down to 16 tokens
+    BH, L1 = B * H, T - int(0.5 * T + 0.0117 * T + 136) // 16 * 16
     expect = (256 + al(BH * 16 * d * d * 4) + al(BH * 16 * d * 4) + al(BH * d * d * 4) + al(BH * d * 4)
-              + al(d * d * 4) + 5 * al(BH * d * d * 4) + 2 * al(BH * d * 4) + al(BH * L1 * d * 4))
+              + al(d * d * 4) + 5 * al(BH * d * d * 4) + 2 * al(BH * d * 4) + al(BH * L1 * d * 4) + al(L1 * d * 4))
     # (the plan: prefix partials over 16 slices of the first half, the cut's A and z^key, the
     #  identity, then S_L, A and z^key scratch, G_T, Pi_T, A and z^key scratch of the
-    #  transition, Pi_t phi_t / den_t)
+    #  transition, Pi_t phi_t / den_t, the transition's zero v rows)
     assert lib.vla_workspace_bytes_ex(B, H, T, d, 6) == expect
     assert lib.vla_workspace_bytes(B, H, T, d) == expect          # few heads, long sequence: segmented
     assert lib.vla_workspace_bytes(B, H, 1000, d) == 256          # shorter than the automatic choice's limit
