@@ -9,10 +9,13 @@
 //            Guu = U^ Z', Guk = U^ W                 (C x C Gram matrices)
 //            I + Guu = L D L^T (eliminated together with Guk: X = L^-1 Guk)
 //            per row i:  z_i = Z'_i L^-T  (the Sherman-Morrison vectors of
-//            eq. 9 for the chunk's tokens), m_i = z_i D^-1 L^-1,
+//            eq. 9 for the chunk's tokens), n_i = z_i D^-1/2,
 //            a_t[i] = w_t[i] - sum_{s<=t} z_s[i] X[s][t] / delta_s
 //            (a_t = A_t k^_t, the unnormalised gate of eq. 10)
-//            A_{c+1} = A_c - M Z'^T                  (tensor cores, rank C)
+//            A_{c+1} = A_c - N N^T                   (tensor cores, rank C)
+//            (Woodbury: Z' (L D L^T)^-1 Z'^T = N N^T, so the update is
+//            symmetric by construction and A keeps no antisymmetric rounding
+//            error, which the downdates would not damp while A shrinks)
 //   S-pass   S_c K^T, S_c Phi^T                      (tensor cores)
 //            Lk[t][s] = k^_t . a_s, Lq[t][s] = phi_t . a_s, ||a_s||^2
 //            per row i: e_t = v_t - S_c k^_t - sum_{s<t} (k^_t . alpha^_s) e_s,
@@ -40,7 +43,7 @@ constexpr int C = 16;           // tokens per chunk
 constexpr int NSTAGE = 4;        // staging warps
 constexpr int THREADS = 32 * (8 + NSTAGE);
 constexpr int ID_A = 1, ID_S = 2, ID_ST = 3;  // named barriers of the A team, S team, staging warps
-constexpr int ID_M = 9;  // A-team rows (arrive) -> warp 3 (sync): -M of a chunk is in place
+constexpr int ID_M = 9;  // A-team rows (arrive) -> warp 3 (sync): -N, N of a chunk are in place
 constexpr int ID_G = 8;  // S-team warps 6 and 7: the chunk's gate rows are in place
 
 // true on one lane of a converged warp (elect.sync). Issuing tcgen05 work
@@ -91,9 +94,9 @@ struct Lay {
     static constexpr size_t OFF_SCR = al(OFF_RAW + (size_t)NRAW * 3 * RAW_T);
     static constexpr size_t OFF_ZP = al(OFF_SCR + (size_t)3 * C * SCR_STRIDE * 4);   // staging phi(k) sums
     static constexpr size_t OFF_XR = al(OFF_ZP + (size_t)NSTAGE * D * 4);
-    static constexpr size_t OFF_PH = al(OFF_XR + (size_t)2 * C * XS * 4);  // -M hi/lo, 128 x C
+    static constexpr size_t OFF_PH = al(OFF_XR + (size_t)2 * C * XS * 4);  // -N hi/lo, 128 x C
     static constexpr size_t OFF_PL = OFF_PH + 128 * C * 4;
-    static constexpr size_t OFF_ZH = OFF_PL + 128 * C * 4;                  // Z' hi/lo, D x C
+    static constexpr size_t OFF_ZH = OFF_PL + 128 * C * 4;                  // N hi/lo, D x C
     static constexpr size_t OFF_ZL = OFF_ZH + (size_t)D * C * 4;
     static constexpr size_t OFF_EH = OFF_ZL + (size_t)D * C * 4;            // E hi/lo, 128 x C
     static constexpr size_t OFF_EL = OFF_EH + 128 * C * 4;
@@ -108,9 +111,10 @@ struct Lay {
     static constexpr size_t OFF_XP = OFF_YP + (size_t)2 * C * D * 4;
     static constexpr size_t OFF_SM = OFF_XP + (size_t)2 * C * GSTR * 4;    // small matrices
     // small matrices: Guu, Guk (two partial sums each, over the halves of
-    // D), L, L^T, Lk^T, Lq (two partials each), 1/delta, ||a||^2
+    // D), 1/sqrt(delta) (one row), L^T, Lk^T, Lq (two partials each),
+    // 1/delta, ||a||^2
     static constexpr int MS = C * GSTR;
-    static constexpr int SM_GUU = 0, SM_GUK = 2 * MS, SM_LM = 4 * MS, SM_LMT = 5 * MS, SM_LKT = 6 * MS,
+    static constexpr int SM_GUU = 0, SM_GUK = 2 * MS, SM_RS = 4 * MS, SM_LMT = 5 * MS, SM_LKT = 6 * MS,
                          SM_LQ = 8 * MS, SM_RD = 10 * MS, SM_LAA = SM_RD + C;
     static constexpr size_t SMEM = al(OFF_SM + (size_t)(10 * MS + 2 * C) * 4);
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -608,7 +612,7 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
         }
         tc_wait_st();
     }
-    // rows D..127 of the -M operand stay zero
+    // rows D..127 of the -N operand stay zero
     for (int e = ta; e < (128 - D) * C; e += 128) {
         ph[cm_off(D + e / C, e % C, C)] = 0.f;
         pl[cm_off(D + e / C, e % C, C)] = 0.f;
@@ -672,10 +676,6 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 xr[(C + t) * XS + i] = v1[t];
                 wp[t * D + i] = v1[t];
             }
-            if (!fixed) {
-                put_row16(zh, i, v0, false);
-                put_row16(zl, i, v0, true);
-            }
         }
         named_bar(ID_A, 128);
         if (!fixed) {
@@ -703,12 +703,15 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             float col[C];
 #pragma unroll
             for (int r = 0; r < C; ++r) col[r] = src[r * L::GSTR + j] + ((mcol && r == j) ? 1.f : 0.f);
-            float myrd = 0.f;
+            float myrd = 0.f, mydl = 1.f;
 #pragma unroll 16
             for (int t = 0; t < C; ++t) {
                 const float piv = __shfl_sync(0xffffffffu, col[t], t);
                 const float rdt = rcp_approx(piv);
-                if (lane == t) myrd = rdt;
+                if (lane == t) {
+                    myrd = rdt;
+                    mydl = piv;  // delta_t; its 1/sqrt is taken after the elimination, off its chain
+                }
                 if (TAPE && lane == t) mypiv = piv;
                 if (!(piv > 0.f) || !isfinite(rdt)) nonfinite = true;
                 // eliminate below pivot t in the columns not yet factored (M
@@ -725,12 +728,10 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
             }
             if (mcol) {
                 sm[L::SM_RD + j] = myrd;
+                sm[L::SM_RS + j] = rsqrtf(mydl);
 #pragma unroll
-                for (int r = 0; r < C; ++r) {
-                    const float l = r > j ? col[r] * myrd : 0.f;  // L[r][j] below the unit diagonal
-                    sm[L::SM_LM + r * L::GSTR + j] = l;
-                    sm[L::SM_LMT + j * L::GSTR + r] = l;
-                }
+                for (int r = 0; r < C; ++r)  // L[r][j] below the unit diagonal, stored transposed
+                    sm[L::SM_LMT + j * L::GSTR + r] = r > j ? col[r] * myrd : 0.f;
             } else {
                 float* xp = x.f(L::OFF_XP) + (size_t)b * C * L::GSTR;  // X for the S team's gate
 #pragma unroll
@@ -759,30 +760,28 @@ __device__ void tc_a_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 for (int t = 0; t < C; ++t)
                     if (t < n) tape_rec<D>(p, bh, c * C + t)[i] = y[t];
             }
+            // row i of N = Z D^-1/2: the rank-C update is A_c - N N^T (Woodbury
+            // with I + Guu = L D L^T), symmetric by construction
+            float nv[C];
+            ld_row16(sm + L::SM_RS, lr);
+#pragma unroll
+            for (int t = 0; t < C; ++t) nv[t] = y[t] * lr[t];
             ld_row16(sm + L::SM_RD, lr);
 #pragma unroll
             for (int t = 0; t < C; ++t) {
                 y[t] *= lr[t];
                 yp[t * D + i] = y[t];  // z_t / delta_t for the S team's gate
             }
-            // m_i = (z_i D^-1) L^-1 (backward substitution); the operand is -m_i
-            float mv[C];
+            put_row16(zh, i, nv, false);
+            put_row16(zl, i, nv, true);
 #pragma unroll
-            for (int t = 0; t < C; ++t) mv[t] = y[t];
-#pragma unroll
-            for (int r = C - 1; r >= 1; --r) {
-                ld_row16(sm + L::SM_LM + r * L::GSTR, lr);  // L[r][t], t < r
-#pragma unroll
-                for (int t = 0; t < r; ++t) mv[t] = fmaf(-lr[t], mv[r], mv[t]);
-            }
-#pragma unroll
-            for (int t = 0; t < C; ++t) mv[t] = -mv[t];
-            put_row16(ph, i, mv, false);
-            put_row16(pl, i, mv, true);
+            for (int t = 0; t < C; ++t) nv[t] = -nv[t];
+            put_row16(ph, i, nv, false);
+            put_row16(pl, i, nv, true);
         }
         fence_proxy_async_smem();
-        // A_{c+1} = A_c - M Z'^T, issued by warp 3 (not a row warp for d <= 96) once
-        // the rows have -M and z / delta in place; then the chunk's hand-over
+        // A_{c+1} = A_c - N N^T, issued by warp 3 (not a row warp for d <= 96) once
+        // the rows have -N, N and z / delta in place; then the chunk's hand-over
         // buffers go to the S team, which forms the gate (eq. 10) off this chain
         if (warp < 3)
             bar_arrive(ID_M, 128);

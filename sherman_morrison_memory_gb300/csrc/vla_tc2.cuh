@@ -10,7 +10,7 @@
 //   CTA rank 0 (A-pass)  stages u, k; A and its tf32 lo part in its own tensor
 //                        memory; per chunk [A u | A k] on the tensor cores,
 //                        the Gram matrices, the LDL^T of I + U^ A U^^T, the
-//                        state update A -= M Z'^T (eq. 9) and the gate rows
+//                        state update A -= N N^T (eq. 9) and the gate rows
 //                        a_t = A_t k^_t (eq. 10), which it sends to rank 1
 //   CTA rank 1 (S-pass)  stages q, k; S and its lo part in its own tensor
 //                        memory; per chunk [S k | S phi] on the tensor cores,
@@ -182,14 +182,14 @@ struct Lay2 {
     static constexpr size_t OFF_GL = OFF_GH + 2 * (size_t)MB_G;                      // a^T lo [2][D x C]
     static constexpr size_t OFF_LAA = OFF_GL + 2 * (size_t)MB_G;                     // ||a||^2 [2][C]
     static constexpr size_t OFF_SM = al(OFF_LAA + 2 * (size_t)MB_LAA);
-    // small matrices, rank 0: Guu, Guk (two partials each), L, L^T, X^T, 1/delta;
+    // small matrices, rank 0: Guu, Guk (two partials each), 1/sqrt(delta), L^T, X^T, 1/delta;
     // rank 1: Lk^T, Lq (two partials each)
     static constexpr int MS = C * GSTR;
-    static constexpr int SM_GUU = 0, SM_GUK = 2 * MS, SM_LM = 4 * MS, SM_LMT = 5 * MS, SM_XGT = 6 * MS,
+    static constexpr int SM_GUU = 0, SM_GUK = 2 * MS, SM_RS = 4 * MS, SM_LMT = 5 * MS, SM_XGT = 6 * MS,
                          SM_RD = 7 * MS, SM_LKT = 0, SM_LQ = 2 * MS;
     static constexpr size_t OFF_U = al(OFF_SM + (size_t)(7 * MS + C) * 4);
-    // role-specific region: rank 0 xr (z' | w rows) [2C x XS], -M hi/lo
-    // [128 x C], Z' hi/lo [D x C]; rank 1 E' hi/lo [128 x C], staging phi(k) sums
+    // role-specific region: rank 0 xr (z' | w rows) [2C x XS], -N hi/lo
+    // [128 x C], N hi/lo [D x C]; rank 1 E' hi/lo [128 x C], staging phi(k) sums
     static constexpr size_t OFF_XR = OFF_U;
     static constexpr size_t OFF_PH = al(OFF_XR + (size_t)2 * C * XS * 4);
     static constexpr size_t OFF_PL = OFF_PH + 128 * C * 4;
@@ -462,7 +462,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         }
         tc_wait_st();
     }
-    // rows D..127 of the -M operand stay zero
+    // rows D..127 of the -N operand stay zero
     for (int e = ta; e < (128 - D) * C; e += NT_A) {
         ph[cm_off(D + e / C, e % C, C)] = 0.f;
         pl[cm_off(D + e / C, e % C, C)] = 0.f;
@@ -513,10 +513,6 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
                 xr[t * XS + i] = v0[t];
                 xr[(C + t) * XS + i] = v1[t];
             }
-            if (!fixed) {
-                tc::put_row16(zh, i, v0, false);
-                tc::put_row16(zl, i, v0, true);
-            }
         }
         named_bar(ID_T, NT_A);
         TC2_STAMP(p, 4, 2, c, nch);
@@ -545,12 +541,15 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             float col[C];
 #pragma unroll
             for (int r = 0; r < C; ++r) col[r] = src[r * L::GSTR + j] + ((mcol && r == j) ? 1.f : 0.f);
-            float myrd = 0.f;
+            float myrd = 0.f, mydl = 1.f;
 #pragma unroll 16
             for (int t = 0; t < C; ++t) {
                 const float piv = __shfl_sync(0xffffffffu, col[t], t);
                 const float rdt = tc::rcp_approx(piv);
-                if (lane == t) myrd = rdt;
+                if (lane == t) {
+                    myrd = rdt;
+                    mydl = piv;  // delta_t; its 1/sqrt is taken after the elimination, off its chain
+                }
                 if (!(piv > 0.f) || !isfinite(rdt)) nonfinite = true;
                 const bool live = !mcol || lane > t;
                 const float ct = col[t] * rdt;
@@ -563,12 +562,10 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             }
             if (mcol) {
                 sm[L::SM_RD + j] = myrd;
+                sm[L::SM_RS + j] = rsqrtf(mydl);
 #pragma unroll
-                for (int r = 0; r < C; ++r) {
-                    const float l = r > j ? col[r] * myrd : 0.f;  // L[r][j] below the unit diagonal
-                    sm[L::SM_LM + r * L::GSTR + j] = l;
-                    sm[L::SM_LMT + j * L::GSTR + r] = l;
-                }
+                for (int r = 0; r < C; ++r)  // L[r][j] below the unit diagonal, stored transposed
+                    sm[L::SM_LMT + j * L::GSTR + r] = r > j ? col[r] * myrd : 0.f;
             } else {
 #pragma unroll
                 for (int r = 0; r < C; ++r) sm[L::SM_XGT + j * L::GSTR + r] = col[r];
@@ -587,7 +584,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         float* gh = x.f(L::OFF_GH) + (size_t)b * D * C;
         float* gl = x.f(L::OFF_GL) + (size_t)b * D * C;
         float* laa = x.f(L::OFF_LAA) + (size_t)b * C;
-        // the -M operand first: the state update is issued before the gate
+        // the update's operands first: the state update is issued before the gate
         float y[C], lr[C];
         if (rw && !fixed) {
             // y = z_i = z'_i L^-T (forward substitution, in place), then y D^-1
@@ -599,28 +596,25 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
 #pragma unroll
                 for (int t = r + 1; t < C; ++t) y[t] = fmaf(-lr[t], y[r], y[t]);
             }
+            // row i of N = Z D^-1/2: A_{c+1} = A_c - N N^T (symmetric by construction)
+            float nv[C];
+            tc::ld_row16(sm + L::SM_RS, lr);
+#pragma unroll
+            for (int t = 0; t < C; ++t) nv[t] = y[t] * lr[t];
             tc::ld_row16(sm + L::SM_RD, lr);
 #pragma unroll
             for (int t = 0; t < C; ++t) y[t] *= lr[t];
-            // m_i = (z_i D^-1) L^-1 (backward substitution); the operand is -m_i
-            float mv[C];
+            tc::put_row16(zh, i, nv, false);
+            tc::put_row16(zl, i, nv, true);
 #pragma unroll
-            for (int t = 0; t < C; ++t) mv[t] = y[t];
-#pragma unroll
-            for (int r = C - 1; r >= 1; --r) {
-                tc::ld_row16(sm + L::SM_LM + r * L::GSTR, lr);  // L[r][t], t < r
-#pragma unroll
-                for (int t = 0; t < r; ++t) mv[t] = fmaf(-lr[t], mv[r], mv[t]);
-            }
-#pragma unroll
-            for (int t = 0; t < C; ++t) mv[t] = -mv[t];
-            tc::put_row16(ph, i, mv, false);
-            tc::put_row16(pl, i, mv, true);
+            for (int t = 0; t < C; ++t) nv[t] = -nv[t];
+            tc::put_row16(ph, i, nv, false);
+            tc::put_row16(pl, i, nv, true);
         }
         fence_proxy_async_smem();
         named_bar(ID_T, NT_A);
         TC2_STAMP(p, 4, 5, c, nch);
-        // A_{c+1} = A_c - M Z'^T
+        // A_{c+1} = A_c - N N^T
         if (warp == 0 && !fixed && tc::elect_one()) {
             tc_fence_after();
             const uint32_t id = tc_idesc_tf32(128, D);

@@ -113,13 +113,13 @@ struct Lay3 {
     static constexpr size_t OFF_GL = OFF_GH + 2 * (size_t)MB_G;             // a^T lo [2][D x C]
     static constexpr size_t OFF_LAA = OFF_GL + 2 * (size_t)MB_G;            // ||a||^2 [2][C] (S ranks)
     static constexpr size_t OFF_SM = al(OFF_LAA + 2 * (size_t)MB_LAA);
-    // small matrices, rank 0: Guu, Guk, L, L^T, X = L^-1 Guk, 1/delta; S ranks: Lk^T, Lq (two partials each)
+    // small matrices, rank 0: Guu, Guk, 1/sqrt(delta), L^T, X = L^-1 Guk, 1/delta; S ranks: Lk^T, Lq (two partials each)
     static constexpr int MS = C * GSTR;
-    static constexpr int SM_GUU = 0, SM_GUK = MS, SM_LM = 2 * MS, SM_LMT = 3 * MS, SM_X = 4 * MS,
+    static constexpr int SM_GUU = 0, SM_GUK = MS, SM_RS = 2 * MS, SM_LMT = 3 * MS, SM_X = 4 * MS,
                          SM_RD = 5 * MS, SM_LKT = 0, SM_LQ = 2 * MS;
     static constexpr size_t OFF_U = al(OFF_SM + (size_t)(5 * MS + C) * 4);
-    // rank 0: xr (z' | w rows, then y = z / delta | w) [2C x XS], -M hi / lo
-    // [128 x C], Z' hi / lo [D x C], Gram partials of quarters 1..3 [2][3][32 x 8]
+    // rank 0: xr (z' | w rows, then y = z / delta | w) [2C x XS], -N hi / lo
+    // [128 x C], N hi / lo [D x C], Gram partials of quarters 1..3 [2][3][32 x 8]
     static constexpr size_t OFF_XR = OFF_U;
     static constexpr size_t OFF_PH = al(OFF_XR + (size_t)2 * C * XS * 4);
     static constexpr size_t OFF_PL = OFF_PH + 128 * C * 4;
@@ -242,10 +242,11 @@ __device__ __forceinline__ void gate16(const float* xr, int xs, const float* xm,
 // ---------------------------------------------------------------------------
 // rank 0, team warps 0-7: Sherman-Morrison steps of eq. 9 and the gate of
 // eq. 10, one chunk at a time (the arithmetic of tc::tc_a_team). Row i < D is
-// owned by thread i of warps 0-3 ("primary": z' columns, the substitutions,
-// the -M row, lo refresh of columns [0, D/2)) and by thread i of warps 4-7
-// ("helper": w columns, the gate row, lo refresh of columns [D/2, D)); the
-// helper forms the gate while the primary runs the backward substitution.
+// owned by thread i of warps 0-3 ("primary": z' columns, the substitution,
+// the rows of N and -N, lo refresh of columns [0, D/2)) and by thread i of
+// warps 4-7 ("helper": w columns, the gate row, lo refresh of columns
+// [D/2, D)); the helper forms the gate while the primary writes the update's
+// operands.
 // Warp 4 also factors I + Guu and sends the gate to the S ranks.
 // ---------------------------------------------------------------------------
 template <int D, typename TIn, int NS>
@@ -286,7 +287,7 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
         }
         tc_wait_st();
     }
-    // rows D..127 of the -M operand stay zero
+    // rows D..127 of the -N operand stay zero
     for (int e = ta; e < (128 - D) * C; e += NTEAM) {
         ph[cm_off(D + e / C, e % C, C)] = 0.f;
         pl[cm_off(D + e / C, e % C, C)] = 0.f;
@@ -333,10 +334,6 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
             for (int t = 0; t < C; ++t) {
                 v[t] *= sc[L::SC_IU + t];  // z'_t = A_c u^_t
                 xr[t * XS + i] = v[t];
-            }
-            if (!fixed) {
-                tc::put_row16(zh, i, v, false);
-                tc::put_row16(zl, i, v, true);
             }
         } else if (help) {
             float v[16];
@@ -389,12 +386,15 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
             float col[C];
 #pragma unroll
             for (int r = 0; r < C; ++r) col[r] = src[r * L::GSTR + j] + ((mcol && r == j) ? 1.f : 0.f);
-            float myrd = 0.f;
+            float myrd = 0.f, mydl = 1.f;
 #pragma unroll 16
             for (int t = 0; t < C; ++t) {
                 const float piv = __shfl_sync(0xffffffffu, col[t], t);
                 const float rdt = tc::rcp_approx(piv);
-                if (lane == t) myrd = rdt;
+                if (lane == t) {
+                    myrd = rdt;
+                    mydl = piv;  // delta_t; its 1/sqrt is taken after the elimination, off its chain
+                }
                 if (!(piv > 0.f) || !isfinite(rdt)) nonfinite = true;
                 const bool live = !mcol || lane > t;
                 const float ct = col[t] * rdt;
@@ -407,12 +407,10 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
             }
             if (mcol) {
                 sm[L::SM_RD + j] = myrd;
+                sm[L::SM_RS + j] = rsqrtf(mydl);
 #pragma unroll
-                for (int r = 0; r < C; ++r) {
-                    const float l = r > j ? col[r] * myrd : 0.f;  // L[r][j] below the unit diagonal
-                    sm[L::SM_LM + r * L::GSTR + j] = l;
-                    sm[L::SM_LMT + j * L::GSTR + r] = l;
-                }
+                for (int r = 0; r < C; ++r)  // L[r][j] below the unit diagonal, stored transposed
+                    sm[L::SM_LMT + j * L::GSTR + r] = r > j ? col[r] * myrd : 0.f;
             } else {
 #pragma unroll
                 for (int r = 0; r < C; ++r) sm[L::SM_X + r * L::GSTR + j] = col[r];  // X[r][j]
@@ -437,6 +435,7 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
             mbar_expect_tx_peer_relaxed(peer_addr(x.b.full_al + b, (uint32_t)lane + 1u), L::MB_BYTES);
         float y[C];
         if (prim) {
+            float nv[C];
             if (!fixed) {
                 // y = z_i = z'_i L^-T (forward substitution, in place), then y D^-1;
                 // published in xr rows 0..C-1 for the helper's gate row
@@ -449,6 +448,10 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
 #pragma unroll
                     for (int t = r + 1; t < C; ++t) y[t] = fmaf(-lr[t], y[r], y[t]);
                 }
+                // row i of N = Z D^-1/2: A_{c+1} = A_c - N N^T (symmetric by construction)
+                tc::ld_row16(sm + L::SM_RS, lr);
+#pragma unroll
+                for (int t = 0; t < C; ++t) nv[t] = y[t] * lr[t];
                 tc::ld_row16(sm + L::SM_RD, lr);
 #pragma unroll
                 for (int t = 0; t < C; ++t) {
@@ -459,24 +462,16 @@ __device__ void a_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
             TC3_STAMP(p, 0, 8, c, nch);
             tc::bar_arrive(ID_Y, 64 * NRW);
             if (!fixed) {
-                // m_i = (z_i D^-1) L^-1 (backward substitution); the operand is -m_i
-                float mv[C], lr[C];
+                tc::put_row16(zh, i, nv, false);
+                tc::put_row16(zl, i, nv, true);
 #pragma unroll
-                for (int t = 0; t < C; ++t) mv[t] = y[t];
-#pragma unroll
-                for (int r = C - 1; r >= 1; --r) {
-                    tc::ld_row16(sm + L::SM_LM + r * L::GSTR, lr);  // L[r][t], t < r
-#pragma unroll
-                    for (int t = 0; t < r; ++t) mv[t] = fmaf(-lr[t], mv[r], mv[t]);
-                }
-#pragma unroll
-                for (int t = 0; t < C; ++t) mv[t] = -mv[t];
-                tc::put_row16(ph, i, mv, false);
-                tc::put_row16(pl, i, mv, true);
+                for (int t = 0; t < C; ++t) nv[t] = -nv[t];
+                tc::put_row16(ph, i, nv, false);
+                tc::put_row16(pl, i, nv, true);
                 fence_proxy_async_smem();
             }
             TC3_STAMP(p, 0, 9, c, nch);
-            // A_{c+1} = A_c - M Z'^T once every row's -M is in place
+            // A_{c+1} = A_c - N N^T once every row's -N and N are in place
             named_bar(ID_M, 32 * NRW);
             if (warp == 0 && !fixed && tc::elect_one()) {
                 tc_fence_after();

@@ -6,8 +6,9 @@ the state A_c, S_c before the chunk (U^, K^ the unit rows u^_t, k^_t):
 
 * eq. 9 over the chunk: with Z' = A_c U^T and Guu = U^ Z', the pivots of the
   LDL^T factorisation of I + Guu are the delta_t, and Z = Z' L^-T holds the
-  Sherman-Morrison vectors z_t = A_{t-1} u^_t; A_{c+1} = A_c - M Z'^T with
-  M = Z D^-1 L^-1 (the Woodbury identity for the chunk's rank-C downdate).
+  Sherman-Morrison vectors z_t = A_{t-1} u^_t; the chunk's rank-C downdate
+  is A_{c+1} = A_c - Z' (I + Guu)^-1 Z'^T (Woodbury) = A_c - N N^T with
+  N = Z D^-1/2, the sum of the tokens' z_t z_t^T / delta_t.
   Gaussian elimination of [I + Guu | Guk] gives L, the pivots and
   X = L^-1 Guk together (Guk = U^ A_c K^T).
 * the gate of eq. 10: a_t = A_t k^_t = w_t - sum_{q<=t} (z_q / delta_q) X[q][t]
@@ -21,7 +22,8 @@ These identities are exact, so the restatement must agree with the oracle to
 fp64 rounding for every chunk size; C = 1 is the per-token loop itself. The
 planted mistakes at the end (a strict triangle where the sum includes its
 diagonal and the reverse, a dropped 1/delta, the wrong triangle of the Gram
-matrices) must each move the result well past that rounding.
+matrices, D^-1 in place of D^-1/2 in the update) must each move the result
+well past that rounding.
 """
 import numpy as np
 import pytest
@@ -72,8 +74,8 @@ def chunked_forward(q, k, v, u, lambda0, eps, chunk, S0=None, A0=None, zk0=None,
         L, delta, X = eliminate(np.eye(n) + Guu, Guk)
         Z = np.linalg.solve(L, Zp.T).T     # Z = Z' L^-T
         Y = Z if mistake == "no_rdelta" else Z / delta
-        M = np.linalg.solve(L.T, Y.T).T    # M = Z D^-1 L^-1
-        A_next = A - M @ Zp.T
+        N = Z / (delta if mistake == "update_rdelta" else np.sqrt(delta))  # N = Z D^-1/2
+        A_next = A - N @ N.T
         # the gate of eq. 10: a_t = w_t - sum_{q<=t} (z_q / delta_q) X[q][t]
         tri = np.triu(X, 1) if mistake == "gate_strict" else np.triu(X)
         Ag = W - Y @ tri
@@ -165,7 +167,28 @@ def test_ldl_pivots_are_the_sherman_morrison_denominators(orc):
     assert np.allclose(delta, delta32, rtol=1e-5)
 
 
-@pytest.mark.parametrize("mistake", ["gate_strict", "solve_diag", "no_rdelta", "gram_triangle"])
+def test_symmetric_update_is_the_woodbury_downdate():
+    """N N^T with N = Z' L^-T D^-1/2 is Z' (I + U^ A U^^T)^-1 Z'^T, the rank-C
+    Woodbury downdate, and also the product of the chunk's C Sherman-Morrison
+    steps of eq. 9 taken one token at a time."""
+    rng = np.random.default_rng(31)
+    d, n = 24, 16
+    B = rng.standard_normal((d, d))
+    A = B @ B.T / d + np.eye(d)                      # symmetric positive definite
+    Uh = unit_rows(rng.standard_normal((n, d)))
+    Zp = A @ Uh.T
+    L, delta, _ = eliminate(np.eye(n) + Uh @ Zp, np.zeros((n, 1)))
+    N = np.linalg.solve(L, Zp.T).T / np.sqrt(delta)
+    woodbury = Zp @ np.linalg.solve(np.eye(n) + Uh @ Zp, Zp.T)
+    assert np.max(np.abs(N @ N.T - woodbury)) < 1e-12 * np.max(np.abs(woodbury))
+    As = A.copy()
+    for t in range(n):                               # eq. 9, token by token
+        z = As @ Uh[t]
+        As = As - np.outer(z, z) / (1.0 + Uh[t] @ z)
+    assert np.max(np.abs((A - N @ N.T) - As)) < 1e-12 * np.max(np.abs(A))
+
+
+@pytest.mark.parametrize("mistake", ["gate_strict", "solve_diag", "no_rdelta", "gram_triangle", "update_rdelta"])
 def test_planted_mistakes_are_caught(orc, mistake):
     BH, T, d = 1, 16 * 2 + 3, 24
     (q, k, v, u), _ = _inputs(23, BH, T, d)

@@ -62,7 +62,7 @@ def forward_chunks(q, k, v, u, lambda0, eps, C, S0=None, A0=None, zk0=None):
         L, delta, X = eliminate(np.eye(n) + Uh @ Zp, Uh @ W)
         Z = np.linalg.solve(L, Zp.T).T
         Y = Z / delta
-        M = np.linalg.solve(L.T, Y.T).T
+        N = Z / np.sqrt(delta)             # A_{c+1} = A_c - N N^T
         Ag = W - Y @ np.triu(X)
         an = np.linalg.norm(Ag, axis=0)
         al = Ag / np.maximum(an, 1e-12)
@@ -79,7 +79,7 @@ def forward_chunks(q, k, v, u, lambda0, eps, C, S0=None, A0=None, zk0=None):
                            a=Ag.T, an=an, al=al.T, E=E.T, PQ=PQ, PK=PK, ZK=ZK, den=den,
                            clamp=raw < eps, O=O))
         S = S + E @ al.T
-        A = A - M @ Zp.T
+        A = A - N @ N.T
         zk = ZK[-1]
     return chunks, (S, A, zk)
 

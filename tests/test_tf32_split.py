@@ -12,8 +12,13 @@ one head of the d_h = 96 workload, all 4096 tokens.
 
 * The split stays well inside the 2e-3 parity tolerance, within a few times
   the error of exact fp32 products.
-* Plain tf32 operands miss the tolerance by a wide margin. That is why the
-  split is there.
+* Plain tf32 operands miss the tolerance. That is why the split is there.
+
+The rank-C update of A is the symmetric N N^T (N = Z D^-1/2), as in the
+kernels. With the earlier form M Z'^T (M = Z D^-1 L^-1) the rounding left an
+antisymmetric part in A that the downdates never damp while A shrinks, so
+the error grew with T: on this head the split's worst o error was about
+8e-5 and plain tf32's above 1e-2; with N N^T they are 2e-6 and 2.9e-3.
 """
 import numpy as np
 import pytest
@@ -84,8 +89,8 @@ def chunked_fp32(q, k, v, u, lambda0, eps, mm, C=16):
         L, delta, X = eliminate(np.eye(n, dtype=f32) + Guu, Guk)
         Z = np.linalg.solve(L, Zp.T).T.astype(f32)
         Y = (Z / delta).astype(f32)
-        M = np.linalg.solve(L.T, Y.T).T.astype(f32)
-        A_next = (A - mm(M, Zp.T)).astype(f32)          # rank-C update of A
+        N = (Z * (f32(1) / np.sqrt(delta.astype(f32)))).astype(f32)  # N = Z D^-1/2
+        A_next = (A - mm(N, N.T)).astype(f32)            # rank-C update of A: A - N N^T
         Ag = (Wm - Y @ np.triu(X)).astype(f32)            # the gate a_t (fp32 FMA)
         nr = np.maximum(np.linalg.norm(Ag, axis=0), f32(1e-12)).astype(f32)
         Lk = (mm(Kh, Ag) / nr).astype(f32)
@@ -125,4 +130,5 @@ def test_split_products_stay_inside_the_tolerance(errors):
 
 
 def test_plain_tf32_products_miss_the_tolerance(errors):
-    assert max(errors["plain"]) > 5 * TOL, errors["plain"]
+    assert max(errors["plain"]) > TOL, errors["plain"]
+    assert max(errors["plain"]) > 100 * max(errors["split"]), errors

@@ -52,7 +52,7 @@ def chunked_backward_fp32(q, k, v, u, lambda0, eps, C, gO, gS, gA, gzk, mm):
         L, delta, X = eliminate(np.eye(n, dtype=f32) + mm(Uh, Zp), mm(Uh, Wm))
         Z = np.linalg.solve(L, Zp.T).T.astype(f32)
         Y = (Z / delta).astype(f32)
-        M = np.linalg.solve(L.T, Y.T).T.astype(f32)
+        N = (Z * (f32(1) / np.sqrt(delta.astype(f32)))).astype(f32)  # N = Z D^-1/2
         Ag = (Wm - Y @ np.triu(X)).astype(f32)
         an = np.linalg.norm(Ag, axis=0).astype(f32)
         al = (Ag / np.maximum(an, f32(1e-12))).astype(f32)
@@ -68,7 +68,7 @@ def chunked_backward_fp32(q, k, v, u, lambda0, eps, C, gO, gS, gA, gzk, mm):
         chunks.append(dict(sl=sl, n=n, S=S, A=A, Uh=Uh, Kh=Kh, Z=Z.T.copy(), delta=delta, a=Ag.T.copy(),
                            al=al.T.copy(), E=E.T.copy(), PQ=PQ, ZK=ZK, den=den, clamp=raw < eps, O=O))
         S = (S + mm(E, al.T)).astype(f32)
-        A = (A - mm(M, Zp.T)).astype(f32)
+        A = (A - mm(N, N.T)).astype(f32)
         zk = ZK[-1]
     dq, dk, dv, du = (np.zeros((T, d), f32) for _ in range(4))
     HS, HA, gz = gS.astype(f32), gA.astype(f32), gzk.astype(f32)
