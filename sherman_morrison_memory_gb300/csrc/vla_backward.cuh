@@ -25,7 +25,7 @@
 //
 // Identities that save a product per reverse step (A is symmetric):
 //   A_t u^ = z / delta,  A_t k^ = alpha^ ||a||,  A_{t-1} g = A_t g + z (z.g) / delta,
-// so the reverse step has two rounds of matrix-vector products, not three.
+// so the reverse step has two passes of matrix-vector products, not three.
 
 namespace bw {
 
@@ -52,11 +52,11 @@ struct BLay {
     // shared memory (bytes)
     static constexpr int RING = 0;
     static constexpr int X1 = RING + NB2 * SLOT_B;    // forward: [2 parities][z | A k^] per row
-    static constexpr int P1 = X1 + 2 * 2 * D * 4;     // reverse round 1 column partials [NW][3][D]
+    static constexpr int P1 = X1 + 2 * 2 * D * 4;     // reverse pass-1 column partials [NW][3][D]
     static constexpr int C1 = P1 + NW * 3 * D * 4;    // their sums [3][D]
-    static constexpr int R1 = C1 + 3 * D * 4;         // round 1 row products [2 parities][2][D]
-    static constexpr int P2 = R1 + 2 * 2 * D * 4;     // round 2 column partials [NW][D]
-    static constexpr int R2 = P2 + NW * D * 4;        // round 2 row products [2][D]
+    static constexpr int R1 = C1 + 3 * D * 4;         // pass-1 row products [2 parities][2][D]
+    static constexpr int P2 = R1 + 2 * 2 * D * 4;     // pass-2 column partials [NW][D]
+    static constexpr int R2 = P2 + NW * D * 4;        // pass-2 row products [2][D]
     static constexpr int DP = R2 + 2 * D * 4;         // per-warp dot partials [4][NW]
     static constexpr int DS = DP + 4 * NW * 4;        // their sums [4]
     static constexpr int RED = DS + 4 * 4;            // [D/32 warps][2] dot partials of the k/u gradients
@@ -190,7 +190,7 @@ __device__ __forceinline__ void prefetch_rev(unsigned char* slot, const TIn* gu,
     }
 }
 
-// dL/dk_t and dL/du_t (column j = 32 jw + lane) from the round-2 products of
+// dL/dk_t and dL/du_t (column j = 32 jw + lane) from the pass-2 products of
 // token t (P2, R2) and its scalars; run by the d/32 warps that the column sums
 // of the next step leave free. Returns false on a non-finite result.
 template <int D, typename TIn>
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
             zc[c] = rec[j];
             al[c] = rec[D + j];
         }
-        // round 1 (gS, gA: adjoints of S_t, A_t before this token's terms)
+        // product pass 1 (gS, gA: adjoints of S_t, A_t before this token's terms)
         //   rows: gS alpha^, gA z;  columns: gS^T e, S_t^T dL/do, gA^T z
         {
             float pg[RW], pz[RW];
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
             dv[orow + r0 + l] = x;
             if (!isfinite(x)) bad = true;
         }
-        // round 2: columns S_t^T g_e; rows A_t g_a, A_t w1
+        // product pass 2: columns S_t^T g_e; rows A_t g_a, A_t w1
         {
             float pa[RW], pw[RW], qg[CL];
 #pragma unroll
@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
         }
         j_ege = e_ge, j_kz = kz, j_gdl = gdl, j_zgz = zgz, j_az = az, j_nac = nac, j_dl = dl, j_nu = nu, j_nk = nk;
     }
-    __syncthreads();  // round-2 products of token 0 visible
+    __syncthreads();  // pass-2 products of token 0 visible
     if (T > 0 && ku_warp) {
         const bool ok = ku_grads<D, TIn>(ring, P2, R2, RED, jw, pick<CL>(gzk, jw), j_ege, j_kz, j_gdl, j_zgz, j_az,
                                          j_nac, j_dl, j_nu, j_nk, dk + (size_t)bh * T * D, du + (size_t)bh * T * D);

@@ -35,10 +35,10 @@ struct SLay {
     static constexpr int K = 0, Q = IN_B, G = 2 * IN_B, TP = 2 * IN_B + 4 * D;
     static constexpr int SLOT_B = TP + 4 * TREC;
     static constexpr int RING = 0;
-    static constexpr int P1 = RING + NB * SLOT_B;   // round 1 column partials [NW][2][D]
+    static constexpr int P1 = RING + NB * SLOT_B;   // pass-1 column partials [NW][2][D]
     static constexpr int C1 = P1 + NW * 2 * D * 4;  // their sums [2][D]
-    static constexpr int R1 = C1 + 2 * D * 4;       // round 1 row products [2 parities][D]
-    static constexpr int P2 = R1 + 2 * D * 4;       // round 2 column partials [NW][D]
+    static constexpr int R1 = C1 + 2 * D * 4;       // pass-1 row products [2 parities][D]
+    static constexpr int P2 = R1 + 2 * D * 4;       // pass-2 column partials [NW][D]
     static constexpr int DP = P2 + NW * D * 4;      // per-warp dot partials [2][NW]
     static constexpr int DS = DP + 2 * NW * 4;      // their sums [2] (+2 unused)
     static constexpr int RED = DS + 4 * 4;          // [CL] dot partials of the deferred dL/dk
@@ -60,10 +60,10 @@ struct ALay {
     static constexpr int U = 0, K = IN_B, TP = 2 * IN_B;
     static constexpr int SLOT_B = TP + 4 * TREC;
     static constexpr int RING = 0;
-    static constexpr int P1 = RING + NB * SLOT_B;  // round 1 column partials [NW][D]
+    static constexpr int P1 = RING + NB * SLOT_B;  // pass-1 column partials [NW][D]
     static constexpr int C1 = P1 + NW * D * 4;     // their sums [D]
-    static constexpr int R1 = C1 + D * 4;          // round 1 row products [2 parities][D]
-    static constexpr int R2 = R1 + 2 * D * 4;      // round 2 row products [2][D]
+    static constexpr int R1 = C1 + D * 4;          // pass-1 row products [2 parities][D]
+    static constexpr int R2 = R1 + 2 * D * 4;      // pass-2 row products [2][D]
     static constexpr int DP = R2 + 2 * D * 4;      // per-warp dot partials [NW]
     static constexpr int DS = DP + NW * 4;         // their sum (+3 unused)
     static constexpr int RED = DS + 4 * 4;         // [CL][2] dot partials of the deferred dL/dk, dL/du
@@ -111,7 +111,7 @@ __device__ __forceinline__ void prefetch_a(unsigned char* slot, const TIn* gu, c
     }
 }
 
-// The S part of dL/dk_t (column j = 32 jw + lane) from token t's round-2
+// The S part of dL/dk_t (column j = 32 jw + lane) from token t's pass-2
 // column partials (S_t^T g_e):
 //   gzk phi'(k) - P(S_{t-1}^T g_e) / ||k||,  S_{t-1}^T g_e = S_t^T g_e - alpha^ (e . g_e),
 // P the projection off k^. Run by the last d/32 warps. False on a non-finite result.
@@ -140,7 +140,7 @@ __device__ __forceinline__ bool k_grad_s(const unsigned char* sl, const float* P
 }
 
 // dL/du_t and the A part of dL/dk_t (column j = 32 jw + lane) from token t's
-// round-2 row products (A_t g_a, A_t w1) and its scalars; the A part
+// pass-2 row products (A_t g_a, A_t w1) and its scalars; the A part
 // P(A_t g_a) / ||k|| is added to the S part already in dk. Run by the last
 // d/32 warps. False on a non-finite result.
 template <int D, typename TIn>
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
             pq[c] = phi(lds_in<TIn>(sl + L::Q, j));
             al[c] = rec[D + j];
         }
-        // round 1: rows gS alpha^; columns gS^T e, S_t^T dL/do
+        // product pass 1: rows gS alpha^; columns gS^T e, S_t^T dL/do
         float d4[4] = {0.f, 0.f, 0.f, 0.f};
         {
             float pg[RW];
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
             dv[orow + r0 + l] = x;
             if (!isfinite(x)) bad = true;
         }
-        // round 2: columns S_t^T g_e
+        // product pass 2: columns S_t^T g_e
         {
             float qg[CL];
 #pragma unroll
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
         }
         j_ege = e_ge, j_nk = nk;
     }
-    __syncthreads();  // round-2 partials of token 0 visible
+    __syncthreads();  // pass-2 partials of token 0 visible
     if (T > 0 && ku_warp) {
         if (!k_grad_s<D, TIn>(ring, P2, RED, jw, pick<CL>(gzk, jw), j_ege, j_nk, dk + (size_t)bh * T * D))
             bad = true;
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
             zc[c] = rec[j];
             gac[c] = rec[2 * D + j];  // g_a, written over e_t by the S side
         }
-        // round 1: rows gA z; columns gA^T z
+        // product pass 1: rows gA z; columns gA^T z
         float d3[3] = {0.f, 0.f, 0.f};
         {
             float pz[RW];
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
             w1c[c] = r1[j] + C1[j];
             gzc[c] = fmaf(gdl, uh[c], -(w1c[c] + fmaf(gac[c], kz, kh[c] * az)) * rdl);
         }
-        // round 2: rows A_t g_a, A_t w1
+        // product pass 2: rows A_t g_a, A_t w1
         {
             float pa[RW], pw[RW];
 #pragma unroll
@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
         }
         j_kz = kz, j_gdl = gdl, j_zgz = zgz, j_az = az, j_nac = nac, j_dl = dl, j_nu = nu, j_nk = nk;
     }
-    __syncthreads();  // round-2 products of token 0 visible
+    __syncthreads();  // pass-2 products of token 0 visible
     if (T > 0 && ku_warp) {
         if (!ku_grad_a<D, TIn>(ring, R2, RED, jw, j_kz, j_gdl, j_zgz, j_az, j_nac, j_dl, j_nu, j_nk,
                                dk + (size_t)bh * T * D, du + (size_t)bh * T * D))

@@ -9,7 +9,7 @@
 // stream them. One persistent CTA per SM runs heads b, b + gridDim.x, ...;
 // while a head computes, TMA bulk copies bring the next head's state and
 // first-token inputs into shared memory. Warp w owns rows 8w .. 8w+7 of S and
-// A and lane l owns columns l, l+32, .. in registers. Per token: one round of row products
+// A and lane l owns columns l, l+32, .. in registers. Per token: one pass of row products
 // (A u^, A k^, S k^, S phi(q), with the states before the token), a
 // warp-shuffle halving exchange for the row sums, one block barrier to share
 // z and A k^, then scalars by warp butterflies and the rank-1 updates in
