@@ -68,22 +68,22 @@ KERNEL_FILES = {
 # was taken on (B, H, T, d, input dtype) and while that kernel's own sources
 # hash to source_sha; otherwise reported as null.
 NCU_TRAFFIC = {
-    "vla_tc_kernel": {"source_sha": "c26cfcf131e87f0a", "workload": (8, 16, 4096, 96, "bf16"),
-                      "bytes_per_launch": 403085056 + 176358912},
+    "vla_tc_kernel": {"source_sha": "e4fa02df82d8ceba", "workload": (8, 16, 4096, 96, "bf16"),
+                      "bytes_per_launch": 402738432 + 176217344},
     # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
-    "vla_tc3_kernel": {"source_sha": "e06afcbbcbab820a", "workload": (1, 32, 65536, 128, "bf16"),
-                       "bytes_per_launch": 8 * (268755968 + 108874240 - 4227072) + 4227072},
+    "vla_tc3_kernel": {"source_sha": "8b2b3debd6495128", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (268544768 + 108853248 - 4227072) + 4227072},
     # the reverse sweep (the step's dominant kernel, after the taped chunked forward), from a capture of
     # the same workload at B=2 (32 heads; a full step holds about 2.8 GB on the device) scaled by 4:
     # every byte it moves is per head-token or per head
-    "vla_backward_kernel": {"source_sha": "8018c1c77adde7f7", "workload": (8, 16, 4096, 96, "bf16"),
-                            "bytes_per_launch": 4 * (437382144 + 177710592)},
+    "vla_backward_kernel": {"source_sha": "7309d7fdbbe5647d", "workload": (8, 16, 4096, 96, "bf16"),
+                            "bytes_per_launch": 4 * (436558848 + 176801024)},
     # the S side of the split reverse sweep (d = 128), on the long-context workload cut to 4096 tokens
-    "vla_backward_s_kernel": {"source_sha": "6e16ee37bd9eeff9", "workload": (1, 32, 4096, 128, "bf16"),
-                              "bytes_per_launch": 478849792 + 237614592},
-    "vla_decode_kernel": {"source_sha": "21f293567c108430", "workload": (128, 16, 1, 96, "bf16"),
-                          "bytes_per_launch": 153430784 + 98220800},
+    "vla_backward_s_kernel": {"source_sha": "dfab26bbfa0604e0", "workload": (1, 32, 4096, 128, "bf16"),
+                              "bytes_per_launch": 477381120 + 237421056},
+    "vla_decode_kernel": {"source_sha": "9266c08b57d2ba6a", "workload": (128, 16, 1, 96, "bf16"),
+                          "bytes_per_launch": 153394432 + 98736640},
 }
 
 
