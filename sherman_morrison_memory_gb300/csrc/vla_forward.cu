@@ -315,6 +315,7 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
     };
 
     bool abort = false;
+    float dchk = 0.f;  // fma(phi(q) . z^key, 0, .) per token: stays 0 unless q made it NaN or Inf
     // this warp's chunks are sw, sw + NSTG, ...; keep RPW of them in flight
     int issued = sw, landed = sw, c = sw;
     if (lane == 0)
@@ -434,7 +435,10 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
 #pragma unroll
         for (int j = 0; j < rs_count<C::CH, 16>(); ++j) {
             const int t = rs_index<C::CH, 16>(lane, j);
-            if (t >= 0 && t < nt) P0[t * LY::PSTRIDE + LY::P_DEN] = fmaxf(qz[j], p.eps);
+            if (t >= 0 && t < nt) {
+                P0[t * LY::PSTRIDE + LY::P_DEN] = fmaxf(qz[j], p.eps);
+                dchk = fmaf(qz[j], 0.f, dchk);
+            }
         }
         // our generic-proxy reads of raw slot rs are done before the TMA refill
         fence_proxy_async_smem();
@@ -451,6 +455,7 @@ __device__ __forceinline__ void stage_role(const Params& p, const Smem& sm, int 
             for (int m = 0; m < E; ++m) p.zk_out[(size_t)bh * D + lane + 32 * m] = zk[m];
         }
     }
+    if (dchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_STAGE, bh, -1);
     if (abort) {
         if (lane == 0) record_failure(p.status, BIT_TIMEOUT, ROLE_STAGE, bh, c * C::CH);
         *sm.abort = 1;
@@ -908,7 +913,7 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
     }
     float* o = p.o + (size_t)bh * p.o_stride;
 
-    bool abort = false, nonfinite = false;
+    bool abort = false;
     int t = 0;
     for (; t < p.T; ++t) {
         const int chunk = t / C::CH, tc = t - chunk * C::CH, ps = chunk % C::NP;
@@ -965,7 +970,6 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
         if (own) {
             const float ov = fmaf(e_own, st, sq_own) * rden;
             o[(size_t)t * D + row0 + cb] = ov;
-            if (!isfinite(ov)) nonfinite = true;
             red[2 * RS * LY::RST + rgl * C::CBS + cb] = e_own;
         }
         __syncwarp();
@@ -1000,19 +1004,26 @@ __device__ __forceinline__ void s_role(const Params& p, const Smem& sm, int bh, 
             if (tc == C::CH - 1 || t == p.T - 1) mbar_arrive(sm.empty_p + ps);
         }
     }
-    if (nonfinite) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
     if (abort) {
         if (ws == 0 && lane == 0) record_failure(p.status, BIT_TIMEOUT, ROLE_S, bh, t);
         *sm.abort = 1;
         return;
     }
+    // Non-finite outputs are detected where they can arise rather than per
+    // output (a check on every o cost this kernel 18%): through q in the
+    // staging warps' phi(q) . z^key, through k and u in the gate and delta
+    // checks, and through v in S, whose row stays non-finite to the end.
     float* So = p.S_out + (size_t)bh * D * D;
+    float schk = 0.f;
 #pragma unroll
     for (int r = 0; r < RS; ++r)
 #pragma unroll
-        for (int c = 0; c < C2; c += 2)
+        for (int c = 0; c < C2; c += 2) {
             *reinterpret_cast<float4*>(So + (size_t)(row0 + r) * D + col0 + 2 * c) =
                 make_float4(s[r][c].x, s[r][c].y, s[r][c + 1].x, s[r][c + 1].y);
+            schk = fmaf(s[r][c].x + s[r][c].y + s[r][c + 1].x + s[r][c + 1].y, 0.f, schk);
+        }
+    if (schk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
 }
 
 template <int D, typename TIn>

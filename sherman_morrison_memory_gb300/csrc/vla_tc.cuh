@@ -864,6 +864,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
     const TIn* gv = static_cast<const TIn*>(p.v) + (p.v_shared ? 0 : (size_t)bh * (p.in_stride ? p.in_stride : (size_t)T * D));
     float* go = p.o + (size_t)bh * p.o_stride;
     bool bad = false, nonfinite = false;
+    float nfchk = 0.f;  // fma(o, 0, .) of every output (branch-free)
 
     // S_0 = 0 unless carried in, and its lo part
     if (rw) {
@@ -1050,7 +1051,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 const float ov = a * nr[t];
                 if (t < n) {
                     go[(size_t)(c * C + t) * D + i] = ov;
-                    if (!isfinite(ov)) nonfinite = true;
+                    nfchk = fmaf(ov, 0.f, nfchk);  // stays 0 unless an o is NaN or Inf
                 }
             }
             if (ts == 0) VLA_TRACE_AT(p, 2, c);
@@ -1104,7 +1105,7 @@ __device__ void tc_s_team(const Params& p, const Ctx<D, TIn>& x, int bh, int war
                 *reinterpret_cast<float4*>(So + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
     }
-    if (nonfinite) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
+    if (nonfinite || nfchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
 }
 
 }  // namespace tc

@@ -734,6 +734,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
     float* go = p.o + (size_t)bh * p.o_stride;
     const uint32_t r_empty_al = peer_addr(x.b.empty_al, 0u);
     bool bad = false, nonfinite = false;
+    float nfchk = 0.f;  // fma(o, 0, .) of every output (branch-free)
     int recv = 0;
 
     // S_0 = 0 unless carried in, and its lo part
@@ -853,7 +854,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
                 const float ov = a * nr[t];
                 if (t < n) {
                     go[(size_t)(c * C + t) * D + i] = ov;
-                    if (!isfinite(ov)) nonfinite = true;
+                    nfchk = fmaf(ov, 0.f, nfchk);  // stays 0 unless an o is NaN or Inf
                 }
             }
             tc::put_row16(eh, i, vv, false);
@@ -913,7 +914,7 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
                 *reinterpret_cast<float4*>(So + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
     }
-    if (nonfinite) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
+    if (nonfinite || nfchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
 }
 
 }  // namespace tc2

@@ -596,6 +596,7 @@ __device__ void s_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
     float* go = p.o + (size_t)bh * p.o_stride;
     const uint32_t r_empty_al = peer_addr(x.b.empty_al, 0u);
     bool bad = false, nonfinite = false;
+    float nfchk = 0.f;  // fma(o, 0, .) of every output (branch-free)
     int recv = 0;
 
     // S_0 rows (0 unless carried in) and their lo part; lanes R..127 hold zeros
@@ -798,7 +799,7 @@ __device__ void s_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
                     const float ov = a * rd[t];
                     if (t < n) {
                         go[(size_t)(c * C + t) * D + gi] = ov;
-                        if (!isfinite(ov)) nonfinite = true;
+                        nfchk = fmaf(ov, 0.f, nfchk);  // stays 0 unless an o is NaN or Inf
                     }
                 }
             }
@@ -841,7 +842,7 @@ __device__ void s_rank(const Params& p, const Ctx3<D, TIn, NS>& x, int bh, int w
             }
         }
     }
-    if (nonfinite) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
+    if (nonfinite || nfchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
 }
 
 }  // namespace tc3
