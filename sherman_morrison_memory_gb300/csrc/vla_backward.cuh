@@ -192,9 +192,10 @@ __device__ __forceinline__ void prefetch_rev(unsigned char* slot, const TIn* gu,
 
 // dL/dk_t and dL/du_t (column j = 32 jw + lane) from the pass-2 products of
 // token t (P2, R2) and its scalars; run by the d/32 warps that the column sums
-// of the next step leave free. Returns false on a non-finite result.
+// of the next step leave free. Returns fma(gradients, 0): 0 unless one is NaN
+// or Inf (branch-free, like every per-element check of the sweep).
 template <int D, typename TIn>
-__device__ __forceinline__ bool ku_grads(const unsigned char* sl, const float* P2, const float* R2, float* RED,
+__device__ __forceinline__ float ku_grads(const unsigned char* sl, const float* P2, const float* R2, float* RED,
                                          int jw, float gzk, float e_ge, float kz, float gdl, float zgz, float az,
                                          float nac, float dl, float nu, float nk, float* dk, float* du) {
     using L = BLay<D, TIn>;
@@ -229,7 +230,7 @@ __device__ __forceinline__ bool ku_grads(const unsigned char* sl, const float* P
     const float dkt = fmaf(gzk, phi_d(kj), nk < 1e-24f ? gkh * 1e12f : fmaf(-khj, kgk, gkh) * ik);
     du[j] = dut;
     dk[j] = dkt;
-    return isfinite(dut) && isfinite(dkt);
+    return fmaf(dut, 0.f, dkt * 0.f);
 }
 
 // MODE 0: both phases (four d x d matrices in registers: d <= 96).
@@ -269,6 +270,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     float* tp = tape + (size_t)bh * T * L::TREC;
     float* cp = ckpt + (size_t)bh * ((T + CK - 1) / CK + 1) * L::CREC;
     bool bad = false;
+    float gchk = 0.f;  // fma(gradient, 0, .) of every gradient written: 0 unless one is NaN or Inf
 
     float S[RW][CL], A[RW][CL], zk[CL];
 #pragma unroll
@@ -597,10 +599,9 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
                 DS[l] = s;
             }
             if (t + 1 < T) {  // dL/dk, dL/du of token t+1
-                const bool ok = ku_grads<D, TIn>(ring + ((t + 1) % NB2) * L::SLOT_B, P2, R2, RED, jw, pick<CL>(gzk, jw),
-                                                 j_ege, j_kz, j_gdl, j_zgz, j_az, j_nac, j_dl, j_nu, j_nk,
-                                                 dk + orow + D, du + orow + D);
-                if (!ok) bad = true;
+                gchk += ku_grads<D, TIn>(ring + ((t + 1) % NB2) * L::SLOT_B, P2, R2, RED, jw, pick<CL>(gzk, jw),
+                                         j_ege, j_kz, j_gdl, j_zgz, j_az, j_nac, j_dl, j_nu, j_nk,
+                                         dk + orow + D, du + orow + D);
             }
         }
         __syncthreads();  // B2
@@ -631,7 +632,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
             if (w == 0) {
                 const float x = gpq * phi_d(lds_in<TIn>(sl + L::Q, j));
                 dq[orow + j] = x;
-                if (!isfinite(x)) bad = true;
+                gchk = fmaf(x, 0.f, gchk);
             }
         }
         // rows: g_e
@@ -646,7 +647,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
         if (l < RW) {
             const float x = pick<RW>(ger, l);
             dv[orow + r0 + l] = x;
-            if (!isfinite(x)) bad = true;
+            gchk = fmaf(x, 0.f, gchk);
         }
         // product pass 2: columns S_t^T g_e; rows A_t g_a, A_t w1
         {
@@ -729,9 +730,8 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     }
     __syncthreads();  // pass-2 products of token 0 visible
     if (T > 0 && ku_warp) {
-        const bool ok = ku_grads<D, TIn>(ring, P2, R2, RED, jw, pick<CL>(gzk, jw), j_ege, j_kz, j_gdl, j_zgz, j_az,
-                                         j_nac, j_dl, j_nu, j_nk, dk + (size_t)bh * T * D, du + (size_t)bh * T * D);
-        if (!ok) bad = true;
+        gchk += ku_grads<D, TIn>(ring, P2, R2, RED, jw, pick<CL>(gzk, jw), j_ege, j_kz, j_gdl, j_zgz, j_az, j_nac,
+                                 j_dl, j_nu, j_nk, dk + (size_t)bh * T * D, du + (size_t)bh * T * D);
     }
 #pragma unroll
     for (int r = 0; r < RW; ++r)
@@ -744,7 +744,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     if (w == 0 && dzk0)
 #pragma unroll
         for (int c = 0; c < CL; ++c) dzk0[(size_t)bh * D + l + 32 * c] = gzk[c];
-    if (bad) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
+    if (bad || gchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
     }  // MODE 0
 }
 

@@ -114,9 +114,10 @@ __device__ __forceinline__ void prefetch_a(unsigned char* slot, const TIn* gu, c
 // The S part of dL/dk_t (column j = 32 jw + lane) from token t's pass-2
 // column partials (S_t^T g_e):
 //   gzk phi'(k) - P(S_{t-1}^T g_e) / ||k||,  S_{t-1}^T g_e = S_t^T g_e - alpha^ (e . g_e),
-// P the projection off k^. Run by the last d/32 warps. False on a non-finite result.
+// P the projection off k^. Run by the last d/32 warps. Returns fma(dL/dk, 0): 0
+// unless it is NaN or Inf.
 template <int D, typename TIn>
-__device__ __forceinline__ bool k_grad_s(const unsigned char* sl, const float* P2, float* RED, int jw, float gzk,
+__device__ __forceinline__ float k_grad_s(const unsigned char* sl, const float* P2, float* RED, int jw, float gzk,
                                          float e_ge, float nk, float* dk) {
     using L = SLay<D, TIn>;
     const int l = threadIdx.x & 31, j = 32 * jw + l;
@@ -136,15 +137,15 @@ __device__ __forceinline__ bool k_grad_s(const unsigned char* sl, const float* P
     for (int v = 0; v < L::CL; ++v) ks += RED[v];
     const float dkt = fmaf(gzk, phi_d(kj), nk < 1e-24f ? -sk * 1e12f : -fmaf(-khj, ks, sk) * ik);
     dk[j] = dkt;
-    return isfinite(dkt);
+    return dkt * 0.f;
 }
 
 // dL/du_t and the A part of dL/dk_t (column j = 32 jw + lane) from token t's
 // pass-2 row products (A_t g_a, A_t w1) and its scalars; the A part
 // P(A_t g_a) / ||k|| is added to the S part already in dk. Run by the last
-// d/32 warps. False on a non-finite result.
+// d/32 warps. Returns fma(gradients, 0): 0 unless one is NaN or Inf.
 template <int D, typename TIn>
-__device__ __forceinline__ bool ku_grad_a(const unsigned char* sl, const float* R2, float* RED, int jw, float kz,
+__device__ __forceinline__ float ku_grad_a(const unsigned char* sl, const float* R2, float* RED, int jw, float kz,
                                           float gdl, float zgz, float az, float nac, float dl, float nu, float nk,
                                           float* dk, float* du) {
     using L = ALay<D, TIn>;
@@ -176,7 +177,7 @@ __device__ __forceinline__ bool ku_grad_a(const unsigned char* sl, const float* 
     du[j] = dut;
     const float dkt = dk[j] + dka;
     dk[j] = dkt;
-    return isfinite(dut) && isfinite(dkt);
+    return fmaf(dut, 0.f, dkt * 0.f);
 }
 
 // S side of the reverse sweep. fin: the forward's final S [BH][D][D] | A | z^key [BH][D].
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
     const float* go_h = dO ? dO + hin : nullptr;
     float* tp = tape + (size_t)bh * T * L::TREC;
     const float* cp = ckpt + (size_t)bh * ((T + CK - 1) / CK + 1) * L::CREC;
-    bool bad = false;
+    float gchk = 0.f;  // fma(x, 0, .) of every gradient and g_a written: 0 unless one is NaN or Inf
 
     float S[RW][CL], gS[RW][CL], zk[CL], gzk[CL];
 #pragma unroll
@@ -314,11 +315,9 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
                 for (int v = 0; v < NW; ++v) s += DP[l * NW + v];
                 DS[l] = s;
             }
-            if (ku_warp && t + 1 < T) {
-                if (!k_grad_s<D, TIn>(ring + ((t + 1) % NB) * L::SLOT_B, P2, RED, jw, pick<CL>(gzk, jw), j_ege,
-                                      j_nk, dk + orow + D))
-                    bad = true;
-            }
+            if (ku_warp && t + 1 < T)
+                gchk += k_grad_s<D, TIn>(ring + ((t + 1) % NB) * L::SLOT_B, P2, RED, jw, pick<CL>(gzk, jw), j_ege,
+                                         j_nk, dk + orow + D);
         }
         __syncthreads();  // B2
 
@@ -340,7 +339,7 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
                 const float x = gpq * phi_d(lds_in<TIn>(sl + L::Q, j));
                 dq[orow + j] = x;
                 tp[(size_t)t * L::TREC + 2 * D + j] = ga;
-                if (!isfinite(x) || !isfinite(ga)) bad = true;
+                gchk = fmaf(x, 0.f, fmaf(ga, 0.f, gchk));
             }
         }
         // rows: g_e = gS alpha^ + dL/do (phi_q . alpha^) / den = dL/dv
@@ -355,7 +354,7 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
         if (l < RW) {
             const float x = pick<RW>(ger, l);
             dv[orow + r0 + l] = x;
-            if (!isfinite(x)) bad = true;
+            gchk = fmaf(x, 0.f, gchk);
         }
         // product pass 2: columns S_t^T g_e
         {
@@ -398,10 +397,7 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
         j_ege = e_ge, j_nk = nk;
     }
     __syncthreads();  // pass-2 partials of token 0 visible
-    if (T > 0 && ku_warp) {
-        if (!k_grad_s<D, TIn>(ring, P2, RED, jw, pick<CL>(gzk, jw), j_ege, j_nk, dk + (size_t)bh * T * D))
-            bad = true;
-    }
+    if (T > 0 && ku_warp) gchk += k_grad_s<D, TIn>(ring, P2, RED, jw, pick<CL>(gzk, jw), j_ege, j_nk, dk + (size_t)bh * T * D);
     cp_wait<0>();
 #pragma unroll
     for (int r = 0; r < RW; ++r)
@@ -411,7 +407,7 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
     if (w == 0 && dzk0)
 #pragma unroll
         for (int c = 0; c < CL; ++c) dzk0[(size_t)bh * D + l + 32 * c] = gzk[c];
-    if (bad) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
+    if (gchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
 }
 
 // A side of the reverse sweep, after the S side: g_a_t is in the tape's e_t slot.
@@ -440,7 +436,7 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
     const TIn* gk = static_cast<const TIn*>(p.k) + hin;
     const float* tp = tape + (size_t)bh * T * L::TREC;
     const float* cp = ckpt + (size_t)bh * ((T + CK - 1) / CK + 1) * L::CREC;
-    bool bad = false;
+    float gchk = 0.f;  // fma(x, 0, .) of every gradient written: 0 unless one is NaN or Inf
 
     float A[RW][CL], gA[RW][CL];
 #pragma unroll
@@ -526,11 +522,9 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
                 for (int v = 0; v < NW; ++v) s += DP[v];
                 DS[0] = s;
             }
-            if (ku_warp && t + 1 < T) {
-                if (!ku_grad_a<D, TIn>(ring + ((t + 1) % NB) * L::SLOT_B, R2, RED, jw, j_kz, j_gdl, j_zgz, j_az,
-                                       j_nac, j_dl, j_nu, j_nk, dk + orow + D, du + orow + D))
-                    bad = true;
-            }
+            if (ku_warp && t + 1 < T)
+                gchk += ku_grad_a<D, TIn>(ring + ((t + 1) % NB) * L::SLOT_B, R2, RED, jw, j_kz, j_gdl, j_zgz, j_az,
+                                          j_nac, j_dl, j_nu, j_nk, dk + orow + D, du + orow + D);
         }
         __syncthreads();  // B2
 
@@ -594,18 +588,16 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
         j_kz = kz, j_gdl = gdl, j_zgz = zgz, j_az = az, j_nac = nac, j_dl = dl, j_nu = nu, j_nk = nk;
     }
     __syncthreads();  // pass-2 products of token 0 visible
-    if (T > 0 && ku_warp) {
-        if (!ku_grad_a<D, TIn>(ring, R2, RED, jw, j_kz, j_gdl, j_zgz, j_az, j_nac, j_dl, j_nu, j_nk,
-                               dk + (size_t)bh * T * D, du + (size_t)bh * T * D))
-            bad = true;
-    }
+    if (T > 0 && ku_warp)
+        gchk += ku_grad_a<D, TIn>(ring, R2, RED, jw, j_kz, j_gdl, j_zgz, j_az, j_nac, j_dl, j_nu, j_nk,
+                                  dk + (size_t)bh * T * D, du + (size_t)bh * T * D);
     cp_wait<0>();
 #pragma unroll
     for (int r = 0; r < RW; ++r)
 #pragma unroll
         for (int c = 0; c < CL; ++c)
             if (dA0) dA0[hdd + (r0 + r) * D + l + 32 * c] = gA[r][c];
-    if (bad) record_failure(p.status, BIT_NONFINITE, ROLE_A, bh, -1);
+    if (gchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_A, bh, -1);
 }
 
 }  // namespace bw
