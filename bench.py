@@ -68,22 +68,24 @@ KERNEL_FILES = {
 # was taken on (B, H, T, d, input dtype) and while that kernel's own sources
 # hash to source_sha; otherwise reported as null.
 NCU_TRAFFIC = {
-    "vla_tc_kernel": {"source_sha": "e4fa02df82d8ceba", "workload": (8, 16, 4096, 96, "bf16"),
-                      "bytes_per_launch": 402738432 + 176217344},
+    "vla_tc_kernel": {"source_sha": "da589c5764bac785", "workload": (8, 16, 4096, 96, "bf16"),
+                      "bytes_per_launch": 403224320 + 176125696},
     # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
-    "vla_tc3_kernel": {"source_sha": "8b2b3debd6495128", "workload": (1, 32, 65536, 128, "bf16"),
-                       "bytes_per_launch": 8 * (268544768 + 108853248 - 4227072) + 4227072},
+    "vla_tc3_kernel": {"source_sha": "b4c1c5b5d98e43a0", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (268544768 + 108939008 - 4227072) + 4227072},
     # the reverse sweep (the step's dominant kernel, after the taped chunked forward), from a capture of
     # the same workload at B=2 (32 heads; a full step holds about 2.8 GB on the device) scaled by 4:
     # every byte it moves is per head-token or per head
-    "vla_backward_kernel": {"source_sha": "7309d7fdbbe5647d", "workload": (8, 16, 4096, 96, "bf16"),
-                            "bytes_per_launch": 4 * (436558848 + 176801024)},
+    "vla_backward_kernel": {"source_sha": "dd6f677c14be50e6", "workload": (8, 16, 4096, 96, "bf16"),
+                            "bytes_per_launch": 4 * (436399360 + 176777472)},
     # the S side of the split reverse sweep (d = 128), on the long-context workload cut to 4096 tokens
-    "vla_backward_s_kernel": {"source_sha": "dfab26bbfa0604e0", "workload": (1, 32, 4096, 128, "bf16"),
-                              "bytes_per_launch": 477381120 + 237421056},
-    "vla_decode_kernel": {"source_sha": "9266c08b57d2ba6a", "workload": (128, 16, 1, 96, "bf16"),
-                          "bytes_per_launch": 153394432 + 98736640},
+    "vla_backward_s_kernel": {"source_sha": "51cc31c4afb81d1a", "workload": (1, 32, 4096, 128, "bf16"),
+                              "bytes_per_launch": 477811200 + 237591040},
+    "vla_decode_kernel": {"source_sha": "6dc773112e35b2c5", "workload": (128, 16, 1, 96, "bf16"),
+                          "bytes_per_launch": 153399040 + 98538240},
+    "vla_fused_kernel": {"source_sha": "d590b5be864eccb8", "workload": (8, 16, 4096, 96, "bf16"),
+                         "bytes_per_launch": 403607808 + 175779584},
 }
 
 

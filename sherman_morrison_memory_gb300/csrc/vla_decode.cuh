@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(DLay<D, TIn>::THREADS, 1) vla_decode_kernel(co
     const int r0 = w * RW, rr = r0 + (l >> 2);
     const int T = p.T;
     bool bad = false;
+    float ochk = 0.f;  // fma(o, 0, .) of every output: 0 unless one is NaN or Inf (branch-free)
 
     if (bulk) {
         if (tid == 0) {
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(DLay<D, TIn>::THREADS, 1) vla_decode_kernel(co
             const float orow = fmaf(erow, d2[1] * ina, sphi) / den;
             if ((l & 3) == 0) {
                 p.o[(size_t)bh * p.o_stride + (size_t)t * D + rr] = orow;
-                if (!isfinite(orow)) bad = true;
+                ochk = fmaf(orow, 0.f, ochk);
             }
             if (l == 0 && w == 0 && (!isfinite(dl) || !isfinite(d2[0]) || !isfinite(pd))) bad = true;
 #pragma unroll
@@ -358,8 +359,9 @@ __global__ void __launch_bounds__(DLay<D, TIn>::THREADS, 1) vla_decode_kernel(co
         if (w == 0 && p.zk_out)
 #pragma unroll
             for (int c = 0; c < CL; ++c) p.zk_out[(size_t)bh * D + l + 32 * c] = zk[c];
-        if (bad) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
+        if (bad || ochk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
         bad = false;
+        ochk = 0.f;
     }
     if (L::BULK_OUT && tid == 0) bulk_wait_all();
 }
