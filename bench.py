@@ -53,7 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 # The source files each kernel is compiled from (besides the launch code).
 KERNEL_FILES = {
     "vla_tc_kernel": ("vla_tc.cuh", "vla_device.cuh"),
-    "vla_fused_kernel": ("vla_forward.cu", "vla_device.cuh"),
+    "vla_fused_kernel": ("vla_fused.cuh", "vla_device.cuh"),
     "vla_backward_kernel": ("vla_backward.cuh", "vla_device.cuh"),
     # the split reverse sweep (d = 128): its S side, its A side
     "vla_backward_s_kernel": ("vla_backward_split.cuh", "vla_backward.cuh", "vla_device.cuh"),
@@ -84,8 +84,8 @@ NCU_TRAFFIC = {
                               "bytes_per_launch": 477811200 + 237591040},
     "vla_decode_kernel": {"source_sha": "6dc773112e35b2c5", "workload": (128, 16, 1, 96, "bf16"),
                           "bytes_per_launch": 153399040 + 98538240},
-    "vla_fused_kernel": {"source_sha": "d590b5be864eccb8", "workload": (8, 16, 4096, 96, "bf16"),
-                         "bytes_per_launch": 403607808 + 175779584},
+    "vla_fused_kernel": {"source_sha": "565a71784acabc88", "workload": (8, 16, 4096, 96, "bf16"),
+                         "bytes_per_launch": 403125248 + 175399936},
 }
 
 

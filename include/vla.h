@@ -72,6 +72,16 @@ typedef struct {
                                     the A team only forms A0 k^), VLA_ALGO_CHUNKED_PAIR and
                                     VLA_ALGO_DECODE; VLA_ALGO_AUTO picks as for the full
                                     recurrence; VLA_ALGO_PER_TOKEN returns VLA_ERR_UNSUPPORTED */
+    void* scratch;               /* the segmented path's buffers for this call, in place of the
+                                    workspace past its status record (NULL: the workspace holds
+                                    them). Device memory of scratch_bytes >=
+                                    vla_workspace_bytes_ex(B, H, T, d, VLA_ALGO_SEGMENTED) bytes,
+                                    256-byte aligned, laid out as that workspace (its first 256
+                                    bytes unused), no zero-fill needed. With it, calls that may
+                                    overlap on the GPU share one status record and each keeps
+                                    buffers of its own; under VLA_ALGO_AUTO the segmented path is
+                                    taken when either buffer holds them */
+    size_t scratch_bytes;
 } vla_options;
 
 /* Kernels behind vla_forward_ex() (vla_options.algo). All compute eq. 9-11
@@ -154,7 +164,11 @@ vla_status vla_workspace_reset(void* workspace, void* stream);
  *  workspace    device memory, its first 256 bytes zero-filled (the device status
  *               record), 16-byte aligned; 256 bytes suffice for every kernel but the
  *               segmented path, which needs vla_workspace_bytes(B, H, T, d) bytes and
- *               256-byte alignment.
+ *               256-byte alignment (or its own buffers, vla_options.scratch). Those
+ *               buffers are the call's scratch: calls that may overlap on the GPU
+ *               (different streams, no ordering between them) need separate ones.
+ *               The status record may be shared: the kernels OR their error bits
+ *               into it atomically and keep the details of the first failure.
  *  stream       cudaStream_t as void*.
  *
  * Inputs and outputs must not overlap (S0/S_out, A0/A_out, zk0/zk_out may be
@@ -249,8 +263,8 @@ vla_status vla_forward_noalloc(const void* q, const void* k, const void* v, cons
  *               chunk by chunk.
  *  chunk_tokens tokens per launch, >= 0 (0 = automatic; values above T mean T).
  *  workspace    device memory of vla_forward_host_workspace_bytes() bytes,
- *               256-byte aligned, its first vla_workspace_bytes(B, H, T, d) bytes
- *               zero-filled before the first use (the status record, read by
+ *               256-byte aligned, its first 256 bytes zero-filled before the
+ *               first use (the status record, read by
  *               vla_get_last_device_status(workspace, stream)). It holds the
  *               carried state and three input and three output slots of one chunk.
  *  stream, opts as for vla_forward_ex (the kernels run on `stream`).

@@ -6,6 +6,7 @@ called on the current CUDA stream. All arithmetic happens in the library.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -48,7 +49,8 @@ class VLAError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("wait_limit_us", ctypes.c_uint), ("test_stall_producer", ctypes.c_int),
-                ("trace", ctypes.c_void_p), ("algo", ctypes.c_int), ("fixed_a", ctypes.c_int)]
+                ("trace", ctypes.c_void_p), ("algo", ctypes.c_int), ("fixed_a", ctypes.c_int),
+                ("scratch", ctypes.c_void_p), ("scratch_bytes", ctypes.c_size_t)]
 
 
 def library_path() -> str:
@@ -139,20 +141,37 @@ def _stream_handle(device: torch.device, stream=None) -> int:
     return int(stream.cuda_stream)
 
 
-def _workspace(device: torch.device, nbytes: int = 0) -> torch.Tensor:
-    """The device's status workspace (shared by the calls on it, so that the
-    status is sticky until vla_get_last_device_status reads it), grown to at
-    least `nbytes` bytes (default: what a call at any supported shape needs)."""
+_STATUS_BYTES = 256
+
+
+def _workspace(device: torch.device) -> torch.Tensor:
+    """The device's status record (shared by the calls on it, so that the
+    status is sticky until vla_get_last_device_status reads it; the kernels OR
+    their error bits into it atomically, so calls on several streams may share
+    it). Make one call on a device before capturing a CUDA graph there."""
     idx = device.index if device.index is not None else torch.cuda.current_device()
-    nbytes = max(int(nbytes), vla_workspace_bytes())
     ws = _WORKSPACES.get(idx)
-    if ws is None or ws.numel() * 4 < nbytes:
-        grown = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=torch.device("cuda", idx))
-        if ws is not None:
-            grown[:ws.numel()].copy_(ws)
-        ws = grown
+    if ws is None:
+        ws = torch.zeros(_STATUS_BYTES // 4, dtype=torch.int32, device=torch.device("cuda", idx))
         _WORKSPACES[idx] = ws
     return ws
+
+
+def _on_stream(stream):
+    """Allocate for `stream`: the caching allocator hands a block freed there
+    to later work only once the work queued on that stream before the free
+    has run, so a call's own buffers need no other lifetime management."""
+    return contextlib.nullcontext() if stream is None else torch.cuda.stream(stream)
+
+
+def _call_buffer(device: torch.device, nbytes: int, zero_status: bool) -> torch.Tensor:
+    """Device memory of one call (the segmented path's buffers, a backward
+    tape, a host-path staging area), 512-byte aligned by the caching
+    allocator; its status record zeroed if asked."""
+    buf = torch.empty((int(nbytes) + 3) // 4, dtype=torch.int32, device=device)
+    if zero_status:
+        buf[:_STATUS_BYTES // 4].zero_()
+    return buf
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -190,7 +209,10 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
     head: A-pass and S-pass on separate SMs; any d), VLA_ALGO_CHUNKED_ROWS (5,
     a cluster of 1 + NS CTAs per head with S's rows split over NS of them) or
     VLA_ALGO_SEGMENTED (6, the sequence's two halves side by side; d <= 96,
-    T >= 32). The workspace is sized for the choice (vla_workspace_bytes_ex).
+    T >= 32). The segmented path's buffers (vla_workspace_bytes_ex) are
+    the call's own, from torch's caching allocator on the call's stream, so
+    calls on different streams may overlap and a call may be captured in a
+    CUDA graph (after one eager call on the device).
     ``fixed_a=True`` runs the fixed-A variant (§3.5 ablation): A stays at its
     initial value, u is not read (it may be None).
     """
@@ -219,22 +241,24 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
         S0 = _check_state(S0, (B, H, d, d), dev, "S0")
         A0 = _check_state(A0, (B, H, d, d), dev, "A0")
         zk0 = _check_state(zk0, (B, H, d), dev, "zk0")
-    if out is None:
-        o = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
-        S = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
-        A = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
-        zk = torch.empty((B, H, d), dtype=torch.float32, device=dev)
-    else:
-        o, S, A, zk = out
-    ws = _workspace(dev, int(load_library().vla_workspace_bytes_ex(B, H, T, d, int(algo))))
-    with torch.cuda.device(dev):
+    ws = _workspace(dev)
+    nbytes = int(lib.vla_workspace_bytes_ex(B, H, T, d, int(algo)))
+    with torch.cuda.device(dev), _on_stream(stream):
+        if out is None:
+            o = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
+            S = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+            A = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+            zk = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+        else:
+            o, S, A, zk = out
+        scratch = _call_buffer(dev, nbytes, False) if nbytes > _STATUS_BYTES else None
         sh = _stream_handle(dev, stream)
         args = (_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d,
                 float(lambda0), float(eps), _ptr(S0), _ptr(A0), _ptr(zk0),
                 _ptr(o), _ptr(S), _ptr(A), _ptr(zk), _ptr(ws), ws.numel() * 4, ctypes.c_void_p(sh))
-        if wait_limit_us or test_stall_producer or algo or fixed_a:
+        if wait_limit_us or test_stall_producer or algo or fixed_a or scratch is not None:
             opts = _Options(int(wait_limit_us), 1 if test_stall_producer else 0, None, int(algo),
-                            1 if fixed_a else 0)
+                            1 if fixed_a else 0, _ptr(scratch), 0 if scratch is None else scratch.numel() * 4)
             st = lib.vla_forward_ex(*args, ctypes.byref(opts))
         else:
             st = lib.vla_forward(*args)
@@ -245,9 +269,6 @@ def vla_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tens
         if st != VLA_OK:
             raise VLAError(st, "vla_forward (device)", detail)
     return o, (S, A, zk)
-
-
-_HOST_WORKSPACES = {}
 
 
 def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False, algo=0, fixed_a=False,
@@ -294,12 +315,8 @@ def _forward_host(q, k, v, u, lambda0, eps, state, out=None, check=False, algo=0
     nbytes = int(lib.vla_forward_host_workspace_bytes(_DTYPES[q.dtype], B, H, T, d, int(chunk_tokens)))
     if nbytes == 0:
         raise ValueError("unsupported sizes for vla_forward_host")
-    ws = _HOST_WORKSPACES.get(dev.index)
-    if ws is None or ws.numel() * 4 < nbytes:
-        _HOST_WORKSPACES.pop(dev.index, None)
-        ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=dev)
-        _HOST_WORKSPACES[dev.index] = ws
-    with torch.cuda.device(dev):
+    with torch.cuda.device(dev), _on_stream(stream):
+        ws = _call_buffer(dev, nbytes, True)
         sh = _stream_handle(dev, stream)
         opts = _Options(0, 0, None, int(algo), 1 if fixed_a else 0)
         st = lib.vla_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d,
@@ -327,9 +344,6 @@ def vla_get_last_device_status(device=None, stream=None) -> Tuple[int, tuple]:
     with torch.cuda.device(dev):
         st = lib.vla_get_last_device_status(_ptr(ws), ctypes.c_void_p(_stream_handle(dev, stream)), detail)
     return int(st), (detail[0], detail[1], detail[2])
-
-
-_BW_WORKSPACES = {}
 
 
 def _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, check, split):
@@ -392,7 +406,8 @@ def vla_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Ten
         gzk = _check_state(gzk, (B, H, d), dev, "dzk_T")
     shapes = [(B, H, T, d)] * 4 + [(B, H, d, d), (B, H, d, d), (B, H, d)]
     if out is None:
-        res = [torch.empty(sh, dtype=torch.float32, device=dev) for sh in shapes]
+        with torch.cuda.device(dev), _on_stream(stream):
+            res = [torch.empty(sh, dtype=torch.float32, device=dev) for sh in shapes]
     else:
         res = list(out)
         if len(res) != 7:
@@ -405,12 +420,8 @@ def vla_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Ten
     nbytes = int(lib.vla_backward_workspace_bytes(B, H, T, d))
     if nbytes == 0:
         raise ValueError("sizes overflow the backward workspace")
-    idx = dev.index if dev.index is not None else torch.cuda.current_device()
-    ws = _BW_WORKSPACES.get(idx)
-    if ws is None or ws.numel() * 4 < nbytes:
-        ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=dev)
-        _BW_WORKSPACES[idx] = ws
-    with torch.cuda.device(dev):
+    with torch.cuda.device(dev), _on_stream(stream):
+        ws = _call_buffer(dev, nbytes, True)
         sh = _stream_handle(dev, stream)
         fn = lib.vla_backward_split if split else lib.vla_backward
         st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d, float(lambda0), float(eps),
@@ -434,8 +445,8 @@ def vla_linear_attention_state(k: torch.Tensor, v: torch.Tensor, stream=None) ->
         raise ValueError("k, v must be matching [B, H, T, d] tensors")
     k, v = k.contiguous(), v.contiguous()
     B, H, T, d = k.shape
-    S = torch.empty((B, H, d, d), dtype=torch.float32, device=k.device)
-    with torch.cuda.device(k.device):
+    with torch.cuda.device(k.device), _on_stream(stream):
+        S = torch.empty((B, H, d, d), dtype=torch.float32, device=k.device)
         st = lib.vla_linear_attention_state(_ptr(k), _ptr(v), _DTYPES[k.dtype], B, H, T, d, _ptr(S),
                                             ctypes.c_void_p(_stream_handle(k.device, stream)))
     if st != VLA_OK:

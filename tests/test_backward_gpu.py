@@ -154,6 +154,30 @@ def test_workload_d96_sampled_heads(orc):
         assert torch.isfinite(g).all()
 
 
+def test_two_streams_at_once(orc):
+    """Two calls on two streams with no ordering between them: each has its
+    own tape (the call's buffer from the caching allocator), so both results
+    are the oracle's."""
+    cases = []
+    for seed in (31, 32):
+        arrs = _inputs(1, 2, 129, 64, "bf16", seed=seed)
+        gO, gst = _seeds(1, 2, 129, 64, seed=seed)
+        cases.append((arrs, gO, gst))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    dev_in = [([_dev(a, torch.bfloat16) for a in arrs], _dev(gO), tuple(_dev(x) for x in gst))
+              for arrs, gO, gst in cases]
+    torch.cuda.synchronize()
+    res = []
+    for (x, g, gs), st in zip(dev_in, streams):
+        with torch.cuda.stream(st):
+            res.append(vla_backward(*x, 0.1, 1e-4, None, g, gs))
+    torch.cuda.synchronize()
+    for (arrs, gO, gst), (grads, dstate) in zip(cases, res):
+        ref = orc.backward(*(_f64(a) for a in arrs), 0.1, 1e-4, None, None, None, _f64(gO),
+                           *(_f64(x) for x in gst))
+        assert_close(_errors(grads, dstate, ref), what="backward on two streams")
+
+
 @pytest.mark.parametrize("tensor", [0, 1, 2, 3])
 def test_nonfinite_input_is_reported(tensor):
     arrs = [np.array(a) for a in _inputs(1, 1, 40, 64, "f32", seed=12)]

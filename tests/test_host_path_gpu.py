@@ -125,7 +125,9 @@ def test_workspace_size_and_arguments():
     assert _binding.vla_get_last_device_status("cuda")[0] == VLA_OK
 
 
-def test_back_to_back_calls_share_workspace(orc):
+def test_back_to_back_calls_of_different_shapes(orc):
+    """Two calls enqueued one after the other, each with its own staging
+    buffers from the caching allocator, before any synchronisation."""
     arrs_a = _inputs(1, 2, 120, 64, "f32", seed=25)
     arrs_b = _inputs(2, 2, 333, 96, "bf16", seed=26)
     oa = vla_forward(*_host(arrs_a, "f32"), chunk_tokens=32)

@@ -157,6 +157,72 @@ def test_segmented_path_is_automatic_for_few_heads(orc):
     assert_close(errors(out, ref), what="automatic segmented path")
 
 
+def test_segmented_path_two_streams_at_once(orc):
+    """Two calls on two streams at the same time share the path's side streams
+    and events (created once per device); each result is the oracle's."""
+    arrs = [_inputs(2, 2, 16 * 20 + 3, 64, "bf16", seed=s) for s in (81, 82)]
+    dev = [to_dev(a, "bf16") for a in arrs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for d_, st in zip(dev, streams):
+        with torch.cuda.stream(st):
+            outs.append(vla_forward(*d_, algo=VLA_ALGO_SEGMENTED))
+    torch.cuda.synchronize()
+    for a, out in zip(arrs, outs):
+        assert_close(errors(out, orc.forward(*a)), what="segmented path, two streams")
+
+
+def test_segmented_path_from_two_threads(orc):
+    """Two host threads, each on a stream of its own, call the segmented path
+    three times each; the side streams are per thread, the buffers per call."""
+    import threading
+    arrs = [_inputs(1, 4, 16 * 24 + 9, 32, "bf16", seed=s) for s in (85, 86)]
+    dev = [to_dev(a, "bf16") for a in arrs]
+    torch.cuda.synchronize()
+    outs, errs = [[], []], []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(0)
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(3):
+                    outs[i].append(vla_forward(*dev[i], algo=VLA_ALGO_SEGMENTED))
+            st.synchronize()
+        except Exception as e:  # surfaced in the main thread
+            errs.append(e)
+
+    th = [threading.Thread(target=work, args=(i,)) for i in (0, 1)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not errs, errs
+    for a, res in zip(arrs, outs):
+        ref = orc.forward(*a)
+        for out in res:
+            assert_close(errors(out, ref), what="segmented path from two threads")
+
+
+def test_segmented_path_in_a_cuda_graph(orc):
+    """The path's fork and join (event waits on its side streams) captured into
+    a CUDA graph after one eager call, then replayed on new inputs copied into
+    the captured buffers."""
+    B, H, T, d = 1, 3, 16 * 12 + 5, 64
+    a1, a2 = _inputs(B, H, T, d, "bf16", seed=83), _inputs(B, H, T, d, "bf16", seed=84)
+    q, k, v, u = to_dev(a1, "bf16")
+    vla_forward(q, k, v, u, algo=VLA_ALGO_SEGMENTED)  # first use: side streams, events, workspace
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        o, (S, A, zk) = vla_forward(q, k, v, u, algo=VLA_ALGO_SEGMENTED)
+    for dst, src in zip((q, k, v, u), to_dev(a2, "bf16")):
+        dst.copy_(src)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_close(errors((o, (S, A, zk)), orc.forward(*a2)), what="segmented path replayed from a CUDA graph")
+
+
 @pytest.mark.parametrize("noise", [0.1, 0.01])
 def test_segmented_path_ill_conditioned(orc, noise):
     """u concentrated on 8 directions plus small noise, so that the penalty
