@@ -55,9 +55,8 @@ KERNEL_FILES = {
     "vla_tc_kernel": ("vla_tc.cuh", "vla_device.cuh"),
     "vla_fused_kernel": ("vla_fused.cuh", "vla_device.cuh"),
     "vla_backward_kernel": ("vla_backward.cuh", "vla_device.cuh"),
-    # the split reverse sweep (d = 128): its S side, its A side
-    "vla_backward_s_kernel": ("vla_backward_split.cuh", "vla_backward.cuh", "vla_device.cuh"),
-    "vla_backward_a_kernel": ("vla_backward_split.cuh", "vla_backward.cuh", "vla_device.cuh"),
+    # the split reverse sweep (d = 128): its S side and A side as a cluster of two CTAs per head
+    "vla_backward_pair_kernel": ("vla_backward_split.cuh", "vla_backward.cuh", "vla_device.cuh"),
     "vla_decode_kernel": ("vla_decode.cuh", "vla_backward.cuh", "vla_device.cuh"),
     "vla_tc2_kernel": ("vla_tc2.cuh", "vla_tc.cuh", "vla_device.cuh"),
     "vla_tc3_kernel": ("vla_tc3.cuh", "vla_tc2.cuh", "vla_tc.cuh", "vla_device.cuh"),
@@ -79,9 +78,9 @@ NCU_TRAFFIC = {
     # every byte it moves is per head-token or per head
     "vla_backward_kernel": {"source_sha": "dd6f677c14be50e6", "workload": (8, 16, 4096, 96, "bf16"),
                             "bytes_per_launch": 4 * (436399360 + 176777472)},
-    # the S side of the split reverse sweep (d = 128), on the long-context workload cut to 4096 tokens
-    "vla_backward_s_kernel": {"source_sha": "51cc31c4afb81d1a", "workload": (1, 32, 4096, 128, "bf16"),
-                              "bytes_per_launch": 477811200 + 237591040},
+    # the split reverse sweep (d = 128) on the long-context workload cut to 4096 tokens
+    "vla_backward_pair_kernel": {"source_sha": "323d472e58ba06ae", "workload": (1, 32, 4096, 128, "bf16"),
+                                 "bytes_per_launch": 648219904 + 307873792},
     "vla_decode_kernel": {"source_sha": "6dc773112e35b2c5", "workload": (128, 16, 1, 96, "bf16"),
                           "bytes_per_launch": 153399040 + 98538240},
     "vla_fused_kernel": {"source_sha": "565a71784acabc88", "workload": (8, 16, 4096, 96, "bf16"),
@@ -775,9 +774,9 @@ def run_ours_backward(args, w):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
     # d <= 96: the taped chunked forward and the single-kernel reverse sweep;
-    # d = 128: the taped per-token forward and the two sweeps of the split form
-    kernel = "vla_backward_kernel" if d <= 96 else "vla_backward_s_kernel"
-    launches_per_step = 2 if d <= 96 else 3
+    # d = 128: the taped per-token forward and the split sweep (one cluster of two CTAs per head)
+    kernel = "vla_backward_kernel" if d <= 96 else "vla_backward_pair_kernel"
+    launches_per_step = 2
     sha = kernel_source_sha(kernel)
     traffic = ncu_traffic(kernel, (w.B, w.H, w.T, w.d, w.dtype))
 

@@ -349,11 +349,13 @@ vla_status vla_backward(const void* q, const void* k, const void* v, const void*
  * (the path d = 128 always takes). The adjoint recursion of S (eq. 10, 11)
  * needs nothing from the A side, and the A side (eq. 9, 10) needs only the
  * gate's gradient g_a = (g_alpha - alpha^ (alpha^ . g_alpha)) / ||A_t k^_t||
- * per token from it. So one kernel sweeps t = T-1 .. 0 with S and its adjoint,
- * writing dq, dv, the S part of dk and g_a (into the workspace's tape); a
- * second sweeps with A and its adjoint, writing du and adding the A part of
- * dk. Same arguments, workspace size, results (to rounding) and errors as
- * vla_backward(). */
+ * per token from it. So one kernel runs a cluster of two CTAs per head: one
+ * sweeps t = T-1 .. 0 with S and its adjoint, writing dq, dv, the S part of
+ * dk and g_a (into the workspace's tape); the other sweeps with A and its
+ * adjoint a few tokens behind, as the first publishes its progress, writing
+ * du and adding the A part of dk. Same arguments, workspace size, results
+ * (to rounding) and errors as vla_backward(), and VLA_ERR_TIMEOUT if the A
+ * side's wait for the S side's progress (2 s) runs out. */
 vla_status vla_backward_split(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype,
                               int B, int H, int T, int d, float lambda0, float eps,
                               const float* S0, const float* A0, const float* zk0,

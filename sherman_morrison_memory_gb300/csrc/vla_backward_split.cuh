@@ -10,14 +10,27 @@
 // and every other S-side quantity (g_e, dL/dv, dL/dq, the z^key adjoint, the
 // S part of dL/dk^) follows from S, gS and the tape. The A side (eq. 9, eq. 10
 // first half) needs g_a and nothing else from the S side. So:
-//  * vla_backward_s_kernel sweeps t = T-1 .. 0 with S and gS in registers,
-//    writes dL/dq, dL/dv, the S part of dL/dk (the z^key term and the
-//    projected -S_{t-1}^T g_e, both linear in the S side), and g_a over the
-//    tape's e_t (no later step reads e_t);
-//  * vla_backward_a_kernel then sweeps with A and gA, reads g_a from the tape,
-//    writes dL/du and adds the A part of dL/dk (the projected A_t g_a).
-// Each kernel holds two d x d matrices, half of the single-kernel sweep, so
+//  * the S side sweeps t = T-1 .. 0 with S and gS in registers, writes
+//    dL/dq, dL/dv, the S part of dL/dk (the z^key term and the projected
+//    -S_{t-1}^T g_e, both linear in the S side), and g_a over the tape's e_t
+//    (no later step reads e_t);
+//  * the A side sweeps with A and gA, reads g_a from the tape, writes dL/du
+//    and adds the A part of dL/dk (the projected A_t g_a).
+// Each side holds two d x d matrices, half of the single-kernel sweep, so
 // d = 128 fits (8 rows x 4 columns of each per thread, 512 threads).
+//
+// vla_backward_pair_kernel runs both sides at once, as a cluster of two CTAs
+// per head: CTA 0 the S side, CTA 1 the A side a few tokens behind it. After
+// the first block barrier of its step for token t, one otherwise idle S-side
+// thread publishes t + 1 (every write of the steps for tokens > t is done:
+// g_a of those tokens, the S part of dL/dk of tokens > t + 1) with a release
+// store at cluster scope into a counter in the A side's shared memory; 0 and
+// -1 follow the last step and the last dL/dk. The A side reads the counter
+// with acquire loads before it prefetches a token's tape record, in one
+// thread and then a block barrier, with a time limit (VLA_ERR_TIMEOUT). The S
+// side never waits for the A side, and both CTAs meet at a cluster barrier
+// before they exit, so neither leaves while the other may still write into
+// its shared memory.
 //
 // The register layout, the row and column products, the checkpoints and the
 // identities that save products are those of vla_backward.cuh.
@@ -73,6 +86,54 @@ struct ALay {
     static_assert(2 * IN_B / 16 + TREC / 4 <= THREADS, "one prefetch chunk per thread");
     static_assert(NW == 4 * CL, "column sums on CL warps, the dot sum on one more, dL/dk, dL/du on the last CL");
 };
+
+// the two-CTA form: the counter sits past both sides' shared memory
+template <int D, typename TIn>
+struct PairLay {
+    static constexpr int FLAG = (std::max(SLay<D, TIn>::SMEM, ALay<D, TIn>::SMEM) + 15) / 16 * 16;
+    static constexpr int SMEM = FLAG + 16;
+    // the S-side thread that publishes progress: lane 31 of a warp with no
+    // work between the step's two block barriers (else of the warp that sums
+    // the two dots, whose lanes 0 and 1 work there)
+    static constexpr int NW = SLay<D, TIn>::NW, CL = SLay<D, TIn>::CL;
+    static constexpr int PUB = 32 * ((2 * CL + 1 < NW - CL) ? 2 * CL + 1 : 2 * CL) + 31;
+    static_assert(SLay<D, TIn>::THREADS == ALay<D, TIn>::THREADS, "both sides run on CTAs of one size");
+};
+
+__device__ __forceinline__ uint32_t pair_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint32_t pair_peer(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+// every thread of both CTAs
+__device__ __forceinline__ void pair_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void pair_publish(uint32_t raddr, int v) {
+    asm volatile("st.release.cluster.shared::cluster.s32 [%0], %1;" ::"r"(raddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int pair_read(const int* f) {
+    int v;
+    asm volatile("ld.acquire.cluster.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(f)) : "memory");
+    return v;
+}
+// wait until the counter is at most `target`; false once `limit_ns` has passed
+__device__ __noinline__ bool pair_wait(const int* f, int target, uint64_t limit_ns) {
+    if (pair_read(f) <= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        __nanosleep(32);
+        if (pair_read(f) <= target) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+}
 
 template <int D, typename TIn>
 __device__ __forceinline__ void prefetch_s(unsigned char* slot, const TIn* gk, const TIn* gq, const float* go,
@@ -175,17 +236,18 @@ __device__ __forceinline__ float ku_grad_a(const unsigned char* sl, const float*
     const float dut = nu < 1e-24f ? guh * 1e12f : fmaf(-uhj, ugu, guh) * iu;
     const float dka = nk < 1e-24f ? aga * 1e12f : fmaf(-khj, kga, aga) * ik;
     du[j] = dut;
-    const float dkt = dk[j] + dka;
+    const float dkt = __ldcg(dk + j) + dka;  // the S part, written by the other CTA of a pair
     dk[j] = dkt;
     return fmaf(dut, 0.f, dkt * 0.f);
 }
 
-// S side of the reverse sweep. fin: the forward's final S [BH][D][D] | A | z^key [BH][D].
+// S side of the reverse sweep for head bh of BH. fin: the forward's final S
+// [BH][D][D] | A | z^key [BH][D]. rflag: the A side's progress counter.
 template <int D, typename TIn>
-__global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
-    vla_backward_s_kernel(const Params p, const float* dO, const float* dST, const float* dzkT, float* dq,
-                          float* dk, float* dv, float* dS0, float* dzk0, float* tape, const float* ckpt,
-                          const float* fin) {
+__device__ __forceinline__ void s_sweep(const Params& p, int bh, size_t BH, const float* dO, const float* dST,
+                                        const float* dzkT, float* dq, float* dk, float* dv, float* dS0,
+                                        float* dzk0, float* tape, const float* ckpt, const float* fin,
+                                        uint32_t rflag) {
     using L = SLay<D, TIn>;
     constexpr int RW = L::RW, CL = L::CL, NW = L::NW, NB = L::NB;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -200,8 +262,8 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
 
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
     const int r0 = w * RW, rr = r0 + (l >> 2);
-    const int bh = blockIdx.x, T = p.T;
-    const size_t BH = gridDim.x, hin = (size_t)bh * T * D, hdd = (size_t)bh * D * D;
+    const int T = p.T;
+    const size_t hin = (size_t)bh * T * D, hdd = (size_t)bh * D * D;
     const TIn* gq = static_cast<const TIn*>(p.q) + hin;
     const TIn* gk = static_cast<const TIn*>(p.k) + hin;
     const float* go_h = dO ? dO + hin : nullptr;
@@ -300,6 +362,7 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
         }
         cp_wait<1>();
         __syncthreads();  // B1 (also publishes token t-1's slot)
+        if (tid == PairLay<D, TIn>::PUB) pair_publish(rflag, t + 1);  // the step for token t+1 is done
         if (t >= 3) prefetch_s<D, TIn>(ring + ((t - 3) % NB) * L::SLOT_B, gk, gq, go_h, tp, t - 3);
         cp_commit();
         if (tid < 2 * D) {
@@ -397,7 +460,10 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
         j_ege = e_ge, j_nk = nk;
     }
     __syncthreads();  // pass-2 partials of token 0 visible
+    if (tid == PairLay<D, TIn>::PUB) pair_publish(rflag, 0);  // every step done
     if (T > 0 && ku_warp) gchk += k_grad_s<D, TIn>(ring, P2, RED, jw, pick<CL>(gzk, jw), j_ege, j_nk, dk + (size_t)bh * T * D);
+    __syncthreads();
+    if (tid == PairLay<D, TIn>::PUB) pair_publish(rflag, -1);  // the S part of dL/dk_0 is written
     cp_wait<0>();
 #pragma unroll
     for (int r = 0; r < RW; ++r)
@@ -410,11 +476,12 @@ __global__ void __launch_bounds__(SLay<D, TIn>::THREADS, 1)
     if (gchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
 }
 
-// A side of the reverse sweep, after the S side: g_a_t is in the tape's e_t slot.
+// A side of the reverse sweep for head bh of BH, behind the S side: g_a_t is
+// in the tape's e_t slot once the counter `flag` is at most t.
 template <int D, typename TIn>
-__global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
-    vla_backward_a_kernel(const Params p, const float* dAT, float* dk, float* du, float* dA0, const float* tape,
-                          const float* ckpt, const float* fin) {
+__device__ __forceinline__ void a_sweep(const Params& p, int bh, size_t BH, const float* dAT, float* dk, float* du,
+                                        float* dA0, const float* tape, const float* ckpt, const float* fin,
+                                        const int* flag) {
     using L = ALay<D, TIn>;
     constexpr int RW = L::RW, CL = L::CL, NW = L::NW, NB = L::NB;
     constexpr unsigned FULL = 0xffffffffu;
@@ -430,13 +497,20 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
 
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
     const int r0 = w * RW, rr = r0 + (l >> 2);
-    const int bh = blockIdx.x, T = p.T;
-    const size_t BH = gridDim.x, hin = (size_t)bh * T * D, hdd = (size_t)bh * D * D;
+    const int T = p.T;
+    const size_t hin = (size_t)bh * T * D, hdd = (size_t)bh * D * D;
     const TIn* gu = static_cast<const TIn*>(p.u) + hin;
     const TIn* gk = static_cast<const TIn*>(p.k) + hin;
     const float* tp = tape + (size_t)bh * T * L::TREC;
     const float* cp = ckpt + (size_t)bh * ((T + CK - 1) / CK + 1) * L::CREC;
     float gchk = 0.f;  // fma(x, 0, .) of every gradient written: 0 unless one is NaN or Inf
+    bool gave_up = false;  // thread 0: a wait for the S side ran out of time
+    auto wait_s = [&](int target) {  // thread 0: the S side's writes for tokens >= target are done
+        if (!gave_up && !pair_wait(flag, target, p.wait_ns)) {
+            gave_up = true;
+            record_failure(p.status, BIT_TIMEOUT, ROLE_A, bh, target);
+        }
+    };
 
     float A[RW][CL], gA[RW][CL];
 #pragma unroll
@@ -447,6 +521,8 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
             A[r][c] = T > 0 ? fin[BH * D * D + e] : 0.f;
             gA[r][c] = dAT ? dAT[e] : 0.f;
         }
+    if (tid == 0 && T > 0) wait_s(max(T - 3, 0));
+    __syncthreads();
     for (int s = 0; s < 3; ++s) {
         const int tok = T - 1 - s;
         if (tok >= 0) prefetch_a<D, TIn>(ring + (tok % NB) * L::SLOT_B, gu, gk, tp, tok);
@@ -506,6 +582,7 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
         }
         allreduce<3, 16>(d3);
         if (l == 0) DP[w] = d3[2];
+        if (tid == 0 && t >= 3) wait_s(t - 3);  // before token t-3's record is prefetched
         cp_wait<1>();
         __syncthreads();  // B1
         if (t >= 3) prefetch_a<D, TIn>(ring + ((t - 3) % NB) * L::SLOT_B, gu, gk, tp, t - 3);
@@ -587,6 +664,7 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
         }
         j_kz = kz, j_gdl = gdl, j_zgz = zgz, j_az = az, j_nac = nac, j_dl = dl, j_nu = nu, j_nk = nk;
     }
+    if (tid == 0) wait_s(-1);  // the S part of dL/dk_0
     __syncthreads();  // pass-2 products of token 0 visible
     if (T > 0 && ku_warp)
         gchk += ku_grad_a<D, TIn>(ring, R2, RED, jw, j_kz, j_gdl, j_zgz, j_az, j_nac, j_dl, j_nu, j_nk,
@@ -598,6 +676,27 @@ __global__ void __launch_bounds__(ALay<D, TIn>::THREADS, 1)
         for (int c = 0; c < CL; ++c)
             if (dA0) dA0[hdd + (r0 + r) * D + l + 32 * c] = gA[r][c];
     if (gchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_A, bh, -1);
+}
+
+// Both sides at once: a cluster of two CTAs per head (grid 2 BH), CTA 0 the S
+// side, CTA 1 the A side.
+template <int D, typename TIn>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SLay<D, TIn>::THREADS, 1)
+    vla_backward_pair_kernel(const Params p, const float* dO, const float* dST, const float* dAT, const float* dzkT,
+                             float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0, float* dzk0,
+                             float* tape, const float* ckpt, const float* fin) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    int* flag = reinterpret_cast<int*>(smem + PairLay<D, TIn>::FLAG);
+    const uint32_t rank = pair_rank();
+    const int bh = blockIdx.x >> 1;
+    const size_t BH = gridDim.x >> 1;
+    if (rank == 1 && threadIdx.x == 0) *flag = p.T;  // no step of the S side done yet
+    pair_sync();
+    if (rank == 0)
+        s_sweep<D, TIn>(p, bh, BH, dO, dST, dzkT, dq, dk, dv, dS0, dzk0, tape, ckpt, fin, pair_peer(flag, 1));
+    else
+        a_sweep<D, TIn>(p, bh, BH, dAT, dk, du, dA0, tape, ckpt, fin, flag);
+    pair_sync();  // neither CTA leaves while the other may still write into its shared memory
 }
 
 }  // namespace bw

@@ -788,16 +788,15 @@ vla_status launch_bw(const vla::Params& p, int BH, const float* dO, const float*
             return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
         }
     }
-    // the split sweep: the S side, then the A side (vla_backward_split.cuh)
-    using SL = vla::bw::SLay<D, TIn>;
-    using AL = vla::bw::ALay<D, TIn>;
-    auto sk = vla::bw::vla_backward_s_kernel<D, TIn>;
-    auto ak = vla::bw::vla_backward_a_kernel<D, TIn>;
-    if (cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(ak, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AL::SMEM) != cudaSuccess)
+    // the split sweep: its S side and A side side by side, a cluster of two
+    // CTAs per head (vla_backward_split.cuh)
+    using PL = vla::bw::PairLay<D, TIn>;
+    if (BH > (1 << 30)) return VLA_ERR_INVALID_ARG;  // grid 2 BH
+    auto pk = vla::bw::vla_backward_pair_kernel<D, TIn>;
+    if (cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PL::SMEM) != cudaSuccess)
         return VLA_ERR_CUDA;
-    sk<<<BH, SL::THREADS, SL::SMEM, s>>>(p, dO, dST, dzkT, dq, dk, dv, dS0, dzk0, tape, ckpt, fin);
-    ak<<<BH, AL::THREADS, AL::SMEM, s>>>(p, dAT, dk, du, dA0, tape, ckpt, fin);
+    pk<<<2 * BH, vla::bw::SLay<D, TIn>::THREADS, PL::SMEM, s>>>(p, dO, dST, dAT, dzkT, dq, dk, dv, du, dS0, dA0, dzk0,
+                                                               tape, ckpt, fin);
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
 }
 
