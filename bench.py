@@ -774,7 +774,7 @@ def run_ours_backward(args, w):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_gbs = (in_bytes + out_bytes) / (ms / 1e3) / 1e9
     # d <= 96: the taped chunked forward and the single-kernel reverse sweep;
-    # d = 128: the taped per-token forward and the split sweep (one cluster of two CTAs per head)
+    # d = 128: the taped cluster-pair chunked forward and the split sweep (one cluster of two CTAs per head)
     kernel = "vla_backward_kernel" if d <= 96 else "vla_backward_pair_kernel"
     launches_per_step = 2
     sha = kernel_source_sha(kernel)

@@ -3,15 +3,16 @@
 // Jacobian of §4.2 eq. 14 is the adjoint step of the S recurrence below).
 // Included by vla_forward.cu inside namespace vla.
 //
-// One CTA per (b, h), two phases:
-//  1. the forward recurrence, token by token, writing a tape to the workspace:
-//     z_t (eq. 9), alpha^_t and ||a_t|| (eq. 10), e_t (eq. 10), delta_t, den_t
-//     (eq. 11) and ||u_t||^2, ||k_t||^2; S, A and z^key every CK tokens;
-//  2. the reverse sweep t = T-1 .. 0 applying the adjoint of each step of
-//     eq. 9-11 in reverse order. S_{t-1} and A_{t-1} are rebuilt from S_t, A_t
-//     by undoing the step's rank-1 update (S_{t-1} = S_t - e alpha^^T,
-//     A_{t-1} = A_t + z z^T / delta) and reloaded from the checkpoint every CK
-//     tokens.
+// The forward pass runs first, on the chunked tensor-core kernels in their
+// TAPE mode (vla_tc.cuh for d <= 96, vla_tc2.cuh for d = 128): they write a
+// tape to the workspace (per token z_t (eq. 9), alpha^_t and ||a_t|| (eq. 10),
+// e_t (eq. 10), delta_t, den_t (eq. 11), ||u_t||^2, ||k_t||^2), S, A and
+// z^key every CK tokens, and the final state. Then one CTA per (b, h) runs
+// the reverse sweep t = T-1 .. 0, applying the adjoint of each step of
+// eq. 9-11 in reverse order. S_{t-1} and A_{t-1} are rebuilt from S_t, A_t by
+// undoing the step's rank-1 update (S_{t-1} = S_t - e alpha^^T,
+// A_{t-1} = A_t + z z^T / delta) and reloaded from the checkpoint every CK
+// tokens.
 //
 // S, A and the adjoints dL/dS, dL/dA stay in registers for the whole kernel:
 // warp w owns rows 8w .. 8w+7 and lane l owns columns l, l+32, .. of each.
@@ -19,9 +20,9 @@
 // halving exchange (9 shuffles for 8 rows); a column product M^T x is a
 // warp-local partial sum reduced across warps through shared memory. Dot
 // products of d-vectors are recomputed by every warp (butterfly shuffles)
-// instead of block-wide reductions. Per token the forward phase needs one
-// block barrier and the reverse phase two. Token inputs and the tape are
-// prefetched NBUF - 1 tokens ahead into a shared-memory ring with cp.async.
+// instead of block-wide reductions. Per token the sweep needs two block
+// barriers. Token inputs and the tape are prefetched 3 tokens ahead into a
+// shared-memory ring with cp.async.
 //
 // Identities that save a product per reverse step (A is symmetric):
 //   A_t u^ = z / delta,  A_t k^ = alpha^ ||a||,  A_{t-1} g = A_t g + z (z.g) / delta,
@@ -41,18 +42,16 @@ struct BLay {
     // negative = the eps floor was taken), ||u||^2, ||k||^2, 3 unused
     static constexpr int TREC = 3 * D + 8;
     static constexpr int CREC = 2 * D * D + D;  // checkpoint: S | A | z^key
-    static constexpr int NB1 = 4;               // forward ring depth (prefetch 3 tokens ahead)
     static constexpr int NB2 = 5;               // reverse ring depth (prefetch 3 tokens ahead, 1 slot in use
                                                 // by the deferred k/u gradients of the previous token)
-    // ring slot (bytes): raw u | k | q (TIn), then v (TIn, forward) or dL/do
-    // (fp32, reverse), then the tape record (reverse)
+    // ring slot (bytes): raw u | k | q (TIn), then dL/do (fp32), then the tape
+    // record
     static constexpr int IN_B = D * (int)sizeof(TIn);
     static constexpr int U = 0, K = IN_B, Q = 2 * IN_B, G = 3 * IN_B, TP = 3 * IN_B + 4 * D;
     static constexpr int SLOT_B = TP + 4 * TREC;
     // shared memory (bytes)
     static constexpr int RING = 0;
-    static constexpr int X1 = RING + NB2 * SLOT_B;    // forward: [2 parities][z | A k^] per row
-    static constexpr int P1 = X1 + 2 * 2 * D * 4;     // reverse pass-1 column partials [NW][3][D]
+    static constexpr int P1 = RING + NB2 * SLOT_B;    // pass-1 column partials [NW][3][D]
     static constexpr int C1 = P1 + NW * 3 * D * 4;    // their sums [3][D]
     static constexpr int R1 = C1 + 3 * D * 4;         // pass-1 row products [2 parities][2][D]
     static constexpr int P2 = R1 + 2 * 2 * D * 4;     // pass-2 column partials [NW][D]
@@ -61,10 +60,9 @@ struct BLay {
     static constexpr int DS = DP + 4 * NW * 4;        // their sums [4]
     static constexpr int RED = DS + 4 * 4;            // [D/32 warps][2] dot partials of the k/u gradients
     static constexpr int SMEM = RED + 8 * 4;
-    static_assert(D % 32 == 0 && D <= 128, "register tiles hold 8 rows x d/32 columns of each d x d matrix");
+    static_assert(D % 32 == 0 && D <= 96, "register tiles hold 8 rows x d/32 columns of each of four d x d matrices");
     static_assert(SLOT_B % 16 == 0 && IN_B % 16 == 0, "cp.async chunks");
     static_assert(3 * IN_B / 16 + D / 4 + TREC / 4 <= THREADS, "one prefetch chunk per thread");
-    static_assert(4 * IN_B <= TP, "forward slot fits");
     static_assert(NW - 3 * CL == CL, "the warps left over by the column sums are d/32");
 };
 
@@ -157,20 +155,6 @@ __device__ __forceinline__ float pick(const float (&x)[N], int c) {
 }
 
 template <int D, typename TIn>
-__device__ __forceinline__ void prefetch_fwd(unsigned char* slot, const TIn* gu, const TIn* gk, const TIn* gq,
-                                             const TIn* gv, int t) {
-    using L = BLay<D, TIn>;
-    constexpr int NC = L::IN_B / 16;
-    const int tid = threadIdx.x;
-    if (tid < 4 * NC) {
-        const int part = tid / NC, off = tid - part * NC;
-        const TIn* src = part == 0 ? gu : part == 1 ? gk : part == 2 ? gq : gv;
-        cp_async16(slot + part * L::IN_B + off * 16,
-                   reinterpret_cast<const unsigned char*>(src + (size_t)t * D) + off * 16);
-    }
-}
-
-template <int D, typename TIn>
 __device__ __forceinline__ void prefetch_rev(unsigned char* slot, const TIn* gu, const TIn* gk, const TIn* gq,
                                              const float* go, const float* tp, int t) {
     using L = BLay<D, TIn>;
@@ -233,21 +217,19 @@ __device__ __forceinline__ float ku_grads(const unsigned char* sl, const float* 
     return fmaf(dut, 0.f, dkt * 0.f);
 }
 
-// MODE 0: both phases (four d x d matrices in registers: d <= 96).
-// MODE 1: phase 1 alone, writing the tape, the checkpoints and the final S, A,
-// z^key to `fin`; the split reverse sweep (vla_backward_split.cuh) follows.
-template <int D, typename TIn, int MODE = 0>
+// The reverse sweep (four d x d matrices in registers: d <= 96). fin: the
+// forward's final S [B*H, d, d] | A [B*H, d, d] | z^key [B*H, d], or NULL for
+// T = 0 (the sweep then starts and ends at the initial state).
+template <int D, typename TIn>
 __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     vla_backward_kernel(const Params p, const float* dO, const float* dST, const float* dAT, const float* dzkT,
                         float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0, float* dzk0,
                         float* tape, float* ckpt, const float* fin) {
     using L = BLay<D, TIn>;
-    static_assert(MODE == 1 || D <= 96, "the single-kernel sweep holds four d x d matrices");
-    constexpr int RW = L::RW, CL = L::CL, NW = L::NW, NB1 = L::NB1, NB2 = L::NB2;
+    constexpr int RW = L::RW, CL = L::CL, NW = L::NW, NB2 = L::NB2;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned char* ring = smem + L::RING;
-    float* X1 = reinterpret_cast<float*>(smem + L::X1);
     float* P1 = reinterpret_cast<float*>(smem + L::P1);
     float* C1 = reinterpret_cast<float*>(smem + L::C1);
     float* R1 = reinterpret_cast<float*>(smem + L::R1);
@@ -264,12 +246,10 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     const size_t hin = (size_t)bh * T * D, hdd = (size_t)bh * D * D;
     const TIn* gq = static_cast<const TIn*>(p.q) + hin;
     const TIn* gk = static_cast<const TIn*>(p.k) + hin;
-    const TIn* gv = static_cast<const TIn*>(p.v) + hin;
     const TIn* gu = static_cast<const TIn*>(p.u) + hin;
     const float* go_h = dO ? dO + hin : nullptr;
     float* tp = tape + (size_t)bh * T * L::TREC;
     float* cp = ckpt + (size_t)bh * ((T + CK - 1) / CK + 1) * L::CREC;
-    bool bad = false;
     float gchk = 0.f;  // fma(gradient, 0, .) of every gradient written: 0 unless one is NaN or Inf
 
     float S[RW][CL], A[RW][CL], zk[CL];
@@ -284,12 +264,9 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
 #pragma unroll
     for (int c = 0; c < CL; ++c) zk[c] = p.zk0 ? p.zk0[(size_t)bh * D + l + 32 * c] : 0.f;
 
-    // ------------------------------------------------------------------
-    // phase 1: forward with tape. When `fin` is given, the chunked forward
-    // kernel has already written the tape and the checkpoints, and `fin`
-    // holds its final S [B*H, d, d] | A [B*H, d, d] | z^key [B*H, d].
-    // ------------------------------------------------------------------
-    if (MODE == 0 && fin) {
+    // the forward kernel (the chunked tensor-core kernel with its tape) has
+    // written the tape, the checkpoints and its final state to `fin`
+    if (fin) {
         const size_t BH = gridDim.x;
 #pragma unroll
         for (int r = 0; r < RW; ++r)
@@ -302,169 +279,9 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < CL; ++c) zk[c] = fin[2 * BH * D * D + (size_t)bh * D + l + 32 * c];
     }
-    if (MODE == 1 || !fin) {
-    for (int s = 0; s < NB1 - 1; ++s) {
-        if (s < T) prefetch_fwd<D, TIn>(ring + s * L::SLOT_B, gu, gk, gq, gv, s);
-        cp_commit();
-    }
-    cp_wait<NB1 - 2>();
-    __syncthreads();
-    // raw u, k, q of the current token (this lane's columns) and its squared norms
-    float uc[CL], kc[CL], qc[CL], nu = 0.f, nk = 0.f;
-    if (T > 0) {
-        float nn[2] = {0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < CL; ++c) {
-            uc[c] = lds_in<TIn>(ring + L::U, l + 32 * c);
-            kc[c] = lds_in<TIn>(ring + L::K, l + 32 * c);
-            qc[c] = lds_in<TIn>(ring + L::Q, l + 32 * c);
-            nn[0] = fmaf(uc[c], uc[c], nn[0]);
-            nn[1] = fmaf(kc[c], kc[c], nn[1]);
-        }
-        allreduce<2, 16>(nn);
-        nu = nn[0];
-        nk = nn[1];
-    }
-    for (int t = 0; t < T; ++t) {
-        const unsigned char* sl = ring + (t % NB1) * L::SLOT_B;
-        // the slot of token t-1 is free: every warp passed token t-1's barrier
-        if (t + NB1 - 1 < T)
-            prefetch_fwd<D, TIn>(ring + ((t + NB1 - 1) % NB1) * L::SLOT_B, gu, gk, gq, gv, t + NB1 - 1);
-        cp_commit();
-        if (t % CK == 0) {  // state before token t
-            float* c = cp + (size_t)(t / CK) * L::CREC;
-#pragma unroll
-            for (int r = 0; r < RW; ++r)
-#pragma unroll
-                for (int cc = 0; cc < CL; ++cc) {
-                    const int e = (r0 + r) * D + l + 32 * cc;
-                    c[e] = S[r][cc];
-                    c[D * D + e] = A[r][cc];
-                }
-            if (w == 0)
-#pragma unroll
-                for (int cc = 0; cc < CL; ++cc) c[2 * D * D + l + 32 * cc] = zk[cc];
-        }
-        const float iu = inv_norm(nu), ik = inv_norm(nk);
-        float uh[CL], kh[CL], pq[CL];
-#pragma unroll
-        for (int c = 0; c < CL; ++c) {
-            uh[c] = uc[c] * iu;
-            kh[c] = kc[c] * ik;
-            pq[c] = phi(qc[c]);
-            zk[c] += phi(kc[c]);  // z^key_t (eq. 11), on raw k
-        }
-        // eq. 9 and 10 products with the states before the token: A u^, A k^, S k^
-        float pa[RW], pk[RW], ps[RW];
-#pragma unroll
-        for (int r = 0; r < RW; ++r) {
-            pa[r] = pk[r] = ps[r] = 0.f;
-#pragma unroll
-            for (int c = 0; c < CL; ++c) {
-                pa[r] = fmaf(A[r][c], uh[c], pa[r]);
-                pk[r] = fmaf(A[r][c], kh[c], pk[r]);
-                ps[r] = fmaf(S[r][c], kh[c], ps[r]);
-            }
-        }
-        const float za = rowsum8(pa), ka = rowsum8(pk), sk = rowsum8(ps);
-        float* x1 = X1 + (t & 1) * 2 * D;
-        if ((l & 3) == 0) {
-            x1[rr] = za;
-            x1[D + rr] = ka;
-        }
-        const float erow = lds_in<TIn>(sl + L::G, rr) - sk;  // e = v - S_{t-1} k^ for row rr
-        cp_wait<NB1 - 2>();
-        __syncthreads();
-        // delta, z.k^, den, and the next token's squared norms (its slot is complete)
-        const unsigned char* sn = ring + ((t + 1) % NB1) * L::SLOT_B;
-        const bool more = t + 1 < T;
-        float zc[CL], d5[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < CL; ++c) {
-            zc[c] = x1[l + 32 * c];
-            d5[0] = fmaf(uh[c], zc[c], d5[0]);
-            d5[1] = fmaf(kh[c], zc[c], d5[1]);
-            d5[2] = fmaf(pq[c], zk[c], d5[2]);
-            if (more) {
-                uc[c] = lds_in<TIn>(sn + L::U, l + 32 * c);
-                kc[c] = lds_in<TIn>(sn + L::K, l + 32 * c);
-                qc[c] = lds_in<TIn>(sn + L::Q, l + 32 * c);
-                d5[3] = fmaf(uc[c], uc[c], d5[3]);
-                d5[4] = fmaf(kc[c], kc[c], d5[4]);
-            }
-        }
-        allreduce<5, 16>(d5);
-        const float dl = 1.f + d5[0], kz = d5[1], pd = d5[2];
-        const float rdl = rcpa(dl);
-        // a = A_t k^ = A_{t-1} k^ - z (z.k^) / delta
-        float al[CL], na2 = 0.f;
-#pragma unroll
-        for (int c = 0; c < CL; ++c) {
-            al[c] = fmaf(-zc[c], kz * rdl, x1[D + l + 32 * c]);
-            na2 = fmaf(al[c], al[c], na2);
-        }
-        allreduce<1, 16>(&na2);
-        const float ina = inv_norm(na2);
-#pragma unroll
-        for (int c = 0; c < CL; ++c) al[c] *= ina;
-        // A_t = A_{t-1} - z z^T / delta;  S_t = S_{t-1} + e alpha^^T
-        float zr[RW];
-        lds8f(x1, r0, zr);
-#pragma unroll
-        for (int r = 0; r < RW; ++r) {
-            const float er = __shfl_sync(FULL, erow, 4 * r);
-            const float zs = -zr[r] * rdl;
-#pragma unroll
-            for (int c = 0; c < CL; ++c) {
-                A[r][c] = fmaf(zs, zc[c], A[r][c]);
-                S[r][c] = fmaf(er, al[c], S[r][c]);
-            }
-        }
-        // tape
-        float* rec = tp + (size_t)t * L::TREC;
-        if (w == 0) {
-#pragma unroll
-            for (int c = 0; c < CL; ++c) {
-                rec[l + 32 * c] = zc[c];
-                rec[D + l + 32 * c] = al[c];
-            }
-            if (l == 0) {
-                const float na = sqrtf(na2);
-                rec[3 * D] = dl;
-                rec[3 * D + 1] = na;
-                rec[3 * D + 2] = pd < p.eps ? -p.eps : pd;
-                rec[3 * D + 3] = nu;
-                rec[3 * D + 4] = nk;
-                if (!isfinite(dl) || !isfinite(na) || !isfinite(pd)) bad = true;
-            }
-        }
-        if ((l & 3) == 0) rec[2 * D + rr] = erow;
-        nu = d5[3];
-        nk = d5[4];
-    }
-    }  // !fin
 
-    if constexpr (MODE == 1) {
-        // the forward's final state for the split reverse sweep
-        float* fo = const_cast<float*>(fin);
-        const size_t BH = gridDim.x;
-#pragma unroll
-        for (int r = 0; r < RW; ++r)
-#pragma unroll
-            for (int c = 0; c < CL; ++c) {
-                const size_t e = hdd + (size_t)(r0 + r) * D + l + 32 * c;
-                fo[e] = S[r][c];
-                fo[BH * D * D + e] = A[r][c];
-            }
-        if (w == 0)
-#pragma unroll
-            for (int c = 0; c < CL; ++c) fo[2 * BH * D * D + (size_t)bh * D + l + 32 * c] = zk[c];
-        cp_wait<0>();
-        if (bad) record_failure(p.status, BIT_NONFINITE, ROLE_A, bh, -1);
-        return;
-    } else {
     // ------------------------------------------------------------------
-    // phase 2: reverse sweep
+    // reverse sweep
     // ------------------------------------------------------------------
     cp_wait<0>();
     __syncthreads();  // ring free, tape visible to the whole CTA
@@ -744,8 +561,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     if (w == 0 && dzk0)
 #pragma unroll
         for (int c = 0; c < CL; ++c) dzk0[(size_t)bh * D + l + 32 * c] = gzk[c];
-    if (bad || gchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
-    }  // MODE 0
+    if (gchk != 0.f) record_failure(p.status, BIT_NONFINITE, ROLE_S, bh, -1);
 }
 
 }  // namespace bw

@@ -759,12 +759,21 @@ vla_status launch_bw_forward(const vla::Params& p, int BH, float* dq, float* tap
             return VLA_ERR_CUDA;
         fk<<<BH, vla::tc::THREADS, TL::SMEM, s>>>(pf);
     } else {
-        using BL = vla::bw::BLay<D, TIn>;
-        auto fk = vla::bw::vla_backward_kernel<D, TIn, 1>;
-        if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BL::SMEM) != cudaSuccess)
+        // d = 128: the cluster-pair chunked kernel (A-pass and S-pass on two SMs)
+        using LY = vla::tc2::Lay2<D, TIn>;
+        if ((long long)BH * 2 > 2147483647LL) return VLA_ERR_INVALID_ARG;
+        vla::Params pf = p;
+        pf.o = dq;
+        pf.o_stride = (size_t)p.T * D;
+        pf.S_out = fin;
+        pf.A_out = fin + (size_t)BH * D * D;
+        pf.zk_out = fin + 2 * (size_t)BH * D * D;
+        pf.tape = tape;
+        pf.ckpt = ckpt;
+        auto fk = vla::vla_tc2_kernel<D, TIn, true>;
+        if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::SMEM_LAUNCH) != cudaSuccess)
             return VLA_ERR_CUDA;
-        fk<<<BH, BL::THREADS, BL::SMEM, s>>>(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                                             nullptr, nullptr, nullptr, nullptr, tape, ckpt, fin);
+        fk<<<2 * BH, vla::tc2::THREADS, LY::SMEM_LAUNCH, s>>>(pf);
     }
     return cudaGetLastError() == cudaSuccess ? VLA_OK : VLA_ERR_CUDA;
 }

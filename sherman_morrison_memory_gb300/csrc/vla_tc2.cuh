@@ -247,9 +247,11 @@ struct Ctx2 {
 // (eq. 11), the k | phi operand tiles; `write_zk`: this CTA writes the final
 // z^key. X is the cluster kernel's context (its layout X::L has the fields
 // used here; x.abort_peers(rank) raises the abort flag of every CTA of the
-// cluster).
+// cluster). TAPE (the backward pass's forward): rank 0 also writes ||u_t||^2
+// and ||k_t||^2 into each token's tape record, rank 1 den_t (negative where
+// the eps floor is taken) and z^key before every 64th token.
 // ---------------------------------------------------------------------------
-template <int D, typename TIn, bool RANK0, typename X>
+template <int D, typename TIn, bool RANK0, typename X, bool TAPE = false>
 __device__ __forceinline__ void stage2(const Params& p, const X& x, int bh, int sw, int lane, uint32_t rank,
                                        bool write_zk = true) {
     using L = typename X::L;
@@ -289,6 +291,13 @@ __device__ __forceinline__ void stage2(const Params& p, const X& x, int bh, int 
         }
         // rank 1's S rows read this chunk's v from global memory a few chunks from now
         if constexpr (!RANK0) tc::prefetch_v_l2<D, TIn>(gv + (size_t)c * C * D, n, sw * 32 + lane);
+        if constexpr (TAPE && !RANK0) {
+            if ((c & 3) == 0 && sw == 0) {  // z^key before token 16 c (= 64 (c / 4))
+                float* ck = tc::ckpt_slot<D>(p, bh, c >> 2) + 2 * D * D;
+#pragma unroll
+                for (int m = 0; m < E; ++m) ck[lane + 32 * m] = zk[m];
+            }
+        }
         const TIn* r0 = reinterpret_cast<const TIn*>(x.raw(rs));
         const TIn* rk = reinterpret_cast<const TIn*>(x.raw(rs) + L::RAW_T);
         float fq[TW][E], pk[TW][E], red[TW][3];
@@ -357,6 +366,17 @@ __device__ __forceinline__ void stage2(const Params& p, const X& x, int bh, int 
                 sc[L::SC_IU + t] = t < n ? rsqrtf(fmaxf(r0v, 1e-24f)) : 0.f;
             else
                 sc[L::SC_RDEN + t] = t < n ? __frcp_rn(fmaxf(r2v, p.eps)) : 1.f;  // 1 / den
+            if constexpr (TAPE) {
+                if (t < n) {
+                    float* rec = tc::tape_rec<D>(p, bh, c * C + t) + 3 * D;
+                    if constexpr (RANK0) {
+                        rec[3] = r0v;  // ||u_t||^2
+                        rec[4] = r1v;  // ||k_t||^2
+                    } else {
+                        rec[2] = r2v < p.eps ? -p.eps : r2v;  // den, negative where the eps floor is taken
+                    }
+                }
+            }
         }
         named_bar(ID_ST, 32 * NSTAGE);
         // scratch rows -> operand tiles, one 8-row group per unit: lane =
@@ -421,9 +441,10 @@ __device__ __forceinline__ void stage2(const Params& p, const X& x, int bh, int 
 // rank 0, warps 0-4: Sherman-Morrison steps of eq. 9 and the gate of eq. 10,
 // one chunk at a time (the arithmetic of tc::tc_a_team). Thread i < D of
 // warps 0-3 owns row i of A (TMEM lane i) and of every d x C intermediate;
-// warp 4 factors I + Guu and sends the gate to rank 1.
+// warp 4 factors I + Guu and sends the gate to rank 1. TAPE: also z_t,
+// delta_t and ||a_t|| into the tape, and A before every 64th token.
 // ---------------------------------------------------------------------------
-template <int D, typename TIn>
+template <int D, typename TIn, bool TAPE = false>
 __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp, int lane, uint32_t rank) {
     using L = Lay2<D, TIn>;
     constexpr int XS = L::XS;
@@ -481,6 +502,10 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
             break;
         }
         TC2_STAMP(p, 4, 0, c, nch);
+        if (TAPE && (c & 3) == 0 && rw) {  // A before token 16 c
+            tc_fence_after();
+            tc::tmem_row_out<D>(tl, L::T_X, tc::ckpt_slot<D>(p, bh, c >> 2) + D * D + (size_t)i * D);
+        }
         const float* hi = x.hi(s);
         const float* sc = x.sc(s);
         // [Z' | W] = A_c [u | k]^T (rows u, k of the chunk; scaled by 1/||.|| below);
@@ -566,6 +591,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
 #pragma unroll
                 for (int r = 0; r < C; ++r)  // L[r][j] below the unit diagonal, stored transposed
                     sm[L::SM_LMT + j * L::GSTR + r] = r > j ? col[r] * myrd : 0.f;
+                if (TAPE && j < n) tc::tape_rec<D>(p, bh, c * C + j)[3 * D] = mydl;  // delta_t = 1 + u^_t . z_t
             } else {
 #pragma unroll
                 for (int r = 0; r < C; ++r) sm[L::SM_XGT + j * L::GSTR + r] = col[r];
@@ -595,6 +621,11 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
                 tc::ld_row16(sm + L::SM_LMT + r * L::GSTR, lr);  // L[t][r], t > r
 #pragma unroll
                 for (int t = r + 1; t < C; ++t) y[t] = fmaf(-lr[t], y[r], y[t]);
+            }
+            if (TAPE) {  // z_t = A_{t-1} u^_t of eq. 9
+#pragma unroll
+                for (int t = 0; t < C; ++t)
+                    if (t < n) tc::tape_rec<D>(p, bh, c * C + t)[i] = y[t];
             }
             // row i of N = Z D^-1/2: A_{c+1} = A_c - N N^T (symmetric by construction)
             float nv[C];
@@ -661,6 +692,7 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
                     acc = __ffma2_rn(f2(a.z, a.w), f2(a.z, a.w), acc);
                 }
                 laa[lane] = acc.x + acc.y;
+                if (TAPE && lane < n) tc::tape_rec<D>(p, bh, c * C + lane)[3 * D + 1] = sqrtf(acc.x + acc.y);  // ||a_t||
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -716,8 +748,9 @@ __device__ void a_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
 // ---------------------------------------------------------------------------
 // rank 1, warps 0-3: residual writes and readout of eq. 10-11 for the chunk
 // rank 0 sent (the arithmetic of tc::tc_s_team). Thread i < D owns row i of S.
+// TAPE: also alpha^_t and e_t into the tape, and S before every 64th token.
 // ---------------------------------------------------------------------------
-template <int D, typename TIn>
+template <int D, typename TIn, bool TAPE = false>
 __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp, int lane, uint32_t rank) {
     using L = Lay2<D, TIn>;
     constexpr int XS = L::XS;
@@ -777,6 +810,10 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
         }
         TC2_STAMP(p, 5, 1, c, nch);
         recv = c + 1;
+        if (TAPE && (c & 3) == 0 && rw) {  // S before token 16 c
+            tc_fence_after();
+            tc::tmem_row_out<D>(tl, L::T_X, tc::ckpt_slot<D>(p, bh, c >> 2) + (size_t)i * D);
+        }
         const float* hi = x.hi(s);
         const float* sc = x.sc(s);
         const float* alr = x.f(L::OFF_AL) + (size_t)b * C * XS;
@@ -843,6 +880,15 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
                 }
             }
             TC2_STAMP(p, 5, 5, c, nch);
+            if (TAPE) {  // alpha^_t = a_t / ||a_t|| and e_t = e'_t ||a_t|| (eq. 10)
+#pragma unroll
+                for (int t = 0; t < C; ++t)
+                    if (t < n) {
+                        float* rec = tc::tape_rec<D>(p, bh, c * C + t);
+                        rec[D + i] = alr[t * XS + i] * nr[t];
+                        rec[2 * D + i] = vv[t] / nr[t];
+                    }
+            }
             // o_t = (S_c phi_t + sum_{s<=t} e_s (alpha^_s . phi_t)) / den_t = S_t phi_t / den_t (eq. 11)
             tc::ld_row16(sc + L::SC_RDEN, nr);
 #pragma unroll
@@ -919,7 +965,9 @@ __device__ void s_rank(const Params& p, const Ctx2<D, TIn>& x, int bh, int warp,
 
 }  // namespace tc2
 
-template <int D, typename TIn>
+// TAPE: the backward pass's forward, which also writes the tape and the
+// 64-token checkpoints that the reverse sweep reads (as vla_tc_kernel does)
+template <int D, typename TIn, bool TAPE = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc2::THREADS, 1) vla_tc2_kernel(const Params p) {
     using L = tc2::Lay2<D, TIn>;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -964,13 +1012,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc2::THREADS, 1) vla
     tc_fence_after();
     if (warp < 8) {
         if (rank == 0 && warp <= tc2::FACTOR_WARP)
-            tc2::a_rank<D, TIn>(p, x, bh, warp, lane, rank);
+            tc2::a_rank<D, TIn, TAPE>(p, x, bh, warp, lane, rank);
         else if (rank == 1 && warp < 4)
-            tc2::s_rank<D, TIn>(p, x, bh, warp, lane, rank);
+            tc2::s_rank<D, TIn, TAPE>(p, x, bh, warp, lane, rank);
     } else if (rank == 0) {
-        tc2::stage2<D, TIn, true>(p, x, bh, warp - 8, lane, rank);
+        tc2::stage2<D, TIn, true, tc2::Ctx2<D, TIn>, TAPE>(p, x, bh, warp - 8, lane, rank);
     } else {
-        tc2::stage2<D, TIn, false>(p, x, bh, warp - 8, lane, rank);
+        tc2::stage2<D, TIn, false, tc2::Ctx2<D, TIn>, TAPE>(p, x, bh, warp - 8, lane, rank);
     }
     tc_fence_before();
     __syncthreads();
