@@ -71,18 +71,18 @@ NCU_TRAFFIC = {
                       "bytes_per_launch": 403224320 + 176125696},
     # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
-    "vla_tc3_kernel": {"source_sha": "b4c1c5b5d98e43a0", "workload": (1, 32, 65536, 128, "bf16"),
-                       "bytes_per_launch": 8 * (268544768 + 108939008 - 4227072) + 4227072},
+    "vla_tc3_kernel": {"source_sha": "b86b909885d02241", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (268663040 + 108134656 - 4227072) + 4227072},
     # the reverse sweep (the step's dominant kernel, after the taped chunked forward), from a capture of
     # the same workload at B=2 (32 heads; a full step holds about 2.8 GB on the device) scaled by 4:
     # every byte it moves is per head-token or per head
-    "vla_backward_kernel": {"source_sha": "dd6f677c14be50e6", "workload": (8, 16, 4096, 96, "bf16"),
-                            "bytes_per_launch": 4 * (436399360 + 176777472)},
+    "vla_backward_kernel": {"source_sha": "1420f755ed301e5d", "workload": (8, 16, 4096, 96, "bf16"),
+                            "bytes_per_launch": 4 * (438042880 + 177031168)},
     # the split reverse sweep (d = 128) on the long-context workload cut to 4096 tokens
-    "vla_backward_pair_kernel": {"source_sha": "323d472e58ba06ae", "workload": (1, 32, 4096, 128, "bf16"),
-                                 "bytes_per_launch": 648219904 + 307873792},
-    "vla_decode_kernel": {"source_sha": "6dc773112e35b2c5", "workload": (128, 16, 1, 96, "bf16"),
-                          "bytes_per_launch": 153399040 + 98538240},
+    "vla_backward_pair_kernel": {"source_sha": "e9dab62803db77ee", "workload": (1, 32, 4096, 128, "bf16"),
+                                 "bytes_per_launch": 649212672 + 307639552},
+    "vla_decode_kernel": {"source_sha": "9c13b0c3ed588538", "workload": (128, 16, 1, 96, "bf16"),
+                          "bytes_per_launch": 153392896 + 98219264},
     "vla_fused_kernel": {"source_sha": "565a71784acabc88", "workload": (8, 16, 4096, 96, "bf16"),
                          "bytes_per_launch": 403125248 + 175399936},
 }
