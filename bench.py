@@ -79,8 +79,8 @@ NCU_TRAFFIC = {
     "vla_backward_kernel": {"source_sha": "1420f755ed301e5d", "workload": (8, 16, 4096, 96, "bf16"),
                             "bytes_per_launch": 4 * (438042880 + 177031168)},
     # the split reverse sweep (d = 128) on the long-context workload cut to 4096 tokens
-    "vla_backward_pair_kernel": {"source_sha": "e9dab62803db77ee", "workload": (1, 32, 4096, 128, "bf16"),
-                                 "bytes_per_launch": 649212672 + 307639552},
+    "vla_backward_pair_kernel": {"source_sha": "c19e0ef0ec50bbe8", "workload": (1, 32, 4096, 128, "bf16"),
+                                 "bytes_per_launch": 647584000 + 307564800},
     "vla_decode_kernel": {"source_sha": "9c13b0c3ed588538", "workload": (128, 16, 1, 96, "bf16"),
                           "bytes_per_launch": 153392896 + 98219264},
     "vla_fused_kernel": {"source_sha": "565a71784acabc88", "workload": (8, 16, 4096, 96, "bf16"),

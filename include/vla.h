@@ -364,6 +364,27 @@ vla_status vla_backward_split(const void* q, const void* k, const void* v, const
                               float* dS0, float* dA0, float* dzk0,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* vla_backward() (split == 0) or vla_backward_split() (split != 0) with
+ * options (opts may be NULL = defaults). Of vla_options only two fields apply:
+ *   wait_limit_us        limit of the split sweep's one wait, where the A side
+ *                        waits for the S side's progress (0 = 2,000,000). The
+ *                        forward pass before the sweep takes the same limit.
+ *   test_stall_producer  TESTING ONLY: nonzero makes the split sweep's S side
+ *                        publish no progress. The A side's wait then runs out
+ *                        and the call records VLA_ERR_TIMEOUT, without faulting
+ *                        the GPU; the gradients are then not meaningful. The
+ *                        single-kernel sweep (split == 0 at d <= 96) has no
+ *                        wait, and the flag does nothing there.
+ * The other fields are ignored. */
+vla_status vla_backward_ex(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype,
+                           int B, int H, int T, int d, float lambda0, float eps,
+                           const float* S0, const float* A0, const float* zk0,
+                           const float* dO, const float* dS_T, const float* dA_T, const float* dzk_T,
+                           float* dq, float* dk, float* dv, float* du,
+                           float* dS0, float* dA0, float* dzk0,
+                           void* workspace, size_t workspace_bytes, void* stream,
+                           int split, const vla_options* opts);
+
 #ifdef __cplusplus
 }
 #endif

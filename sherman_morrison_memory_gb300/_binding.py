@@ -95,6 +95,8 @@ def load_library():
         lib.vla_backward.restype = ci
         lib.vla_backward_split.argtypes = lib.vla_backward.argtypes
         lib.vla_backward_split.restype = ci
+        lib.vla_backward_ex.argtypes = lib.vla_backward.argtypes + [ci, ctypes.POINTER(_Options)]
+        lib.vla_backward_ex.restype = ci
         lib.vla_forward_host_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
         lib.vla_forward_host_workspace_bytes.restype = ctypes.c_size_t
         lib.vla_forward_host.argtypes = (fwd_args[:18] + [ci, vp, ctypes.c_size_t, vp, ctypes.POINTER(_Options)])
@@ -366,21 +368,27 @@ def _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, che
 
 def vla_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tensor,
                  lambda0: float = 0.1, eps: float = 1e-4, state=None, grad_o=None, grad_state=None, *,
-                 out=None, stream=None, check: bool = False, split: bool = False):
+                 out=None, stream=None, check: bool = False, split: bool = False, wait_limit_us: int = 0,
+                 test_stall_producer: bool = False):
     """Gradient of a scalar loss through vla_forward (reverse mode, §3.3 eq. 9-11).
 
     ``grad_o`` = dL/do [B,H,T,d] and ``grad_state`` = (dL/dS_T, dL/dA_T,
     dL/dz^key_T) (each optional, None = zero); ``state`` = the forward's
     optional initial (S0, A0, zk0). Returns ``((dq, dk, dv, du), (dS0, dA0,
     dzk0))``, float32 on the inputs' device. d in {32, 64, 96, 128}.
-    ``split=True`` runs the reverse sweep as two kernels, one per state
-    (vla_backward_split; the path d = 128 always takes).
+    ``split=True`` runs the reverse sweep split by state, as a cluster of two
+    CTAs per head (vla_backward_split; the path d = 128 always takes).
+    ``wait_limit_us`` bounds the split sweep's wait for its S side's progress;
+    ``test_stall_producer=True`` (testing only) makes that wait run out, so
+    that the call records VLA_ERR_TIMEOUT (vla_backward_ex).
     ``out`` may hold the seven result tensors (float32, contiguous, on the
     inputs' device). CPU inputs run on the current CUDA device with
     host<->device copies. ``check=True`` synchronises and raises on an
     in-kernel failure.
     """
     if q.device.type == "cpu":
+        if wait_limit_us or test_stall_producer:
+            raise ValueError("wait_limit_us and test_stall_producer apply to device inputs")
         return _backward_host(q, k, v, u, lambda0, eps, state, grad_o, grad_state, out, check, split)
     lib = load_library()
     for name, x in (("k", k), ("v", v), ("u", u)):
@@ -423,10 +431,14 @@ def vla_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Ten
     with torch.cuda.device(dev), _on_stream(stream):
         ws = _call_buffer(dev, nbytes, True)
         sh = _stream_handle(dev, stream)
-        fn = lib.vla_backward_split if split else lib.vla_backward
-        st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d, float(lambda0), float(eps),
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(u), _DTYPES[q.dtype], B, H, T, d, float(lambda0), float(eps),
                 _ptr(S0), _ptr(A0), _ptr(zk0), _ptr(gO), _ptr(gS), _ptr(gA), _ptr(gzk), *(_ptr(x) for x in outs),
                 _ptr(dS0), _ptr(dA0), _ptr(dzk0), _ptr(ws), ws.numel() * 4, ctypes.c_void_p(sh))
+        if wait_limit_us or test_stall_producer:
+            opts = _Options(int(wait_limit_us), 1 if test_stall_producer else 0, None, 0, 0)
+            st = lib.vla_backward_ex(*args, 1 if split else 0, ctypes.byref(opts))
+        else:
+            st = (lib.vla_backward_split if split else lib.vla_backward)(*args)
     if st != VLA_OK:
         raise VLAError(st, "vla_backward_split" if split else "vla_backward")
     if check:

@@ -27,8 +27,10 @@
 // store at cluster scope into a counter in the A side's shared memory; 0 and
 // -1 follow the last step and the last dL/dk. The A side reads the counter
 // with acquire loads before it prefetches a token's tape record, in one
-// thread and then a block barrier, with a time limit (VLA_ERR_TIMEOUT). The S
-// side never waits for the A side, and both CTAs meet at a cluster barrier
+// thread and then a block barrier, with a time limit (VLA_ERR_TIMEOUT; after
+// it runs out the A side waits no more and its results are not meaningful).
+// The test hook Params::stall_producer makes the S side publish nothing, so
+// that the limit runs out. The S side never waits for the A side, and both CTAs meet at a cluster barrier
 // before they exit, so neither leaves while the other may still write into
 // its shared memory.
 //
@@ -362,7 +364,7 @@ __device__ __forceinline__ void s_sweep(const Params& p, int bh, size_t BH, cons
         }
         cp_wait<1>();
         __syncthreads();  // B1 (also publishes token t-1's slot)
-        if (tid == PairLay<D, TIn>::PUB) pair_publish(rflag, t + 1);  // the step for token t+1 is done
+        if (tid == PairLay<D, TIn>::PUB && !p.stall_producer) pair_publish(rflag, t + 1);  // the step for t+1 is done
         if (t >= 3) prefetch_s<D, TIn>(ring + ((t - 3) % NB) * L::SLOT_B, gk, gq, go_h, tp, t - 3);
         cp_commit();
         if (tid < 2 * D) {
@@ -460,10 +462,10 @@ __device__ __forceinline__ void s_sweep(const Params& p, int bh, size_t BH, cons
         j_ege = e_ge, j_nk = nk;
     }
     __syncthreads();  // pass-2 partials of token 0 visible
-    if (tid == PairLay<D, TIn>::PUB) pair_publish(rflag, 0);  // every step done
+    if (tid == PairLay<D, TIn>::PUB && !p.stall_producer) pair_publish(rflag, 0);  // every step done
     if (T > 0 && ku_warp) gchk += k_grad_s<D, TIn>(ring, P2, RED, jw, pick<CL>(gzk, jw), j_ege, j_nk, dk + (size_t)bh * T * D);
     __syncthreads();
-    if (tid == PairLay<D, TIn>::PUB) pair_publish(rflag, -1);  // the S part of dL/dk_0 is written
+    if (tid == PairLay<D, TIn>::PUB && !p.stall_producer) pair_publish(rflag, -1);  // dL/dk_0's S part is written
     cp_wait<0>();
 #pragma unroll
     for (int r = 0; r < RW; ++r)

@@ -754,6 +754,7 @@ vla_status launch_bw_forward(const vla::Params& p, int BH, float* dq, float* tap
         pf.zk_out = fin + 2 * (size_t)BH * D * D;
         pf.tape = tape;
         pf.ckpt = ckpt;
+        pf.stall_producer = 0;  // the test hook is for the reverse sweep's wait
         auto fk = vla::vla_tc_kernel<D, TIn, true>;
         if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TL::SMEM) != cudaSuccess)
             return VLA_ERR_CUDA;
@@ -770,6 +771,7 @@ vla_status launch_bw_forward(const vla::Params& p, int BH, float* dq, float* tap
         pf.zk_out = fin + 2 * (size_t)BH * D * D;
         pf.tape = tape;
         pf.ckpt = ckpt;
+        pf.stall_producer = 0;  // the test hook is for the reverse sweep's wait
         auto fk = vla::vla_tc2_kernel<D, TIn, true>;
         if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::SMEM_LAUNCH) != cudaSuccess)
             return VLA_ERR_CUDA;
@@ -834,7 +836,7 @@ vla_status backward_impl(const void* q, const void* k, const void* v, const void
                          int T, int d, float lambda0, float eps, const float* S0, const float* A0, const float* zk0,
                          const float* dO, const float* dS_T, const float* dA_T, const float* dzk_T, float* dq,
                          float* dk, float* dv, float* du, float* dS0, float* dA0, float* dzk0, void* workspace,
-                         size_t workspace_bytes, void* stream, bool split) {
+                         size_t workspace_bytes, void* stream, bool split, const vla_options* opts) {
     if (B < 0 || H < 0 || T < 0) return VLA_ERR_INVALID_ARG;
     if (dtype != VLA_F32 && dtype != VLA_BF16) return VLA_ERR_INVALID_ARG;
     if (d != 32 && d != 64 && d != 96 && d != 128) return VLA_ERR_UNSUPPORTED;
@@ -867,7 +869,8 @@ vla_status backward_impl(const void* q, const void* k, const void* v, const void
     p.T = T;
     p.inv_lambda0 = 1.0f / lambda0;
     p.eps = eps;
-    p.wait_ns = 1000ull * kDefaultWaitUs;
+    p.wait_ns = 1000ull * ((opts && opts->wait_limit_us) ? opts->wait_limit_us : kDefaultWaitUs);
+    p.stall_producer = (opts && opts->test_stall_producer) ? 1 : 0;
     unsigned char* w = static_cast<unsigned char*>(workspace);
     float* tape = reinterpret_cast<float*>(w + kWorkspaceBytes);
     float* ckpt = reinterpret_cast<float*>(w + kWorkspaceBytes + z.tape);
@@ -894,7 +897,7 @@ vla_status vla_backward(const void* q, const void* k, const void* v, const void*
                         const float* dzk_T, float* dq, float* dk, float* dv, float* du, float* dS0, float* dA0,
                         float* dzk0, void* workspace, size_t workspace_bytes, void* stream) {
     return backward_impl(q, k, v, u, dtype, B, H, T, d, lambda0, eps, S0, A0, zk0, dO, dS_T, dA_T, dzk_T, dq, dk, dv,
-                         du, dS0, dA0, dzk0, workspace, workspace_bytes, stream, false);
+                         du, dS0, dA0, dzk0, workspace, workspace_bytes, stream, false, nullptr);
 }
 
 vla_status vla_backward_split(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B,
@@ -903,7 +906,16 @@ vla_status vla_backward_split(const void* q, const void* k, const void* v, const
                               const float* dzk_T, float* dq, float* dk, float* dv, float* du, float* dS0,
                               float* dA0, float* dzk0, void* workspace, size_t workspace_bytes, void* stream) {
     return backward_impl(q, k, v, u, dtype, B, H, T, d, lambda0, eps, S0, A0, zk0, dO, dS_T, dA_T, dzk_T, dq, dk, dv,
-                         du, dS0, dA0, dzk0, workspace, workspace_bytes, stream, true);
+                         du, dS0, dA0, dzk0, workspace, workspace_bytes, stream, true, nullptr);
+}
+
+vla_status vla_backward_ex(const void* q, const void* k, const void* v, const void* u, vla_dtype dtype, int B, int H,
+                           int T, int d, float lambda0, float eps, const float* S0, const float* A0, const float* zk0,
+                           const float* dO, const float* dS_T, const float* dA_T, const float* dzk_T, float* dq,
+                           float* dk, float* dv, float* du, float* dS0, float* dA0, float* dzk0, void* workspace,
+                           size_t workspace_bytes, void* stream, int split, const vla_options* opts) {
+    return backward_impl(q, k, v, u, dtype, B, H, T, d, lambda0, eps, S0, A0, zk0, dO, dS_T, dA_T, dzk_T, dq, dk, dv,
+                         du, dS0, dA0, dzk0, workspace, workspace_bytes, stream, split != 0, opts);
 }
 
 }  // extern "C"

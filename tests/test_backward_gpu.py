@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from parity_util import assert_close, rel_heads, rel_rows
-from sherman_morrison_memory_gb300 import (VLA_ERR_NONFINITE, VLA_OK, VLAError,
+from sherman_morrison_memory_gb300 import (VLA_ERR_NONFINITE, VLA_ERR_TIMEOUT, VLA_OK, VLAError,
                                            vla_backward, vla_get_last_device_status)
 from sherman_morrison_memory_gb300 import workloads as W
 
@@ -250,6 +250,22 @@ def test_split_single_upstream_seeds(orc):
     for with_o in (True, False):
         gO, gst = _seeds(B, H, T, d, seed=40, with_o=with_o, with_state=not with_o)
         assert_close(_errors(*_run(orc, arrs, "f32", gO, gst)), what=f"backward d=128 seeds o={with_o}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_split_wait_runs_out_and_is_reported(orc, d):
+    """The split sweep's one wait (its A side waits for the S side's
+    progress) is bounded: with the S side publishing nothing (test hook) it
+    runs out after the limit and the call reports VLA_ERR_TIMEOUT, without a
+    hang or a fault; a normal call afterwards is the oracle's again."""
+    arrs = _inputs(1, 2, 70, d, "f32", seed=d + 5)
+    gO, _ = _seeds(1, 2, 70, d, seed=d + 5, with_state=False)
+    dev_in = [_dev(a) for a in arrs]
+    with pytest.raises(VLAError) as ei:
+        vla_backward(*dev_in, 0.1, 1e-4, None, _dev(gO), check=True, split=True, wait_limit_us=2000,
+                     test_stall_producer=True)
+    assert ei.value.status == VLA_ERR_TIMEOUT
+    assert_close(_errors(*_run(orc, arrs, "f32", gO, None, split=True)), what=f"split sweep after a timeout d={d}")
 
 
 def test_split_nonfinite_input_is_reported():
