@@ -145,6 +145,11 @@ __device__ __forceinline__ float rowsum8(const float (&p)[8]) {
     return s;
 }
 
+// (x, x), and rows r, r+1 of an 8-row register tile, as packed FMA operands
+// (the d x d tiles hold rows r0 + 2 rp and r0 + 2 rp + 1 in one float2)
+__device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 pair2(const float (&x)[8], int r) { return make_float2(x[r], x[r + 1]); }
+
 // x[c] for the warp-uniform column index c < N, without local memory
 template <int N>
 __device__ __forceinline__ float pick(const float (&x)[N], int c) {
@@ -252,14 +257,19 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     float* cp = ckpt + (size_t)bh * ((T + CK - 1) / CK + 1) * L::CREC;
     float gchk = 0.f;  // fma(gradient, 0, .) of every gradient written: 0 unless one is NaN or Inf
 
-    float S[RW][CL], A[RW][CL], zk[CL];
+    // S, A (and gS, gA below): rows r0 + 2 rp (.x) and r0 + 2 rp + 1 (.y),
+    // columns l + 32 c, updated by packed FP32 FMAs (two rows per instruction)
+    float2 S2[RW / 2][CL], A2[RW / 2][CL];
+    float zk[CL];
+    auto a0 = [&](int i, int j) { return p.A0 ? p.A0[hdd + i * D + j] : (i == j ? p.inv_lambda0 : 0.f); };
+    auto s0 = [&](int i, int j) { return p.S0 ? p.S0[hdd + i * D + j] : 0.f; };
 #pragma unroll
-    for (int r = 0; r < RW; ++r)
+    for (int rp = 0; rp < RW / 2; ++rp)
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
-            const int i = r0 + r, j = l + 32 * c;
-            A[r][c] = p.A0 ? p.A0[hdd + i * D + j] : (i == j ? p.inv_lambda0 : 0.f);
-            S[r][c] = p.S0 ? p.S0[hdd + i * D + j] : 0.f;
+            const int i = r0 + 2 * rp, j = l + 32 * c;
+            A2[rp][c] = make_float2(a0(i, j), a0(i + 1, j));
+            S2[rp][c] = make_float2(s0(i, j), s0(i + 1, j));
         }
 #pragma unroll
     for (int c = 0; c < CL; ++c) zk[c] = p.zk0 ? p.zk0[(size_t)bh * D + l + 32 * c] : 0.f;
@@ -269,12 +279,12 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     if (fin) {
         const size_t BH = gridDim.x;
 #pragma unroll
-        for (int r = 0; r < RW; ++r)
+        for (int rp = 0; rp < RW / 2; ++rp)
 #pragma unroll
             for (int c = 0; c < CL; ++c) {
-                const size_t e = hdd + (size_t)(r0 + r) * D + l + 32 * c;
-                S[r][c] = fin[e];
-                A[r][c] = fin[BH * D * D + e];
+                const size_t e = hdd + (size_t)(r0 + 2 * rp) * D + l + 32 * c;
+                S2[rp][c] = make_float2(fin[e], fin[e + D]);
+                A2[rp][c] = make_float2(fin[BH * D * D + e], fin[BH * D * D + e + D]);
             }
 #pragma unroll
         for (int c = 0; c < CL; ++c) zk[c] = fin[2 * BH * D * D + (size_t)bh * D + l + 32 * c];
@@ -285,14 +295,15 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
     // ------------------------------------------------------------------
     cp_wait<0>();
     __syncthreads();  // ring free, tape visible to the whole CTA
-    float gS[RW][CL], gA[RW][CL], gzk[CL];
+    float2 gS2[RW / 2][CL], gA2[RW / 2][CL];
+    float gzk[CL];
 #pragma unroll
-    for (int r = 0; r < RW; ++r)
+    for (int rp = 0; rp < RW / 2; ++rp)
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
-            const size_t e = hdd + (r0 + r) * D + l + 32 * c;
-            gS[r][c] = dST ? dST[e] : 0.f;
-            gA[r][c] = dAT ? dAT[e] : 0.f;
+            const size_t e = hdd + (r0 + 2 * rp) * D + l + 32 * c;
+            gS2[rp][c] = dST ? make_float2(dST[e], dST[e + D]) : dup2(0.f);
+            gA2[rp][c] = dAT ? make_float2(dAT[e], dAT[e + D]) : dup2(0.f);
         }
 #pragma unroll
     for (int c = 0; c < CL; ++c) gzk[c] = dzkT ? dzkT[(size_t)bh * D + l + 32 * c] : 0.f;
@@ -341,13 +352,17 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
         {
             float pg[RW], pz[RW];
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                pg[r] = pz[r] = 0.f;
+            for (int rp = 0; rp < RW / 2; ++rp) {
+                float2 ag = dup2(0.f), az2 = dup2(0.f);
 #pragma unroll
                 for (int c = 0; c < CL; ++c) {
-                    pg[r] = fmaf(gS[r][c], al[c], pg[r]);
-                    pz[r] = fmaf(gA[r][c], zc[c], pz[r]);
+                    ag = __ffma2_rn(gS2[rp][c], dup2(al[c]), ag);
+                    az2 = __ffma2_rn(gA2[rp][c], dup2(zc[c]), az2);
                 }
+                pg[2 * rp] = ag.x;
+                pg[2 * rp + 1] = ag.y;
+                pz[2 * rp] = az2.x;
+                pz[2 * rp + 1] = az2.y;
             }
             const float gsal = rowsum8(pg), gaz = rowsum8(pz);
             if ((l & 3) == 0) {
@@ -364,16 +379,25 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
             lds8f(rec + 2 * D, r0, er);
             lds8f(gov, r0, gor);
             lds8f(rec, r0, zr);
+            {
+                float2 qe2[CL], qo2[CL], qz2[CL];
 #pragma unroll
-            for (int c = 0; c < CL; ++c) qe[c] = qo[c] = qz[c] = 0.f;
+                for (int c = 0; c < CL; ++c) qe2[c] = qo2[c] = qz2[c] = dup2(0.f);
 #pragma unroll
-            for (int r = 0; r < RW; ++r)
+                for (int rp = 0; rp < RW / 2; ++rp)
+#pragma unroll
+                    for (int c = 0; c < CL; ++c) {
+                        qe2[c] = __ffma2_rn(gS2[rp][c], pair2(er, 2 * rp), qe2[c]);
+                        qo2[c] = __ffma2_rn(S2[rp][c], pair2(gor, 2 * rp), qo2[c]);
+                        qz2[c] = __ffma2_rn(gA2[rp][c], pair2(zr, 2 * rp), qz2[c]);
+                    }
 #pragma unroll
                 for (int c = 0; c < CL; ++c) {
-                    qe[c] = fmaf(gS[r][c], er[r], qe[c]);
-                    qo[c] = fmaf(S[r][c], gor[r], qo[c]);
-                    qz[c] = fmaf(gA[r][c], zr[r], qz[c]);
+                    qe[c] = qe2[c].x + qe2[c].y;
+                    qo[c] = qo2[c].x + qo2[c].y;
+                    qz[c] = qz2[c].x + qz2[c].y;
                 }
+            }
 #pragma unroll
             for (int c = 0; c < CL; ++c) {
                 const int j = l + 32 * c;
@@ -468,18 +492,23 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
         }
         // product pass 2: columns S_t^T g_e; rows A_t g_a, A_t w1
         {
-            float pa[RW], pw[RW], qg[CL];
+            float pa[RW], pw[RW];
+            float2 qg2[CL];
 #pragma unroll
-            for (int c = 0; c < CL; ++c) qg[c] = 0.f;
+            for (int c = 0; c < CL; ++c) qg2[c] = dup2(0.f);
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                pa[r] = pw[r] = 0.f;
+            for (int rp = 0; rp < RW / 2; ++rp) {
+                float2 a2 = dup2(0.f), w2 = dup2(0.f);
 #pragma unroll
                 for (int c = 0; c < CL; ++c) {
-                    qg[c] = fmaf(S[r][c], ger[r], qg[c]);
-                    pa[r] = fmaf(A[r][c], gac[c], pa[r]);
-                    pw[r] = fmaf(A[r][c], w1c[c], pw[r]);
+                    qg2[c] = __ffma2_rn(S2[rp][c], pair2(ger, 2 * rp), qg2[c]);
+                    a2 = __ffma2_rn(A2[rp][c], dup2(gac[c]), a2);
+                    w2 = __ffma2_rn(A2[rp][c], dup2(w1c[c]), w2);
                 }
+                pa[2 * rp] = a2.x;
+                pa[2 * rp + 1] = a2.y;
+                pw[2 * rp] = w2.x;
+                pw[2 * rp + 1] = w2.y;
             }
             const float aga = rowsum8(pa), aw1 = rowsum8(pw);
             if ((l & 3) == 0) {
@@ -487,7 +516,7 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
                 R2[D + rr] = aw1;
             }
 #pragma unroll
-            for (int c = 0; c < CL; ++c) P2[w * D + l + 32 * c] = qg[c];
+            for (int c = 0; c < CL; ++c) P2[w * D + l + 32 * c] = qg2[c].x + qg2[c].y;
         }
         // adjoints of S_{t-1}, A_{t-1}:
         //   gS += dL/do phi_q^T / den - g_e k^^T;  gA += g_a k^^T + g_z u^^T
@@ -495,10 +524,12 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
             float gor[RW];
             lds8f(gov, r0, gor);
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                const float gs = gor[r] * rden;
+            for (int rp = 0; rp < RW / 2; ++rp) {
+                const float2 gs = make_float2(gor[2 * rp] * rden, gor[2 * rp + 1] * rden);
+                const float2 mg = make_float2(-ger[2 * rp], -ger[2 * rp + 1]);
 #pragma unroll
-                for (int c = 0; c < CL; ++c) gS[r][c] = fmaf(gs, pq[c], fmaf(-ger[r], kh[c], gS[r][c]));
+                for (int c = 0; c < CL; ++c)
+                    gS2[rp][c] = __ffma2_rn(gs, dup2(pq[c]), __ffma2_rn(mg, dup2(kh[c]), gS2[rp][c]));
             }
         }
         {
@@ -507,10 +538,12 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
             const int cs = r0 >> 5, lb = r0 & 31;
             const float ga_s = pick<CL>(gac, cs), gz_s = pick<CL>(gzc, cs);
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                const float gar = __shfl_sync(FULL, ga_s, lb + r), gzr = __shfl_sync(FULL, gz_s, lb + r);
+            for (int rp = 0; rp < RW / 2; ++rp) {
+                const float2 gar = make_float2(__shfl_sync(FULL, ga_s, lb + 2 * rp), __shfl_sync(FULL, ga_s, lb + 2 * rp + 1));
+                const float2 gzr = make_float2(__shfl_sync(FULL, gz_s, lb + 2 * rp), __shfl_sync(FULL, gz_s, lb + 2 * rp + 1));
 #pragma unroll
-                for (int c = 0; c < CL; ++c) gA[r][c] = fmaf(gar, kh[c], fmaf(gzr, uh[c], gA[r][c]));
+                for (int c = 0; c < CL; ++c)
+                    gA2[rp][c] = __ffma2_rn(gar, dup2(kh[c]), __ffma2_rn(gzr, dup2(uh[c]), gA2[rp][c]));
             }
         }
         // states before the token: S_{t-1} = S_t - e alpha^^T, A_{t-1} = A_t + z z^T / delta,
@@ -518,12 +551,12 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
         if (t % CK == 0) {
             const float* c = cp + (size_t)(t / CK) * L::CREC;
 #pragma unroll
-            for (int r = 0; r < RW; ++r)
+            for (int rp = 0; rp < RW / 2; ++rp)
 #pragma unroll
                 for (int cc = 0; cc < CL; ++cc) {
-                    const int e = (r0 + r) * D + l + 32 * cc;
-                    S[r][cc] = c[e];
-                    A[r][cc] = c[D * D + e];
+                    const int e = (r0 + 2 * rp) * D + l + 32 * cc;
+                    S2[rp][cc] = make_float2(c[e], c[e + D]);
+                    A2[rp][cc] = make_float2(c[D * D + e], c[D * D + e + D]);
                 }
 #pragma unroll
             for (int cc = 0; cc < CL; ++cc) zk[cc] = c[2 * D * D + l + 32 * cc];
@@ -532,12 +565,13 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
             lds8f(rec + 2 * D, r0, er);
             lds8f(rec, r0, zr);
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                const float zs = zr[r] * rdl;
+            for (int rp = 0; rp < RW / 2; ++rp) {
+                const float2 zs = make_float2(zr[2 * rp] * rdl, zr[2 * rp + 1] * rdl);
+                const float2 me = make_float2(-er[2 * rp], -er[2 * rp + 1]);
 #pragma unroll
                 for (int c = 0; c < CL; ++c) {
-                    S[r][c] = fmaf(-er[r], al[c], S[r][c]);
-                    A[r][c] = fmaf(zs, zc[c], A[r][c]);
+                    S2[rp][c] = __ffma2_rn(me, dup2(al[c]), S2[rp][c]);
+                    A2[rp][c] = __ffma2_rn(zs, dup2(zc[c]), A2[rp][c]);
                 }
             }
 #pragma unroll
@@ -551,12 +585,18 @@ __global__ void __launch_bounds__(BLay<D, TIn>::THREADS, 1)
                                  j_dl, j_nu, j_nk, dk + (size_t)bh * T * D, du + (size_t)bh * T * D);
     }
 #pragma unroll
-    for (int r = 0; r < RW; ++r)
+    for (int rp = 0; rp < RW / 2; ++rp)
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
-            const size_t e = hdd + (r0 + r) * D + l + 32 * c;
-            if (dS0) dS0[e] = gS[r][c];
-            if (dA0) dA0[e] = gA[r][c];
+            const size_t e = hdd + (r0 + 2 * rp) * D + l + 32 * c;
+            if (dS0) {
+                dS0[e] = gS2[rp][c].x;
+                dS0[e + D] = gS2[rp][c].y;
+            }
+            if (dA0) {
+                dA0[e] = gA2[rp][c].x;
+                dA0[e + D] = gA2[rp][c].y;
+            }
         }
     if (w == 0 && dzk0)
 #pragma unroll

@@ -273,14 +273,17 @@ __device__ __forceinline__ void s_sweep(const Params& p, int bh, size_t BH, cons
     const float* cp = ckpt + (size_t)bh * ((T + CK - 1) / CK + 1) * L::CREC;
     float gchk = 0.f;  // fma(x, 0, .) of every gradient and g_a written: 0 unless one is NaN or Inf
 
-    float S[RW][CL], gS[RW][CL], zk[CL], gzk[CL];
+    // S and gS: rows r0 + 2 rp (.x) and r0 + 2 rp + 1 (.y), columns l + 32 c,
+    // updated by packed FP32 FMAs (two rows per instruction)
+    float2 S2[RW / 2][CL], gS2[RW / 2][CL];
+    float zk[CL], gzk[CL];
 #pragma unroll
-    for (int r = 0; r < RW; ++r)
+    for (int rp = 0; rp < RW / 2; ++rp)
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
-            const size_t e = hdd + (size_t)(r0 + r) * D + l + 32 * c;
-            S[r][c] = T > 0 ? fin[e] : 0.f;
-            gS[r][c] = dST ? dST[e] : 0.f;
+            const size_t e = hdd + (size_t)(r0 + 2 * rp) * D + l + 32 * c;
+            S2[rp][c] = T > 0 ? make_float2(fin[e], fin[e + D]) : dup2(0.f);
+            gS2[rp][c] = dST ? make_float2(dST[e], dST[e + D]) : dup2(0.f);
         }
 #pragma unroll
     for (int c = 0; c < CL; ++c) {
@@ -326,25 +329,35 @@ __device__ __forceinline__ void s_sweep(const Params& p, int bh, size_t BH, cons
         {
             float pg[RW];
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                pg[r] = 0.f;
+            for (int rp = 0; rp < RW / 2; ++rp) {
+                float2 a = dup2(0.f);
 #pragma unroll
-                for (int c = 0; c < CL; ++c) pg[r] = fmaf(gS[r][c], al[c], pg[r]);
+                for (int c = 0; c < CL; ++c) a = __ffma2_rn(gS2[rp][c], dup2(al[c]), a);
+                pg[2 * rp] = a.x;
+                pg[2 * rp + 1] = a.y;
             }
             const float gsal = rowsum8(pg);
             if ((l & 3) == 0) r1[rr] = gsal;
             float er[RW], gor[RW], qe[CL], qo[CL];
             lds8f(rec + 2 * D, r0, er);
             lds8f(gov, r0, gor);
+            {
+                float2 qe2[CL], qo2[CL];
 #pragma unroll
-            for (int c = 0; c < CL; ++c) qe[c] = qo[c] = 0.f;
+                for (int c = 0; c < CL; ++c) qe2[c] = qo2[c] = dup2(0.f);
 #pragma unroll
-            for (int r = 0; r < RW; ++r)
+                for (int rp = 0; rp < RW / 2; ++rp)
+#pragma unroll
+                    for (int c = 0; c < CL; ++c) {
+                        qe2[c] = __ffma2_rn(gS2[rp][c], pair2(er, 2 * rp), qe2[c]);
+                        qo2[c] = __ffma2_rn(S2[rp][c], pair2(gor, 2 * rp), qo2[c]);
+                    }
 #pragma unroll
                 for (int c = 0; c < CL; ++c) {
-                    qe[c] = fmaf(gS[r][c], er[r], qe[c]);
-                    qo[c] = fmaf(S[r][c], gor[r], qo[c]);
+                    qe[c] = qe2[c].x + qe2[c].y;
+                    qo[c] = qo2[c].x + qo2[c].y;
                 }
+            }
             // token dots phi_q . alpha^, dL/do . e; this warp's shares of phi_q . S_t^T dL/do, alpha^ . gS^T e
 #pragma unroll
             for (int c = 0; c < CL; ++c) {
@@ -423,39 +436,46 @@ __device__ __forceinline__ void s_sweep(const Params& p, int bh, size_t BH, cons
         }
         // product pass 2: columns S_t^T g_e
         {
-            float qg[CL];
+            float2 qg2[CL];
 #pragma unroll
-            for (int c = 0; c < CL; ++c) qg[c] = 0.f;
+            for (int c = 0; c < CL; ++c) qg2[c] = dup2(0.f);
 #pragma unroll
-            for (int r = 0; r < RW; ++r)
+            for (int rp = 0; rp < RW / 2; ++rp)
 #pragma unroll
-                for (int c = 0; c < CL; ++c) qg[c] = fmaf(S[r][c], ger[r], qg[c]);
+                for (int c = 0; c < CL; ++c) qg2[c] = __ffma2_rn(S2[rp][c], pair2(ger, 2 * rp), qg2[c]);
 #pragma unroll
-            for (int c = 0; c < CL; ++c) P2[w * D + l + 32 * c] = qg[c];
+            for (int c = 0; c < CL; ++c) P2[w * D + l + 32 * c] = qg2[c].x + qg2[c].y;
         }
         // gS += dL/do phi_q^T / den - g_e k^^T
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
-            const float gs = gor[r] * rden;
+        for (int rp = 0; rp < RW / 2; ++rp) {
+            const float2 gs = make_float2(gor[2 * rp] * rden, gor[2 * rp + 1] * rden);
+            const float2 mg = make_float2(-ger[2 * rp], -ger[2 * rp + 1]);
 #pragma unroll
-            for (int c = 0; c < CL; ++c) gS[r][c] = fmaf(gs, pq[c], fmaf(-ger[r], kh[c], gS[r][c]));
+            for (int c = 0; c < CL; ++c)
+                gS2[rp][c] = __ffma2_rn(gs, dup2(pq[c]), __ffma2_rn(mg, dup2(kh[c]), gS2[rp][c]));
         }
         // S_{t-1} = S_t - e alpha^^T, z^key_{t-1} = z^key_t - phi(k_t); exact copies at checkpoints
         if (t % CK == 0) {
             const float* c = cp + (size_t)(t / CK) * L::CREC;
 #pragma unroll
-            for (int r = 0; r < RW; ++r)
+            for (int rp = 0; rp < RW / 2; ++rp)
 #pragma unroll
-                for (int cc = 0; cc < CL; ++cc) S[r][cc] = c[(r0 + r) * D + l + 32 * cc];
+                for (int cc = 0; cc < CL; ++cc) {
+                    const int e = (r0 + 2 * rp) * D + l + 32 * cc;
+                    S2[rp][cc] = make_float2(c[e], c[e + D]);
+                }
 #pragma unroll
             for (int cc = 0; cc < CL; ++cc) zk[cc] = c[2 * D * D + l + 32 * cc];
         } else {
             float er[RW];
             lds8f(rec + 2 * D, r0, er);
 #pragma unroll
-            for (int r = 0; r < RW; ++r)
+            for (int rp = 0; rp < RW / 2; ++rp) {
+                const float2 me = make_float2(-er[2 * rp], -er[2 * rp + 1]);
 #pragma unroll
-                for (int c = 0; c < CL; ++c) S[r][c] = fmaf(-er[r], al[c], S[r][c]);
+                for (int c = 0; c < CL; ++c) S2[rp][c] = __ffma2_rn(me, dup2(al[c]), S2[rp][c]);
+            }
 #pragma unroll
             for (int c = 0; c < CL; ++c) zk[c] -= phi(lds_in<TIn>(sl + L::K, l + 32 * c));
         }
@@ -468,10 +488,14 @@ __device__ __forceinline__ void s_sweep(const Params& p, int bh, size_t BH, cons
     if (tid == PairLay<D, TIn>::PUB && !p.stall_producer) pair_publish(rflag, -1);  // dL/dk_0's S part is written
     cp_wait<0>();
 #pragma unroll
-    for (int r = 0; r < RW; ++r)
+    for (int rp = 0; rp < RW / 2; ++rp)
 #pragma unroll
         for (int c = 0; c < CL; ++c)
-            if (dS0) dS0[hdd + (r0 + r) * D + l + 32 * c] = gS[r][c];
+            if (dS0) {
+                const size_t e = hdd + (size_t)(r0 + 2 * rp) * D + l + 32 * c;
+                dS0[e] = gS2[rp][c].x;
+                dS0[e + D] = gS2[rp][c].y;
+            }
     if (w == 0 && dzk0)
 #pragma unroll
         for (int c = 0; c < CL; ++c) dzk0[(size_t)bh * D + l + 32 * c] = gzk[c];

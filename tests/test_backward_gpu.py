@@ -154,6 +154,33 @@ def test_workload_d96_sampled_heads(orc):
         assert torch.isfinite(g).all()
 
 
+def test_workload4_cut_d128_sampled_heads(orc):
+    """The backward bench line's d = 128 configuration in its full launch: the
+    long-context workload cut to 4096 tokens (B=1, H=32, bf16 inputs, the
+    bench's seeded dL/do), on the taped cluster-pair forward and the
+    cluster-pair sweep; the oracle checks two sampled heads, every token."""
+    import dataclasses
+    w = dataclasses.replace(W.WORKLOADS[4], T=4096)
+    arrs = W.make(w)
+    gO = W.upstream_grad(w)
+    B, H, T, d = w.B, w.H, w.T, w.d
+    q, k, v, u = (_dev(a, torch.bfloat16) for a in arrs)
+    grads, dstate = vla_backward(q, k, v, u, w.lambda0, w.eps, None, _dev(gO), check=True)
+    heads = [0, B * H - 1]
+    flat = lambda x: x.reshape((B * H,) + x.shape[2:])[heads][None]
+    ref = orc.backward(*(flat(a).astype(np.float64) for a in arrs), w.lambda0, w.eps,
+                       gO=flat(gO).astype(np.float64))
+    pick = lambda x: flat(x.cpu().numpy())
+    dq, dk, dv, du = (pick(x) for x in grads)
+    dS0, dA0, dzk0 = (pick(x) for x in dstate)
+    errs = dict(dq=rel_rows(dq, ref["dq"]), dk=rel_rows(dk, ref["dk"]), dv=rel_rows(dv, ref["dv"]),
+                du=rel_rows(du, ref["du"]), dS0=rel_heads(dS0, ref["dS0"]), dA0=rel_heads(dA0, ref["dA0"]),
+                dzk0=rel_heads(dzk0, ref["dzk0"]))
+    assert_close(errs, what="backward d128 workload cut to T=4096")
+    for g in grads + dstate:
+        assert torch.isfinite(g).all()
+
+
 def test_two_streams_at_once(orc):
     """Two calls on two streams with no ordering between them: each has its
     own tape (the call's buffer from the caching allocator), so both results
