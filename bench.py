@@ -76,13 +76,13 @@ NCU_TRAFFIC = {
     # the reverse sweep (the step's dominant kernel, after the taped chunked forward), from a capture of
     # the same workload at B=2 (32 heads; a full step holds about 2.8 GB on the device) scaled by 4:
     # every byte it moves is per head-token or per head
-    "vla_backward_kernel": {"source_sha": "1420f755ed301e5d", "workload": (8, 16, 4096, 96, "bf16"),
-                            "bytes_per_launch": 4 * (438042880 + 177031168)},
+    "vla_backward_kernel": {"source_sha": "5315436c0f21b084", "workload": (8, 16, 4096, 96, "bf16"),
+                            "bytes_per_launch": 4 * (436128256 + 176882432)},
     # the split reverse sweep (d = 128) on the long-context workload cut to 4096 tokens
-    "vla_backward_pair_kernel": {"source_sha": "c19e0ef0ec50bbe8", "workload": (1, 32, 4096, 128, "bf16"),
-                                 "bytes_per_launch": 647584000 + 307564800},
-    "vla_decode_kernel": {"source_sha": "9c13b0c3ed588538", "workload": (128, 16, 1, 96, "bf16"),
-                          "bytes_per_launch": 153392896 + 98219264},
+    "vla_backward_pair_kernel": {"source_sha": "5df2099d1b2bece4", "workload": (1, 32, 4096, 128, "bf16"),
+                                 "bytes_per_launch": 648319488 + 307634432},
+    "vla_decode_kernel": {"source_sha": "46994107829e6084", "workload": (128, 16, 1, 96, "bf16"),
+                          "bytes_per_launch": 153393408 + 98091264},
     "vla_fused_kernel": {"source_sha": "565a71784acabc88", "workload": (8, 16, 4096, 96, "bf16"),
                          "bytes_per_launch": 403125248 + 175399936},
 }
