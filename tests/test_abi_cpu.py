@@ -192,19 +192,26 @@ def test_backward_workspace_bytes(lib):
     assert lib.vla_backward_workspace_bytes(1 << 30, 1 << 30, 4, 64) == 0
 
 
-def _bw_call(lib, split=False, **kw):
+def _bw_call(lib, split=False, ex=False, **kw):
+    """vla_backward / vla_backward_split, or with ex=True the same call
+    through vla_backward_ex (options with a wait limit)."""
     a = dict(q=FAKE, k=FAKE, v=FAKE, u=FAKE, dtype=1, B=1, H=1, T=4, d=64, lambda0=0.1, eps=1e-4,
              S0=None, A0=None, zk0=None, gO=FAKE, gS=None, gA=None, gzk=None,
              dq=FAKE, dk=FAKE, dv=FAKE, du=FAKE, dS0=FAKE, dA0=FAKE, dzk0=FAKE, ws=FAKE, wsb=1 << 30)
     a.update(kw)
     vp = ctypes.c_void_p
     p = lambda n: vp(a[n])
-    fn = lib.vla_backward_split if split else lib.vla_backward
-    return fn(p("q"), p("k"), p("v"), p("u"), a["dtype"], a["B"], a["H"], a["T"], a["d"], a["lambda0"], a["eps"],
-              p("S0"), p("A0"), p("zk0"), p("gO"), p("gS"), p("gA"), p("gzk"), p("dq"), p("dk"), p("dv"), p("du"),
-              p("dS0"), p("dA0"), p("dzk0"), p("ws"), a["wsb"], None)
+    args = (p("q"), p("k"), p("v"), p("u"), a["dtype"], a["B"], a["H"], a["T"], a["d"], a["lambda0"], a["eps"],
+            p("S0"), p("A0"), p("zk0"), p("gO"), p("gS"), p("gA"), p("gzk"), p("dq"), p("dk"), p("dv"), p("du"),
+            p("dS0"), p("dA0"), p("dzk0"), p("ws"), a["wsb"], None)
+    if ex:
+        from sherman_morrison_memory_gb300 import _binding
+        opts = _binding._Options(5000, 0, None, 0, 0)
+        return lib.vla_backward_ex(*args, 1 if split else 0, ctypes.byref(opts))
+    return (lib.vla_backward_split if split else lib.vla_backward)(*args)
 
 
+@pytest.mark.parametrize("ex", [False, True])
 @pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("kw,status", [
     (dict(d=160), 2), (dict(d=48), 2), (dict(d=0), 2),
@@ -216,14 +223,15 @@ def _bw_call(lib, split=False, **kw):
     (dict(dS0=FAKE + 2), 1), (dict(S0=FAKE + 1), 1),
     (dict(B=1 << 30, H=1 << 30), 1),
 ])
-def test_backward_argument_errors(lib, kw, status, split):
-    assert _bw_call(lib, split, **kw) == status
+def test_backward_argument_errors(lib, kw, status, split, ex):
+    assert _bw_call(lib, split, ex, **kw) == status
 
 
+@pytest.mark.parametrize("ex", [False, True])
 @pytest.mark.parametrize("split", [False, True])
-def test_backward_empty_batch_is_a_no_op(lib, split):
-    assert _bw_call(lib, split, B=0) == 0
-    assert _bw_call(lib, split, B=0, d=128) == 0
+def test_backward_empty_batch_is_a_no_op(lib, split, ex):
+    assert _bw_call(lib, split, ex, B=0) == 0
+    assert _bw_call(lib, split, ex, B=0, d=128) == 0
 
 
 def _host_call(lib, **kw):

@@ -181,10 +181,11 @@ def test_workload4_cut_d128_sampled_heads(orc):
         assert torch.isfinite(g).all()
 
 
-def test_two_streams_at_once(orc):
+@pytest.mark.parametrize("split", [False, True])
+def test_two_streams_at_once(orc, split):
     """Two calls on two streams with no ordering between them: each has its
     own tape (the call's buffer from the caching allocator), so both results
-    are the oracle's."""
+    are the oracle's; split=True runs the cluster-pair sweep."""
     cases = []
     for seed in (31, 32):
         arrs = _inputs(1, 2, 129, 64, "bf16", seed=seed)
@@ -197,7 +198,7 @@ def test_two_streams_at_once(orc):
     res = []
     for (x, g, gs), st in zip(dev_in, streams):
         with torch.cuda.stream(st):
-            res.append(vla_backward(*x, 0.1, 1e-4, None, g, gs))
+            res.append(vla_backward(*x, 0.1, 1e-4, None, g, gs, split=split))
     torch.cuda.synchronize()
     for (arrs, gO, gst), (grads, dstate) in zip(cases, res):
         ref = orc.backward(*(_f64(a) for a in arrs), 0.1, 1e-4, None, None, None, _f64(gO),
