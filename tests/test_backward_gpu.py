@@ -228,9 +228,12 @@ def test_nonfinite_then_clean_call_succeeds(orc):
     assert_close(_errors(*_run(orc, arrs, "f32", gO, None)), what="backward after a non-finite call")
 
 
-@pytest.mark.parametrize("T", [1, 37, 129])
+@pytest.mark.parametrize("T", [1, 2, 3, 16, 37, 64, 65, 129])
 def test_d128_small_f32(orc, T):
-    """d = 128: the per-token forward with tape, then the split reverse sweep."""
+    """d = 128: the taped cluster-pair forward, then the split reverse sweep
+    on a cluster pair. T = 2, 3: the A side's first wait is for a token the
+    S side reaches only at its end; T = 16, 64, 65: exactly one chunk, one
+    checkpoint interval, and one token past it (a second checkpoint slot)."""
     B, H, d = 1, 2, 128
     arrs = _inputs(B, H, T, d, "f32", seed=20 + T)
     gO, gst = _seeds(B, H, T, d, seed=20 + T)
