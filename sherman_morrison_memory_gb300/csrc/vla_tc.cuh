@@ -60,8 +60,11 @@ template <int D, typename TIn>
 struct Lay {
     static constexpr bool F32IN = sizeof(TIn) == 4;
     static constexpr int NRW = D / 32;          // row warps per team
-    static constexpr int NP = F32IN ? 2 : 3;    // prepared chunk slots
-    static constexpr int NRAW = F32IN ? 1 : 2;  // raw chunk slots
+    // prepared and raw chunk slots: three and two, so that the staging warps
+    // run up to two chunks ahead of the A team; fp32 inputs at d = 96 leave
+    // room for only two and one
+    static constexpr int NP = (F32IN && D > 64) ? 2 : 3;
+    static constexpr int NRAW = (F32IN && D > 64) ? 1 : 2;
     // prepared chunk: HI tile rows u (0..C-1) | k (C..2C-1) | phi (2C..3C-1)
     // (raw values; bf16 u, k are exact in tf32), LO tile rows = lo parts that
     // are nonzero: phi_lo only for bf16 inputs, u_lo | k_lo | phi_lo for fp32
