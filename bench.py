@@ -67,12 +67,12 @@ KERNEL_FILES = {
 # was taken on (B, H, T, d, input dtype) and while that kernel's own sources
 # hash to source_sha; otherwise reported as null.
 NCU_TRAFFIC = {
-    "vla_tc_kernel": {"source_sha": "da589c5764bac785", "workload": (8, 16, 4096, 96, "bf16"),
-                      "bytes_per_launch": 403224320 + 176125696},
+    "vla_tc_kernel": {"source_sha": "a42f512597716e3c", "workload": (8, 16, 4096, 96, "bf16"),
+                      "bytes_per_launch": 403375360 + 175656448},
     # from a capture at T = 8192 (the full launch holds about 3.2 GB on the device), the per-token part
     # scaled by 8; the final S, A, z^key writes (32 x (2 d^2 + d) x 4 bytes) are per head
-    "vla_tc3_kernel": {"source_sha": "b86b909885d02241", "workload": (1, 32, 65536, 128, "bf16"),
-                       "bytes_per_launch": 8 * (268663040 + 108134656 - 4227072) + 4227072},
+    "vla_tc3_kernel": {"source_sha": "dfea88a0086d207e", "workload": (1, 32, 65536, 128, "bf16"),
+                       "bytes_per_launch": 8 * (268556544 + 108200448 - 4227072) + 4227072},
     # the reverse sweep (the step's dominant kernel, after the taped chunked forward), from a capture of
     # the same workload at B=2 (32 heads; a full step holds about 2.8 GB on the device) scaled by 4:
     # every byte it moves is per head-token or per head
