@@ -154,9 +154,9 @@ def test_status_read_rejects_null(lib):
 def test_algo_argument_errors(lib, algo, d, fixed, status):
     """VLA_ALGO_* outside {0, ..., 6} is an argument error; the chunked kernel
     and the segmented path report d = 128 as unsupported; the segmented path
-    with a 256-byte workspace (or T < 32) is an argument error; the
-    reports d = 128 as unsupported; the fixed-A variant does not run on the
-    per-token kernel. All are decided before any CUDA call."""
+    with a 256-byte workspace (or T < 32) is an argument error; the fixed-A
+    variant does not run on the per-token kernel. All are decided before any
+    CUDA call."""
     from sherman_morrison_memory_gb300 import _binding
     vp = ctypes.c_void_p
     opts = _binding._Options(0, 0, None, algo, fixed)
@@ -164,6 +164,21 @@ def test_algo_argument_errors(lib, algo, d, fixed, status):
                             ctypes.c_float(1e-4), None, None, None, vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE),
                             ctypes.c_size_t(256), None, ctypes.byref(opts))
     assert st == status
+
+
+@pytest.mark.parametrize("scratch_off,scratch_bytes", [(16, 1 << 30), (0, 256), (0, 0)])
+def test_segmented_scratch_argument_errors(lib, scratch_off, scratch_bytes):
+    """The segmented path's own buffers (vla_options.scratch) must be 256-byte
+    aligned and hold vla_workspace_bytes_ex(..., VLA_ALGO_SEGMENTED) bytes,
+    whatever the workspace holds; both are checked before any CUDA call."""
+    from sherman_morrison_memory_gb300 import _binding
+    vp = ctypes.c_void_p
+    opts = _binding._Options(0, 0, None, 6, 0, vp(FAKE + scratch_off), scratch_bytes)
+    st = lib.vla_forward_ex(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 1, 1, 1, 64, 64, ctypes.c_float(0.1),
+                            ctypes.c_float(1e-4), None, None, None, vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE),
+                            ctypes.c_size_t(1 << 30), None, ctypes.byref(opts))
+    assert st == 1
+    assert lib.vla_workspace_bytes_ex(1, 1, 64, 64, 6) > 256
 
 
 def test_u_may_be_null_only_for_fixed_a(lib):
